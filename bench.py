@@ -1,0 +1,402 @@
+"""Benchmark of the TurboQuant hot path on B300: long-context batched decode over a
+compressed KV cache.
+
+Workload (one step = one decode step of every sequence):
+  batch 8, 8 KV heads, 32 query heads (GQA groups of 4), head_dim 128, 131072 cached tokens
+  (bf16 keys/values from the anisotropic generator, quantized at prefill: keys 3 bits =
+  2-bit codes + 1 QJL bit, values 3-bit MSE-only codes), then per step:
+    append the new token's key and value (rotate + code + pack, QJL signs for the key),
+    advance the lengths, score all cached keys (attention logits, written to HBM), and the
+    attention output (softmax-weighted sum of the dequantized values).
+Metric: compressed-key logit scores per second (query heads x cached keys / time), plus
+the HBM bandwidth those kernels achieve.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a bounded sample.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, HKV, G, D, N0 = 8, 8, 4, 128, 131072
+HQ = HKV * G
+KBITS, VBITS = 3, 3
+SEED_ROT, SEED_DATA = 0, 3
+METRIC = "compressed-key logit scores/sec and achieved HBM GB/s (% of B300 roofline)"
+UNIT = "logit scores/s"
+WORKLOAD = ("long-context batched decode: batch 8, 8 KV heads, 32 query heads, head_dim 128, "
+            "131072 cached tokens + 1 appended per step; keys 3 bits (2 MSE + 1 QJL), values 3-bit MSE")
+
+# Algorithmic bytes per cached key for one (batch, KV head) group at d = 128
+K_BYTES = 2 * 16 + 16 + 2 + 2        # 2 code planes, sign words, norm, residual norm = 52
+V_BYTES = 3 * 16 + 2                 # 3 code planes + norm = 50
+LOGIT_BYTES = K_BYTES + G * 4        # keys read + 4 fp32 logits written = 68
+OUTPUT_BYTES = K_BYTES + V_BYTES     # keys + values read = 102
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 6:
+                self.rows.append(parts)
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4) if r[2 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- the TQ arm
+
+def build_state(dev):
+    from compressed_kv_cache_02_b300 import inputs, tq
+    kctx = tq.Context(D, KBITS, seed=SEED_ROT)
+    vctx = tq.Context(D, VBITS, seed=SEED_ROT + 1, mode=tq.TQ_MODE_MSE)
+    cap = N0 + 4096
+    kc = kctx.alloc_codes(B, HKV, cap, device=dev)
+    vc = vctx.alloc_codes(B, HKV, cap, device=dev)
+    kfac = inputs.anisotropic_factors(HKV, D, seed=SEED_DATA, device=dev)
+    vfac = inputs.anisotropic_factors(HKV, D, seed=SEED_DATA + 1000, device=dev)
+    t_pre = 0.0
+    for b in range(B):   # prefill one batch row at a time: 2 x 256 MB of bf16 at a time
+        K = inputs.anisotropic(1, HKV, N0, D, kfac, seed=SEED_DATA * 100 + b, device=dev)
+        V = inputs.anisotropic(1, HKV, N0, D, vfac, seed=SEED_DATA * 100 + 1000 + b, device=dev)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for h in range(HKV):
+            kctx.quantize(K[0, h], out=tq.Codes(kc.planes[b, h, :N0], kc.norm[b, h, :N0], kc.signs[b, h, :N0],
+                                                kc.rnorm[b, h, :N0]))
+            vctx.quantize(V[0, h], out=tq.Codes(vc.planes[b, h, :N0], vc.norm[b, h, :N0]))
+        e1.record()
+        torch.cuda.synchronize()
+        t_pre += e0.elapsed_time(e1) / 1e3
+        del K, V
+    flags = kctx.sync_status() | vctx.sync_status()
+    if flags:
+        raise RuntimeError(f"device error flags {flags} after prefill")
+    return dict(kctx=kctx, vctx=vctx, kc=kc, vc=vc, cap=cap, kfac=kfac, vfac=vfac,
+                prefill_s=t_pre, prefill_vectors=2 * B * HKV * N0)
+
+
+def step_inputs(state, nsteps, dev):
+    from compressed_kv_cache_02_b300 import inputs
+    ks, vs, qs = [], [], []
+    for s in range(nsteps):
+        ks.append(inputs.anisotropic(B, HKV, 1, D, state["kfac"], seed=10_000 + s, device=dev)[:, :, 0])
+        vs.append(inputs.anisotropic(B, HKV, 1, D, state["vfac"], seed=20_000 + s, device=dev)[:, :, 0])
+        q = inputs.anisotropic(B, HKV, G, D, state["kfac"], seed=30_000 + s, device=dev, dtype=torch.float32)
+        qs.append(q.reshape(B, HQ, D).contiguous())
+    return ks, vs, qs
+
+
+def run_tq(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    state = build_state(dev)
+    kctx, vctx, kc, vc, cap = state["kctx"], state["vctx"], state["kc"], state["vc"], state["cap"]
+    total = args.warmup + args.steps
+    assert N0 - args.warmup >= 1 and N0 + args.steps <= cap
+    ks, vs, qs = step_inputs(state, total, dev)
+    length = torch.full((B,), N0 - args.warmup, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, HQ, cap, device=dev)
+    out = torch.empty(B, HQ, D, device=dev)
+    ws = kctx.attn_workspace(B, HQ, HKV, cap, device=dev)
+    scale = 1.0 / D ** 0.5
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev=None):
+        kctx.append(ks[s], kc, cap, length)
+        vctx.append(vs[s], vc, cap, length)
+        kctx.advance_len(length, cap)
+        if ev:
+            ev[0].record()
+        kctx.attn_logits(qs[s], kc, cap, length, scale, out=logits, workspace=ws)
+        if ev:
+            ev[1].record()
+        kctx.attn_output(qs[s], kc, cap, length, scale, vc, vctx=vctx, out=out, workspace=ws)
+        if ev:
+            ev[2].record()
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if kctx.sync_status() or vctx.sync_status():
+        raise RuntimeError("device error flags after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lens_timed = [N0 + s + 1 for s in range(args.steps)]    # cache length seen by step s
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            step(args.warmup + s, evs[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, world)
+    if kctx.sync_status() or vctx.sync_status():
+        raise RuntimeError("device error flags after the timed steps")
+    t_logits = [e[0].elapsed_time(e[1]) / 1e3 for e in evs]
+    t_output = [e[1].elapsed_time(e[2]) / 1e3 for e in evs]
+    keys = sum(lens_timed) * B * HKV
+    scores = keys * G
+    value = scores * world / elapsed
+
+    # end to end through the public API: pinned host inputs in, the step's output back out
+    hk = [k.cpu().pin_memory() for k in ks]
+    hv = [v.cpu().pin_memory() for v in vs]
+    hq = [q.cpu().pin_memory() for q in qs]
+    hout = torch.empty(B, HQ, D).pin_memory()
+    dk, dv, dq = torch.empty_like(ks[0]), torch.empty_like(vs[0]), torch.empty_like(qs[0])
+    length.fill_(N0 - args.warmup)
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        i = args.warmup + s
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dq.copy_(hq[i], non_blocking=True)
+        kctx.append(dk, kc, cap, length)
+        vctx.append(dv, vc, cap, length)
+        kctx.advance_len(length, cap)
+        kctx.attn_logits(dq, kc, cap, length, scale, out=logits, workspace=ws)
+        kctx.attn_output(dq, kc, cap, length, scale, vc, vctx=vctx, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    h2d = dk.numel() * dk.element_size() + dv.numel() * dv.element_size() + dq.numel() * 4
+    d2h = hout.numel() * 4
+
+    hbm, peak_kind = peaks()
+    logits_bytes = [LOGIT_BYTES * B * HKV * L for L in lens_timed]
+    output_bytes = [OUTPUT_BYTES * B * HKV * L for L in lens_timed]
+    gbs_logits = sum(logits_bytes) / sum(t_logits) / 1e9
+    gbs_output = sum(output_bytes) / sum(t_output) / 1e9
+    dominant = "attn_output" if sum(t_output) >= sum(t_logits) else "attn_logits"
+    dom_gbs = gbs_output if dominant == "attn_output" else gbs_logits
+    launches_per_step = 3 + 3 + 4   # append x2 + advance; logits: prep x2 + kernel; output: prep x2 + partial + combine
+    step_bytes = (sum(logits_bytes) + sum(output_bytes)) / args.steps
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "kv_heads": HKV, "query_heads": HQ, "head_dim": D,
+                   "cached_tokens": N0, "key_bits": KBITS, "value_bits": VBITS, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (cache codes ~0.9 GB)"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": dom_gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs", "traffic": None},
+        "kernels": {
+            "attn_logits": {"ms": statistics.mean(t_logits) * 1e3, "GB_s": gbs_logits,
+                            "bytes_per_key": LOGIT_BYTES, "frac_of_measured": gbs_logits / hbm,
+                            "frac_of_8TBs": gbs_logits / 8000.0},
+            "attn_output": {"ms": statistics.mean(t_output) * 1e3, "GB_s": gbs_output,
+                            "bytes_per_key": OUTPUT_BYTES, "frac_of_measured": gbs_output / hbm,
+                            "frac_of_8TBs": gbs_output / 8000.0},
+            "step_GB_s": step_bytes / (elapsed / args.steps) / 1e9,
+            "prefill_quantize": {"vectors": state["prefill_vectors"], "s": state["prefill_s"],
+                                 "vectors_per_s": state["prefill_vectors"] / state["prefill_s"]},
+        },
+        "e2e": {"value": scores * world / e2e_elapsed, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
+    return res
+
+
+# ----------------------------------------------------------------------------- the oracle arm
+
+def oracle_step_sample(n_keys: int, seed: int = SEED_DATA):
+    """Bounded oracle sample of one decode step: one (batch, KV head) group with n_keys cached
+    keys and values, its 4 query heads: quantize the new key and value, score every key
+    (logits) and form the attention output.  Returns (logit scores computed, seconds)."""
+    import oracle
+    from compressed_kv_cache_02_b300 import inputs
+    Pi, S = oracle.method_matrices(SEED_ROT, D, D)
+    Piv, _ = oracle.method_matrices(SEED_ROT + 1, D, 1)
+    cbk = oracle.sphere_codebook(D, KBITS - 1)
+    cbv = oracle.sphere_codebook(D, VBITS)
+    fk = inputs.anisotropic_factors(1, D, seed=seed)
+    fv = inputs.anisotropic_factors(1, D, seed=seed + 1000)
+    K = inputs.anisotropic(1, 1, n_keys + 1, D, fk, seed=seed).float().numpy()
+    V = inputs.anisotropic(1, 1, n_keys + 1, D, fv, seed=seed + 1000).float().numpy()
+    q = inputs.anisotropic(1, 1, G, D, fk, seed=seed + 2000, dtype=torch.float32).numpy().reshape(1, G, D)
+    kz = oracle.quantize(K[0, 0, :n_keys], Pi, cbk, S)          # prefill (not timed)
+    vz = oracle.quantize(V[0, 0, :n_keys], Piv, cbv)
+    t = time.perf_counter()
+    kn = oracle.quantize(K[0, 0, n_keys:], Pi, cbk, S)          # the step's append
+    vn = oracle.quantize(V[0, 0, n_keys:], Piv, cbv)
+    keys = oracle.Quantized(idx=np.concatenate([kz.idx, kn.idx])[None, None],
+                            norm16=np.concatenate([kz.norm16, kn.norm16])[None, None],
+                            signs=np.concatenate([kz.signs, kn.signs])[None, None],
+                            rnorm16=np.concatenate([kz.rnorm16, kn.rnorm16])[None, None])
+    vals = oracle.Quantized(idx=np.concatenate([vz.idx, vn.idx])[None, None],
+                            norm16=np.concatenate([vz.norm16, vn.norm16])[None, None])
+    L = np.array([n_keys + 1])
+    oracle.attention_logits(q, keys, L, Pi, S, cbk, 1.0 / D ** 0.5)
+    oracle.attention_output(q, keys, L, Pi, S, cbk, 1.0 / D ** 0.5, values=vals, Pi_v=Piv, cb_v=cbv)
+    return G * (n_keys + 1), time.perf_counter() - t
+
+
+def cpu_threads() -> int:
+    """Threads the oracle's numpy actually runs on: the BLAS pool size (elementwise work is serial)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return 1
+
+
+def cpu_baseline(args, budget_s: float = 15.0):
+    n_keys = 32768
+    done, spent, reps = 0, 0.0, 0
+    while spent < budget_s or reps == 0:
+        s, t = oracle_step_sample(n_keys)
+        done += s
+        spent += t
+        reps += 1
+        if reps >= 64:
+            break
+    return {"value": done / spent, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{reps} x one decode step of one (batch, KV head) group: 4 query heads x {n_keys + 1} "
+                      f"cached keys (append + logits + output), numpy float64"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    n_keys = 32768
+    for _ in range(args.warmup):
+        oracle_step_sample(n_keys)
+    done, spent = 0, 0.0
+    for _ in range(args.steps):
+        s, t = oracle_step_sample(n_keys)
+        done += s
+        spent += t
+    v = done / spent
+    sample = (f"each step: one (batch, KV head) group of the decode workload, 4 query heads x {n_keys + 1} "
+              f"cached keys (append + logits + output), numpy float64 oracle")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_tq(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+// Host-side set-up of a TurboQuant context: seeded matrices, the Lloyd-Max table and its
+// Walsh form.  Runs once per context, in float64, on the CPU.
+//
+// Pages: freelamp.com article 0328, section 技术突破 (a random orthogonal rotation first,
+// after which the coordinates follow a predictable law); gitcode.csdn.net tutorial,
+// section QJL step 1 (Gaussian JL projection of the residual); nonndazone.ru essay,
+// sections 3.2 and 3.4 (centroids placed where probability is high, precomputed once
+// for all tokens and layers).
+#include <algorithm>
+#include <cmath>
+#include <stdexcept>
+#include <vector>
+
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+// ---------------------------------------------------------------- random numbers
+// splitmix64 (Steele, Lea, Flood, OOPSLA 2014), output k uses state seed + (k+1)*gamma.
+struct SplitMix64 {
+    uint64_t state;
+    explicit SplitMix64(uint64_t s) : state(s) {}
+    uint64_t next() {
+        state += 0x9E3779B97F4A7C15ULL;
+        uint64_t z = state;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+        return z ^ (z >> 31);
+    }
+    // uniform in (0, 1]
+    double uniform() { return (static_cast<double>(next() >> 11) + 1.0) * 0x1.0p-53; }
+};
+
+// Box-Muller: each pair of uniforms (u1, u2) yields r cos(2 pi u2), r sin(2 pi u2).
+std::vector<double> normals(uint64_t seed, size_t count) {
+    SplitMix64 g(seed);
+    std::vector<double> out(count + 1);
+    for (size_t k = 0; k < count; k += 2) {
+        double u1 = g.uniform(), u2 = g.uniform();
+        double r = std::sqrt(-2.0 * std::log(u1));
+        double th = 2.0 * M_PI * u2;
+        out[k] = r * std::cos(th);
+        out[k + 1] = r * std::sin(th);
+    }
+    out.resize(count);
+    return out;
+}
+
+// Householder QR of the row-major n x n matrix A; returns Q with the columns' signs fixed
+// so that diag(R) > 0 (Q diag(sign(diag R)) is Haar-distributed when A is Gaussian).
+std::vector<double> haar_from_gaussian(std::vector<double> A, int n) {
+    std::vector<std::vector<double>> vs(n);
+    std::vector<double> rdiag(n);
+    for (int k = 0; k < n; ++k) {
+        double norm2 = 0.0;
+        for (int i = k; i < n; ++i) norm2 += A[(size_t)i * n + k] * A[(size_t)i * n + k];
+        double nx = std::sqrt(norm2);
+        double x0 = A[(size_t)k * n + k];
+        double alpha = (x0 >= 0.0) ? -nx : nx;   // reflect onto -sign(x0) ||x|| e1
+        std::vector<double> v(n - k);
+        for (int i = k; i < n; ++i) v[i - k] = A[(size_t)i * n + k];
+        v[0] -= alpha;
+        double vn2 = 0.0;
+        for (double e : v) vn2 += e * e;
+        if (vn2 > 0.0) {
+            double inv = 1.0 / std::sqrt(vn2);
+            for (double& e : v) e *= inv;
+            for (int j = k; j < n; ++j) {
+                double dot = 0.0;
+                for (int i = k; i < n; ++i) dot += v[i - k] * A[(size_t)i * n + j];
+                for (int i = k; i < n; ++i) A[(size_t)i * n + j] -= 2.0 * v[i - k] * dot;
+            }
+        } else {
+            alpha = x0;
+        }
+        rdiag[k] = alpha;
+        vs[k] = std::move(v);
+    }
+    // Q = H_0 H_1 ... H_{n-1}: apply the reflectors in reverse order to the identity.
+    std::vector<double> Q((size_t)n * n, 0.0);
+    for (int i = 0; i < n; ++i) Q[(size_t)i * n + i] = 1.0;
+    for (int k = n - 1; k >= 0; --k) {
+        const std::vector<double>& v = vs[k];
+        if (v.empty()) continue;
+        for (int j = 0; j < n; ++j) {
+            double dot = 0.0;
+            for (int i = k; i < n; ++i) dot += v[i - k] * Q[(size_t)i * n + j];
+            for (int i = k; i < n; ++i) Q[(size_t)i * n + j] -= 2.0 * v[i - k] * dot;
+        }
+    }
+    for (int j = 0; j < n; ++j) {
+        if (rdiag[j] < 0.0)
+            for (int i = 0; i < n; ++i) Q[(size_t)i * n + j] = -Q[(size_t)i * n + j];
+    }
+    return Q;
+}
+
+// ---------------------------------------------------------------- quadrature
+struct GaussLegendre {
+    std::vector<double> x, w;   // nodes and weights on [-1, 1]
+    explicit GaussLegendre(int n) : x(n), w(n) {
+        for (int i = 0; i < n; ++i) {
+            double z = std::cos(M_PI * (i + 0.75) / (n + 0.5));
+            double dp = 0.0;
+            for (int it = 0; it < 100; ++it) {
+                double p0 = 1.0, p1 = z;
+                for (int k = 2; k <= n; ++k) {
+                    double p2 = ((2.0 * k - 1.0) * z * p1 - (k - 1.0) * p0) / k;
+                    p0 = p1;
+                    p1 = p2;
+                }
+                dp = n * (z * p1 - p0) / (z * z - 1.0);
+                double dz = p1 / dp;
+                z -= dz;
+                if (std::fabs(dz) < 1e-16) break;
+            }
+            x[i] = z;
+            w[i] = 2.0 / ((1.0 - z * z) * dp * dp);
+        }
+    }
+};
+
+struct SphereMarginal {
+    int d;
+    double log_c;
+    double reach;   // beyond |t| > reach the density is below 1e-40 of its peak
+    GaussLegendre gl{32};
+    explicit SphereMarginal(int d_) : d(d_) {
+        log_c = std::lgamma(d / 2.0) - 0.5 * std::log(M_PI) - std::lgamma((d - 1) / 2.0);
+        reach = std::min(1.0, 14.0 / std::sqrt((double)d));
+    }
+    double pdf(double t) const {
+        if (std::fabs(t) >= 1.0) return 0.0;
+        return std::exp(log_c + 0.5 * (d - 3) * std::log1p(-t * t));
+    }
+    // (integral of f, integral of t f) over (a, b), composite 32-point Gauss-Legendre.
+    void moments(double a, double b, double& m0, double& m1) const {
+        a = std::max(a, -reach);
+        b = std::min(b, reach);
+        m0 = m1 = 0.0;
+        if (b <= a) return;
+        double h = 0.25 / std::sqrt((double)d);
+        int panels = std::max(1, (int)std::ceil((b - a) / h));
+        double step = (b - a) / panels;
+        for (int p = 0; p < panels; ++p) {
+            double lo = a + p * step, mid = lo + 0.5 * step, half = 0.5 * step;
+            for (size_t i = 0; i < gl.x.size(); ++i) {
+                double t = mid + half * gl.x[i];
+                double f = pdf(t) * gl.w[i] * half;
+                m0 += f;
+                m1 += t * f;
+            }
+        }
+    }
+};
+
+}  // namespace
+
+void seeded_matrices(uint64_t seed, int d, int m, std::vector<double>& Pi, std::vector<double>& S) {
+    std::vector<double> g = normals(seed, (size_t)m * d + (size_t)d * d);
+    S.assign(g.begin(), g.begin() + (size_t)m * d);
+    std::vector<double> G(g.begin() + (size_t)m * d, g.end());
+    Pi = haar_from_gaussian(std::move(G), d);
+}
+
+// Lloyd-Max: thresholds at midpoints of adjacent centroids, centroids at the conditional
+// means of their cells; repeated to a fixed point (unique: f_d is log-concave for d >= 3).
+void lloyd_max_codebook(int d, int bits, std::vector<double>& c, std::vector<double>& t) {
+    const int L = 1 << bits;
+    SphereMarginal f(d);
+    c.resize(L);
+    t.resize(L - 1);
+    const double spread = std::min(1.0, 2.0 / std::sqrt((double)d));   // start inside (-1, 1)
+    for (int k = 0; k < L; ++k) c[k] = (2.0 * k + 1.0 - L) / L * spread;
+    std::vector<double> cn(L);
+    for (int it = 0; it < 200000; ++it) {
+        for (int k = 0; k + 1 < L; ++k) t[k] = 0.5 * (c[k] + c[k + 1]);
+        double moved = 0.0;
+        for (int k = 0; k < L; ++k) {
+            double a = (k == 0) ? -1.0 : t[k - 1];
+            double b = (k == L - 1) ? 1.0 : t[k];
+            double m0, m1;
+            f.moments(a, b, m0, m1);
+            cn[k] = m0 > 0.0 ? m1 / m0 : c[k];
+            moved = std::max(moved, std::fabs(cn[k] - c[k]));
+        }
+        c = cn;
+        if (moved < 4e-16) break;   // at the fixed point up to rounding
+    }
+    for (int k = 0; k < L / 2; ++k) {   // the density is even: symmetrise
+        double s = 0.5 * (c[L - 1 - k] - c[k]);
+        c[k] = -s;
+        c[L - 1 - k] = s;
+    }
+    for (int k = 0; k + 1 < L; ++k) t[k] = 0.5 * (c[k] + c[k + 1]);
+    if (L % 2 == 0) t[L / 2 - 1] = 0.0;
+}
+
+// Walsh form of a table indexed by bits b_0..b_{P-1} (b_0 the least significant): with
+// s_i = 2 b_i - 1, c(idx) = sum_S chat_S prod_{i in S} s_i, chat_S = mean_idx c(idx)
+// prod_{i in S} s_i(idx).  Since prod_{i in S} s_i = (-1)^|S| (1 - 2 x_S), x_S the parity
+// of the bits in S, a dot product with a query q becomes
+//     sum_j q_j c(idx_j) = c(0) sum_j q_j + sum_{S != 0} kappa_S sum_j q_j x_{S,j},
+// kappa_S = -2 (-1)^|S| chat_S: masked sums of q over whole bit-plane words (XORs of planes).
+// For the symmetric Lloyd-Max table only the odd-|S| terms are nonzero.
+void walsh_form(const std::vector<double>& c, int bits, double& c0, std::vector<int>& masks,
+                std::vector<double>& kappa) {
+    const int L = 1 << bits;
+    double cmax = 0.0;
+    for (double v : c) cmax = std::max(cmax, std::fabs(v));
+    masks.clear();
+    kappa.clear();
+    c0 = c[0];
+    for (int S = 1; S < L; ++S) {
+        double acc = 0.0;
+        for (int idx = 0; idx < L; ++idx) {
+            double p = 1.0;
+            for (int i = 0; i < bits; ++i)
+                if (S >> i & 1) p *= ((idx >> i) & 1) ? 1.0 : -1.0;
+            acc += c[idx] * p;
+        }
+        double chat = acc / L;
+        if (std::fabs(chat) <= 1e-14 * cmax) continue;
+        int pc = __builtin_popcount(S);
+        masks.push_back(S);
+        kappa.push_back(-2.0 * ((pc & 1) ? -1.0 : 1.0) * chat);
+    }
+}
+
+}  // namespace tq

@@ -1,0 +1,369 @@
+// Attention over a compressed KV cache: logits (the operation the juejin.cn post, section
+// 三, reports the blog timing on H100) and the softmax-weighted sum of values (keys and
+// values are both cached and compressed: nonndazone.ru essay, section 2).
+//
+// Work split: one CTA per (sequence chunk, batch x KV head, quad of query heads); the GQA
+// group's 4 query heads share every key load and every table lookup (lut.cuh).  The
+// output kernel runs flash-decoding style: per chunk a running max, a running sum and the
+// weighted value sum (in the value context's rotated basis), then one log-sum-exp combine
+// per query head which also rotates back (o = Pi_v^T a, one d x d product per head).
+#include <cfloat>
+
+#include "lut.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr size_t kSmemLimit = 227 * 1024;
+
+struct AttnArgs {
+    Params prm;
+    const float* qrot;
+    const float* qproj;
+    int B, Hq, Hkv, G;
+    KeyCache k;
+    float scale;
+    int chunk, nchunk;
+    int* err;
+    float* logits;        // logits kernel
+    // output kernel
+    int vmode;            // 0: bf16 values, 1: MSE codes
+    Params vprm;
+    const void* values;
+    const uint16_t* vnorm;
+    float* partials;      // [(b*Hq + h)*nchunk + c][2 + d]
+};
+
+template <int W, int P>
+__global__ void __launch_bounds__(kThreads) logits_kernel(const AttnArgs a) {
+    extern __shared__ float4 sm[];
+    const Params& prm = a.prm;
+    const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
+    const int L = checked_len(a.k.len, b, a.k.cap, a.err);
+    const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
+    if (i0 >= L) return;
+    const int hbase = kvh * a.G + 4 * blockIdx.z;
+    const int nh = min(4, kvh * a.G + a.G - hbase);
+    Scorer<W, P> sc;
+    sc.setup(sm, prm, a.qrot, a.qproj, (size_t)b * a.Hq + hbase, nh);
+    const int64_t iend = min((int64_t)L, i0 + a.chunk);
+    const size_t rowbase = (size_t)bh * a.k.cap;
+    const size_t cap = a.k.cap;
+    float* out = a.logits + ((size_t)b * a.Hq + hbase) * cap;
+    for (int64_t i = i0 + threadIdx.x; i < iend; i += blockDim.x) {
+        const float4 e = sc(prm, a.k.planes, a.k.signs, a.k.norm, a.k.rnorm, rowbase + i);
+        out[i] = a.scale * e.x;
+        if (nh > 1) out[cap + i] = a.scale * e.y;
+        if (nh > 2) out[2 * cap + i] = a.scale * e.z;
+        if (nh > 3) out[3 * cap + i] = a.scale * e.w;
+    }
+}
+
+__device__ __forceinline__ float4 f4_max(float4 a, float4 b) {
+    return make_float4(fmaxf(a.x, b.x), fmaxf(a.y, b.y), fmaxf(a.z, b.z), fmaxf(a.w, b.w));
+}
+__device__ __forceinline__ float4 warp_max4(float4 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, o));
+        v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, o));
+        v.z = fmaxf(v.z, __shfl_xor_sync(0xffffffffu, v.z, o));
+        v.w = fmaxf(v.w, __shfl_xor_sync(0xffffffffu, v.w, o));
+    }
+    return v;
+}
+__device__ __forceinline__ float4 warp_sum4(float4 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+    }
+    return v;
+}
+// exp(l - m) with exp(-inf - anything) = 0 (no NaN when both are -inf).
+__device__ __forceinline__ float safe_exp(float l, float m) { return l == -INFINITY ? 0.f : expf(l - m); }
+__device__ __forceinline__ float rescale(float m_old, float m_new) {
+    return m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+}
+
+// CODED: values are MSE codes of vprm (else bf16).  Value words per plane equal the key's W
+// (same d).  Needs d <= kThreads (each thread owns one coordinate of the value accumulator).
+template <int W, int P, bool CODED>
+__global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a) {
+    extern __shared__ float4 sm[];
+    const Params& prm = a.prm;
+    const int d = prm.d;
+    const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
+    const int L = checked_len(a.k.len, b, a.k.cap, a.err);
+    const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
+    if (i0 >= L) return;
+    const int hbase = kvh * a.G + 4 * blockIdx.z;
+    const int nh = min(4, kvh * a.G + a.G - hbase);
+
+    Scorer<W, P> sc;
+    sc.setup(sm, prm, a.qrot, a.qproj, (size_t)b * a.Hq + hbase, nh);
+    float4* sW = sm + Scorer<W, P>::smem_bytes(prm) / sizeof(float4);   // [kThreads] weights
+    float4* sRed = sW + kThreads;                                        // [kThreads / 32]
+    __shared__ float4 s_m, s_l, s_alpha;
+    __shared__ float s_cv[kMaxLevels];
+    if (threadIdx.x == 0) {
+        s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        s_l = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
+
+    const int dpad = 32 * ((d + 31) / 32);
+    const int nparts = kThreads / dpad;
+    const int part = threadIdx.x / dpad, j = threadIdx.x - part * dpad;
+    const bool active = part < nparts && j < d;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    const int64_t iend = min((int64_t)L, i0 + a.chunk);
+    const size_t rowbase = (size_t)bh * a.k.cap;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+
+    for (int64_t t0 = i0; t0 < iend; t0 += kThreads) {
+        const int ntile = (int)min((int64_t)kThreads, iend - t0);
+        const int t = threadIdx.x;
+        float4 l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float vn = 0.f;
+        if (t < ntile) {
+            const float4 e = sc(prm, a.k.planes, a.k.signs, a.k.norm, a.k.rnorm, rowbase + t0 + t);
+            l4.x = a.scale * e.x;
+            if (nh > 1) l4.y = a.scale * e.y;
+            if (nh > 2) l4.z = a.scale * e.z;
+            if (nh > 3) l4.w = a.scale * e.w;
+            vn = CODED ? half_bits_to_float(__ldg(a.vnorm + rowbase + t0 + t)) : 1.f;
+        }
+        float4 wm = warp_max4(l4);
+        if (lane == 0) sRed[warp] = wm;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float4 mx = sRed[0];
+            for (int w = 1; w < kThreads / 32; ++w) mx = f4_max(mx, sRed[w]);
+            const float4 mo = s_m;
+            const float4 mn = f4_max(mo, mx);
+            s_alpha = make_float4(rescale(mo.x, mn.x), rescale(mo.y, mn.y), rescale(mo.z, mn.z),
+                                  rescale(mo.w, mn.w));
+            s_m = mn;
+        }
+        __syncthreads();
+        const float4 mn = s_m, alpha = s_alpha;
+        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z),
+                                     safe_exp(l4.w, mn.w));
+        sW[t] = f4_scale(vn, p);
+        const float4 ps = warp_sum4(p);
+        __syncthreads();   // sRed reuse: everyone has read the max
+        if (lane == 0) sRed[warp] = ps;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float4 s = sRed[0];
+            for (int w = 1; w < kThreads / 32; ++w) s = f4_add(s, sRed[w]);
+            const float4 lo = s_l;
+            s_l = make_float4(fmaf(lo.x, alpha.x, s.x), fmaf(lo.y, alpha.y, s.y), fmaf(lo.z, alpha.z, s.z),
+                              fmaf(lo.w, alpha.w, s.w));
+        }
+        acc = make_float4(acc.x * alpha.x, acc.y * alpha.y, acc.z * alpha.z, acc.w * alpha.w);
+        if (active) {
+            if constexpr (CODED) {
+                const uint32_t* vp = static_cast<const uint32_t*>(a.values);
+                const int vw = W > 0 ? W : a.vprm.W;
+                const int VP = a.vprm.P;
+                const int word = j >> 5, bit = j & 31;
+                for (int tt = part; tt < ntile; tt += nparts) {
+                    const uint32_t* row = vp + (rowbase + t0 + tt) * (size_t)(VP * vw);
+                    int idx = 0;
+                    for (int pp = 0; pp < VP; ++pp) idx |= ((__ldg(row + pp * vw + word) >> bit) & 1u) << pp;
+                    acc = f4_fma(s_cv[idx], sW[tt], acc);
+                }
+            } else {
+                const uint16_t* vb = static_cast<const uint16_t*>(a.values);
+                for (int tt = part; tt < ntile; tt += nparts) {
+                    const float v = bf16_bits_to_float(__ldg(vb + (rowbase + t0 + tt) * (size_t)d + j));
+                    acc = f4_fma(v, sW[tt], acc);
+                }
+            }
+        }
+        __syncthreads();   // sW and sRed are rewritten by the next tile
+    }
+    // sum the parts of each coordinate, then write this chunk's partial state
+    float4* sAcc = sW;   // reuse: [nparts][dpad]
+    if (part < nparts) sAcc[part * dpad + j] = acc;
+    __syncthreads();
+    const size_t stride = (size_t)d + 2;
+    float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
+    const size_t hstride = (size_t)a.nchunk * stride;
+    if (threadIdx.x < d) {
+        float4 s = sAcc[threadIdx.x];
+        for (int q = 1; q < nparts; ++q) s = f4_add(s, sAcc[q * dpad + threadIdx.x]);
+        const float v[4] = {s.x, s.y, s.z, s.w};
+        for (int h = 0; h < nh; ++h) pbase[h * hstride + 2 + threadIdx.x] = v[h];
+    }
+    if (threadIdx.x == 0) {
+        const float4 mm = s_m, ll = s_l;
+        const float mv[4] = {mm.x, mm.y, mm.z, mm.w}, lv[4] = {ll.x, ll.y, ll.z, ll.w};
+        for (int h = 0; h < nh; ++h) {
+            pbase[h * hstride] = mv[h];
+            pbase[h * hstride + 1] = lv[h];
+        }
+    }
+}
+
+// out[b][h] = Pi_v^T (sum_c e^{m_c - M} a_c) / (sum_c e^{m_c - M} l_c) over the chunks that
+// hold keys; Pi_v NULL for bf16 values (no rotation).
+__global__ void attn_combine_kernel(const float* __restrict__ partials, int nchunk, int chunk, int d,
+                                    int Hq, const int32_t* len, int64_t cap, const float* PiV,
+                                    float* __restrict__ out) {
+    extern __shared__ float orot[];
+    const int bh = blockIdx.x, b = bh / Hq;
+    int L = len[b];
+    L = L < 0 ? 0 : (L > cap ? (int)cap : L);
+    const int nc = (L + chunk - 1) / chunk;
+    float* o = out + (size_t)bh * d;
+    if (nc == 0) {
+        for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = 0.f;
+        return;
+    }
+    const size_t stride = (size_t)d + 2;
+    const float* p = partials + (size_t)bh * nchunk * stride;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, p[c * stride]);
+    float tot = 0.f;
+    for (int c = 0; c < nc; ++c) tot += p[c * stride + 1] * rescale(p[c * stride], M);
+    const float inv = 1.f / tot;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) {
+        float s = 0.f;
+        for (int c = 0; c < nc; ++c) s = fmaf(p[c * stride + 2 + j], rescale(p[c * stride], M), s);
+        orot[j] = s * inv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        if (PiV) {
+            float s = 0.f;
+            for (int j = 0; j < d; ++j) s = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s);
+            o[i] = s;
+        } else {
+            o[i] = orot[i];
+        }
+    }
+}
+
+template <typename K>
+cudaError_t launch_with_smem(K kernel, dim3 grid, size_t smem, const AttnArgs& a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+struct LogitsLaunch {
+    template <int W, int P>
+    static cudaError_t run(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+        const size_t smem = Scorer<W, P>::smem_bytes(a.prm);
+        return launch_with_smem(logits_kernel<W, P>, grid, smem, a, s);
+    }
+};
+
+struct OutputLaunch {
+    template <int W, int P>
+    static cudaError_t run(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+        const size_t smem = Scorer<W, P>::smem_bytes(a.prm) + (kThreads + kThreads / 32) * sizeof(float4);
+        if (a.vmode) return launch_with_smem(attn_partial_kernel<W, P, true>, grid, smem, a, s);
+        return launch_with_smem(attn_partial_kernel<W, P, false>, grid, smem, a, s);
+    }
+};
+
+template <class Op>
+cudaError_t dispatch(const AttnArgs& a, bool lut, dim3 grid, cudaStream_t s) {
+    if (!lut) return Op::template run<0, 0>(a, grid, s);
+#define TQ_CASE_P(WV)                                                  \
+    switch (a.prm.P) {                                                 \
+        case 1: return Op::template run<WV, 1>(a, grid, s);            \
+        case 2: return Op::template run<WV, 2>(a, grid, s);            \
+        case 3: return Op::template run<WV, 3>(a, grid, s);            \
+        case 4: return Op::template run<WV, 4>(a, grid, s);            \
+    }                                                                  \
+    break;
+    switch (a.prm.W) {
+        case 1: TQ_CASE_P(1)
+        case 2: TQ_CASE_P(2)
+        case 3: TQ_CASE_P(3)
+        case 4: TQ_CASE_P(4)
+        case 5: TQ_CASE_P(5)
+        case 6: TQ_CASE_P(6)
+        case 7: TQ_CASE_P(7)
+    }
+#undef TQ_CASE_P
+    return cudaErrorInvalidValue;
+}
+
+AttnArgs make_args(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
+                   const KeyCache& k, float scale) {
+    AttnArgs a{};
+    a.prm = kc->prm;
+    a.qrot = qrot;
+    a.qproj = qproj;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.k = k;
+    a.scale = scale;
+    a.err = kc->derr;
+    attn_chunking(kc, B, Hq, Hkv, k.cap, &a.chunk, &a.nchunk);
+    return a;
+}
+
+}  // namespace
+
+void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* chunk, int* nchunk) {
+    // Aim for ~4 waves of one CTA per SM over all (batch, KV head, head quad) groups; at
+    // least 4 tiles of keys per CTA so the table build is amortised.
+    const int quads = (Hq / Hkv + 3) / 4;
+    const int64_t groups = (int64_t)B * Hkv * quads;
+    int64_t c = (groups * cap + 148 * 4 - 1) / (148 * 4);
+    c = ((c + kThreads - 1) / kThreads) * kThreads;
+    if (c < 4 * kThreads) c = 4 * kThreads;
+    if (c > (1 << 20)) c = 1 << 20;
+    *chunk = (int)c;
+    *nchunk = (int)((cap + c - 1) / c);
+    (void)kc;
+}
+
+cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
+                          int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s) {
+    AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
+    a.logits = logits;
+    const bool lut = lut_path_ok(a.prm, 0, kSmemLimit);
+    dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
+    return dispatch<LogitsLaunch>(a, lut, grid, s);
+}
+
+cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,
+                               const float* qproj, int B, int Hq, int Hkv, const KeyCache& k,
+                               float scale, const void* values, const uint16_t* vnorm,
+                               float* partials, float* out, cudaStream_t s) {
+    AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
+    a.vmode = vc ? 1 : 0;
+    if (vc) a.vprm = vc->prm;
+    a.values = values;
+    a.vnorm = vnorm;
+    a.partials = partials;
+    const size_t extra = (kThreads + kThreads / 32) * sizeof(float4);
+    const bool lut = lut_path_ok(a.prm, extra, kSmemLimit);
+    dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
+    cudaError_t e = dispatch<OutputLaunch>(a, lut, grid, s);
+    if (e != cudaSuccess) return e;
+    const int d = kc->d;
+    const int threads = d >= 256 ? 256 : ((d + 31) / 32) * 32;
+    attn_combine_kernel<<<B * Hq, threads, d * sizeof(float), s>>>(partials, a.nchunk, a.chunk, d, Hq, k.len,
+                                                                  k.cap, vc ? vc->dPi : nullptr, out);
+    return cudaGetLastError();
+}
+
+}  // namespace tq

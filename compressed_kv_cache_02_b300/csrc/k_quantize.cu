@@ -1,0 +1,282 @@
+// Quantization kernels: rotate + norm + scalar code + bit-pack (PolarQuant stage) fused with
+// the residual and its QJL sign sketch; decode-step append; query preparation.
+//
+// Pages: gitcode.csdn.net tutorial, sections PolarQuant (rotate first), 将笛卡尔积坐标转为
+// 极坐标 (r = ||x|| kept as FP16) and QJL steps 1-2 (residual = original - reconstruction,
+// Gaussian projection, keep signs > 0 -> 1); juejin.cn post section 二 (most bits on the
+// rotated scalar codes, ~1 bit of QJL on the residual).
+//
+// The residual's projection is computed in the rotated basis: with r' = Pi x - n16 c[idx],
+// S r = S Pi^T (Pi x - n16 c[idx]) = (S Pi^T) r'   (Pi orthogonal), and ||r|| = ||r'||.
+// S Pi^T is formed once on the host in float64 (tq_api.cu).
+#include "tq_device.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int kApplyRows = 8;     // input rows per CTA in apply_rows_kernel
+constexpr int kQuantRows = 16;    // vectors per CTA in quantize_kernel
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// out[v][i] = sum_j MT[j][i] in[v][j] for kApplyRows rows per CTA: MT is read coalesced
+// along i, each value reused for all rows staged in shared memory.
+__global__ void apply_rows_kernel(const float* __restrict__ MT, int din, int dout,
+                                  const float* __restrict__ in, size_t ldi, int64_t nv,
+                                  float* __restrict__ out, size_t ldo) {
+    extern __shared__ float4 xs4[];   // [din][kApplyRows] floats
+    float* xs = reinterpret_cast<float*>(xs4);
+    const int64_t v0 = (int64_t)blockIdx.x * kApplyRows;
+    for (int e = threadIdx.x; e < din * kApplyRows; e += blockDim.x) {
+        const int v = e / din, j = e - v * din;
+        xs[j * kApplyRows + v] = (v0 + v < nv) ? in[(size_t)(v0 + v) * ldi + j] : 0.f;
+    }
+    __syncthreads();
+    for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < dout; i += gridDim.y * blockDim.x) {
+        float acc[kApplyRows];
+#pragma unroll
+        for (int v = 0; v < kApplyRows; ++v) acc[v] = 0.f;
+        for (int j = 0; j < din; ++j) {
+            const float mv = __ldg(MT + (size_t)j * dout + i);
+            const float4 a = xs4[j * 2], b = xs4[j * 2 + 1];
+            acc[0] = fmaf(mv, a.x, acc[0]); acc[1] = fmaf(mv, a.y, acc[1]);
+            acc[2] = fmaf(mv, a.z, acc[2]); acc[3] = fmaf(mv, a.w, acc[3]);
+            acc[4] = fmaf(mv, b.x, acc[4]); acc[5] = fmaf(mv, b.y, acc[5]);
+            acc[6] = fmaf(mv, b.z, acc[6]); acc[7] = fmaf(mv, b.w, acc[7]);
+        }
+#pragma unroll
+        for (int v = 0; v < kApplyRows; ++v)
+            if (v0 + v < nv) out[(size_t)(v0 + v) * ldo + i] = acc[v];
+    }
+}
+
+struct QuantArgs {
+    Params prm;
+    const float* PiT;   // [d][d]
+    const float* StT;   // [d][m]
+    const void* x;
+    int dtype;
+    int64_t n, ld_x;
+    int H;
+    int64_t cap;
+    const int32_t* len;
+    uint32_t* planes;
+    uint32_t* signs;
+    uint16_t* norm;
+    uint16_t* rnorm;
+    int* err;
+};
+
+// One CTA codes kQuantRows vectors.  Shared memory: the input tile and the residual tile,
+// both stored [coordinate][vector] so the matrix-vector loops read 16 vectors per j with
+// four 16-byte broadcasts.
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs a) {
+    extern __shared__ float4 sm4[];
+    const Params& prm = a.prm;
+    const int d = prm.d, m = prm.m;
+    float* xT = reinterpret_cast<float*>(sm4);   // [d][kQuantRows]
+    float* rT = xT + (size_t)d * kQuantRows;      // [d][kQuantRows]
+    __shared__ float s_n[kQuantRows], s_n16[kQuantRows], s_r[kQuantRows];
+    __shared__ long long s_row[kQuantRows];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t v0 = (int64_t)blockIdx.x * kQuantRows;
+
+    if (tid < kQuantRows) {
+        const int64_t v = v0 + tid;
+        long long row = -1;
+        if (v < a.n) {
+            if (a.cap == 0) {
+                row = v;
+            } else {
+                const int L = a.len[v / a.H];
+                if (L < 0 || L >= a.cap) set_error(a.err, TQ_DEVERR_LEN_RANGE);
+                else row = (long long)v * a.cap + L;
+            }
+        }
+        s_row[tid] = row;
+    }
+    for (int e = tid; e < kQuantRows * d; e += kQuantThreads) {
+        const int v = e / d, j = e - v * d;
+        float val = 0.f;
+        if (v0 + v < a.n) {
+            const size_t off = (size_t)(v0 + v) * a.ld_x + j;
+            val = (a.dtype == TQ_BF16) ? bf16_bits_to_float(static_cast<const uint16_t*>(a.x)[off])
+                                       : static_cast<const float*>(a.x)[off];
+        }
+        xT[j * kQuantRows + v] = val;
+    }
+    __syncthreads();
+
+    // n = ||x||, n16 = fp16(n)
+    for (int v = warp; v < kQuantRows; v += kQuantThreads / 32) {
+        float s = 0.f;
+        for (int j = lane; j < d; j += 32) { const float t = xT[j * kQuantRows + v]; s = fmaf(t, t, s); }
+        s = warp_sum(s);
+        if (lane == 0) {
+            const float n = sqrtf(s);
+            s_n[v] = n;
+            s_n16[v] = half_bits_to_float(float_to_half_bits(n));
+        }
+    }
+    __syncthreads();
+
+    // y = Pi x; idx_j = #(thresholds < y_j / n); planes by warp ballots; r' = y - n16 c[idx]
+    const float4* xT4 = reinterpret_cast<const float4*>(xT);
+    for (int i0 = 0; i0 < d; i0 += kQuantThreads) {
+        const int i = i0 + tid;
+        const bool valid = i < d;
+        float acc[kQuantRows];
+#pragma unroll
+        for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
+        if (valid) {
+            for (int j = 0; j < d; ++j) {
+                const float p = __ldg(a.PiT + (size_t)j * d + i);
+#pragma unroll
+                for (int q = 0; q < kQuantRows / 4; ++q) {
+                    const float4 xv = xT4[j * (kQuantRows / 4) + q];
+                    acc[4 * q] = fmaf(p, xv.x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(p, xv.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(p, xv.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(p, xv.w, acc[4 * q + 3]);
+                }
+            }
+        }
+        const int word = (i0 >> 5) + warp;
+#pragma unroll
+        for (int v = 0; v < kQuantRows; ++v) {
+            const float n = s_n[v];
+            const float u = (n > 0.f) ? acc[v] / n : 0.f;
+            int idx = 0;
+            for (int k = 0; k < prm.L - 1; ++k) idx += (u > prm.thresholds[k]) ? 1 : 0;
+            if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * prm.centroids[idx];
+            const long long row = s_row[v];
+            for (int p = 0; p < prm.P; ++p) {
+                const unsigned bits = __ballot_sync(0xffffffffu, valid && ((idx >> p) & 1));
+                if (lane == 0 && word < prm.W && row >= 0)
+                    a.planes[(size_t)row * prm.P * prm.W + (size_t)p * prm.W + word] = bits;
+            }
+        }
+    }
+
+    if (prm.qjl) {
+        __syncthreads();
+        for (int v = warp; v < kQuantRows; v += kQuantThreads / 32) {
+            float s = 0.f;
+            for (int j = lane; j < d; j += 32) { const float t = rT[j * kQuantRows + v]; s = fmaf(t, t, s); }
+            s = warp_sum(s);
+            if (lane == 0) s_r[v] = sqrtf(s);
+        }
+        // sign_j = [((S Pi^T) r')_j > 0]
+        const float4* rT4 = reinterpret_cast<const float4*>(rT);
+        for (int i0 = 0; i0 < m; i0 += kQuantThreads) {
+            const int i = i0 + tid;
+            const bool valid = i < m;
+            float acc[kQuantRows];
+#pragma unroll
+            for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
+            if (valid) {
+                for (int j = 0; j < d; ++j) {
+                    const float st = __ldg(a.StT + (size_t)j * m + i);
+#pragma unroll
+                    for (int q = 0; q < kQuantRows / 4; ++q) {
+                        const float4 rv = rT4[j * (kQuantRows / 4) + q];
+                        acc[4 * q] = fmaf(st, rv.x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(st, rv.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(st, rv.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(st, rv.w, acc[4 * q + 3]);
+                    }
+                }
+            }
+            const int word = (i0 >> 5) + warp;
+#pragma unroll
+            for (int v = 0; v < kQuantRows; ++v) {
+                const unsigned bits = __ballot_sync(0xffffffffu, valid && acc[v] > 0.f);
+                const long long row = s_row[v];
+                if (lane == 0 && word < prm.Ws && row >= 0) a.signs[(size_t)row * prm.Ws + word] = bits;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < kQuantRows && s_row[tid] >= 0) {
+        const long long row = s_row[tid];
+        const uint16_t nh = float_to_half_bits(s_n[tid]);
+        a.norm[row] = nh;
+        bool overflow = __hisinf(__ushort_as_half(nh));
+        if (prm.qjl) {
+            const uint16_t rh = float_to_half_bits(s_r[tid]);
+            a.rnorm[row] = rh;
+            overflow = overflow || __hisinf(__ushort_as_half(rh));
+        }
+        if (overflow) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+    }
+}
+
+__global__ void advance_len_kernel(int32_t* len, int B, int64_t cap, int step, int* err) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    long long v = (long long)len[b] + step;
+    if (v < 0 || v > cap) {
+        set_error(err, TQ_DEVERR_LEN_RANGE);
+        v = v < 0 ? 0 : cap;
+    }
+    len[b] = static_cast<int32_t>(v);
+}
+
+}  // namespace
+
+cudaError_t launch_apply_rows(const float* MT, int din, int dout, const float* in, size_t ldi,
+                              int64_t nv, float* out, size_t ldo, cudaStream_t s) {
+    if (nv <= 0) return cudaSuccess;
+    const int threads = dout >= 256 ? 256 : ((dout + 31) / 32) * 32;
+    const size_t smem = (size_t)din * kApplyRows * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(apply_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)((nv + kApplyRows - 1) / kApplyRows), (dout + threads - 1) / threads);
+    apply_rows_kernel<<<grid, threads, smem, s>>>(MT, din, dout, in, ldi, nv, out, ldo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n, int64_t ld_x,
+                            int H, int64_t cap, const int32_t* len, uint32_t* planes,
+                            uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    QuantArgs a;
+    a.prm = c->prm;
+    a.PiT = c->dPiT;
+    a.StT = c->dStT;
+    a.x = x;
+    a.dtype = dtype;
+    a.n = n;
+    a.ld_x = ld_x;
+    a.H = H;
+    a.cap = cap;
+    a.len = len;
+    a.planes = planes;
+    a.signs = signs;
+    a.norm = norm;
+    a.rnorm = rnorm;
+    a.err = c->derr;
+    const size_t smem = 2ull * c->d * kQuantRows * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)((n + kQuantRows - 1) / kQuantRows);
+    quantize_kernel<<<blocks, kQuantThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_advance_len(int32_t* len, int B, int64_t cap, int step, int* err, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    advance_len_kernel<<<(B + 127) / 128, 128, 0, s>>>(len, B, cap, step, err);
+    return cudaGetLastError();
+}
+
+}  // namespace tq

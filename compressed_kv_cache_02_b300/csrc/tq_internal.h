@@ -1,0 +1,54 @@
+// Internal types shared by the host set-up code and the CUDA translation units of libtq.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kMaxLevels = 1 << TQ_MAX_MSE_BITS;   // 16 centroids at most
+constexpr int kMaxTerms = kMaxLevels - 1;          // nonzero subsets of the bit planes
+
+// Everything a kernel needs about a context, passed by value as a kernel parameter.
+struct Params {
+    int d, m, P, L, W, Ws;   // dimension, JL rows (0 in MSE mode), planes, levels, words
+    int qjl;                 // 1 in PROD mode
+    float qjl_scale;         // sqrt(pi/2) / m
+    float centroids[kMaxLevels];
+    float thresholds[kMaxLevels];
+    // Walsh form of the table (see host_setup.cpp): c(idx) = c0 + sum_t kappa[t] * x_t(idx),
+    // where x_t(idx) = parity of the idx bits selected by mask[t].
+    float c0;
+    int nterms;
+    int mask[kMaxTerms];
+    float kappa[kMaxTerms];
+};
+
+// Host-side set-up (host_setup.cpp).
+void lloyd_max_codebook(int d, int bits, std::vector<double>& centroids,
+                        std::vector<double>& thresholds);
+void seeded_matrices(uint64_t seed, int d, int m, std::vector<double>& Pi,
+                     std::vector<double>& S);
+void walsh_form(const std::vector<double>& centroids, int bits, double& c0,
+                std::vector<int>& masks, std::vector<double>& kappa);
+
+// Thread-local error message (tq_api.cu).
+int fail(int code, const std::string& msg);
+
+}  // namespace tq
+
+struct tq_ctx {
+    int device = 0;
+    int d = 0, m = 0, bits = 0, mode = 0, P = 0, L = 0, W = 0, Ws = 0;
+    std::vector<float> Pi, S;                 // float32 host copies, row-major
+    std::vector<double> centroids, thresholds;
+    tq::Params prm{};
+    float* dPiT = nullptr;    // [d][d]  PiT[j*d+i] = Pi[i][j]      (y = Pi x)
+    float* dPi = nullptr;     // [d][d]  row-major Pi                (o = Pi^T a)
+    float* dST = nullptr;     // [d][m]  ST[j*m+i] = S[i][j]        (u = S q)
+    float* dStT = nullptr;    // [d][m]  StT[j*m+i] = (S Pi^T)[i][j] (S r = (S Pi^T)(Pi x - n c))
+    int* derr = nullptr;      // device error word
+};

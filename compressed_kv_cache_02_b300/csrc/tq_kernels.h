@@ -1,0 +1,52 @@
+// Launchers of the libtq kernels (host side).  Each returns cudaGetLastError() of its
+// launches; arguments are already validated by tq_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+// rows v < nv: out[v*ldo + i] = sum_j MT[j*dout + i] * in[v*ldi + j],  i < dout, j < din.
+cudaError_t launch_apply_rows(const float* MT, int din, int dout, const float* in, size_t ldi,
+                              int64_t nv, float* out, size_t ldo, cudaStream_t s);
+
+// Quantize rows.  Row v of the input is x + v*ld_x; its output row is v (cap == 0) or
+// v*cap + len[v / H] (decode append, cap > 0).
+cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n, int64_t ld_x,
+                            int H, int64_t cap, const int32_t* len, uint32_t* planes,
+                            uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s);
+
+cudaError_t launch_advance_len(int32_t* len, int B, int64_t cap, int step, int* err, cudaStream_t s);
+
+struct KeyCache {
+    const uint32_t* planes;
+    const uint32_t* signs;
+    const uint16_t* norm;
+    const uint16_t* rnorm;
+    int64_t cap;
+    const int32_t* len;
+};
+
+// Keys per CTA and the number of sequence chunks for an attention launch.
+void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* chunk, int* nchunk);
+
+// logits[b][h][i] for i < len[b]; qrot/qproj prepared rows [B*Hq][d] / [B*Hq][m].
+cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
+                          int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s);
+
+// Split-sequence attention output: per-chunk partials (max, sum, acc[d]) then the combine.
+cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,
+                               const float* qproj, int B, int Hq, int Hkv, const KeyCache& k,
+                               float scale, const void* values, const uint16_t* vnorm,
+                               float* partials, float* out, cudaStream_t s);
+
+// Search: per-chunk top-k candidates into cand (score, index pairs), then the merge.
+void search_chunking(int64_t n, int k, int* chunk, int* nchunk);
+cudaError_t launch_search(const tq_ctx* c, const float* qrot, const float* qproj, int64_t nq,
+                          const uint32_t* planes, const uint32_t* signs, const uint16_t* norm,
+                          const uint16_t* rnorm, int64_t n, int k, float* cand_s, int* cand_i,
+                          float* top_s, int32_t* top_i, cudaStream_t s);
+
+}  // namespace tq

@@ -1,0 +1,259 @@
+"""Thin ctypes binding of libtq (include/tq.h): argument marshalling only.
+
+Every compute call passes device pointers of caller-owned torch tensors and the current
+CUDA stream to the C-ABI; all arithmetic happens in the library's kernels.  Importing
+this module loads ``libtq.so`` from this package directory and raises if it is missing:
+there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtq.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libtq.so not found at {_LIB_PATH}; build it with "
+                      "`python -m compressed_kv_cache_02_b300.build`")
+lib = ctypes.CDLL(_LIB_PATH)
+
+TQ_OK, TQ_ERR_ARG, TQ_ERR_CUDA, TQ_ERR_OOM, TQ_ERR_UNSUPPORTED, TQ_ERR_DEVICE = range(6)
+TQ_F32, TQ_BF16 = 0, 1
+TQ_MODE_PROD, TQ_MODE_MSE = 0, 1
+TQ_MAX_TOPK = 128
+TQ_DEVERR_NORM_OVERFLOW, TQ_DEVERR_LEN_RANGE = 1, 2
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "tq_host_codebook": [_i, _i, _p, _p],
+    "tq_host_matrices": [_u64, _i, _i, _p, _p],
+    "tq_init": [ctypes.POINTER(_p), _u64, _i, _i],
+    "tq_init_ex": [ctypes.POINTER(_p), _u64, _i, _i, _i, _i, _p, _p],
+    "tq_info": [_p, _p, _p, _p, _p],
+    "tq_layout": [_p, _p, _p, _p],
+    "tq_export_matrices": [_p, _p, _p, _p, _p],
+    "tq_quantize": [_p, _p, _i, _i64, _i64, _p, _p, _p, _p, _p],
+    "tq_append": [_p, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _p],
+    "tq_advance_len": [_p, _p, _i, _i64, _i, _p],
+    "tq_prep_queries": [_p, _p, _i64, _p, _p, _p],
+    "tq_attn_workspace_size": [_p, _i, _i, _i, _i64, ctypes.POINTER(_sz)],
+    "tq_attn_logits": [_p, _p, _i, _i, _i, _p, _p, _p, _p, _i64, _p, _f, _p, _p, _sz, _p],
+    "tq_attn_output": [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _i64, _p, _f, _p, _p, _p, _p, _sz, _p],
+    "tq_search_workspace_size": [_p, _i64, _i64, _i, ctypes.POINTER(_sz)],
+    "tq_search_topk": [_p, _p, _i64, _p, _p, _p, _p, _i64, _i, _p, _p, _p, _sz, _p],
+    "tq_sync_status": [_p, _p, _p],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _i
+lib.tq_destroy.argtypes = [_p]
+lib.tq_destroy.restype = None
+lib.tq_last_error.argtypes = []
+lib.tq_last_error.restype = ctypes.c_char_p
+
+
+class TQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed with status {code}: {lib.tq_last_error().decode()}")
+
+
+def _check(code: int, where: str) -> None:
+    if code != TQ_OK:
+        raise TQError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr() if t.numel() else None
+    return t
+
+
+def _stream(stream=None):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def host_codebook(d: int, mse_bits: int):
+    import numpy as np
+    c = np.zeros(1 << mse_bits)
+    t = np.zeros((1 << mse_bits) - 1)
+    _check(lib.tq_host_codebook(d, mse_bits, c.ctypes.data, t.ctypes.data if t.size else None), "tq_host_codebook")
+    return c, t
+
+
+def host_matrices(seed: int, d: int, m: int):
+    import numpy as np
+    Pi = np.zeros((d, d), dtype=np.float32)
+    S = np.zeros((m, d), dtype=np.float32)
+    _check(lib.tq_host_matrices(seed, d, m, Pi.ctypes.data, S.ctypes.data), "tq_host_matrices")
+    return Pi, S
+
+
+@dataclass
+class Codes:
+    """Packed codes of a batch of vectors (device tensors, layout of include/tq.h)."""
+    planes: torch.Tensor
+    norm: torch.Tensor
+    signs: torch.Tensor | None = None
+    rnorm: torch.Tensor | None = None
+
+
+class Context:
+    """A tq_ctx: seeded rotation, JL matrix and codebook on the current device."""
+
+    def __init__(self, d: int, bits: int, seed: int = 0, mode: int = TQ_MODE_PROD, m: int | None = None,
+                 Pi=None, S=None):
+        import numpy as np
+        h = _p()
+        Pi_a = None if Pi is None else np.ascontiguousarray(Pi, dtype=np.float32)
+        S_a = None if S is None else np.ascontiguousarray(S, dtype=np.float32)
+        if m is None:
+            m = d
+        _check(lib.tq_init_ex(ctypes.byref(h), seed, d, bits, mode, m,
+                              None if Pi_a is None else Pi_a.ctypes.data,
+                              None if S_a is None else S_a.ctypes.data), "tq_init_ex")
+        self.h = h
+        d_, m_, p_, mode_ = _i(), _i(), _i(), _i()
+        _check(lib.tq_info(h, ctypes.byref(d_), ctypes.byref(m_), ctypes.byref(p_), ctypes.byref(mode_)), "tq_info")
+        self.d, self.m, self.P, self.mode = d_.value, m_.value, p_.value, mode_.value
+        w, ws = _i(), _i()
+        _check(lib.tq_layout(h, None, ctypes.byref(w), ctypes.byref(ws)), "tq_layout")
+        self.W, self.Ws = w.value, ws.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib.tq_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def qjl(self) -> bool:
+        return self.mode == TQ_MODE_PROD
+
+    def export(self):
+        import numpy as np
+        Pi = np.zeros((self.d, self.d), dtype=np.float32)
+        S = np.zeros((max(self.m, 1), self.d), dtype=np.float32)
+        c = np.zeros(1 << self.P)
+        t = np.zeros((1 << self.P) - 1)
+        _check(lib.tq_export_matrices(self.h, Pi.ctypes.data, S.ctypes.data if self.m else None, c.ctypes.data,
+                                      t.ctypes.data if t.size else None), "tq_export_matrices")
+        return Pi, (S if self.m else None), c, t
+
+    def alloc_codes(self, *shape, device="cuda") -> Codes:
+        """Zeroed code buffers for rows of the given leading shape."""
+        planes = torch.zeros(*shape, self.P, self.W, dtype=torch.int32, device=device)
+        norm = torch.zeros(*shape, dtype=torch.int16, device=device)
+        if not self.qjl:
+            return Codes(planes=planes, norm=norm)
+        signs = torch.zeros(*shape, self.Ws, dtype=torch.int32, device=device)
+        rnorm = torch.zeros(*shape, dtype=torch.int16, device=device)
+        return Codes(planes=planes, norm=norm, signs=signs, rnorm=rnorm)
+
+    # -- calls (names follow the C-ABI) ---------------------------------------------------
+    def quantize(self, x: torch.Tensor, out: Codes | None = None, stream=None) -> Codes:
+        x2 = x.reshape(-1, self.d)
+        if out is None:
+            out = self.alloc_codes(x2.shape[0], device=x.device)
+        dtype = TQ_BF16 if x.dtype == torch.bfloat16 else TQ_F32
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("x must be float32 or bfloat16")
+        _check(lib.tq_quantize(self.h, _ptr(x2), dtype, x2.shape[0], x2.stride(0), _ptr(out.planes), _ptr(out.signs),
+                               _ptr(out.norm), _ptr(out.rnorm), _stream(stream)), "tq_quantize")
+        return out
+
+    def append(self, x: torch.Tensor, cache: Codes, cap: int, length: torch.Tensor, stream=None) -> None:
+        B, H, d = x.shape
+        dtype = TQ_BF16 if x.dtype == torch.bfloat16 else TQ_F32
+        _check(lib.tq_append(self.h, _ptr(x.contiguous()), dtype, B, H, cap, _ptr(length), _ptr(cache.planes),
+                             _ptr(cache.signs), _ptr(cache.norm), _ptr(cache.rnorm), _stream(stream)), "tq_append")
+
+    def advance_len(self, length: torch.Tensor, cap: int, step: int = 1, stream=None) -> None:
+        _check(lib.tq_advance_len(self.h, _ptr(length), length.numel(), cap, step, _stream(stream)), "tq_advance_len")
+
+    def prep_queries(self, q: torch.Tensor, stream=None):
+        q2 = q.reshape(-1, self.d).contiguous()
+        qrot = torch.empty_like(q2)
+        qproj = torch.empty(q2.shape[0], self.m, device=q.device, dtype=torch.float32) if self.qjl else None
+        _check(lib.tq_prep_queries(self.h, _ptr(q2), q2.shape[0], _ptr(qrot), _ptr(qproj), _stream(stream)),
+               "tq_prep_queries")
+        return qrot, qproj
+
+    def attn_workspace(self, B, Hq, Hkv, cap, device="cuda") -> torch.Tensor:
+        n = _sz()
+        _check(lib.tq_attn_workspace_size(self.h, B, Hq, Hkv, cap, ctypes.byref(n)), "tq_attn_workspace_size")
+        return torch.empty(n.value, dtype=torch.uint8, device=device)
+
+    def attn_logits(self, q, keys: Codes, cap, length, scale, out=None, workspace=None, stream=None):
+        B, Hq, d = q.shape
+        Hkv = keys.planes.shape[1]
+        if out is None:
+            out = torch.empty(B, Hq, cap, device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = self.attn_workspace(B, Hq, Hkv, cap, device=q.device)
+        _check(lib.tq_attn_logits(self.h, _ptr(q), B, Hq, Hkv, _ptr(keys.planes), _ptr(keys.signs), _ptr(keys.norm),
+                                  _ptr(keys.rnorm), cap, _ptr(length), float(scale), _ptr(out), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "tq_attn_logits")
+        return out
+
+    def attn_output(self, q, keys: Codes, cap, length, scale, values, vctx: "Context | None" = None,
+                    out=None, workspace=None, stream=None):
+        """values: a bf16 tensor [B, Hkv, cap, d] (vctx None) or Codes of an MSE-mode vctx."""
+        B, Hq, d = q.shape
+        Hkv = keys.planes.shape[1]
+        if out is None:
+            out = torch.empty(B, Hq, d, device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = self.attn_workspace(B, Hq, Hkv, cap, device=q.device)
+        if vctx is None:
+            vptr, vnorm = _ptr(values), None
+        else:
+            vptr, vnorm = _ptr(values.planes), _ptr(values.norm)
+        _check(lib.tq_attn_output(self.h, None if vctx is None else vctx.h, _ptr(q), B, Hq, Hkv, _ptr(keys.planes),
+                                  _ptr(keys.signs), _ptr(keys.norm), _ptr(keys.rnorm), cap, _ptr(length),
+                                  float(scale), vptr, vnorm, _ptr(out), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "tq_attn_output")
+        return out
+
+    def search_workspace(self, nq, n, k, device="cuda") -> torch.Tensor:
+        s = _sz()
+        _check(lib.tq_search_workspace_size(self.h, nq, n, k, ctypes.byref(s)), "tq_search_workspace_size")
+        return torch.empty(s.value, dtype=torch.uint8, device=device)
+
+    def search_topk(self, q, db: Codes, k, workspace=None, stream=None):
+        nq = q.shape[0]
+        n = db.planes.shape[0]
+        scores = torch.empty(nq, k, device=q.device, dtype=torch.float32)
+        idx = torch.empty(nq, k, device=q.device, dtype=torch.int32)
+        if workspace is None:
+            workspace = self.search_workspace(nq, n, k, device=q.device)
+        _check(lib.tq_search_topk(self.h, _ptr(q), nq, _ptr(db.planes), _ptr(db.signs), _ptr(db.norm),
+                                  _ptr(db.rnorm), n, k, _ptr(scores), _ptr(idx), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "tq_search_topk")
+        return scores, idx
+
+    def sync_status(self, stream=None) -> int:
+        flags = _i(0)
+        code = lib.tq_sync_status(self.h, _stream(stream), ctypes.byref(flags))
+        if code not in (TQ_OK, TQ_ERR_DEVICE):
+            raise TQError(code, "tq_sync_status")
+        return flags.value

@@ -1,0 +1,236 @@
+/*
+ * tq.h -- C-ABI of libtq: the TurboQuant hot path on B300 (sm_103a).
+ *
+ * Method (source pages, by title and section):
+ *   - juejin.cn post 7621817220135075850, section 二 "TurboQuant 的两段式": a random
+ *     rotation then scalar quantization that spends most of the bits (PolarQuant), and
+ *     ~1 bit of QJL on the residual; an asymmetric estimator pairs a high-precision query
+ *     with the low-precision codes.
+ *   - gitcode.csdn.net TurboQuant tutorial, sections "TurboQuant原理剖析" (r at 16 bits,
+ *     2- or 3-bit codes plus 1 QJL bit = 3 or 4 bits in total), "PolarQuant" (rotate
+ *     first), "将笛卡尔积坐标转为极坐标" (r = ||x|| kept as FP16) and "QJL" steps 1-3
+ *     (residual = original minus reconstruction, Gaussian JL projection, keep the signs:
+ *     > 0 -> 1, < 0 -> 0; the query against the signs gives an unbiased correction).
+ *   - freelamp.com article 0328, sections "技术突破：极坐标量化" (random orthogonal
+ *     rotation, no per-block scaling constants) and "误差补偿：QJL 变换与 1-bit 残差修正"
+ *     (zero-bias estimate from 1-bit residual signs and the high-precision query).
+ *   - juejin.cn post, section 三 (attention logits over the compressed KV cache; GloVe
+ *     d=200 Recall@1@k search) and section 四 (data-oblivious, online, near-optimal).
+ *
+ * What a context computes, for a vector x in R^d (the readings the pages leave open are
+ * stated with each step):
+ *   n      = ||x||_2, stored as IEEE binary16 (round to nearest even)
+ *   u      = Pi x / n            (u = 0 when n = 0); Pi a d x d random orthogonal matrix
+ *   idx_j  = number of thresholds t_k with t_k < u_j  (nearest centroid; a value exactly on
+ *            a threshold takes the lower index); centroids/thresholds are the Lloyd-Max
+ *            quantizer of one coordinate of a uniform unit vector in R^d (reading: the
+ *            rotated direction is exactly uniform on the sphere, so this table is
+ *            data-oblivious and the same for every token and layer)
+ *   PROD mode (bits = MSE bits + 1 QJL bit):
+ *   r      = x - n16 Pi^T c[idx]  (the residual of the PolarQuant reconstruction)
+ *   rnorm  = ||r||_2 as binary16 (reading: needed by the unbiased estimator)
+ *   sign_j = [(S r)_j > 0] for j < m, S an m x d matrix of i.i.d. N(0,1) (exact 0 -> bit 0)
+ *   MSE mode: only n and idx (bits = MSE bits).
+ * Estimator for a full-precision query q (PROD keys):
+ *   est(q, x) = n16 <Pi q, c[idx]> + rnorm16 sqrt(pi/2)/m <S q, 2 sign - 1>
+ *   (the constant makes the correction unbiased: E_S[...] = <q, r>; the pages do not print it).
+ *   MSE keys: est = n16 <Pi q, c[idx]>.
+ *
+ * Packed layout (the library's contract; the CPU oracle produces the same bytes):
+ *   planes  uint32 [rows][P][W]   P = MSE bits, W = ceil(d/32); bit (j mod 32) of word
+ *                                 j/32 of plane p holds bit p of idx_j; pad bits are 0
+ *   signs   uint32 [rows][Ws]     Ws = ceil(m/32); bit (j mod 32) of word j/32 = sign_j
+ *   norm    uint16 [rows]         binary16 bit pattern of n
+ *   rnorm   uint16 [rows]         binary16 bit pattern of ||r||
+ *   A KV cache is [B][Hkv][cap] rows; query head h reads KV head h / (Hq/Hkv).
+ *
+ * Conventions for every call:
+ *   - Return value: TQ_OK or a TQ_ERR_* code; tq_last_error() gives a thread-local message.
+ *     No call aborts the process.
+ *   - Host arguments are checked before any launch (TQ_ERR_ARG / TQ_ERR_UNSUPPORTED).
+ *   - Device pointers are caller-owned device memory (e.g. allocated by PyTorch); the
+ *     library never allocates or frees them.  uint32 and float arrays must be 16-byte
+ *     aligned; uint16 arrays 2-byte aligned.  bf16 inputs are raw bfloat16 bit patterns.
+ *   - Compute calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream).  The return status covers validation and launch errors;
+ *     checks that can only run on the device (an fp16 norm overflow, len > cap) set bits of
+ *     the context's device error word, which tq_sync_status() returns and clears.
+ *   - The context must be used on the device that was current at tq_init*; calls on one
+ *     context are not thread-safe against each other.
+ *   - The library does not allocate in compute calls: scratch is the caller's `workspace`,
+ *     sized by the *_workspace_size() calls.  tq_init* allocates the context's tables.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum tq_status {
+    TQ_OK = 0,
+    TQ_ERR_ARG = 1,          /* an argument is out of range, NULL or misaligned      */
+    TQ_ERR_CUDA = 2,         /* a CUDA runtime call or kernel launch failed          */
+    TQ_ERR_OOM = 3,          /* tq_init* could not allocate the context's tables     */
+    TQ_ERR_UNSUPPORTED = 4,  /* a valid request this build does not implement        */
+    TQ_ERR_DEVICE = 5        /* tq_sync_status: a device-side check failed           */
+};
+
+enum tq_dtype { TQ_F32 = 0, TQ_BF16 = 1 };
+enum tq_mode { TQ_MODE_PROD = 0, TQ_MODE_MSE = 1 };
+
+/* Bits of the device error word (returned through tq_sync_status' *flags). */
+enum tq_device_error {
+    TQ_DEVERR_NORM_OVERFLOW = 1,   /* a norm or residual norm rounded to binary16 infinity */
+    TQ_DEVERR_LEN_RANGE = 2        /* a len[b] was negative or above cap (clamped)         */
+};
+
+#define TQ_MAX_D 1024
+#define TQ_MAX_MSE_BITS 4
+#define TQ_MAX_TOPK 256
+
+typedef struct tq_ctx tq_ctx;
+
+/* ---------------------------------------------------------------- host-only helpers
+ * These run on the CPU and need no GPU.                                              */
+
+/* The Lloyd-Max codebook of one coordinate of a uniform unit vector in R^d: 2^mse_bits
+ * centroids (ascending, index 0 the most negative) and 2^mse_bits - 1 thresholds, in
+ * float64, computed by the Lloyd iteration with Gauss-Legendre quadrature of the density
+ * Gamma(d/2)/(sqrt(pi)Gamma((d-1)/2)) (1-t^2)^((d-3)/2).  Pages: nonndazone.ru essay,
+ * sections 3.2 (centroids where probability is higher) and 3.4 (precomputed once);
+ * freelamp article, section 技术突破 (predictable law after rotation).
+ * 3 <= d <= TQ_MAX_D, 1 <= mse_bits <= TQ_MAX_MSE_BITS.  Arrays are caller-owned.     */
+int tq_host_codebook(int d, int mse_bits, double* centroids, double* thresholds);
+
+/* The seeded matrices of tq_init: Pi (d x d, row-major, Haar-random orthogonal) and S
+ * (m x d, row-major, i.i.d. N(0,1)), rounded to float32.  Generator: splitmix64(seed) ->
+ * uniforms ((z >> 11) + 1) * 2^-53 -> Box-Muller pairs (cos, sin); S takes normals
+ * 0..m*d-1, the Gaussian G for Pi the next d*d; Pi = Q diag(sign(diag R)), G = QR
+ * (Householder, float64).  Pages: freelamp article, section 技术突破 (random orthogonal
+ * rotation); csdn tutorial, section QJL step 1 (Gaussian projection).  S may be NULL.  */
+int tq_host_matrices(uint64_t seed, int d, int m, float* Pi, float* S);
+
+/* ---------------------------------------------------------------- contexts */
+
+/* PROD-mode context: bits = MSE bits + 1 QJL bit (2..TQ_MAX_MSE_BITS+1), m = d, matrices
+ * from tq_host_matrices(seed, d, d).  Allocates the context's device tables on the
+ * current device.  Pages: csdn tutorial, section TurboQuant原理剖析 (2+1 and 3+1 bits).   */
+int tq_init(tq_ctx** out, uint64_t seed, int d, int bits);
+
+/* General context.  mode TQ_MODE_PROD: bits = MSE bits + 1, m = JL rows (1..TQ_MAX_D);
+ * mode TQ_MODE_MSE: bits = MSE bits (1..TQ_MAX_MSE_BITS), m ignored (no QJL stage).
+ * Pi_host (d x d) and S_host (m x d, PROD only) are float32 row-major host arrays used as
+ * given (copied); NULL means "generate from seed" as tq_host_matrices does.  Pi_host must
+ * be orthogonal to float32 precision (not checked beyond finiteness).                  */
+int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m,
+               const float* Pi_host, const float* S_host);
+
+void tq_destroy(tq_ctx* ctx);   /* frees the context's tables; NULL is a no-op */
+
+/* d, m (0 in MSE mode), MSE bits and mode of a context.  Any output may be NULL.       */
+int tq_info(const tq_ctx* ctx, int* d, int* m, int* mse_bits, int* mode);
+
+/* Packed sizes per vector in 32-bit words: planes = MSE bits, words_per_plane = W,
+ * sign_words = Ws (0 in MSE mode).  Any output may be NULL.                            */
+int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_words);
+
+/* Copies the context's float32 Pi (d*d), S (m*d; PROD only) and float64 centroids
+ * (2^P) and thresholds (2^P - 1) to host arrays.  Any output may be NULL.              */
+int tq_export_matrices(const tq_ctx* ctx, float* Pi, float* S, double* centroids,
+                       double* thresholds);
+
+/* ---------------------------------------------------------------- quantization */
+
+/* Quantize n rows of x (dtype TQ_F32 or TQ_BF16; row i at x + i*ld_x elements,
+ * ld_x >= d) into row i of planes/signs/norm/rnorm (layout above).  signs and rnorm must
+ * be NULL in MSE mode and non-NULL in PROD mode.  n may be 0.  Pages: csdn tutorial,
+ * sections PolarQuant, 将笛卡尔积坐标转为极坐标 and QJL steps 1-2; juejin post §二.   */
+int tq_quantize(tq_ctx* ctx, const void* x, int dtype, int64_t n, int64_t ld_x,
+                uint32_t* planes, uint32_t* signs, uint16_t* norm, uint16_t* rnorm,
+                void* stream);
+
+/* Decode-step append: x is [B][H][d] contiguous (one new vector per (batch, KV head));
+ * vector (b, h) is quantized into cache row (b*H + h)*cap + len[b].  len is a device
+ * int32 [B], read only; a len[b] outside [0, cap) skips that batch's rows and sets
+ * TQ_DEVERR_LEN_RANGE.  Pages: csdn tutorial, 背景 (every new token's vector enters the
+ * KV cache); juejin post §四 (online quantization, no re-fit).                          */
+int tq_append(tq_ctx* ctx, const void* x, int dtype, int B, int H, int64_t cap,
+              const int32_t* len, uint32_t* planes, uint32_t* signs, uint16_t* norm,
+              uint16_t* rnorm, void* stream);
+
+/* len[b] += step for b < B on the device (clamped to [0, cap], TQ_DEVERR_LEN_RANGE when
+ * clamped), so a captured decode step can advance the cache without a host round trip. */
+int tq_advance_len(tq_ctx* ctx, int32_t* len, int B, int64_t cap, int step, void* stream);
+
+/* Query preparation: qrot = Pi q ([nq][d]) and, in PROD mode, qproj = S q ([nq][m]) for
+ * nq float32 rows q ([nq][d], contiguous).  qproj may be NULL in MSE mode.  Pages:
+ * juejin post §二 (the query stays in high precision).                                  */
+int tq_prep_queries(tq_ctx* ctx, const float* q, int64_t nq, float* qrot, float* qproj,
+                    void* stream);
+
+/* ---------------------------------------------------------------- attention */
+
+/* Workspace bytes for tq_attn_logits / tq_attn_output with these shapes (the same size
+ * serves both calls).                                                                  */
+int tq_attn_workspace_size(const tq_ctx* kctx, int B, int Hq, int Hkv, int64_t cap,
+                           size_t* bytes);
+
+/* Attention logits over compressed keys: logits[b][h][i] = scale * est(q[b][h], key(b,
+ * h / (Hq/Hkv), i)) for i < len[b]; entries i >= len[b] are not written.  q float32
+ * [B][Hq][d]; keys in a [B][Hkv][cap] cache (k_signs, k_rnorm NULL for an MSE-mode kctx);
+ * len device int32 [B]; logits float32 [B][Hq][cap].  Hq must be a multiple of Hkv.
+ * Pages: juejin post §三 (attention logits from the compressed KV cache, the operation the
+ * blog times on H100); csdn tutorial, QJL step 3 (estimator).                           */
+int tq_attn_logits(tq_ctx* kctx, const float* q, int B, int Hq, int Hkv,
+                   const uint32_t* k_planes, const uint32_t* k_signs, const uint16_t* k_norm,
+                   const uint16_t* k_rnorm, int64_t cap, const int32_t* len, float scale,
+                   float* logits, void* workspace, size_t ws_bytes, void* stream);
+
+/* Attention output: out[b][h] = sum_{i < len[b]} softmax_i(logits) v_hat(b, h/(Hq/Hkv), i),
+ * the logits as in tq_attn_logits.  vctx NULL: values are bfloat16 [B][Hkv][cap][d] in
+ * `values` and v_norm is ignored.  vctx an MSE-mode context of the same d: `values` holds
+ * its planes [B][Hkv][cap][P][W] and v_norm its norms, and v_hat = n16 Pi_v^T c_v[idx].
+ * out float32 [B][Hq][d]; a batch with len[b] == 0 gets zeros.  Pages: nonndazone.ru
+ * essay §2 (keys and values are both cached and compressed); juejin post §三.          */
+int tq_attn_output(tq_ctx* kctx, const tq_ctx* vctx, const float* q, int B, int Hq,
+                   int Hkv, const uint32_t* k_planes, const uint32_t* k_signs,
+                   const uint16_t* k_norm, const uint16_t* k_rnorm, int64_t cap,
+                   const int32_t* len, float scale, const void* values,
+                   const uint16_t* v_norm, float* out, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* ---------------------------------------------------------------- search */
+
+/* Workspace bytes for tq_search_topk.                                                  */
+int tq_search_workspace_size(const tq_ctx* ctx, int64_t nq, int64_t n, int k, size_t* bytes);
+
+/* Top-k search: for each of nq float32 queries ([nq][d]) the k database rows (coded by
+ * ctx, rows 0..n-1) with the largest est(q, x), ordered by score descending and equal
+ * scores by row ascending.  top_score float32 [nq][k], top_idx int32 [nq][k].
+ * 1 <= k <= min(n, TQ_MAX_TOPK); n < 2^31.  Pages: juejin post §三 (GloVe Recall@1@k
+ * against PQ and RabitQ) and §四 (near-zero indexing time).                            */
+int tq_search_topk(tq_ctx* ctx, const float* q, int64_t nq, const uint32_t* planes,
+                   const uint32_t* signs, const uint16_t* norm, const uint16_t* rnorm,
+                   int64_t n, int k, float* top_score, int32_t* top_idx, void* workspace,
+                   size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Synchronises `stream`, then reads and clears the context's device error word.  Returns
+ * TQ_OK when it was 0, TQ_ERR_DEVICE (flags in *flags, which may be NULL) otherwise, or
+ * TQ_ERR_CUDA when the synchronisation itself failed.                                   */
+int tq_sync_status(tq_ctx* ctx, void* stream, int* flags);
+
+/* Message for the last failing call on this thread ("" if none).  Valid until the next
+ * call on this thread.                                                                  */
+const char* tq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

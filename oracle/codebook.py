@@ -111,13 +111,14 @@ class Codebook:
         return float(1.0 - self.d * np.sum(self.cell_prob * self.centroids ** 2))
 
 
-def sphere_codebook(d: int, bits: int, tol: float = 1e-13, max_iter: int = 200000) -> Codebook:
+def sphere_codebook(d: int, bits: int, tol: float = 4e-16, max_iter: int = 200000) -> Codebook:
     """Lloyd-Max quantizer with 2**bits levels for the density f_d.
 
     Start: the levels of the N(0, 1/d) quantiles at (k + 1/2) / L (a start only).
     Step:  thresholds t_k = (c_k + c_{k+1}) / 2; centroids c_k = E[T | t_{k-1} < T < t_k]
            with t_{-1} = -1 and t_{L-1} = 1.
-    Stop:  when no centroid moves by more than ``tol``; then symmetrise (f_d is even).
+    Stop:  when no centroid moves by more than ``tol`` (rounding level: the fixed point is
+           reached to ~1e-16, not just slowed down); then symmetrise (f_d is even).
     """
     if d < 3:
         raise ValueError("the sphere-marginal codebook needs d >= 3")

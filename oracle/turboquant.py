@@ -173,7 +173,8 @@ def attention_logits(q: np.ndarray, keys: Quantized, lens: np.ndarray, Pi: np.nd
                      S: np.ndarray, cb: Codebook, scale: float) -> np.ndarray:
     """logits [B, Hq, N]: scale * est(q[b, h], key[b, h // G, i]) for i < lens[b], NaN beyond.
 
-    keys carries idx [B, Hkv, N, d], norm16 [B, Hkv, N], signs [B, Hkv, N, m], rnorm16 [B, Hkv, N].
+    keys carries idx [B, Hkv, N, d], norm16 [B, Hkv, N], signs [B, Hkv, N, m], rnorm16 [B, Hkv, N];
+    S None (and no signs) means MSE-only keys, est = n16 <Pi q, c[idx]>.
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, _ = q.shape
@@ -183,8 +184,9 @@ def attention_logits(q: np.ndarray, keys: Quantized, lens: np.ndarray, Pi: np.nd
         L = int(lens[b])
         for h in range(Hq):
             g = _group(h, Hq, Hkv)
-            z = Quantized(idx=keys.idx[b, g, :L], norm16=keys.norm16[b, g, :L],
-                          signs=keys.signs[b, g, :L], rnorm16=keys.rnorm16[b, g, :L])
+            z = Quantized(idx=keys.idx[b, g, :L], norm16=keys.norm16[b, g, :L])
+            if S is not None:
+                z.signs, z.rnorm16 = keys.signs[b, g, :L], keys.rnorm16[b, g, :L]
             out[b, h, :L] = scale * estimate(q[b, h], z, Pi, cb, S)
     return out
 

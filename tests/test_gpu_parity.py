@@ -1,0 +1,276 @@
+"""GPU parity of the libtq kernels against the oracle, through the C-ABI.
+
+Inputs come from the seeded generators; the oracle's codes are packed and fed to the
+attention and search kernels so both sides score identical encodings, and separate
+end-to-end checks compare rows whose encodings agree."""
+from math import sqrt
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_kv_cache_02_b300 import inputs
+from gpu_helpers import Pair, assert_close, check_codes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from compressed_kv_cache_02_b300 import tq  # noqa: F401  (fails loudly without libtq.so)
+
+
+def _tq():
+    from compressed_kv_cache_02_b300 import tq
+    return tq
+
+
+# ------------------------------------------------------------------ quantization
+
+@pytest.mark.parametrize("d,bits,n", [(128, 3, 4096), (128, 4, 777), (200, 2, 1000), (200, 4, 513),
+                                      (33, 3, 300), (300, 3, 100), (8, 2, 65)])
+def test_quantize_fp32_gaussian(d, bits, n):
+    pr = Pair(d, bits)
+    X = inputs.gaussian(n, d, seed=0).cuda()
+    codes = pr.ctx.quantize(X)
+    assert pr.ctx.sync_status() == 0
+    same = check_codes(pr, X.cpu().numpy(), codes)
+    assert same.mean() > 0.99
+
+
+@pytest.mark.parametrize("bits", [3, 4, 5])
+def test_quantize_bf16_anisotropic(bits):
+    d = 128
+    pr = Pair(d, bits, seed=4)
+    fac = inputs.anisotropic_factors(2, d, seed=4)
+    X = inputs.anisotropic(1, 2, 1500, d, fac, seed=4)
+    codes = pr.ctx.quantize(X.cuda())
+    same = check_codes(pr, X.float().numpy().reshape(-1, d), codes)
+    assert same.mean() > 0.99
+
+
+@pytest.mark.parametrize("bits", [1, 3, 4])
+def test_quantize_mse_mode(bits):
+    tq = _tq()
+    pr = Pair(128, bits, mode=tq.TQ_MODE_MSE, seed=1)
+    X = inputs.gaussian(700, 128, seed=5).cuda()
+    codes = pr.ctx.quantize(X)
+    assert codes.signs is None
+    check_codes(pr, X.cpu().numpy(), codes)
+
+
+def test_quantize_strided_rows_zero_rows_and_empty():
+    pr = Pair(64, 3)
+    X = inputs.gaussian(40, 96, seed=6)
+    X[3] = 0.0
+    Xc = X.cuda()
+    sub = Xc[:, 10:74]                     # row stride 96 > d
+    codes = pr.ctx.quantize(sub)
+    check_codes(pr, X[:, 10:74].numpy(), codes)
+    idx, n16, signs, r16 = pr.from_device(codes)
+    assert n16[3] == 0 and r16[3] == 0 and not signs[3].any()
+    empty = pr.ctx.alloc_codes(0)
+    pr.ctx.quantize(Xc[:0, :64], out=empty)
+    assert pr.ctx.sync_status() == 0
+
+
+def test_norm_overflow_sets_device_flag():
+    tq = _tq()
+    pr = Pair(16, 3)
+    X = torch.full((2, 16), 1.0e5).cuda()   # ||x|| = 4e5 > fp16 max
+    pr.ctx.quantize(X)
+    assert pr.ctx.sync_status() == tq.TQ_DEVERR_NORM_OVERFLOW
+    assert pr.ctx.sync_status() == 0        # cleared by the previous read
+
+
+def test_argument_errors_raise():
+    tq = _tq()
+    pr = Pair(16, 3)
+    X = inputs.gaussian(4, 16, seed=1).cuda()
+    with pytest.raises(tq.TQError):
+        pr.ctx.quantize(X.double())
+    out = pr.ctx.alloc_codes(4)
+    code = tq.lib.tq_quantize(pr.ctx.h, X.data_ptr(), 0, 4, 8, out.planes.data_ptr(), out.signs.data_ptr(),
+                              out.norm.data_ptr(), out.rnorm.data_ptr(), None)
+    assert code == tq.TQ_ERR_ARG                                   # ld_x < d
+    code = tq.lib.tq_quantize(pr.ctx.h, X.data_ptr(), 0, 4, 16, out.planes.data_ptr(), None,
+                              out.norm.data_ptr(), None, None)
+    assert code == tq.TQ_ERR_ARG                                   # PROD needs signs
+    with pytest.raises(tq.TQError):
+        tq.Context(16, 6)                                          # 5 MSE bits unsupported
+
+
+# ------------------------------------------------------------------ attention
+
+def _kv_case(B, Hkv, G, N, d, kbits, vmode, seed, lens):
+    """Oracle-coded keys (and values) on the device plus the oracle's reference pieces."""
+    tq = _tq()
+    kp = Pair(d, kbits, seed=seed)
+    fac = inputs.anisotropic_factors(Hkv, d, seed=seed)
+    K = inputs.anisotropic(B, Hkv, N, d, fac, seed=seed)
+    V = inputs.anisotropic(B, Hkv, N, d, inputs.anisotropic_factors(Hkv, d, seed=seed + 1000), seed=seed + 1000)
+    Q = inputs.anisotropic(B, Hkv, G, d, fac, seed=seed + 2000, dtype=torch.float32)
+    q = Q.reshape(B, Hkv * G, d)
+    kz = kp.oquant(K.float().numpy())
+    keys = kp.to_device(kz, (B, Hkv, N))
+    case = dict(kp=kp, K=K, V=V, q=q, kz=kz, keys=keys, lens=np.array(lens), B=B, Hkv=Hkv, Hq=Hkv * G, N=N, d=d)
+    if vmode == "mse":
+        vp = Pair(d, 3, mode=tq.TQ_MODE_MSE, seed=seed + 7)
+        vz = vp.oquant(V.float().numpy())
+        case.update(vp=vp, vz=vz, vcodes=vp.to_device(vz, (B, Hkv, N)))
+    return case
+
+
+def _run_logits(c, scale):
+    length = torch.tensor(c["lens"], dtype=torch.int32).cuda()
+    return c["kp"].ctx.attn_logits(c["q"].cuda(), c["keys"], c["N"], length, scale)
+
+
+@pytest.mark.parametrize("B,Hkv,G,N,d,bits,lens", [
+    (1, 1, 16, 4096, 128, 3, [4096]),            # tiny correctness workload: 16 queries x 4096 keys
+    (1, 8, 4, 1100, 128, 4, [1100]),             # decode layer shape (4-bit keys), ragged tail
+    (2, 2, 4, 1500, 128, 3, [1500, 731]),        # long-context shape (3-bit keys), two lengths
+    (1, 2, 6, 300, 128, 3, [300]),               # GQA group of 6: a padded head quad
+    (2, 1, 4, 400, 200, 2, [400, 0]),            # d=200 (7 words), an empty sequence
+    (1, 2, 4, 257, 300, 3, [257]),               # d=300: generic (table-free) path
+    (1, 1, 4, 100, 33, 5, [100]),                # ragged d, 4 MSE bits
+])
+def test_logits(B, Hkv, G, N, d, bits, lens):
+    c = _kv_case(B, Hkv, G, N, d, bits, None, seed=3, lens=lens)
+    scale = 1.0 / sqrt(d)
+    got = _run_logits(c, scale).cpu().numpy()
+    assert c["kp"].ctx.sync_status() == 0
+    ref = oracle.attention_logits(c["q"].numpy(), c["kz"], c["lens"], c["kp"].Pi, c["kp"].S, c["kp"].cb, scale)
+    for b in range(B):
+        L = lens[b]
+        assert_close(got[b, :, :L], ref[b, :, :L], "logits")
+
+
+def test_logits_mse_keys():
+    tq = _tq()
+    d, N = 128, 600
+    kp = Pair(d, 3, mode=tq.TQ_MODE_MSE, seed=9)
+    K = inputs.gaussian(2 * N, d, seed=9).reshape(1, 2, N, d)
+    q = inputs.gaussian(8, d, seed=10).reshape(1, 8, d)
+    kz = kp.oquant(K.numpy())
+    keys = kp.to_device(kz, (1, 2, N))
+    got = kp.ctx.attn_logits(q.cuda(), keys, N, torch.tensor([N], dtype=torch.int32).cuda(), 0.5).cpu().numpy()
+    ref = oracle.attention_logits(q.numpy(), kz, np.array([N]), kp.Pi, None, kp.cb, 0.5)
+    assert_close(got, ref, "mse-key logits")
+
+
+@pytest.mark.parametrize("vmode", ["bf16", "mse"])
+@pytest.mark.parametrize("B,Hkv,G,N,bits,lens", [
+    (1, 8, 4, 1100, 4, [1100]),
+    (2, 2, 4, 2600, 3, [2600, 1]),
+    (2, 1, 6, 700, 3, [0, 699]),
+])
+def test_attention_output(vmode, B, Hkv, G, N, bits, lens):
+    d = 128
+    c = _kv_case(B, Hkv, G, N, d, bits, vmode, seed=11, lens=lens)
+    scale = 1.0 / sqrt(d)
+    length = torch.tensor(lens, dtype=torch.int32).cuda()
+    kp = c["kp"]
+    if vmode == "bf16":
+        got = kp.ctx.attn_output(c["q"].cuda(), c["keys"], N, length, scale, c["V"].cuda())
+        ref = oracle.attention_output(c["q"].numpy(), c["kz"], c["lens"], kp.Pi, kp.S, kp.cb, scale,
+                                      values_dense=c["V"].float().numpy())
+    else:
+        vp = c["vp"]
+        got = kp.ctx.attn_output(c["q"].cuda(), c["keys"], N, length, scale, c["vcodes"], vctx=vp.ctx)
+        ref = oracle.attention_output(c["q"].numpy(), c["kz"], c["lens"], kp.Pi, kp.S, kp.cb, scale,
+                                      values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
+    assert kp.ctx.sync_status() == 0
+    assert_close(got.cpu().numpy(), ref, "attention output")
+
+
+def test_decode_append_and_advance():
+    tq = _tq()
+    d, B, H, cap = 128, 2, 3, 40
+    pr = Pair(d, 3, seed=2)
+    cache = pr.ctx.alloc_codes(B, H, cap)
+    length = torch.tensor([5, 17], dtype=torch.int32).cuda()
+    steps = [inputs.gaussian(B * H, d, seed=100 + s).reshape(B, H, d) for s in range(3)]
+    for x in steps:
+        pr.ctx.append(x.cuda(), cache, cap, length)
+        pr.ctx.advance_len(length, cap)
+    assert pr.ctx.sync_status() == 0
+    assert length.cpu().tolist() == [8, 20]
+    idx, n16, signs, r16 = pr.from_device(cache)
+    idx = idx.reshape(B, H, cap, d)
+    for s, x in enumerate(steps):
+        z = pr.oquant(x.numpy())
+        for b, L0 in enumerate([5, 17]):
+            rows = idx[b, :, L0 + s]
+            assert (rows == z.idx[b]).mean() > 0.999
+    # an out-of-range length is flagged and skipped, not written
+    bad = torch.tensor([cap, 0], dtype=torch.int32).cuda()
+    before = cache.planes.clone()
+    pr.ctx.append(steps[0].cuda(), cache, cap, bad)
+    assert pr.ctx.sync_status() == tq.TQ_DEVERR_LEN_RANGE
+    assert torch.equal(cache.planes[0], before[0])
+    pr.ctx.advance_len(torch.tensor([cap], dtype=torch.int32).cuda(), cap)
+    assert pr.ctx.sync_status() == tq.TQ_DEVERR_LEN_RANGE
+
+
+def test_end_to_end_quantize_then_logits():
+    d, N, G = 128, 2048, 4
+    pr = Pair(d, 3, seed=21)
+    K = inputs.gaussian(N, d, seed=21).reshape(1, 1, N, d)
+    q = inputs.gaussian(G, d, seed=22).reshape(1, G, d)
+    codes = pr.ctx.quantize(K.cuda().reshape(N, d))
+    same = check_codes(pr, K.numpy().reshape(N, d), codes)
+    keys = _tq().Codes(planes=codes.planes.reshape(1, 1, N, pr.P, -1), norm=codes.norm.reshape(1, 1, N),
+                       signs=codes.signs.reshape(1, 1, N, -1), rnorm=codes.rnorm.reshape(1, 1, N))
+    got = pr.ctx.attn_logits(q.cuda(), keys, N, torch.tensor([N], dtype=torch.int32).cuda(), 1.0).cpu().numpy()
+    kz = pr.oquant(K.numpy())
+    ref = oracle.attention_logits(q.numpy(), kz, np.array([N]), pr.Pi, pr.S, pr.cb, 1.0)
+    assert_close(got[0][:, same], ref[0][:, same], "end-to-end logits (rows with identical codes)")
+
+
+# ------------------------------------------------------------------ search
+
+def _topk_ok(got_s, got_i, ref_s, ref_i, all_scores):
+    """Identical top-k sets apart from near-ties at the k-th score."""
+    for r in range(ref_i.shape[0]):
+        g, o = set(got_i[r].tolist()), set(ref_i[r].tolist())
+        kth = ref_s[r, -1]
+        tol = max(1e-4, 1e-3 * abs(kth))
+        for i in g ^ o:
+            assert abs(all_scores[r, i] - kth) <= tol, f"query {r}: item {i} differs away from a tie"
+        assert np.all(np.diff(got_s[r]) <= 0)
+        assert_close(got_s[r], all_scores[r, got_i[r]], "returned scores")
+
+
+@pytest.mark.parametrize("d,bits,n,nq,k", [(200, 2, 5000, 13, 10), (200, 4, 3000, 8, 100), (128, 3, 4096, 16, 1),
+                                         (200, 4, 1000, 5, 128), (64, 2, 300, 3, 50)])
+def test_search_topk(d, bits, n, nq, k):
+    pr = Pair(d, bits, seed=5)
+    X = inputs.cone(n, d, seed=5, mu_seed=77)
+    Q = inputs.cone(nq, d, seed=6, mu_seed=77)
+    z = pr.oquant(X.numpy())
+    db = pr.to_device(z, (n,))
+    s, i = pr.ctx.search_topk(Q.cuda(), db, k)
+    assert pr.ctx.sync_status() == 0
+    ref_s, ref_i = oracle.search_topk(Q.numpy(), z, pr.Pi, pr.cb, pr.S, k)
+    scores = oracle.estimate_all(Q.numpy(), z, pr.Pi, pr.cb, pr.S)
+    _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
+
+
+def test_search_ties_resolve_to_lower_index():
+    d, n = 64, 600
+    pr = Pair(d, 3, seed=8)
+    X = inputs.cone(n, d, seed=8, mu_seed=1)
+    X[400] = X[17]
+    X[555] = X[17]
+    z = pr.oquant(X.numpy())
+    db = pr.to_device(z, (n,))
+    Q = X[17:18].clone()
+    s, i = pr.ctx.search_topk(Q.cuda(), db, 5)
+    i = i.cpu().numpy()[0].tolist()
+    s = s.cpu().numpy()[0]
+    assert i.index(17) < i.index(400) < i.index(555)
+    assert s[i.index(17)] == s[i.index(400)] == s[i.index(555)]

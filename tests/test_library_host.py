@@ -1,0 +1,73 @@
+"""CPU-side checks of libtq: it loads, exports every symbol of include/tq.h, and its host
+set-up (codebook by Gauss-Legendre quadrature, seeded matrices by its own C++ generator)
+agrees with the oracle's independent computations.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.codebook import sphere_codebook
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tq.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from compressed_kv_cache_02_b300 import build
+    build.build()
+    from compressed_kv_cache_02_b300 import tq as mod
+    return mod
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("tq_init", "tq_quantize", "tq_attn_logits", "tq_attn_output", "tq_search_topk"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tq):
+    missing = [n for n in _declared_functions() if not hasattr(tq.lib, n)]
+    assert missing == []
+
+
+@pytest.mark.parametrize("d", [3, 16, 128, 200, 1024])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_host_codebook_matches_oracle(tq, d, bits):
+    c, t = tq.host_codebook(d, bits)
+    ref = sphere_codebook(d, bits)
+    assert np.max(np.abs(c - ref.centroids)) < 1e-12
+    assert np.max(np.abs(t - ref.thresholds)) < 1e-12
+
+
+@pytest.mark.parametrize("d,m", [(4, 4), (16, 16), (128, 128), (200, 200), (40, 24)])
+def test_host_matrices_match_oracle_generator(tq, d, m):
+    Pi, S = tq.host_matrices(7, d, m)
+    Pi_o, S_o = oracle.method_matrices(7, d, m)
+    assert np.array_equal(S, S_o.astype(np.float32))
+    # both QRs give the same Haar matrix up to float64 rounding, then one float32 rounding
+    assert np.max(np.abs(Pi.astype(np.float64) - Pi_o)) < 2 ** -23
+    assert np.max(np.abs(Pi.astype(np.float64).T @ Pi - np.eye(d))) < 1e-5
+
+
+def test_host_argument_errors(tq):
+    c = np.zeros(2)
+    assert tq.lib.tq_host_codebook(2, 1, c.ctypes.data, None) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_host_codebook(128, 5, c.ctypes.data, None) == tq.TQ_ERR_ARG
+    assert b"mse_bits" in tq.lib.tq_last_error()
+    assert tq.lib.tq_host_matrices(0, 2000, 4, None, None) == tq.TQ_ERR_ARG
+
+
+def test_context_calls_reject_null_context(tq):
+    assert tq.lib.tq_quantize(None, None, 0, 1, 1, None, None, None, None, None) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_info(None, None, None, None, None) == tq.TQ_ERR_ARG
+    tq.lib.tq_destroy(None)   # no-op
