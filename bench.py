@@ -6,8 +6,8 @@ Workload (one step = one decode step of every sequence):
   (bf16 keys/values from the anisotropic generator, quantized at prefill: keys 3 bits =
   2-bit codes + 1 QJL bit, values 3-bit MSE-only codes), then per step:
     append the new token's key and value (rotate + code + pack, QJL signs for the key),
-    advance the lengths, score all cached keys (attention logits, written to HBM), and the
-    attention output (softmax-weighted sum of the dequantized values).
+    advance the lengths, score all cached keys (attention logits, written to HBM), then the
+    softmax over those logits and the weighted sum of the dequantized values.
 Metric: compressed-key logit scores per second (query heads x cached keys / time), plus
 the HBM bandwidth those kernels achieve.
 
@@ -44,7 +44,14 @@ WORKLOAD = ("long-context batched decode: batch 8, 8 KV heads, 32 query heads, h
 K_BYTES = 2 * 16 + 16 + 2 + 2        # 2 code planes, sign words, norm, residual norm = 52
 V_BYTES = 3 * 16 + 2                 # 3 code planes + norm = 50
 LOGIT_BYTES = K_BYTES + G * 4        # keys read + 4 fp32 logits written = 68
-OUTPUT_BYTES = K_BYTES + V_BYTES     # keys + values read = 102
+VALUES_BYTES = G * 4 + V_BYTES       # 4 logits read + value codes read = 66
+
+
+def set_batch(b: int) -> None:
+    global B, WORKLOAD
+    if b != B:
+        WORKLOAD = WORKLOAD.replace("batch 8", f"batch {b}")
+        B = b
 
 
 def peaks():
@@ -156,17 +163,20 @@ def build_state(dev):
 
 
 def step_inputs(state, nsteps, dev):
+    """Per step: the new key and value [B, Hkv, d] (bf16) and the queries [B, Hq, d] (fp32)."""
     from compressed_kv_cache_02_b300 import inputs
-    ks, vs, qs = [], [], []
-    for s in range(nsteps):
-        ks.append(inputs.anisotropic(B, HKV, 1, D, state["kfac"], seed=10_000 + s, device=dev)[:, :, 0])
-        vs.append(inputs.anisotropic(B, HKV, 1, D, state["vfac"], seed=20_000 + s, device=dev)[:, :, 0])
-        q = inputs.anisotropic(B, HKV, G, D, state["kfac"], seed=30_000 + s, device=dev, dtype=torch.float32)
-        qs.append(q.reshape(B, HQ, D).contiguous())
+    K = inputs.anisotropic(B, HKV, nsteps, D, state["kfac"], seed=10_000, device=dev)
+    V = inputs.anisotropic(B, HKV, nsteps, D, state["vfac"], seed=20_000, device=dev)
+    Q = inputs.anisotropic(B, HKV, nsteps * G, D, state["kfac"], seed=30_000, device=dev, dtype=torch.float32)
+    Q = Q.reshape(B, HKV, nsteps, G, D)
+    ks = [K[:, :, s].contiguous() for s in range(nsteps)]
+    vs = [V[:, :, s].contiguous() for s in range(nsteps)]
+    qs = [Q[:, :, s].reshape(B, HQ, D).contiguous() for s in range(nsteps)]
     return ks, vs, qs
 
 
 def run_tq(args, world, rank, local):
+    from compressed_kv_cache_02_b300 import tq
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     state = build_state(dev)
@@ -181,6 +191,8 @@ def run_tq(args, world, rank, local):
     scale = 1.0 / D ** 0.5
     stream = torch.cuda.current_stream()
 
+    vws = tq.values_workspace(D, B, HQ, HKV, cap, device=dev)
+
     def step(s, ev=None):
         kctx.append(ks[s], kc, cap, length)
         vctx.append(vs[s], vc, cap, length)
@@ -190,7 +202,7 @@ def run_tq(args, world, rank, local):
         kctx.attn_logits(qs[s], kc, cap, length, scale, out=logits, workspace=ws)
         if ev:
             ev[1].record()
-        kctx.attn_output(qs[s], kc, cap, length, scale, vc, vctx=vctx, out=out, workspace=ws)
+        tq.attn_values(logits, length, vc, vctx=vctx, out=out, workspace=vws)
         if ev:
             ev[2].record()
 
@@ -243,7 +255,7 @@ def run_tq(args, world, rank, local):
         vctx.append(dv, vc, cap, length)
         kctx.advance_len(length, cap)
         kctx.attn_logits(dq, kc, cap, length, scale, out=logits, workspace=ws)
-        kctx.attn_output(dq, kc, cap, length, scale, vc, vctx=vctx, out=out, workspace=ws)
+        tq.attn_values(logits, length, vc, vctx=vctx, out=out, workspace=vws)
         hout.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -254,12 +266,12 @@ def run_tq(args, world, rank, local):
 
     hbm, peak_kind = peaks()
     logits_bytes = [LOGIT_BYTES * B * HKV * L for L in lens_timed]
-    output_bytes = [OUTPUT_BYTES * B * HKV * L for L in lens_timed]
+    output_bytes = [VALUES_BYTES * B * HKV * L for L in lens_timed]
     gbs_logits = sum(logits_bytes) / sum(t_logits) / 1e9
     gbs_output = sum(output_bytes) / sum(t_output) / 1e9
-    dominant = "attn_output" if sum(t_output) >= sum(t_logits) else "attn_logits"
-    dom_gbs = gbs_output if dominant == "attn_output" else gbs_logits
-    launches_per_step = 3 + 3 + 4   # append x2 + advance; logits: prep x2 + kernel; output: prep x2 + partial + combine
+    dominant = "attn_values" if sum(t_output) >= sum(t_logits) else "attn_logits"
+    dom_gbs = gbs_output if dominant == "attn_values" else gbs_logits
+    launches_per_step = 3 + 3 + 2   # append x2 + advance; logits: prep x2 + kernel; values: partial + combine
     step_bytes = (sum(logits_bytes) + sum(output_bytes)) / args.steps
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -274,8 +286,8 @@ def run_tq(args, world, rank, local):
             "attn_logits": {"ms": statistics.mean(t_logits) * 1e3, "GB_s": gbs_logits,
                             "bytes_per_key": LOGIT_BYTES, "frac_of_measured": gbs_logits / hbm,
                             "frac_of_8TBs": gbs_logits / 8000.0},
-            "attn_output": {"ms": statistics.mean(t_output) * 1e3, "GB_s": gbs_output,
-                            "bytes_per_key": OUTPUT_BYTES, "frac_of_measured": gbs_output / hbm,
+            "attn_values": {"ms": statistics.mean(t_output) * 1e3, "GB_s": gbs_output,
+                            "bytes_per_key": VALUES_BYTES, "frac_of_measured": gbs_output / hbm,
                             "frac_of_8TBs": gbs_output / 8000.0},
             "step_GB_s": step_bytes / (elapsed / args.steps) / 1e9,
             "prefill_quantize": {"vectors": state["prefill_vectors"], "s": state["prefill_s"],
@@ -383,7 +395,9 @@ def main():
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     args = ap.parse_args()
+    set_batch(args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

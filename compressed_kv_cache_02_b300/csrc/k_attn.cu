@@ -11,6 +11,7 @@
 
 #include "lut.cuh"
 #include "tq_kernels.h"
+#include "values.cuh"
 
 namespace tq {
 namespace {
@@ -90,13 +91,85 @@ __device__ __forceinline__ float rescale(float m_old, float m_new) {
     return m_old == -INFINITY ? 0.f : expf(m_old - m_new);
 }
 
-// CODED: values are MSE codes of vprm (else bf16).  Value words per plane equal the key's W
-// (same d).  Needs d <= kThreads (each thread owns one coordinate of the value accumulator).
-template <int W, int P, bool CODED>
+// Online softmax over one tile of keys and the weighted value sum, shared by the fused
+// output kernel (logits from the scorer) and the values kernel (logits read from HBM).
+// Every thread of the block calls it with its own key's logits l4 (-inf when it has none)
+// and value norm vn; the warps then sweep the tile's keys with lanes owning coordinates.
+template <int C, bool CODED, bool NIB, int NT>
+__device__ __forceinline__ void softmax_tile(float4 l4, float vn, int ntile, size_t row0, const ValueSrc& v,
+                                             float4* sW, float4* sRed, float4& s_m, float4& s_l, float4& s_alpha,
+                                             const float* cv, float4 (&acc)[C]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int NW = NT / 32;
+    const float4 wm = warp_max4(l4);
+    if (lane == 0) sRed[warp] = wm;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float4 mx = sRed[0];
+        for (int w = 1; w < NW; ++w) mx = f4_max(mx, sRed[w]);
+        const float4 mo = s_m;
+        const float4 mn = f4_max(mo, mx);
+        s_alpha = make_float4(rescale(mo.x, mn.x), rescale(mo.y, mn.y), rescale(mo.z, mn.z), rescale(mo.w, mn.w));
+        s_m = mn;
+    }
+    __syncthreads();
+    const float4 mn = s_m, alpha = s_alpha;
+    const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z),
+                                 safe_exp(l4.w, mn.w));
+    sW[threadIdx.x] = f4_scale(vn, p);
+    const float4 ps = warp_sum4(p);
+    __syncthreads();   // everyone has read sRed (the max) and written sW
+    if (lane == 0) sRed[warp] = ps;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float4 sum = sRed[0];
+        for (int w = 1; w < NW; ++w) sum = f4_add(sum, sRed[w]);
+        const float4 lo = s_l;
+        s_l = make_float4(fmaf(lo.x, alpha.x, sum.x), fmaf(lo.y, alpha.y, sum.y), fmaf(lo.z, alpha.z, sum.z),
+                          fmaf(lo.w, alpha.w, sum.w));
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+        acc[c] = make_float4(acc[c].x * alpha.x, acc[c].y * alpha.y, acc[c].z * alpha.z, acc[c].w * alpha.w);
+    for (int t = warp; t < ntile; t += NW) accumulate_key<C, CODED, NIB>(acc, v, row0 + t, sW[t], cv, lane);
+    __syncthreads();   // sW and sRed are rewritten by the next tile
+}
+
+// Sums the warps' accumulators (through shared memory at red, NW * 32 * C float4) and writes
+// this chunk's partial state (max, sum, acc[d]) for the nh heads of the quad.
+template <int C, bool NIB, int NT>
+__device__ __forceinline__ void write_partial(const float4 (&acc)[C], float4* red, const float4& s_m,
+                                              const float4& s_l, float* pbase, size_t hstride, int nh, int d) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int c = 0; c < C; ++c) red[(warp * C + c) * 32 + lane] = acc[c];
+    __syncthreads();
+    for (int e = threadIdx.x; e < 32 * C; e += NT) {
+        const int c = e / 32, l = e % 32;
+        float4 s = red[c * 32 + l];
+        for (int w = 1; w < NW; ++w) s = f4_add(s, red[(w * C + c) * 32 + l]);
+        const int j = owned_coord<NIB>(l, c);
+        if (j < d) {
+            const float vv[4] = {s.x, s.y, s.z, s.w};
+            for (int h = 0; h < nh; ++h) pbase[h * hstride + 2 + j] = vv[h];
+        }
+    }
+    if (threadIdx.x == 0) {
+        const float mv[4] = {s_m.x, s_m.y, s_m.z, s_m.w}, lv[4] = {s_l.x, s_l.y, s_l.z, s_l.w};
+        for (int h = 0; h < nh; ++h) {
+            pbase[h * hstride] = mv[h];
+            pbase[h * hstride + 1] = lv[h];
+        }
+    }
+}
+
+// Fused output: logits from the key codes (scorer), then softmax_tile.  C = ceil(d/32)
+// coordinates per lane (nibble layout when NIB); d <= 32 * C.
+template <int W, int P, int C, bool CODED, bool NIB>
 __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a) {
     extern __shared__ float4 sm[];
     const Params& prm = a.prm;
-    const int d = prm.d;
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
     const int L = checked_len(a.k.len, b, a.k.cap, a.err);
     const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
@@ -106,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
 
     Scorer<W, P> sc;
     sc.setup(sm, prm, a.qrot, a.qproj, (size_t)b * a.Hq + hbase, nh);
-    float4* sW = sm + Scorer<W, P>::smem_bytes(prm) / sizeof(float4);   // [kThreads] weights
+    float4* sW = sm + Scorer<W, P>::smem_bytes(prm) / sizeof(float4);   // [kThreads]
     float4* sRed = sW + kThreads;                                        // [kThreads / 32]
     __shared__ float4 s_m, s_l, s_alpha;
     __shared__ float s_cv[kMaxLevels];
@@ -115,103 +188,90 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
         s_l = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
-
-    const int dpad = 32 * ((d + 31) / 32);
-    const int nparts = kThreads / dpad;
-    const int part = threadIdx.x / dpad, j = threadIdx.x - part * dpad;
-    const bool active = part < nparts && j < d;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-
+    const ValueSrc v{a.values, a.vnorm, a.vprm.P, a.vprm.W, prm.d};
+    float4 acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int64_t iend = min((int64_t)L, i0 + a.chunk);
     const size_t rowbase = (size_t)bh * a.k.cap;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __syncthreads();
-
     for (int64_t t0 = i0; t0 < iend; t0 += kThreads) {
         const int ntile = (int)min((int64_t)kThreads, iend - t0);
-        const int t = threadIdx.x;
         float4 l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         float vn = 0.f;
-        if (t < ntile) {
-            const float4 e = sc(prm, a.k.planes, a.k.signs, a.k.norm, a.k.rnorm, rowbase + t0 + t);
+        if ((int)threadIdx.x < ntile) {
+            const float4 e = sc(prm, a.k.planes, a.k.signs, a.k.norm, a.k.rnorm, rowbase + t0 + threadIdx.x);
             l4.x = a.scale * e.x;
             if (nh > 1) l4.y = a.scale * e.y;
             if (nh > 2) l4.z = a.scale * e.z;
             if (nh > 3) l4.w = a.scale * e.w;
-            vn = CODED ? half_bits_to_float(__ldg(a.vnorm + rowbase + t0 + t)) : 1.f;
+            vn = CODED ? half_bits_to_float(__ldg(a.vnorm + rowbase + t0 + threadIdx.x)) : 1.f;
         }
-        float4 wm = warp_max4(l4);
-        if (lane == 0) sRed[warp] = wm;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float4 mx = sRed[0];
-            for (int w = 1; w < kThreads / 32; ++w) mx = f4_max(mx, sRed[w]);
-            const float4 mo = s_m;
-            const float4 mn = f4_max(mo, mx);
-            s_alpha = make_float4(rescale(mo.x, mn.x), rescale(mo.y, mn.y), rescale(mo.z, mn.z),
-                                  rescale(mo.w, mn.w));
-            s_m = mn;
-        }
-        __syncthreads();
-        const float4 mn = s_m, alpha = s_alpha;
-        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z),
-                                     safe_exp(l4.w, mn.w));
-        sW[t] = f4_scale(vn, p);
-        const float4 ps = warp_sum4(p);
-        __syncthreads();   // sRed reuse: everyone has read the max
-        if (lane == 0) sRed[warp] = ps;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float4 s = sRed[0];
-            for (int w = 1; w < kThreads / 32; ++w) s = f4_add(s, sRed[w]);
-            const float4 lo = s_l;
-            s_l = make_float4(fmaf(lo.x, alpha.x, s.x), fmaf(lo.y, alpha.y, s.y), fmaf(lo.z, alpha.z, s.z),
-                              fmaf(lo.w, alpha.w, s.w));
-        }
-        acc = make_float4(acc.x * alpha.x, acc.y * alpha.y, acc.z * alpha.z, acc.w * alpha.w);
-        if (active) {
-            if constexpr (CODED) {
-                const uint32_t* vp = static_cast<const uint32_t*>(a.values);
-                const int vw = W > 0 ? W : a.vprm.W;
-                const int VP = a.vprm.P;
-                const int word = j >> 5, bit = j & 31;
-                for (int tt = part; tt < ntile; tt += nparts) {
-                    const uint32_t* row = vp + (rowbase + t0 + tt) * (size_t)(VP * vw);
-                    int idx = 0;
-                    for (int pp = 0; pp < VP; ++pp) idx |= ((__ldg(row + pp * vw + word) >> bit) & 1u) << pp;
-                    acc = f4_fma(s_cv[idx], sW[tt], acc);
-                }
-            } else {
-                const uint16_t* vb = static_cast<const uint16_t*>(a.values);
-                for (int tt = part; tt < ntile; tt += nparts) {
-                    const float v = bf16_bits_to_float(__ldg(vb + (rowbase + t0 + tt) * (size_t)d + j));
-                    acc = f4_fma(v, sW[tt], acc);
-                }
-            }
-        }
-        __syncthreads();   // sW and sRed are rewritten by the next tile
+        softmax_tile<C, CODED, NIB, kThreads>(l4, vn, ntile, rowbase + t0, v, sW, sRed, s_m, s_l, s_alpha, s_cv, acc);
     }
-    // sum the parts of each coordinate, then write this chunk's partial state
-    float4* sAcc = sW;   // reuse: [nparts][dpad]
-    if (part < nparts) sAcc[part * dpad + j] = acc;
-    __syncthreads();
-    const size_t stride = (size_t)d + 2;
+    const size_t stride = (size_t)prm.d + 2;
     float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
-    const size_t hstride = (size_t)a.nchunk * stride;
-    if (threadIdx.x < d) {
-        float4 s = sAcc[threadIdx.x];
-        for (int q = 1; q < nparts; ++q) s = f4_add(s, sAcc[q * dpad + threadIdx.x]);
-        const float v[4] = {s.x, s.y, s.z, s.w};
-        for (int h = 0; h < nh; ++h) pbase[h * hstride + 2 + threadIdx.x] = v[h];
-    }
+    write_partial<C, NIB, kThreads>(acc, sm, s_m, s_l, pbase, (size_t)a.nchunk * stride, nh, prm.d);
+}
+
+// Softmax + value sum from logits already in HBM ([B][Hq][cap], scaled).
+constexpr int kValThreads = 256;
+
+struct ValuesArgs {
+    const float* logits;
+    int B, Hq, Hkv, G, d;
+    int64_t cap;
+    const int32_t* len;
+    int chunk, nchunk;
+    int* err;
+    Params vprm;          // centroids of the value context (coded values)
+    ValueSrc v;
+    float* partials;
+};
+
+template <int C, bool CODED, bool NIB>
+__global__ void __launch_bounds__(kValThreads) values_kernel(const ValuesArgs a) {
+    __shared__ float4 sW[kValThreads];
+    __shared__ float4 sRed[kValThreads / 32];
+    extern __shared__ float4 red[];   // [kValThreads / 32][C][32]
+    __shared__ float4 s_m, s_l, s_alpha;
+    __shared__ float s_cv[kMaxLevels];
+    const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
+    const int L = checked_len(a.len, b, a.cap, a.err);
+    const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
+    if (i0 >= L) return;
+    const int hbase = kvh * a.G + 4 * blockIdx.z;
+    const int nh = min(4, kvh * a.G + a.G - hbase);
     if (threadIdx.x == 0) {
-        const float4 mm = s_m, ll = s_l;
-        const float mv[4] = {mm.x, mm.y, mm.z, mm.w}, lv[4] = {ll.x, ll.y, ll.z, ll.w};
-        for (int h = 0; h < nh; ++h) {
-            pbase[h * hstride] = mv[h];
-            pbase[h * hstride + 1] = lv[h];
-        }
+        s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        s_l = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
+    float4 acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t iend = min((int64_t)L, i0 + a.chunk);
+    const size_t rowbase = (size_t)bh * a.cap;
+    const float* lg = a.logits + ((size_t)b * a.Hq + hbase) * a.cap;
+    __syncthreads();
+    for (int64_t t0 = i0; t0 < iend; t0 += kValThreads) {
+        const int ntile = (int)min((int64_t)kValThreads, iend - t0);
+        float4 l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float vn = 0.f;
+        const int64_t i = t0 + threadIdx.x;
+        if ((int)threadIdx.x < ntile) {
+            l4.x = __ldg(lg + i);
+            if (nh > 1) l4.y = __ldg(lg + a.cap + i);
+            if (nh > 2) l4.z = __ldg(lg + 2 * a.cap + i);
+            if (nh > 3) l4.w = __ldg(lg + 3 * a.cap + i);
+            vn = CODED ? half_bits_to_float(__ldg(a.v.norm + rowbase + i)) : 1.f;
+        }
+        softmax_tile<C, CODED, NIB, kValThreads>(l4, vn, ntile, rowbase + t0, a.v, sW, sRed, s_m, s_l, s_alpha, s_cv,
+                                                 acc);
+    }
+    const size_t stride = (size_t)a.d + 2;
+    float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
+    write_partial<C, NIB, kValThreads>(acc, red, s_m, s_l, pbase, (size_t)a.nchunk * stride, nh, a.d);
 }
 
 // out[b][h] = Pi_v^T (sum_c e^{m_c - M} a_c) / (sum_c e^{m_c - M} l_c) over the chunks that
@@ -269,12 +329,24 @@ struct LogitsLaunch {
     }
 };
 
+// Coordinates per lane for the value sum: C = W on the table path (d <= 224); 16 on the
+// generic path (d <= 512).  The nibble layout serves W == 4.
+template <int W, int P, bool CODED>
+cudaError_t run_output(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+    constexpr int C = W > 0 ? W : 16;
+    const size_t scorer = Scorer<W, P>::smem_bytes(a.prm) + (kThreads + kThreads / 32) * sizeof(float4);
+    const size_t red = (size_t)(kThreads / 32) * 32 * C * sizeof(float4);
+    const size_t smem = scorer > red ? scorer : red;
+    const bool nib = (W == 4) && (CODED || a.prm.d == 128);
+    if (nib) return launch_with_smem(attn_partial_kernel<W, P, C, CODED, (W == 4)>, grid, smem, a, s);
+    return launch_with_smem(attn_partial_kernel<W, P, C, CODED, false>, grid, smem, a, s);
+}
+
 struct OutputLaunch {
     template <int W, int P>
     static cudaError_t run(const AttnArgs& a, dim3 grid, cudaStream_t s) {
-        const size_t smem = Scorer<W, P>::smem_bytes(a.prm) + (kThreads + kThreads / 32) * sizeof(float4);
-        if (a.vmode) return launch_with_smem(attn_partial_kernel<W, P, true>, grid, smem, a, s);
-        return launch_with_smem(attn_partial_kernel<W, P, false>, grid, smem, a, s);
+        if (a.vmode) return run_output<W, P, true>(a, grid, s);
+        return run_output<W, P, false>(a, grid, s);
     }
 };
 
@@ -319,6 +391,15 @@ AttnArgs make_args(const tq_ctx* kc, const float* qrot, const float* qproj, int 
     return a;
 }
 
+template <int C, bool CODED, bool NIB>
+cudaError_t run_values(const ValuesArgs& a, dim3 grid, cudaStream_t s) {
+    const size_t smem = (size_t)(kValThreads / 32) * 32 * C * sizeof(float4);
+    cudaError_t e = cudaFuncSetAttribute(values_kernel<C, CODED, NIB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    values_kernel<C, CODED, NIB><<<grid, kValThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* chunk, int* nchunk) {
@@ -342,6 +423,37 @@ cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qpro
     const bool lut = lut_path_ok(a.prm, 0, kSmemLimit);
     dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
     return dispatch<LogitsLaunch>(a, lut, grid, s);
+}
+
+cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                               const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
+                               float* partials, float* out, cudaStream_t s) {
+    ValuesArgs a{};
+    a.logits = logits;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.d = d;
+    a.cap = cap;
+    a.len = len;
+    a.err = err;
+    if (vc) a.vprm = vc->prm;
+    a.v = ValueSrc{values, vnorm, vc ? vc->P : 0, vc ? vc->W : 0, d};
+    a.partials = partials;
+    attn_chunking(nullptr, B, Hq, Hkv, cap, &a.chunk, &a.nchunk);
+    dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
+    const int W = (d + 31) / 32;
+    cudaError_t e;
+    if (vc && W == 4) e = run_values<4, true, true>(a, grid, s);
+    else if (!vc && d == 128) e = run_values<4, false, true>(a, grid, s);
+    else if (W <= 8) e = vc ? run_values<8, true, false>(a, grid, s) : run_values<8, false, false>(a, grid, s);
+    else e = vc ? run_values<16, true, false>(a, grid, s) : run_values<16, false, false>(a, grid, s);
+    if (e != cudaSuccess) return e;
+    const int threads = d >= 256 ? 256 : ((d + 31) / 32) * 32;
+    attn_combine_kernel<<<B * Hq, threads, d * sizeof(float), s>>>(partials, a.nchunk, a.chunk, d, Hq, len, cap,
+                                                                  vc ? vc->dPi : nullptr, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,

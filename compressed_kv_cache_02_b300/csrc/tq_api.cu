@@ -350,6 +350,49 @@ int tq_attn_output(tq_ctx* c, const tq_ctx* vc, const float* q, int B, int Hq, i
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_output launch");
 }
 
+static size_t values_ws_bytes(int d, int B, int Hq, int Hkv, int64_t cap) {
+    int chunk, nchunk;
+    attn_chunking(nullptr, B, Hq, Hkv, cap, &chunk, &nchunk);
+    return round_up((size_t)B * Hq * nchunk * (d + 2) * sizeof(float), 256);
+}
+
+int tq_attn_values_workspace_size(int d, int B, int Hq, int Hkv, int64_t cap, size_t* bytes) {
+    TQ_REQUIRE(bytes != nullptr, TQ_ERR_ARG, "bytes is NULL");
+    TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_ARG, "d must be in [1, 512]");
+    TQ_REQUIRE(B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && cap >= 1, TQ_ERR_ARG,
+               "need B >= 1, cap >= 1 and Hq a positive multiple of Hkv");
+    *bytes = values_ws_bytes(d, B, Hq, Hkv, cap);
+    return TQ_OK;
+}
+
+int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                   const int32_t* len, const void* values, const uint16_t* v_norm, float* out, void* ws,
+                   size_t ws_bytes, void* stream) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (vc) {
+        int rc = check_ctx(vc);
+        if (rc) return rc;
+        TQ_REQUIRE(vc->mode == TQ_MODE_MSE, TQ_ERR_ARG, "vctx must be an MSE-mode context");
+        TQ_REQUIRE(vc->d == d, TQ_ERR_ARG, "d must equal vctx's d");
+        TQ_REQUIRE(v_norm && aligned(v_norm, 2), TQ_ERR_ARG, "coded values need v_norm");
+    }
+    TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_values supports d <= 512");
+    TQ_REQUIRE(B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0, TQ_ERR_ARG, "need B >= 1 and Hq a positive multiple of Hkv");
+    TQ_REQUIRE(cap >= 1 && cap < (int64_t)1 << 31, TQ_ERR_ARG, "cap must be in [1, 2^31)");
+    TQ_REQUIRE(logits && len && values && out && ws, TQ_ERR_ARG, "a required pointer is NULL");
+    TQ_REQUIRE(aligned(logits, 4) && aligned(len, 4) && aligned(values, 16) && aligned(out, 4) && aligned(ws, 256),
+               TQ_ERR_ARG, "misaligned pointer");
+    TQ_REQUIRE(ws_bytes >= values_ws_bytes(d, B, Hq, Hkv, cap), TQ_ERR_ARG,
+               "workspace too small (see tq_attn_values_workspace_size)");
+    // without a context (bf16 values) there is no error word: out-of-range lengths are clamped
+    int* err = vc ? vc->derr : nullptr;
+    e = launch_attn_values(vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, err, static_cast<float*>(ws), out,
+                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_values launch");
+}
+
 struct SearchWs {
     size_t qrot, qproj, cs, ci, total;
 };

@@ -36,7 +36,7 @@ __device__ __forceinline__ float4 f4_scale(float s, float4 a) {
 __device__ __forceinline__ int checked_len(const int32_t* len, int b, int64_t cap, int* err) {
     int L = len[b];
     if (L < 0 || L > cap) {
-        if (threadIdx.x == 0) set_error(err, TQ_DEVERR_LEN_RANGE);
+        if (threadIdx.x == 0 && err) set_error(err, TQ_DEVERR_LEN_RANGE);
         L = L < 0 ? 0 : static_cast<int>(cap);
     }
     return L;

@@ -42,6 +42,11 @@ cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* 
                                float scale, const void* values, const uint16_t* vnorm,
                                float* partials, float* out, cudaStream_t s);
 
+// Softmax + value sum from precomputed logits, then the combine (vc NULL: bf16 values of dim d).
+cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                               const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
+                               float* partials, float* out, cudaStream_t s);
+
 // Search: per-chunk top-k candidates into cand (score, index pairs), then the merge.
 void search_chunking(int64_t n, int k, int* chunk, int* nchunk);
 cudaError_t launch_search(const tq_ctx* c, const float* qrot, const float* qproj, int64_t nq,

@@ -48,6 +48,8 @@ _SIGS = {
     "tq_attn_workspace_size": [_p, _i, _i, _i, _i64, ctypes.POINTER(_sz)],
     "tq_attn_logits": [_p, _p, _i, _i, _i, _p, _p, _p, _p, _i64, _p, _f, _p, _p, _sz, _p],
     "tq_attn_output": [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _i64, _p, _f, _p, _p, _p, _p, _sz, _p],
+    "tq_attn_values_workspace_size": [_i, _i, _i, _i, _i64, ctypes.POINTER(_sz)],
+    "tq_attn_values": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _sz, _p],
     "tq_search_workspace_size": [_p, _i64, _i64, _i, ctypes.POINTER(_sz)],
     "tq_search_topk": [_p, _p, _i64, _p, _p, _p, _p, _i64, _i, _p, _p, _p, _sz, _p],
     "tq_sync_status": [_p, _p, _p],
@@ -110,6 +112,31 @@ class Codes:
     norm: torch.Tensor
     signs: torch.Tensor | None = None
     rnorm: torch.Tensor | None = None
+
+
+def values_workspace(d, B, Hq, Hkv, cap, device="cuda") -> torch.Tensor:
+    n = _sz()
+    _check(lib.tq_attn_values_workspace_size(d, B, Hq, Hkv, cap, ctypes.byref(n)), "tq_attn_values_workspace_size")
+    return torch.empty(n.value, dtype=torch.uint8, device=device)
+
+
+def attn_values(logits, length, values, vctx=None, d=None, Hkv=None, out=None, workspace=None, stream=None):
+    """Softmax over logits [B, Hq, cap] and the weighted sum of values: bf16 [B, Hkv, cap, d]
+    (vctx None) or the Codes of an MSE-mode vctx."""
+    B, Hq, cap = logits.shape
+    if vctx is None:
+        Hkv, d = values.shape[1], values.shape[3]
+        vptr, vnorm, vh = _ptr(values), None, None
+    else:
+        Hkv, d = values.planes.shape[1], vctx.d
+        vptr, vnorm, vh = _ptr(values.planes), _ptr(values.norm), vctx.h
+    if out is None:
+        out = torch.empty(B, Hq, d, device=logits.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = values_workspace(d, B, Hq, Hkv, cap, device=logits.device)
+    _check(lib.tq_attn_values(vh, d, _ptr(logits), B, Hq, Hkv, cap, _ptr(length), vptr, vnorm, _ptr(out),
+                              _ptr(workspace), workspace.numel(), _stream(stream)), "tq_attn_values")
+    return out
 
 
 class Context:

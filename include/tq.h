@@ -90,7 +90,7 @@ enum tq_device_error {
 
 #define TQ_MAX_D 1024
 #define TQ_MAX_MSE_BITS 4
-#define TQ_MAX_TOPK 256
+#define TQ_MAX_TOPK 128
 
 typedef struct tq_ctx tq_ctx;
 
@@ -202,6 +202,20 @@ int tq_attn_output(tq_ctx* kctx, const tq_ctx* vctx, const float* q, int B, int 
                    const int32_t* len, float scale, const void* values,
                    const uint16_t* v_norm, float* out, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* Workspace bytes for tq_attn_values with these shapes.                               */
+int tq_attn_values_workspace_size(int d, int B, int Hq, int Hkv, int64_t cap, size_t* bytes);
+
+/* Softmax + value sum from logits already computed (e.g. by tq_attn_logits):
+ * out[b][h] = sum_{i < len[b]} softmax_i(logits[b][h][0..len[b])) v_hat(b, h/(Hq/Hkv), i).
+ * logits float32 [B][Hq][cap] (already scaled); values and v_norm as in tq_attn_output
+ * (vctx NULL: bfloat16 values of dimension d; else vctx's MSE codes and d == vctx's d).
+ * d <= 512.  With vctx NULL there is no device error word: a len[b] outside [0, cap] is
+ * clamped without a flag.  Pages: nonndazone.ru essay §2 (compressed values); the softmax-weighted sum
+ * of the values is the attention step that follows the logits of juejin.cn post §三.    */
+int tq_attn_values(const tq_ctx* vctx, int d, const float* logits, int B, int Hq, int Hkv,
+                   int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
+                   float* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- search */
 

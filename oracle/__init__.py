@@ -48,7 +48,7 @@ from .rng import splitmix64_stream, gaussian_stream, haar_rotation, jl_matrix, m
 from .codebook import Codebook, sphere_codebook, sphere_marginal_pdf, sphere_cell_prob, sphere_cell_first_moment
 from .turboquant import (
     Quantized, quantize, dequantize, qjl_signs, pack_planes, unpack_planes, pack_signs,
-    unpack_signs, estimate, estimate_all, attention_logits, attention_output,
+    unpack_signs, estimate, estimate_all, attention_logits, attention_values, attention_output,
     search_topk, recall_at_1, fp16_round, QJL_CONST,
 )
 
@@ -57,6 +57,6 @@ __all__ = [
     "Codebook", "sphere_codebook", "sphere_marginal_pdf", "sphere_cell_prob",
     "sphere_cell_first_moment", "Quantized", "quantize", "dequantize", "qjl_signs",
     "pack_planes", "unpack_planes", "pack_signs", "unpack_signs", "estimate", "estimate_all",
-    "attention_logits", "attention_output", "search_topk", "recall_at_1", "fp16_round",
+    "attention_logits", "attention_values", "attention_output", "search_topk", "recall_at_1", "fp16_round",
     "QJL_CONST",
 ]

@@ -197,20 +197,16 @@ def softmax(logits: np.ndarray) -> np.ndarray:
     return e / np.sum(e)
 
 
-def attention_output(q: np.ndarray, keys: Quantized, lens: np.ndarray, Pi: np.ndarray,
-                     S: np.ndarray, cb: Codebook, scale: float,
-                     values_dense: Optional[np.ndarray] = None,
-                     values: Optional[Quantized] = None, Pi_v: Optional[np.ndarray] = None,
-                     cb_v: Optional[Codebook] = None) -> np.ndarray:
-    """o [B, Hq, d] = sum_i softmax(logits)_i v_hat_i over i < lens[b]; zeros when lens[b] == 0.
+def attention_values(logits: np.ndarray, lens: np.ndarray, Hkv: int,
+                     values_dense: Optional[np.ndarray] = None, values: Optional[Quantized] = None,
+                     Pi_v: Optional[np.ndarray] = None, cb_v: Optional[Codebook] = None) -> np.ndarray:
+    """o [B, Hq, d] = sum_{i < lens[b]} softmax(logits[b, h, :lens[b]])_i v_hat_i; zeros when lens[b] == 0.
 
     Values are either dense [B, Hkv, N, d] (``values_dense``) or MSE-only codes
     (``values`` with idx and norm16, rotation ``Pi_v`` and table ``cb_v``).
     """
-    logits = attention_logits(q, keys, lens, Pi, S, cb, scale)
     B, Hq, _ = logits.shape
-    Hkv = keys.idx.shape[1]
-    d = Pi.shape[0]
+    d = values_dense.shape[-1] if values_dense is not None else Pi_v.shape[0]
     out = np.zeros((B, Hq, d))
     for b in range(B):
         L = int(lens[b])
@@ -218,13 +214,23 @@ def attention_output(q: np.ndarray, keys: Quantized, lens: np.ndarray, Pi: np.nd
             continue
         for h in range(Hq):
             g = _group(h, Hq, Hkv)
-            p = softmax(logits[b, h, :L])
+            p = softmax(np.asarray(logits[b, h, :L], dtype=np.float64))
             if values_dense is not None:
                 V = np.asarray(values_dense[b, g, :L], dtype=np.float64)
             else:
                 V = dequantize(values.idx[b, g, :L], values.norm16[b, g, :L], Pi_v, cb_v)
             out[b, h] = p @ V
     return out
+
+
+def attention_output(q: np.ndarray, keys: Quantized, lens: np.ndarray, Pi: np.ndarray,
+                     S: np.ndarray, cb: Codebook, scale: float,
+                     values_dense: Optional[np.ndarray] = None,
+                     values: Optional[Quantized] = None, Pi_v: Optional[np.ndarray] = None,
+                     cb_v: Optional[Codebook] = None) -> np.ndarray:
+    """Logits over the compressed keys, then the softmax-weighted value sum (attention_values)."""
+    logits = attention_logits(q, keys, lens, Pi, S, cb, scale)
+    return attention_values(logits, lens, keys.idx.shape[1], values_dense, values, Pi_v, cb_v)
 
 
 # ----------------------------------------------------------------------------- search

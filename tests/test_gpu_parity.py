@@ -90,7 +90,7 @@ def test_argument_errors_raise():
     tq = _tq()
     pr = Pair(16, 3)
     X = inputs.gaussian(4, 16, seed=1).cuda()
-    with pytest.raises(tq.TQError):
+    with pytest.raises(TypeError):
         pr.ctx.quantize(X.double())
     out = pr.ctx.alloc_codes(4)
     code = tq.lib.tq_quantize(pr.ctx.h, X.data_ptr(), 0, 4, 8, out.planes.data_ptr(), out.signs.data_ptr(),
@@ -185,6 +185,29 @@ def test_attention_output(vmode, B, Hkv, G, N, bits, lens):
                                       values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
     assert kp.ctx.sync_status() == 0
     assert_close(got.cpu().numpy(), ref, "attention output")
+
+
+@pytest.mark.parametrize("vmode", ["bf16", "mse"])
+@pytest.mark.parametrize("B,Hkv,G,N,lens", [(1, 8, 4, 1100, [1100]), (2, 2, 4, 2600, [2600, 1]),
+                                           (2, 1, 6, 700, [0, 699])])
+def test_attention_values_from_logits(vmode, B, Hkv, G, N, lens):
+    """The softmax + value step on its own: oracle logits in, weighted values out."""
+    tq = _tq()
+    d = 128
+    c = _kv_case(B, Hkv, G, N, d, 3, vmode, seed=13, lens=lens)
+    kp = c["kp"]
+    ref_l = oracle.attention_logits(c["q"].numpy(), c["kz"], c["lens"], kp.Pi, kp.S, kp.cb, 1.0 / sqrt(d))
+    logits = torch.from_numpy(np.nan_to_num(ref_l, nan=0.0).astype(np.float32)).cuda()
+    length = torch.tensor(lens, dtype=torch.int32).cuda()
+    if vmode == "bf16":
+        got = tq.attn_values(logits, length, c["V"].cuda())
+        ref = oracle.attention_values(logits.cpu().numpy(), c["lens"], Hkv, values_dense=c["V"].float().numpy())
+    else:
+        vp = c["vp"]
+        got = tq.attn_values(logits, length, c["vcodes"], vctx=vp.ctx)
+        ref = oracle.attention_values(logits.cpu().numpy(), c["lens"], Hkv, values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
+    torch.cuda.synchronize()
+    assert_close(got.cpu().numpy(), ref, "softmax-weighted values")
 
 
 def test_decode_append_and_advance():
