@@ -50,6 +50,7 @@ _SIGS = {
     "tq_attn_output": [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _i64, _p, _f, _p, _p, _p, _p, _sz, _p],
     "tq_attn_values_workspace_size": [_i, _i, _i, _i, _i64, ctypes.POINTER(_sz)],
     "tq_attn_values": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _sz, _p],
+    "tq_attn_values_noalloc": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p],
     "tq_search_workspace_size": [_p, _i64, _i64, _i, ctypes.POINTER(_sz)],
     "tq_search_topk": [_p, _p, _i64, _p, _p, _p, _p, _i64, _i, _p, _p, _p, _sz, _p],
     "tq_sync_status": [_p, _p, _p],

@@ -217,6 +217,24 @@ int tq_attn_values(const tq_ctx* vctx, int d, const float* logits, int B, int Hq
                    int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
                    float* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the static scratch array behind tq_attn_values_noalloc (8 MiB per device).     */
+#define TQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* tq_attn_values without a workspace argument, for callers that may not allocate device
+ * memory while they run (a server that reserves all device memory in its own pool at
+ * start-up and forbids cudaMalloc afterwards, since an allocation can synchronise the device
+ * and can fail mid-request; a plugin host that passes buffers but no allocator).  The pages
+ * have no counterpart: this is an interface variant, the arithmetic is tq_attn_values'.
+ * Scratch: a file-scope device array of TQ_NOALLOC_SCRATCH_BYTES that every GPU loading the
+ * library keeps until exit.  Shapes needing more than that (B*Hq*nchunk*(d+2)*4 bytes, as
+ * tq_attn_values_workspace_size reports) are rejected with TQ_ERR_UNSUPPORTED.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  No call allocates or
+ * frees memory.  All calls on a device share the array: calls that overlap on the GPU race. */
+int tq_attn_values_noalloc(const tq_ctx* vctx, int d, const float* logits, int B, int Hq, int Hkv,
+                           int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
+                           float* out, void* stream);
+
 /* ---------------------------------------------------------------- search */
 
 /* Workspace bytes for tq_search_topk.                                                  */
