@@ -62,6 +62,226 @@ __global__ void __launch_bounds__(kThreads) logits_kernel(const AttnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Logits at W == 4 (96 < d <= 128, m <= 128), thread per key, without bank conflicts.
+// The byte tables of lut.cuh are stored as T[v][k] (entry v of group k at v * 16 + k, 16 groups
+// of 8 bits).  At step j a thread looks up group k = (j + r) mod 16, r = lane mod 8, so the 8
+// lanes of each quarter-warp always hit 8 different bank slots (k mod 8) whatever their byte
+// values.  To keep the byte positions static, each thread first rotates its 128-bit code
+// vectors right by r bytes.  Arithmetic on the 4 query heads runs as packed fp32 pairs.
+//
+// Scheduling is persistent: one CTA per SM walks a contiguous share of all (batch, KV head,
+// head quad) groups' keys, rebuilding the tables only when the group changes.
+using u64 = unsigned long long;
+__device__ __forceinline__ u64 pk2(float x, float y) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(u64 r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+    u64 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// The t-th positive integer with an odd number of set bits (t < 8): 2t + 1 - parity(t).  For
+// t < 2^(P-1) these are the odd-size subsets of P bits in increasing order.  Plain arithmetic,
+// so it folds to a constant once the loop over t is unrolled.
+__host__ __device__ constexpr int odd_mask(int t) { return (2 * t) | (((t ^ (t >> 1) ^ (t >> 2)) & 1) ^ 1); }
+static_assert(odd_mask(0) == 1 && odd_mask(1) == 2 && odd_mask(2) == 4 && odd_mask(3) == 7 && odd_mask(4) == 8 &&
+                  odd_mask(5) == 11 && odd_mask(6) == 13 && odd_mask(7) == 14,
+              "odd-size subsets of 4 bits");
+template <int P> struct OddMasks {
+    static constexpr int n = 1 << (P - 1);
+};
+
+
+__device__ __forceinline__ void build_tables_vk(float4* T, const float* a, int stride) {
+    if (threadIdx.x < 16) T[threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    for (int i = 0; i < 8; ++i) {
+        const int half = 1 << i;
+        for (int e = threadIdx.x; e < (16 << i); e += blockDim.x) {
+            const int k = e & 15;
+            const int v = half + (e >> 4);
+            const int j = 8 * k + i;
+            const float4 add = make_float4(a[j], a[stride + j], a[2 * stride + j], a[3 * stride + j]);
+            T[v * 16 + k] = f4_add(T[(v - half) * 16 + k], add);
+        }
+        __syncthreads();
+    }
+}
+
+// x rotated right by r bytes (0 <= r < 8) as a 128-bit little-endian vector.
+__device__ __forceinline__ void rot_bytes(const uint32_t (&x)[4], int r, uint32_t (&y)[4]) {
+    const bool w1 = r >= 4;
+    const uint32_t a0 = w1 ? x[1] : x[0], a1 = w1 ? x[2] : x[1], a2 = w1 ? x[3] : x[2], a3 = w1 ? x[0] : x[3];
+    const int sh = 8 * (r & 3);
+    y[0] = __funnelshift_r(a0, a1, sh);
+    y[1] = __funnelshift_r(a1, a2, sh);
+    y[2] = __funnelshift_r(a2, a3, sh);
+    y[3] = __funnelshift_r(a3, a0, sh);
+}
+
+constexpr int kQ8Threads = 512;
+
+template <int P>
+__device__ __forceinline__ float4 score_key(const float4* __restrict__ Tq, const float4* __restrict__ Tu,
+                                            const uint32_t (&pl)[P][4], const uint32_t (&sg)[4], float n, float rho,
+                                            int r, const float* kap, float4 cq, float4 cu, float kq2, bool qjl) {
+    constexpr int NT = OddMasks<P>::n;
+    uint32_t y[P][4];
+#pragma unroll
+    for (int p = 0; p < P; ++p) rot_bytes(pl[p], r, y[p]);
+    uint32_t ys[4];
+    if (qjl) rot_bytes(sg, r, ys);
+    float4 m[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) m[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int k = (j + r) & 15;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            uint32_t x = 0u;
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                if ((odd_mask(t) >> p) & 1) x ^= y[p][j >> 2];
+            m[t] = f4_add(m[t], Tq[((x >> (8 * (j & 3))) & 255u) * 16 + k]);
+        }
+        if (qjl) u = f4_add(u, Tu[((ys[j >> 2] >> (8 * (j & 3))) & 255u) * 16 + k]);
+    }
+    float4 e = cq;   // c0 sum(q'), then the masked sums
+#pragma unroll
+    for (int t = 0; t < NT; ++t) e = f4_fma(kap[t], m[t], e);
+    e = f4_scale(n, e);
+    if (qjl) {   // + rho kq (2 M_u - sum u)
+        e = f4_fma(rho, cu, e);
+        e = f4_fma(rho * kq2, u, e);
+    }
+    return e;
+}
+
+template <int P>
+__global__ void __launch_bounds__(kQ8Threads, 1) logits_q8_kernel(const AttnArgs a) {
+    extern __shared__ float4 sm[];
+    const Params& prm = a.prm;
+    float4* Tq = sm;
+    float4* Tu = sm + 4096;
+    float* qs = reinterpret_cast<float*>(sm + 8192);
+    float* us = qs + 4 * 128;
+    __shared__ float4 s_sum[2];
+    const bool qjl = prm.qjl != 0;
+    const int quads = (a.G + 3) / 4;
+    const int ngroups = a.B * a.Hkv * quads;
+    // keys of all groups in blocks of 32, split evenly across the CTAs
+    int64_t total = 0;
+    for (int g = 0; g < ngroups; ++g) {
+        const int b = g / (a.Hkv * quads);
+        int L = a.k.len[b];
+        L = L < 0 ? 0 : (L > a.k.cap ? (int)a.k.cap : L);
+        total += (L + 31) / 32;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (int b = 0; b < a.B; ++b)
+            if (a.k.len[b] < 0 || a.k.len[b] > a.k.cap) set_error(a.err, TQ_DEVERR_LEN_RANGE);
+    }
+    const int64_t lo = total * blockIdx.x / gridDim.x, hi = total * (blockIdx.x + 1) / gridDim.x;
+    float kap[OddMasks<P>::n];
+#pragma unroll
+    for (int t = 0; t < OddMasks<P>::n; ++t) kap[t] = prm.kappa[t];
+    const int r = threadIdx.x & 7;
+    int64_t acc = 0;
+    for (int g = 0; g < ngroups && acc < hi; ++g) {
+        const int b = g / (a.Hkv * quads), kvh = (g / quads) % a.Hkv, quad = g % quads;
+        int L = a.k.len[b];
+        L = L < 0 ? 0 : (L > a.k.cap ? (int)a.k.cap : L);
+        const int64_t nblk = (L + 31) / 32;
+        const int64_t b0 = max(lo, acc) - acc, b1 = min(hi, acc + nblk) - acc;
+        acc += nblk;
+        if (b0 >= b1) continue;
+        const int hbase = kvh * a.G + 4 * quad;
+        const int nh = min(4, kvh * a.G + a.G - hbase);
+        const size_t qrow0 = (size_t)b * a.Hq + hbase;
+        __syncthreads();   // the previous group's tables are no longer read
+        stage_quad(qs, 128, a.qrot + qrow0 * prm.d, prm.d, 0, nh, prm.d);
+        if (qjl) stage_quad(us, 128, a.qproj + qrow0 * prm.m, prm.m, 0, nh, prm.m);
+        __syncthreads();
+        build_tables_vk(Tq, qs, 128);
+        if (qjl) build_tables_vk(Tu, us, 128);
+        if (threadIdx.x == 0) {
+            float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), su = sq;
+            for (int k = 0; k < 16; ++k) {
+                sq = f4_add(sq, Tq[255 * 16 + k]);
+                if (qjl) su = f4_add(su, Tu[255 * 16 + k]);
+            }
+            s_sum[0] = sq;
+            s_sum[1] = su;
+        }
+        __syncthreads();
+        const float4 qsum = s_sum[0], usum = s_sum[1];
+        const float kq = prm.qjl_scale, c0 = prm.c0;
+        const float4 cq = f4_scale(c0, qsum), cu = f4_scale(-kq, usum);
+        const size_t rowbase = ((size_t)b * a.Hkv + kvh) * a.k.cap;
+        const size_t cap = a.k.cap;
+        float* out = a.logits + qrow0 * cap;
+        const int64_t kend = min((int64_t)L, b1 * 32);
+        for (int64_t k0 = b0 * 32 + threadIdx.x; k0 < kend; k0 += 2 * kQ8Threads) {
+            // two keys per thread per pass: both loads are in flight before either is scored
+            const int64_t kk[2] = {k0, k0 + kQ8Threads};
+            uint32_t pl[2][P][4], sg[2][4];
+            float n[2], rho[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool valid = kk[u] < kend;
+                const size_t row = rowbase + (valid ? kk[u] : 0);
+                const uint4* pr = reinterpret_cast<const uint4*>(a.k.planes + row * (P * 4));
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const uint4 v = valid ? __ldg(pr + p) : make_uint4(0u, 0u, 0u, 0u);
+                    pl[u][p][0] = v.x; pl[u][p][1] = v.y; pl[u][p][2] = v.z; pl[u][p][3] = v.w;
+                }
+                n[u] = valid ? half_bits_to_float(__ldg(a.k.norm + row)) : 0.f;
+                if (qjl && valid) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.k.signs + row * 4));
+                    sg[u][0] = v.x; sg[u][1] = v.y; sg[u][2] = v.z; sg[u][3] = v.w;
+                    rho[u] = half_bits_to_float(__ldg(a.k.rnorm + row));
+                } else {
+                    sg[u][0] = sg[u][1] = sg[u][2] = sg[u][3] = 0u;
+                    rho[u] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (kk[u] < kend) {
+                    const float4 e = score_key<P>(Tq, Tu, pl[u], sg[u], n[u], rho[u], r, kap, cq, cu, 2.f * kq, qjl);
+                    const int64_t key = kk[u];
+                    out[key] = a.scale * e.x;
+                    if (nh > 1) out[cap + key] = a.scale * e.y;
+                    if (nh > 2) out[2 * cap + key] = a.scale * e.z;
+                    if (nh > 3) out[3 * cap + key] = a.scale * e.w;
+                }
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float4 f4_max(float4 a, float4 b) {
     return make_float4(fmaxf(a.x, b.x), fmaxf(a.y, b.y), fmaxf(a.z, b.z), fmaxf(a.w, b.w));
 }
@@ -391,6 +611,164 @@ AttnArgs make_args(const tq_ctx* kc, const float* qrot, const float* qproj, int 
     return a;
 }
 
+// ---------------------------------------------------------------------------------------
+// Tuned paths for W == 4 (96 < d <= 128), the head dimension of the decode workloads.
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
+
+// Softmax + value sum for MSE-coded values at W == 4.  Tiles of 256 keys: each thread owns
+// one key of the tile for the softmax; the tile's value rows are copied to shared memory
+// with cp.async one tile ahead, and the next tile's logits are prefetched into registers.
+// In the value sum a warp takes one key at a time; lane l owns coordinates 4l..4l+3 (a
+// nibble of word l/8 of every plane) and gathers their P-bit indices with one bit spread
+// per plane: (nibble * 0x204081) & 0x01010101 moves bit c of the nibble to bit 8c.
+constexpr int kV2Threads = 256;
+
+template <int P>
+__global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const ValuesArgs a) {
+    constexpr int ROW = P * 4;                        // words per value row
+    constexpr int ROWS = ROW < 8 ? 8 : ROW;           // room for the final warp reduction too
+    __shared__ __align__(16) uint32_t sV[2][kV2Threads * ROWS];
+    __shared__ float4 sW[kV2Threads];
+    __shared__ float4 sRed[kV2Threads / 32];
+    __shared__ float4 s_m, s_l, s_alpha;
+    __shared__ u64 s_cv2[kMaxLevels];   // (c, c) pairs for the packed multiply
+    const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
+    const int L = checked_len(a.len, b, a.cap, a.err);
+    const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
+    if (i0 >= L) return;
+    const int hbase = kvh * a.G + 4 * blockIdx.z;
+    const int nh = min(4, kvh * a.G + a.G - hbase);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        s_l = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (threadIdx.x < kMaxLevels) s_cv2[threadIdx.x] = pk2(a.vprm.centroids[threadIdx.x], a.vprm.centroids[threadIdx.x]);
+    u64 alo[4], ahi[4];   // heads (0,1) and (2,3) of the 4 owned coordinates
+#pragma unroll
+    for (int c = 0; c < 4; ++c) alo[c] = ahi[c] = 0ull;
+    const int64_t iend = min((int64_t)L, i0 + a.chunk);
+    const size_t rowbase = (size_t)bh * a.cap;
+    const float* lg = a.logits + ((size_t)b * a.Hq + hbase) * a.cap;
+    const uint32_t* vrows = static_cast<const uint32_t*>(a.v.values);
+
+    auto issue_tile = [&](int64_t t0, int buf) {
+        const int n = (int)min((int64_t)kV2Threads, iend - t0);
+        const uint4* src = reinterpret_cast<const uint4*>(vrows + (rowbase + t0) * ROW);
+        uint4* dst = reinterpret_cast<uint4*>(sV[buf]);
+        for (int e = threadIdx.x; e < n * P; e += kV2Threads) cp_async16(dst + e, src + e);
+    };
+    auto load_logits = [&](int64_t t0, float4& l4, float& vn) {
+        const int64_t i = t0 + threadIdx.x;
+        l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        vn = 0.f;
+        if (i < iend) {
+            l4.x = __ldg(lg + i);
+            if (nh > 1) l4.y = __ldg(lg + a.cap + i);
+            if (nh > 2) l4.z = __ldg(lg + 2 * a.cap + i);
+            if (nh > 3) l4.w = __ldg(lg + 3 * a.cap + i);
+            vn = half_bits_to_float(__ldg(a.v.norm + rowbase + i));
+        }
+    };
+
+    float4 l4;
+    float vn;
+    load_logits(i0, l4, vn);
+    issue_tile(i0, 0);
+    cp_async_commit();
+    __syncthreads();
+    int buf = 0;
+    for (int64_t t0 = i0; t0 < iend; t0 += kV2Threads, buf ^= 1) {
+        const int ntile = (int)min((int64_t)kV2Threads, iend - t0);
+        const int64_t tn = t0 + kV2Threads;
+        if (tn < iend) issue_tile(tn, buf ^ 1);
+        cp_async_commit();
+        float4 nl4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float nvn = 0.f;
+        if (tn < iend) load_logits(tn, nl4, nvn);
+
+        // online softmax over this tile (one key per thread)
+        const float4 wm = warp_max4(l4);
+        if (lane == 0) sRed[warp] = wm;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float4 mx = sRed[0];
+            for (int w = 1; w < kV2Threads / 32; ++w) mx = f4_max(mx, sRed[w]);
+            const float4 mo = s_m, mn = f4_max(mo, mx);
+            s_alpha = make_float4(rescale(mo.x, mn.x), rescale(mo.y, mn.y), rescale(mo.z, mn.z), rescale(mo.w, mn.w));
+            s_m = mn;
+        }
+        __syncthreads();
+        const float4 mn = s_m, alpha = s_alpha;
+        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z),
+                                     safe_exp(l4.w, mn.w));
+        sW[threadIdx.x] = f4_scale(vn, p);
+        const float4 ps = warp_sum4(p);
+        cp_async_wait1();   // this tile's value rows have landed
+        __syncthreads();
+        if (lane == 0) sRed[warp] = ps;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float4 sum = sRed[0];
+            for (int w = 1; w < kV2Threads / 32; ++w) sum = f4_add(sum, sRed[w]);
+            const float4 lo = s_l;
+            s_l = make_float4(fmaf(lo.x, alpha.x, sum.x), fmaf(lo.y, alpha.y, sum.y), fmaf(lo.z, alpha.z, sum.z),
+                              fmaf(lo.w, alpha.w, sum.w));
+        }
+        const u64 al_lo = pk2(alpha.x, alpha.y), al_hi = pk2(alpha.z, alpha.w);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            alo[c] = mul2(alo[c], al_lo);
+            ahi[c] = mul2(ahi[c], al_hi);
+        }
+        const uint32_t* tile = sV[buf];
+        const ulonglong2* sW2 = reinterpret_cast<const ulonglong2*>(sW);
+        const int sh = 4 * (lane & 7), wsel = lane >> 3;
+#pragma unroll 2
+        for (int t = warp; t < ntile; t += kV2Threads / 32) {
+            const uint32_t* row = tile + t * ROW;
+            uint32_t z = 0u;
+#pragma unroll
+            for (int pp = 0; pp < P; ++pp) {
+                const uint32_t nib = (row[pp * 4 + wsel] >> sh) & 15u;
+                z |= ((nib * 0x00204081u) & 0x01010101u) << pp;
+            }
+            const ulonglong2 w = sW2[t];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const u64 v = s_cv2[(z >> (8 * c)) & 15u];
+                alo[c] = fma2(v, w.x, alo[c]);
+                ahi[c] = fma2(v, w.y, ahi[c]);
+            }
+        }
+        __syncthreads();   // sW, sRed and this buffer are reused
+        l4 = nl4;
+        vn = nvn;
+    }
+    const size_t stride = (size_t)a.d + 2;
+    float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
+    float4 acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 x = upk2(alo[c]), y = upk2(ahi[c]);
+        acc[c] = make_float4(x.x, x.y, y.x, y.y);
+    }
+    write_partial<4, true, kV2Threads>(acc, reinterpret_cast<float4*>(sV), s_m, s_l, pbase,
+                                       (size_t)a.nchunk * stride, nh, a.d);
+}
+
+template <int P>
+cudaError_t run_values_coded128(const ValuesArgs& a, dim3 grid, cudaStream_t s) {
+    values_coded128_kernel<P><<<grid, kV2Threads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int C, bool CODED, bool NIB>
 cudaError_t run_values(const ValuesArgs& a, dim3 grid, cudaStream_t s) {
     const size_t smem = (size_t)(kValThreads / 32) * 32 * C * sizeof(float4);
@@ -416,10 +794,30 @@ void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* c
     (void)kc;
 }
 
+template <int P>
+cudaError_t run_logits_q8(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+    const size_t smem = 8192 * sizeof(float4) + 2 * 4 * 128 * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(logits_q8_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    logits_q8_kernel<P><<<grid, kQ8Threads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
                           int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s) {
     AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
     a.logits = logits;
+    if (a.prm.W == 4 && (!a.prm.qjl || a.prm.Ws == 4) && a.prm.odd_walsh) {
+        static int sms = 0;
+        if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, kc->device) != cudaSuccess) sms = 148;
+        dim3 grid(sms);
+        switch (a.prm.P) {
+            case 1: return run_logits_q8<1>(a, grid, s);
+            case 2: return run_logits_q8<2>(a, grid, s);
+            case 3: return run_logits_q8<3>(a, grid, s);
+            case 4: return run_logits_q8<4>(a, grid, s);
+        }
+    }
     const bool lut = lut_path_ok(a.prm, 0, kSmemLimit);
     dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
     return dispatch<LogitsLaunch>(a, lut, grid, s);
@@ -445,7 +843,14 @@ cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int
     dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
     const int W = (d + 31) / 32;
     cudaError_t e;
-    if (vc && W == 4) e = run_values<4, true, true>(a, grid, s);
+    if (vc && W == 4) {
+        switch (vc->P) {
+            case 1: e = run_values_coded128<1>(a, grid, s); break;
+            case 2: e = run_values_coded128<2>(a, grid, s); break;
+            case 3: e = run_values_coded128<3>(a, grid, s); break;
+            default: e = run_values_coded128<4>(a, grid, s); break;
+        }
+    }
     else if (!vc && d == 128) e = run_values<4, false, true>(a, grid, s);
     else if (W <= 8) e = vc ? run_values<8, true, false>(a, grid, s) : run_values<8, false, false>(a, grid, s);
     else e = vc ? run_values<16, true, false>(a, grid, s) : run_values<16, false, false>(a, grid, s);

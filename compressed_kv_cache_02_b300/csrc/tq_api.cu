@@ -142,6 +142,12 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
     walsh_form(c->centroids, P, c0, masks, kappa);
     p.c0 = static_cast<float>(c0);
     p.nterms = static_cast<int>(masks.size());
+    {
+        std::vector<int> odd;
+        for (int S = 1; S < c->L; ++S)
+            if (__builtin_popcount(S) & 1) odd.push_back(S);
+        p.odd_walsh = (masks == odd) ? 1 : 0;
+    }
     for (int t = 0; t < kMaxTerms; ++t) {
         p.mask[t] = t < p.nterms ? masks[t] : 0;
         p.kappa[t] = t < p.nterms ? static_cast<float>(kappa[t]) : 0.f;

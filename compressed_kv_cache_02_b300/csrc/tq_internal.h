@@ -23,6 +23,7 @@ struct Params {
     // where x_t(idx) = parity of the idx bits selected by mask[t].
     float c0;
     int nterms;
+    int odd_walsh;   // 1 when the terms are exactly the odd-size subsets in increasing order
     int mask[kMaxTerms];
     float kappa[kMaxTerms];
 };

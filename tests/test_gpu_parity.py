@@ -137,6 +137,8 @@ def _run_logits(c, scale):
     (2, 1, 4, 400, 200, 2, [400, 0]),            # d=200 (7 words), an empty sequence
     (1, 2, 4, 257, 300, 3, [257]),               # d=300: generic (table-free) path
     (1, 1, 4, 100, 33, 5, [100]),                # ragged d, 4 MSE bits
+    (1, 2, 4, 999, 100, 2, [999]),               # d=100 on the d<=128 path, 1 MSE bit
+    (1, 1, 4, 2049, 128, 5, [2049]),             # 4 MSE bits on the d<=128 path
 ])
 def test_logits(B, Hkv, G, N, d, bits, lens):
     c = _kv_case(B, Hkv, G, N, d, bits, None, seed=3, lens=lens)
