@@ -306,7 +306,7 @@ __device__ __forceinline__ float4 warp_sum4(float4 v) {
     return v;
 }
 // exp(l - m) with exp(-inf - anything) = 0 (no NaN when both are -inf).
-__device__ __forceinline__ float safe_exp(float l, float m) { return l == -INFINITY ? 0.f : expf(l - m); }
+__device__ __forceinline__ float safe_exp(float l, float m) { return l == -INFINITY ? 0.f : __expf(l - m); }
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
     return m_old == -INFINITY ? 0.f : expf(m_old - m_new);
 }
@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const Value
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
                 const uint32_t nib = (row[pp * 4 + wsel] >> sh) & 15u;
-                z |= ((nib * 0x00204081u) & 0x01010101u) << pp;
+                z |= (nib * (0x00204081u << pp)) & (0x01010101u << pp);
             }
             const ulonglong2 w = sW2[t];
 #pragma unroll
@@ -805,6 +805,8 @@ cudaError_t run_logits_q8(const AttnArgs& a, dim3 grid, cudaStream_t s) {
 
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
                           int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s) {
+    if (kc->kernel_path == TQ_PATH_TENSOR && logits_mma_supported(kc))
+        return launch_logits_mma(kc, qrot, qproj, B, Hq, Hkv, k, scale, logits, s);
     AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
     a.logits = logits;
     if (a.prm.W == 4 && (!a.prm.qjl || a.prm.Ws == 4) && a.prm.odd_walsh) {

@@ -201,6 +201,14 @@ int tq_layout(const tq_ctx* c, int* planes, int* words_per_plane, int* sign_word
     return TQ_OK;
 }
 
+int tq_set_kernel_path(tq_ctx* c, int path) {
+    TQ_REQUIRE(c != nullptr, TQ_ERR_ARG, "context is NULL");
+    TQ_REQUIRE(path == TQ_PATH_AUTO || path == TQ_PATH_CUDA_CORE || path == TQ_PATH_TENSOR, TQ_ERR_ARG,
+               "path must be TQ_PATH_AUTO, TQ_PATH_CUDA_CORE or TQ_PATH_TENSOR");
+    c->kernel_path = path;
+    return TQ_OK;
+}
+
 int tq_export_matrices(const tq_ctx* c, float* Pi, float* S, double* centroids, double* thresholds) {
     TQ_REQUIRE(c != nullptr, TQ_ERR_ARG, "context is NULL");
     if (Pi) std::memcpy(Pi, c->Pi.data(), c->Pi.size() * sizeof(float));

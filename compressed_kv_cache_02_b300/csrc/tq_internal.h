@@ -52,4 +52,5 @@ struct tq_ctx {
     float* dST = nullptr;     // [d][m]  ST[j*m+i] = S[i][j]        (u = S q)
     float* dStT = nullptr;    // [d][m]  StT[j*m+i] = (S Pi^T)[i][j] (S r = (S Pi^T)(Pi x - n c))
     int* derr = nullptr;      // device error word
+    int kernel_path = TQ_PATH_AUTO;   // logits kernel family (tq_set_kernel_path)
 };

@@ -36,6 +36,11 @@ void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* c
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
                           int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s);
 
+// Tensor-core logits (mma.sync e4m3) for 96 < d <= 128, m <= 128, 1..3 MSE bits.
+bool logits_mma_supported(const tq_ctx* kc);
+cudaError_t launch_logits_mma(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
+                              const KeyCache& k, float scale, float* logits, cudaStream_t s);
+
 // Split-sequence attention output: per-chunk partials (max, sum, acc[d]) then the combine.
 cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,
                                const float* qproj, int B, int Hq, int Hkv, const KeyCache& k,

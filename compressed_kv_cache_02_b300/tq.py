@@ -25,6 +25,7 @@ TQ_F32, TQ_BF16 = 0, 1
 TQ_MODE_PROD, TQ_MODE_MSE = 0, 1
 TQ_MAX_TOPK = 128
 TQ_DEVERR_NORM_OVERFLOW, TQ_DEVERR_LEN_RANGE = 1, 2
+TQ_PATH_AUTO, TQ_PATH_CUDA_CORE, TQ_PATH_TENSOR = 0, 1, 2
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -41,6 +42,7 @@ _SIGS = {
     "tq_info": [_p, _p, _p, _p, _p],
     "tq_layout": [_p, _p, _p, _p],
     "tq_export_matrices": [_p, _p, _p, _p, _p],
+    "tq_set_kernel_path": [_p, _i],
     "tq_quantize": [_p, _p, _i, _i64, _i64, _p, _p, _p, _p, _p],
     "tq_append": [_p, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _p],
     "tq_advance_len": [_p, _p, _i, _i64, _i, _p],
@@ -176,6 +178,9 @@ class Context:
     @property
     def qjl(self) -> bool:
         return self.mode == TQ_MODE_PROD
+
+    def set_kernel_path(self, path: int) -> None:
+        _check(lib.tq_set_kernel_path(self.h, path), "tq_set_kernel_path")
 
     def export(self):
         import numpy as np

@@ -138,6 +138,15 @@ int tq_info(const tq_ctx* ctx, int* d, int* m, int* mse_bits, int* mode);
  * sign_words = Ws (0 in MSE mode).  Any output may be NULL.                            */
 int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_words);
 
+/* Kernel family for tq_attn_logits on this context.  TQ_PATH_AUTO (the default) picks the
+ * fastest measured family (currently the table kernels); TQ_PATH_CUDA_CORE forces the
+ * shared-memory table kernels; TQ_PATH_TENSOR
+ * asks for the tensor-core kernel (mma.sync, e4m3 operands, fp32 accumulation; available for
+ * 96 < d <= 128, m <= 128 and 1-3 MSE bits, else the call falls back to the table kernels).
+ * Both families compute the same estimator within the documented tolerance.              */
+enum tq_kernel_path { TQ_PATH_AUTO = 0, TQ_PATH_CUDA_CORE = 1, TQ_PATH_TENSOR = 2 };
+int tq_set_kernel_path(tq_ctx* ctx, int path);
+
 /* Copies the context's float32 Pi (d*d), S (m*d; PROD only) and float64 centroids
  * (2^P) and thresholds (2^P - 1) to host arrays.  Any output may be NULL.              */
 int tq_export_matrices(const tq_ctx* ctx, float* Pi, float* S, double* centroids,

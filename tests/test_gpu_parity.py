@@ -129,6 +129,11 @@ def _run_logits(c, scale):
     return c["kp"].ctx.attn_logits(c["q"].cuda(), c["keys"], c["N"], length, scale)
 
 
+@pytest.fixture(params=["cuda_core", "tensor"])
+def kernel_path(request):
+    return request.param
+
+
 @pytest.mark.parametrize("B,Hkv,G,N,d,bits,lens", [
     (1, 1, 16, 4096, 128, 3, [4096]),            # tiny correctness workload: 16 queries x 4096 keys
     (1, 8, 4, 1100, 128, 4, [1100]),             # decode layer shape (4-bit keys), ragged tail
@@ -140,8 +145,10 @@ def _run_logits(c, scale):
     (1, 2, 4, 999, 100, 2, [999]),               # d=100 on the d<=128 path, 1 MSE bit
     (1, 1, 4, 2049, 128, 5, [2049]),             # 4 MSE bits on the d<=128 path
 ])
-def test_logits(B, Hkv, G, N, d, bits, lens):
+def test_logits(B, Hkv, G, N, d, bits, lens, kernel_path):
+    tq = _tq()
     c = _kv_case(B, Hkv, G, N, d, bits, None, seed=3, lens=lens)
+    c["kp"].ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     scale = 1.0 / sqrt(d)
     got = _run_logits(c, scale).cpu().numpy()
     assert c["kp"].ctx.sync_status() == 0
@@ -151,10 +158,11 @@ def test_logits(B, Hkv, G, N, d, bits, lens):
         assert_close(got[b, :, :L], ref[b, :, :L], "logits")
 
 
-def test_logits_mse_keys():
+def test_logits_mse_keys(kernel_path):
     tq = _tq()
     d, N = 128, 600
     kp = Pair(d, 3, mode=tq.TQ_MODE_MSE, seed=9)
+    kp.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     K = inputs.gaussian(2 * N, d, seed=9).reshape(1, 2, N, d)
     q = inputs.gaussian(8, d, seed=10).reshape(1, 8, d)
     kz = kp.oquant(K.numpy())
