@@ -300,7 +300,112 @@ def run_tq(args, world, rank, local):
     }
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
+    if not args.no_extra:
+        del logits, ws, vws, state, kc, vc
+        torch.cuda.empty_cache()
+        res["other_workloads"] = {"search": measure_search(dev), "prefill": measure_prefill(dev)}
     return res
+
+
+# ----------------------------------------------------------------------------- secondary workloads
+
+def _event_time(fn, reps=1):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        out = fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps, out
+
+
+def measure_search(dev):
+    """Vector search: 10^6 unit vectors (d=200, cone law) coded at 2 and 4 total bits, 10^4
+    queries, top-100 (top-1 and top-10 are its prefixes); recall@1@k against the exact fp32
+    top-1 (fp32 GEMM, TF32 off)."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    d, n, nq, k = 200, 1_000_000, 10_000, 100
+    X = inputs.cone(n, d, seed=5, mu_seed=55, device=dev)
+    Q = inputs.cone(nq, d, seed=6, mu_seed=55, device=dev)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    true1 = torch.cat([torch.argmax(Q[i:i + 1000] @ X.T, dim=1) for i in range(0, nq, 1000)])
+    torch.backends.cuda.matmul.allow_tf32 = prev
+    res = {}
+    for bits in (2, 4):
+        ctx = tq.Context(d, bits, seed=0)
+        db = ctx.alloc_codes(n, device=dev)
+        ctx.quantize(X, out=db)
+        t_index, _ = _event_time(lambda: ctx.quantize(X, out=db))
+        ws = ctx.search_workspace(nq, n, k, device=dev)
+        ctx.search_topk(Q, db, k, workspace=ws)
+        t_search, (sc, idx) = _event_time(lambda: ctx.search_topk(Q, db, k, workspace=ws))
+        hit = idx.long() == true1[:, None]
+        recall = {f"recall@1@{kk}": float(hit[:, :kk].any(dim=1).float().mean()) for kk in (1, 10, 100)}
+        code_bytes = (ctx.P * ctx.W + ctx.Ws) * 4 + 4
+        res[f"{bits}bit"] = {"search_ms": t_search * 1e3, "pairs_per_s": n * nq / t_search,
+                             "index_ms": t_index * 1e3, "index_vectors_per_s": n / t_index,
+                             "db_bytes_per_vector": code_bytes, **recall}
+        del db, ws
+    return {"workload": "1e6 cone vectors d=200, 1e4 queries, top-100", **res}
+
+
+def _decode_codes(ctx, codes, Pi, cent):
+    """x_hat = n16 Pi^T c[idx] from packed codes, in torch (measurement only)."""
+    planes = codes.planes.view(torch.int32)
+    n, P, W = planes.shape
+    j = torch.arange(ctx.d, device=planes.device)
+    idx = torch.zeros(n, ctx.d, dtype=torch.long, device=planes.device)
+    for p in range(P):
+        words = planes[:, p, :].long() & 0xFFFFFFFF
+        idx |= ((words[:, j // 32] >> (j % 32)) & 1) << p
+    nrm = codes.norm.view(torch.float16).float()
+    return nrm[:, None] * (cent[idx] @ Pi)
+
+
+def measure_prefill(dev):
+    """Prefill-time bulk quantization: 32 layers x 8 KV heads x 16384 tokens x d=128 (bf16,
+    anisotropic), MSE bits 2, 3, 4 plus 1 QJL bit.  Throughput of the quantize kernel and the
+    distortions D_mse = E||x - x_hat||^2/||x||^2 (2^16 sampled vectors) and D_prod =
+    E(est - <q,x>)^2 / (||q||^2 ||x||^2) (1024 queries x 2^14 sampled keys, est from the logits
+    kernel with scale 1)."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    L_, H_, T_ = 32, 8, 16384
+    n = L_ * H_ * T_
+    fac = inputs.anisotropic_factors(H_, D, seed=4, device=dev)
+    X = inputs.anisotropic(L_, H_, T_, D, fac, seed=4, device=dev).reshape(n, D)
+    Qs = inputs.anisotropic(1, 1, 1024, D, (fac[0][:1], fac[1][:1]), seed=40, device=dev,
+                            dtype=torch.float32).reshape(1024, D)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    sample = torch.randperm(n, generator=g, device=dev)[: 1 << 16]
+    res = {}
+    for bits in (3, 4, 5):
+        ctx = tq.Context(D, bits, seed=0)
+        out = ctx.alloc_codes(n, device=dev)
+        ctx.quantize(X, out=out)
+        t, _ = _event_time(lambda: ctx.quantize(X, out=out))
+        Pi, _, cent, _ = ctx.export()
+        Pi_t = torch.from_numpy(Pi).to(dev)
+        cent_t = torch.from_numpy(cent).float().to(dev)
+        xs = X[sample].float()
+        sub = tq.Codes(out.planes[sample], out.norm[sample], out.signs[sample], out.rnorm[sample])
+        xh = _decode_codes(ctx, sub, Pi_t, cent_t)
+        d_mse = float(((xs - xh) ** 2).sum(1).div(xs.pow(2).sum(1)).mean())
+        ks = 1 << 14
+        keys = tq.Codes(sub.planes[:ks].reshape(1, 1, ks, ctx.P, -1), sub.norm[:ks].reshape(1, 1, ks),
+                        sub.signs[:ks].reshape(1, 1, ks, -1), sub.rnorm[:ks].reshape(1, 1, ks))
+        est = ctx.attn_logits(Qs.reshape(1, 1024, D), keys, ks, torch.tensor([ks], dtype=torch.int32, device=dev),
+                              1.0)[0]
+        exact = Qs @ xs[:ks].T
+        den = Qs.pow(2).sum(1)[:, None] * xs[:ks].pow(2).sum(1)[None, :]
+        d_prod = float(((est - exact) ** 2 / den).mean())
+        bytes_per_vec = 2 * D + (ctx.P * ctx.W + ctx.Ws) * 4 + 4
+        res[f"{bits - 1}+1bit"] = {"quantize_ms": t * 1e3, "vectors_per_s": n / t,
+                                  "GB_s": n * bytes_per_vec / t / 1e9, "D_mse": d_mse, "D_prod": d_prod}
+        del out
+    return {"workload": "32 layers x 8 KV heads x 16384 tokens x d=128 bf16", **res}
 
 
 # ----------------------------------------------------------------------------- the oracle arm
@@ -394,6 +499,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extra", action="store_true", help="skip the search and prefill workloads")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     args = ap.parse_args()
