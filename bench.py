@@ -502,11 +502,18 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the search and prefill workloads")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
+    ap.add_argument("--only", choices=["search", "prefill"], default=None,
+                    help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()
     set_batch(args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+    if args.only:
+        torch.cuda.set_device(local)
+        fn = measure_search if args.only == "search" else measure_prefill
+        print(json.dumps({"only": args.only, **fn(torch.device("cuda", local))}), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
     else:

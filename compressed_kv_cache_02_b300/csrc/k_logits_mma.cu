@@ -18,9 +18,7 @@
 // g+8, k = 4t..4t+3 and 4t+16..4t+19; B column g, the same k; C rows g, g+8, columns 2t, 2t+1.
 // Coordinates map to k so that thread t only needs word t of each bit plane: at k-step s,
 // a0 byte i (k = 4t+i) is bit 2s+8i of the word and a2 byte i (k = 4t+16+i) is bit 2s+1+8i.
-#include <cuda_fp8.h>
-
-#include "tq_device.cuh"
+#include "mma_e4m3.cuh"
 #include "tq_kernels.h"
 
 namespace tq {
@@ -40,40 +38,6 @@ struct MmaArgs {
     float* logits;
     int* err;
 };
-
-__host__ __device__ constexpr int odd_mask(int t) { return (2 * t) | (((t ^ (t >> 1) ^ (t >> 2)) & 1) ^ 1); }
-
-__device__ __forceinline__ uint32_t to_e4m3(float x) {
-    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-}
-// exact value of an e4m3 byte
-__device__ __forceinline__ float from_e4m3(uint32_t b) {
-    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-    float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
-    return (b & 0x80u) ? -v : v;
-}
-// piece pc of v * 2^e0 (pieces b0 + b1/16 + b2/256 + b3/4096)
-__device__ __forceinline__ uint32_t piece(float v, int e0, int pc) {
-    float x = ldexpf(v, e0);
-    uint32_t b = to_e4m3(x);
-    for (int p = 0; p < pc; ++p) {
-        x = (x - from_e4m3(b)) * 16.f;
-        b = to_e4m3(x);
-    }
-    return b;
-}
-// bits q, q+8, q+16, q+24 of x as e4m3 bytes 0 / 2^-6
-__device__ __forceinline__ uint32_t ext(uint32_t x, int q) {
-    return (q <= 3 ? (x << (3 - q)) : (x >> (q - 3))) & 0x08080808u;
-}
-
-__device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint2 b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
-}
 
 template <int P>
 struct Smem {
@@ -251,8 +215,8 @@ __global__ void __launch_bounds__(kThreads) logits_mma_kernel(const MmaArgs a) {
                     for (int s = 0; s < 4; ++s) {
                         const uint32_t a0 = ext(xa, 2 * s), a1 = ext(xb, 2 * s);
                         const uint32_t a2 = ext(xa, 2 * s + 1), a3 = ext(xb, 2 * s + 1);
-                        mma(am[0], a0, a1, a2, a3, S.Bm[(t * 4 + s) * 2 + 0][lane]);
-                        mma(am[1], a0, a1, a2, a3, S.Bm[(t * 4 + s) * 2 + 1][lane]);
+                        mma_e4m3(am[0], a0, a1, a2, a3, S.Bm[(t * 4 + s) * 2 + 0][lane]);
+                        mma_e4m3(am[1], a0, a1, a2, a3, S.Bm[(t * 4 + s) * 2 + 1][lane]);
                     }
                 }
                 if (qjl) {
@@ -260,8 +224,8 @@ __global__ void __launch_bounds__(kThreads) logits_mma_kernel(const MmaArgs a) {
                     for (int s = 0; s < 4; ++s) {
                         const uint32_t a0 = ext(sw[u][0], 2 * s), a1 = ext(sw[u][1], 2 * s);
                         const uint32_t a2 = ext(sw[u][0], 2 * s + 1), a3 = ext(sw[u][1], 2 * s + 1);
-                        mma(aq[0], a0, a1, a2, a3, S.Bq[s * 2 + 0][lane]);
-                        mma(aq[1], a0, a1, a2, a3, S.Bq[s * 2 + 1][lane]);
+                        mma_e4m3(aq[0], a0, a1, a2, a3, S.Bq[s * 2 + 0][lane]);
+                        mma_e4m3(aq[1], a0, a1, a2, a3, S.Bq[s * 2 + 1][lane]);
                     }
                 }
 #pragma unroll

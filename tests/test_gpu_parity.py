@@ -280,8 +280,10 @@ def _topk_ok(got_s, got_i, ref_s, ref_i, all_scores):
 
 @pytest.mark.parametrize("d,bits,n,nq,k", [(200, 2, 5000, 13, 10), (200, 4, 3000, 8, 100), (128, 3, 4096, 16, 1),
                                          (200, 4, 1000, 5, 128), (64, 2, 300, 3, 50)])
-def test_search_topk(d, bits, n, nq, k):
+def test_search_topk(d, bits, n, nq, k, kernel_path):
+    tq = _tq()
     pr = Pair(d, bits, seed=5)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     X = inputs.cone(n, d, seed=5, mu_seed=77)
     Q = inputs.cone(nq, d, seed=6, mu_seed=77)
     z = pr.oquant(X.numpy())
@@ -293,9 +295,12 @@ def test_search_topk(d, bits, n, nq, k):
     _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
 
 
-def test_search_ties_resolve_to_lower_index():
-    d, n = 64, 600
+@pytest.mark.parametrize("d", [64, 128])
+def test_search_ties_resolve_to_lower_index(d, kernel_path):
+    tq = _tq()
+    n = 600
     pr = Pair(d, 3, seed=8)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     X = inputs.cone(n, d, seed=8, mu_seed=1)
     X[400] = X[17]
     X[555] = X[17]
