@@ -1,0 +1,369 @@
+// Bulk quantization on the 5th-generation tensor cores (tcgen05.mma, TMEM accumulators) for
+// bf16 rows with d = m = 128: the dense rotation and JL projection of batched keys.
+//
+// Pages: juejin.cn post section 二 and csdn tutorial sections PolarQuant / QJL (rotate, code,
+// residual, signs); the arithmetic is that of quantize_kernel (k_quantize.cu), only the two
+// d x d products move to tensor cores:
+//   phase 1  Y = X Pi^T          A = the tile's x rows (bf16, exact), B = Pi as 3 bf16 pieces
+//                                (hi + mid + lo = the float32 Pi exactly), one TMEM
+//                                accumulator of 128 columns per piece; y = (lo + mid) + hi.
+//   epilogue n = ||x||, n16, u = y / n, idx, bit planes, r' = y - n16 c[idx], ||r'||.
+//   phase 2  Z = r' (S Pi^T)^T   A = r' split into bf16 hi and lo (two passes into the same
+//                                accumulators), B = S Pi^T as 3 bf16 pieces; sign_j = [z_j > 0].
+// Pi and S Pi^T stay resident in shared memory (6 x 32 KB), so one CTA per SM walks the
+// tiles of 128 rows.  Operands use the K-major no-swizzle core-matrix layout (8 rows x 16
+// bytes per core matrix; LBO = 128 B between core matrices along K, SBO = 2048 B between
+// 8-row groups).  Warps w, w+4, w+8, w+12 share TMEM lanes 32(w%4)..+31 (rows) and split
+// each row's 128 coordinates in quarters of 32, one bit-plane word each.  One thread issues the MMAs; tcgen05.commit signals an mbarrier
+// whose waits are bounded (TQ_DEVERR_TIMEOUT).
+#include <cuda_bf16.h>
+
+#include <cstring>
+#include <vector>
+
+#include "tq_device.cuh"
+#include "tq_kernels.h"
+
+namespace tq {
+namespace {
+
+constexpr int kTcThreads = 512;   // 4 threads per row, 32 coordinates each
+constexpr int kTile = 128;
+constexpr uint32_t kMatBytes = 128 * 128 * 2;   // one 128 x 128 bf16 operand
+constexpr uint32_t kSmemB = 6 * kMatBytes;      // Pi pieces then S Pi^T pieces
+constexpr uint32_t kSmemA = kMatBytes;          // the tile (x, then r' hi, then r' lo)
+constexpr uint32_t kSmemTotal = kSmemB + kSmemA + 4 * kTile * sizeof(float);   // + norm partials [4][128]
+constexpr long kWaitLimit = 1L << 26;
+
+__host__ __device__ constexpr uint32_t kmajor_off(int r, int k) {
+    return (uint32_t)(((r >> 3) * 16 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(2048 >> 4) << 32) |
+           ((uint64_t)1 << 46);
+}
+
+// kind::f16: D f32, A and B bf16, both K-major, N = 128, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem),
+        "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
+}
+
+// D[p] (+)= A B_p^T for the three B pieces p: 8 K-steps of 16 per piece.  The descriptors of
+// later K-steps and pieces differ only in the start-address field (16-byte units), which
+// stays below 2^14 for any shared-memory offset.
+__device__ __forceinline__ void issue_pieces(uint32_t tmem, uint32_t a_saddr, uint32_t b_saddr, bool accumulate) {
+    const uint64_t da = smem_desc(a_saddr), db = smem_desc(b_saddr);
+#pragma unroll 1
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            mma_bf16(tmem + p * 128, da + (uint64_t)(s * 16), db + (uint64_t)((p * kMatBytes + s * 256) >> 4),
+                     (accumulate || s > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void commit(uint64_t* mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar)));
+}
+
+// Waits for the given phase parity; false after kWaitLimit polls.
+__device__ __forceinline__ bool wait_phase(uint64_t* mbar, uint32_t parity) {
+    for (long it = 0; it < kWaitLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(done)
+            : "r"(smem_u32(mbar)), "r"(parity));
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// The 32 coordinates [32 part, 32 part + 32) of this thread's row from the 3 piece
+// accumulators (columns p*128 + ...), summed small pieces first.
+__device__ __forceinline__ void load_row_part(uint32_t tmem_row, int part, float (&y)[32]) {
+#pragma unroll
+    for (int p = 2; p >= 0; --p) {
+#pragma unroll
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+            float v[16];
+            ld16(tmem_row + p * 128 + 32 * part + c0, v);
+            asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[c0 + j] = (p == 2) ? v[j] : y[c0 + j] + v[j];
+        }
+    }
+}
+
+// Writes 32 bf16 values (coordinates [32 part, 32 part + 32) of row r) into a K-major operand.
+__device__ __forceinline__ void store_row_part(unsigned char* sA, int r, int part, const float (&v)[32]) {
+#pragma unroll
+    for (int kc = 0; kc < 4; ++kc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * kc + 2 * i], v[8 * kc + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&pr);
+        }
+        *reinterpret_cast<uint4*>(sA + kmajor_off(r, 32 * part + 8 * kc)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+struct TcArgs {
+    Params prm;
+    const uint16_t* x;       // bf16 rows
+    int64_t n, ld_x;
+    const uint4* bops;       // 6 pre-laid-out 128 x 128 bf16 operands (Pi pieces, S Pi^T pieces)
+    uint32_t* planes;
+    uint32_t* signs;
+    uint16_t* norm;
+    uint16_t* rnorm;
+    int* err;
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char* sB = sm;
+    unsigned char* sA = sm + kSmemB;
+    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemA);   // [4][128] x-norm, then r-norm parts
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ uint32_t s_tmem;
+    const Params& prm = a.prm;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, part = warp >> 2, row = 32 * q + lane;
+    const int ntiles = (int)((a.n + kTile - 1) / kTile);
+    if (blockIdx.x >= ntiles) return;
+
+    for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) cp_async16(sB + 16 * e, a.bops + e);
+    asm volatile("cp.async.commit_group;");
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar)));
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = s_tmem;
+    const uint32_t tmem_row = tmem + ((uint32_t)(32 * q) << 16);
+    const int nthr = prm.L - 1;
+    uint32_t phase = 0;
+    bool ok = true;
+
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int64_t r0 = (int64_t)tile * kTile;
+        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+        // stage the tile's x rows (zeros beyond n)
+        for (int e = tid; e < kTile * 16; e += kTcThreads) {
+            const int r = e >> 4, kc = e & 15;
+            unsigned char* dst = sA + kmajor_off(r, 8 * kc);
+            if (r < nvalid) cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("cp.async.commit_group;");
+        asm volatile("cp.async.wait_all;");
+        asm volatile("fence.proxy.async.shared::cta;");
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        // phase 1: Y = X Pi^T (3 pieces)
+        if (tid == 0) {
+            issue_pieces(tmem, smem_u32(sA), smem_u32(sB), false);
+            commit(&mbar);
+        }
+        // ||x|| partial from the staged tile while the MMAs run
+        float xs = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+            const uint4 w = *reinterpret_cast<const uint4*>(sA + kmajor_off(row, 32 * part + 8 * kc));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
+                xs = fmaf(lo, lo, xs);
+                xs = fmaf(hi, hi, xs);
+            }
+        }
+        s_part[part * kTile + row] = xs;
+        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;   // also: x-norm partials visible
+        phase ^= 1u;
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        float y[32];
+        load_row_part(tmem_row, part, y);
+        const float nrm = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
+        const float n16 = half_bits_to_float(float_to_half_bits(nrm));
+        const int64_t grow = r0 + row;
+        const bool valid = row < nvalid;
+        // idx = #{k : t_k < y / n}; compared as t_k n < y (n > 0), or all u = 0 when n = 0
+        float tn[kMaxLevels];
+#pragma unroll
+        for (int k = 0; k < kMaxLevels - 1; ++k) tn[k] = prm.thresholds[k] * nrm;
+        uint32_t pw[TQ_MAX_MSE_BITS] = {};
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float yc = nrm > 0.f ? y[c] : 0.f;
+            int idx = 0;
+#pragma unroll
+            for (int k = 0; k < kMaxLevels - 1; ++k)
+                if (k < nthr) idx += (nrm > 0.f ? yc > tn[k] : 0.f > prm.thresholds[k]) ? 1 : 0;
+#pragma unroll
+            for (int p = 0; p < TQ_MAX_MSE_BITS; ++p) pw[p] |= (uint32_t)((idx >> p) & 1) << c;
+            const float r = y[c] - n16 * prm.centroids[idx];
+            y[c] = r;
+            rs = fmaf(r, r, rs);
+        }
+        if (valid)
+            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * (prm.P * 4) + p * 4 + part] = pw[p];
+        if (!prm.qjl) {   // MSE mode: no residual sketch
+            if (valid && part == 0) {
+                const uint16_t nh = float_to_half_bits(nrm);
+                a.norm[grow] = nh;
+                if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncthreads();   // TMEM reads and x reads done before the next tile
+            continue;
+        }
+        store_row_part(sA, row, part, y);   // r' hi (rounded to bf16 by the store)
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        asm volatile("fence.proxy.async.shared::cta;");
+        __syncthreads();   // everyone has read its x-norm partials and written r' hi
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
+        // phase 2a: Z = r'_hi (S Pi^T)^T
+        if (tid == 0) {
+            issue_pieces(tmem, smem_u32(sA), smem_u32(sB) + 3 * kMatBytes, false);
+            commit(&mbar);
+        }
+        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
+        phase ^= 1u;
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
+        store_row_part(sA, row, part, y);   // r' lo = r' - bf16(r')
+        asm volatile("fence.proxy.async.shared::cta;");
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        // phase 2b: Z += r'_lo (S Pi^T)^T
+        if (tid == 0) {
+            issue_pieces(tmem, smem_u32(sA), smem_u32(sB) + 3 * kMatBytes, true);
+            commit(&mbar);
+        }
+        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
+        phase ^= 1u;
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        float z[32];
+        load_row_part(tmem_row, part, z);
+        uint32_t sw = 0u;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
+        if (valid) a.signs[(size_t)grow * 4 + part] = sw;
+        if (valid && part == 0) {
+            const uint16_t nh = float_to_half_bits(nrm);
+            const float rn = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
+            const uint16_t rh = float_to_half_bits(rn);
+            a.norm[grow] = nh;
+            a.rnorm[grow] = rh;
+            if (__hisinf(__ushort_as_half(nh)) || __hisinf(__ushort_as_half(rh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
+    }
+    if (!ok) {
+        if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
+        return;   // an MMA may still be in flight: leave the TMEM allocation to the context teardown
+    }
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+}  // namespace
+
+bool quantize_tc_supported(const tq_ctx* c, int dtype, const void* x, int64_t n, int64_t ld_x) {
+    return c->bops != nullptr && c->kernel_path != TQ_PATH_CUDA_CORE && dtype == TQ_BF16 && n >= 4096 &&
+           (ld_x % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
+}
+
+// Host layout of the six B operands (Pi pieces hi, mid, lo, then S Pi^T pieces): element (i, j)
+// of each 128 x 128 matrix at kmajor_off(i, j); St NULL leaves the last three zero.
+void build_tc_operands(const float* Pi, const float* St, std::vector<uint16_t>& out) {
+    out.assign(6 * 128 * 128, 0);
+    auto bf16_rne = [](float v) -> uint16_t {
+        uint32_t u;
+        std::memcpy(&u, &v, 4);
+        const uint32_t lsb = (u >> 16) & 1u;
+        return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+    };
+    auto bf16_val = [](uint16_t b) -> float {
+        uint32_t u = (uint32_t)b << 16;
+        float v;
+        std::memcpy(&v, &u, 4);
+        return v;
+    };
+    for (int which = 0; which < (St ? 2 : 1); ++which)
+        for (int i = 0; i < 128; ++i)
+            for (int j = 0; j < 128; ++j) {
+                const float v = which == 0 ? Pi[i * 128 + j] : St[i * 128 + j];
+                const uint16_t h = bf16_rne(v);
+                const float r1 = v - bf16_val(h);
+                const uint16_t m = bf16_rne(r1);
+                const uint16_t l = bf16_rne(r1 - bf16_val(m));
+                const uint16_t piece[3] = {h, m, l};
+                for (int p = 0; p < 3; ++p)
+                    out[((size_t)(3 * which + p) * 128 * 128 * 2 + kmajor_off(i, j)) / 2] = piece[p];
+            }
+}
+
+cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_t ld_x, uint32_t* planes,
+                               uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s) {
+    TcArgs a{};
+    a.prm = c->prm;
+    a.x = static_cast<const uint16_t*>(x);
+    a.n = n;
+    a.ld_x = ld_x;
+    a.bops = reinterpret_cast<const uint4*>(c->bops);
+    a.planes = planes;
+    a.signs = signs;
+    a.norm = norm;
+    a.rnorm = rnorm;
+    a.err = c->derr;
+    cudaError_t e = cudaFuncSetAttribute(quantize_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+    if (e != cudaSuccess) return e;
+    int sms = 148;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+    const int64_t ntiles = (n + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    quantize_tc_kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace tq

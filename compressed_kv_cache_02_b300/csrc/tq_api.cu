@@ -62,6 +62,7 @@ void free_ctx(tq_ctx* c) {
     cudaFree(c->dST);
     cudaFree(c->dStT);
     cudaFree(c->derr);
+    cudaFree(c->bops);
     delete c;
 }
 
@@ -172,6 +173,21 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
             }
         if ((rc = upload(&c->dST, ST)) != TQ_OK || (rc = upload(&c->dStT, StT)) != TQ_OK) { free_ctx(c); return rc; }
     }
+    if (d == 128 && (m == 0 || m == 128)) {   // tcgen05 operands for bulk quantization
+        std::vector<float> St;
+        if (m) {
+            St.resize((size_t)128 * 128);
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    double acc = 0.0;
+                    for (int k = 0; k < 128; ++k) acc += (double)c->S[(size_t)i * 128 + k] * (double)c->Pi[(size_t)j * 128 + k];
+                    St[(size_t)i * 128 + j] = static_cast<float>(acc);
+                }
+        }
+        std::vector<uint16_t> ops;
+        build_tc_operands(c->Pi.data(), m ? St.data() : nullptr, ops);
+        if ((rc = upload(&c->bops, ops)) != TQ_OK) { free_ctx(c); return rc; }
+    }
     std::vector<int> zero(1, 0);
     if ((rc = upload(&c->derr, zero)) != TQ_OK) { free_ctx(c); return rc; }
     *out = c;
@@ -241,8 +257,10 @@ int tq_quantize(tq_ctx* c, const void* x, int dtype, int64_t n, int64_t ld_x, ui
     TQ_REQUIRE(aligned(x, dtype == TQ_F32 ? 4 : 2), TQ_ERR_ARG, "x is misaligned for its dtype");
     TQ_REQUIRE(ld_x >= c->d, TQ_ERR_ARG, "ld_x must be >= d");
     if ((rc = check_codes_out(c, planes, signs, norm, rnorm))) return rc;
-    cudaError_t e = launch_quantize(c, x, dtype, n, ld_x, 1, 0, nullptr, planes, signs, norm, rnorm,
-                                    static_cast<cudaStream_t>(stream));
+    cudaError_t e = quantize_tc_supported(c, dtype, x, n, ld_x)
+                        ? launch_quantize_tc(c, x, n, ld_x, planes, signs, norm, rnorm, static_cast<cudaStream_t>(stream))
+                        : launch_quantize(c, x, dtype, n, ld_x, 1, 0, nullptr, planes, signs, norm, rnorm,
+                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_quantize launch");
 }
 

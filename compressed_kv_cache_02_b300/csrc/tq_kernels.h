@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <vector>
+
 #include "tq_internal.h"
 
 namespace tq {
@@ -17,6 +19,12 @@ cudaError_t launch_apply_rows(const float* MT, int din, int dout, const float* i
 cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n, int64_t ld_x,
                             int H, int64_t cap, const int32_t* len, uint32_t* planes,
                             uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s);
+
+// tcgen05 bulk quantize (bf16 rows, d = 128).
+bool quantize_tc_supported(const tq_ctx* c, int dtype, const void* x, int64_t n, int64_t ld_x);
+void build_tc_operands(const float* Pi, const float* St, std::vector<uint16_t>& out);
+cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_t ld_x, uint32_t* planes,
+                               uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s);
 
 cudaError_t launch_advance_len(int32_t* len, int B, int64_t cap, int step, int* err, cudaStream_t s);
 

@@ -85,7 +85,8 @@ enum tq_mode { TQ_MODE_PROD = 0, TQ_MODE_MSE = 1 };
 /* Bits of the device error word (returned through tq_sync_status' *flags). */
 enum tq_device_error {
     TQ_DEVERR_NORM_OVERFLOW = 1,   /* a norm or residual norm rounded to binary16 infinity */
-    TQ_DEVERR_LEN_RANGE = 2        /* a len[b] was negative or above cap (clamped)         */
+    TQ_DEVERR_LEN_RANGE = 2,       /* a len[b] was negative or above cap (clamped)         */
+    TQ_DEVERR_TIMEOUT = 4          /* a bounded wait for the tensor cores gave up          */
 };
 
 #define TQ_MAX_D 1024
@@ -138,11 +139,13 @@ int tq_info(const tq_ctx* ctx, int* d, int* m, int* mse_bits, int* mode);
  * sign_words = Ws (0 in MSE mode).  Any output may be NULL.                            */
 int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_words);
 
-/* Kernel family for tq_attn_logits on this context.  TQ_PATH_AUTO (the default) picks the
- * fastest measured family (currently the table kernels); TQ_PATH_CUDA_CORE forces the
- * shared-memory table kernels; TQ_PATH_TENSOR
- * asks for the tensor-core kernel (mma.sync, e4m3 operands, fp32 accumulation; available for
- * 96 < d <= 128, m <= 128 and 1-3 MSE bits, else the call falls back to the table kernels).
+/* Kernel family on this context.  TQ_PATH_AUTO (the default) picks the fastest measured
+ * family: tcgen05 tensor cores for bulk tq_quantize of bf16 rows at d = 128 (n >= 4096,
+ * ld_x a multiple of 8, 16-byte aligned x), mma.sync tensor cores for tq_search_topk at d in
+ * (96,128], (192,256] or d = 200-224, and the table kernels for tq_attn_logits.
+ * TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere; TQ_PATH_TENSOR also
+ * moves tq_attn_logits to its tensor-core kernel (mma.sync, e4m3 operands, fp32
+ * accumulation; 96 < d <= 128, m <= 128 and 1-3 MSE bits, else the table kernels).
  * Both families compute the same estimator within the documented tolerance.              */
 enum tq_kernel_path { TQ_PATH_AUTO = 0, TQ_PATH_CUDA_CORE = 1, TQ_PATH_TENSOR = 2 };
 int tq_set_kernel_path(tq_ctx* ctx, int path);

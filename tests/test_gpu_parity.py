@@ -52,6 +52,22 @@ def test_quantize_bf16_anisotropic(bits):
     assert same.mean() > 0.99
 
 
+@pytest.mark.parametrize("mode,bits", [(0, 3), (0, 4), (0, 5), (1, 3), (1, 4)])
+@pytest.mark.parametrize("n,ld", [(4096, 128), (5003, 128), (4500, 136)])
+def test_quantize_bulk_bf16(mode, bits, n, ld, kernel_path):
+    """Bulk bf16 rows at d=128: tcgen05 tensor-core path (n >= 4096) and CUDA-core path."""
+    tq = _tq()
+    pr = Pair(128, bits, mode=mode, seed=12)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
+    fac = inputs.anisotropic_factors(1, ld, seed=12)
+    X = inputs.anisotropic(1, 1, n, ld, fac, seed=13)[0, 0]          # rows of ld values; the first 128 are used
+    Xd = X.cuda()[:, :128]
+    codes = pr.ctx.quantize(Xd)
+    assert pr.ctx.sync_status() == 0
+    same = check_codes(pr, X[:, :128].float().numpy(), codes)
+    assert same.mean() > 0.99
+
+
 @pytest.mark.parametrize("bits", [1, 3, 4])
 def test_quantize_mse_mode(bits):
     tq = _tq()
