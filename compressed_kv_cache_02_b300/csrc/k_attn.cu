@@ -804,9 +804,9 @@ cudaError_t run_logits_q8(const AttnArgs& a, dim3 grid, cudaStream_t s) {
 }
 
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
-                          int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s) {
-    if (kc->kernel_path == TQ_PATH_TENSOR && logits_mma_supported(kc))
-        return launch_logits_mma(kc, qrot, qproj, B, Hq, Hkv, k, scale, logits, s);
+                          int Hkv, const KeyCache& k, float scale, float* logits, void* image, cudaStream_t s) {
+    if (kc->kernel_path == TQ_PATH_TENSOR && logits_tc_ok(kc, k))
+        return launch_logits_tc(kc, qrot, qproj, B, Hq, Hkv, k, scale, logits, image, s);
     AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
     a.logits = logits;
     if (a.prm.W == 4 && (!a.prm.qjl || a.prm.Ws == 4) && a.prm.odd_walsh) {

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) search_merge_kernel(const float* __r
 // queries and a database chunk, streamed in tiles of 128 vectors staged in shared memory.
 // Each warp scores 16 vectors against the 8 queries: A = the vectors' bit planes (a k-step is
 // one 32-bit word; thread t's bytes are bits 4t..4t+3 and 16+4t..16+4t+3, each 0 or 2^-6), B =
-// the queries split into 4 e4m3 pieces (columns = query x piece), as in k_logits_mma.cu.  The
+// the queries split into 4 e4m3 pieces (columns = query x piece).  The
 // fp32 scores go straight into the per-query top-k of the CTA.
 constexpr int kSQ = 8;         // queries per CTA
 constexpr int kSTile = 128;    // vectors per tile (8 warps x 16)

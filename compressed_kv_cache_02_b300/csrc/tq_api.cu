@@ -304,7 +304,7 @@ int tq_prep_queries(tq_ctx* c, const float* q, int64_t nq, float* qrot, float* q
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct AttnWs {
-    size_t qrot, qproj, partials, total;
+    size_t qrot, qproj, partials, image, total;
 };
 
 static AttnWs attn_ws_layout(const tq_ctx* c, int B, int Hq, int Hkv, int64_t cap) {
@@ -314,7 +314,8 @@ static AttnWs attn_ws_layout(const tq_ctx* c, int B, int Hq, int Hkv, int64_t ca
     w.qrot = 0;
     w.qproj = round_up((size_t)B * Hq * c->d * sizeof(float), 256);
     w.partials = w.qproj + round_up((size_t)B * Hq * c->m * sizeof(float), 256);
-    w.total = w.partials + round_up((size_t)B * Hq * nchunk * (c->d + 2) * sizeof(float), 256);
+    w.image = w.partials + round_up((size_t)B * Hq * nchunk * (c->d + 2) * sizeof(float), 256);
+    w.total = w.image + (logits_tc_supported(c) ? round_up(logits_tc_image_bytes(B, Hq, Hkv), 256) : 0);
     return w;
 }
 
@@ -353,7 +354,8 @@ int tq_attn_logits(tq_ctx* c, const float* q, int B, int Hq, int Hkv, const uint
     float* qproj = c->m ? reinterpret_cast<float*>(base + w.qproj) : nullptr;
     if ((rc = tq_prep_queries(c, q, (int64_t)B * Hq, qrot, qproj, stream))) return rc;
     KeyCache k{kp, ks, kn, kr, cap, len};
-    cudaError_t e = launch_logits(c, qrot, qproj, B, Hq, Hkv, k, scale, logits, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_logits(c, qrot, qproj, B, Hq, Hkv, k, scale, logits, base + w.image,
+                                  static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_logits launch");
 }
 

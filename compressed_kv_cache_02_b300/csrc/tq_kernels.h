@@ -41,13 +41,18 @@ struct KeyCache {
 void attn_chunking(const tq_ctx* kc, int B, int Hq, int Hkv, int64_t cap, int* chunk, int* nchunk);
 
 // logits[b][h][i] for i < len[b]; qrot/qproj prepared rows [B*Hq][d] / [B*Hq][m].
+// image: scratch of logits_tc_image_bytes(B, Hq, Hkv) bytes for the tensor-core path.
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
-                          int Hkv, const KeyCache& k, float scale, float* logits, cudaStream_t s);
+                          int Hkv, const KeyCache& k, float scale, float* logits, void* image, cudaStream_t s);
 
-// Tensor-core logits (mma.sync e4m3) for 96 < d <= 128, m <= 128, 1..3 MSE bits.
-bool logits_mma_supported(const tq_ctx* kc);
-cudaError_t launch_logits_mma(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
-                              const KeyCache& k, float scale, float* logits, cudaStream_t s);
+// Tensor-core logits (tcgen05.mma kind::f8f6f4, A in TMEM) for 96 < d <= 128, m <= 128 and
+// 1..3 MSE bits; usable when the cache also meets the bulk-copy alignment (16-byte fields,
+// capacity a multiple of 8).  image: logits_tc_image_bytes(B, Hq, Hkv) bytes, 128-byte aligned.
+bool logits_tc_supported(const tq_ctx* kc);
+bool logits_tc_ok(const tq_ctx* kc, const KeyCache& k);
+size_t logits_tc_image_bytes(int B, int Hq, int Hkv);
+cudaError_t launch_logits_tc(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
+                             const KeyCache& k, float scale, float* logits, void* image, cudaStream_t s);
 
 // Split-sequence attention output: per-chunk partials (max, sum, acc[d]) then the combine.
 cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,

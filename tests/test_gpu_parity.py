@@ -160,6 +160,12 @@ def kernel_path(request):
     (1, 1, 4, 100, 33, 5, [100]),                # ragged d, 4 MSE bits
     (1, 2, 4, 999, 100, 2, [999]),               # d=100 on the d<=128 path, 1 MSE bit
     (1, 1, 4, 2049, 128, 5, [2049]),             # 4 MSE bits on the d<=128 path
+    # capacities that are multiples of 8: the bulk-copy tensor-core path takes these
+    (2, 2, 4, 1504, 128, 3, [1500, 731]),        # ragged lengths inside 32-key units
+    (1, 8, 4, 1104, 128, 4, [1100]),             # 3 MSE bits
+    (1, 2, 6, 304, 128, 3, [300]),               # padded head quad
+    (1, 2, 4, 1000, 100, 2, [999]),              # d=100, 1 MSE bit
+    (3, 2, 4, 4104, 128, 3, [4100, 33, 0]),      # long, short and empty sequences in one launch
 ])
 def test_logits(B, Hkv, G, N, d, bits, lens, kernel_path):
     tq = _tq()
