@@ -45,13 +45,14 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kWorkers = 16;                      // warps 0..15
 constexpr int kProducerWarp = kWorkers;           // then one mma warp per bit vector
-constexpr long kWaitLimit = 1L << 24;
+constexpr int kSuspendNs = 20000;     // suspend-time hint of one try_wait
+constexpr int kWaitLimit = 1 << 16;   // tries before a wait gives up (bounded by ~1.3 s)
 
 template <int P>
 struct TcCfg {
     static constexpr int T = 1 << (P - 1);      // Walsh terms
     static constexpr int NV = T + 1;            // bit vectors per key (terms, then signs)
-    static constexpr int kSplit = P <= 2 ? 2 : 1;   // mma warps per bit vector (each its K share)
+    static constexpr int kSplit = 1;                // mma warps per bit vector (each its K share)
     static constexpr int NI = NV * kSplit;          // mma warps
     static constexpr int kThreads = (kWorkers + 1 + NI) * 32;
     static constexpr int kACols = NV * 32;      // A: NV x 4 words x 8 columns (4 e4m3 each)
@@ -102,13 +103,16 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// Waits for the phase with the given parity to complete.  Each try_wait may suspend the thread
+// for up to kSuspendNs (it resumes as soon as the phase completes), so waiting warps do not
+// spin on the issue slots; false after kWaitLimit tries (~1 s).
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-    for (long it = 0; it < kWaitLimit; ++it) {
+    for (int it = 0; it < kWaitLimit; ++it) {
         uint32_t done;
         asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity)
+            : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
             : "memory");
         if (done) return true;
     }
@@ -382,42 +386,69 @@ __device__ __forceinline__ void finish_group(const TcArgs& a, int g, int h, Fini
     F.cu = __ldg(cst + 12 + h);
 }
 
-// Logit of key `row` for head h from the tile's D blocks (column base d_tmem, this thread's lanes).
+// Finishing a tile is split so that its TMEM loads overlap other work: finish_load issues the
+// loads of the D blocks (head h, this thread's lanes), finish_store waits for them and writes the
+// logit of key `row`.
 template <int P>
-__device__ __forceinline__ void finish_tile(const TcArgs& a, const unsigned char* st, uint32_t d_tmem,
-                                            const Cursor& c, const FinishGroup& F, int row, int h) {
+struct FinishRegs {
+    float dm[TcCfg<P>::T * TcCfg<P>::kSplit][4];
+    float dq[TcCfg<P>::kSplit][4];
+};
+
+template <int P>
+__device__ __forceinline__ void finish_load(const TcArgs& a, uint32_t d_tmem, int h, FinishRegs<P>& R) {
+    using C = TcCfg<P>;
+    constexpr int T = C::T, KS = C::kSplit;
+#pragma unroll
+    for (int i = 0; i < T * KS; ++i) tmem_ld4(d_tmem + 16 * i + 4 * h, R.dm[i]);
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        if (a.prm.qjl) tmem_ld4(d_tmem + 16 * (T * KS + i) + 4 * h, R.dq[i]);
+        else R.dq[i][0] = R.dq[i][1] = R.dq[i][2] = R.dq[i][3] = 0.f;
+    }
+}
+
+template <int P>
+__device__ __forceinline__ void finish_store(const TcArgs& a, const unsigned char* st, FinishRegs<P>& R,
+                                             const Cursor& c, const FinishGroup& F, int row, int h) {
     using C = TcCfg<P>;
     constexpr int T = C::T, KS = C::kSplit;
     const bool qjl = a.prm.qjl != 0;
-    float dm[T * KS][4], dq[KS][4];
-#pragma unroll
-    for (int i = 0; i < T * KS; ++i) tmem_ld4(d_tmem + 16 * i + 4 * h, dm[i]);
-#pragma unroll
-    for (int i = 0; i < KS; ++i) {
-        if (qjl) tmem_ld4(d_tmem + 16 * (T * KS + i) + 4 * h, dq[i]);
-        else dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
-    }
+    const float n = half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[row]);
+    const float rho = qjl ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[row]) : 0.f;
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 1; i < T * KS; ++i)
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) dm[0][pc] += dm[i][pc];
+        for (int pc = 0; pc < 4; ++pc) R.dm[0][pc] += R.dm[i][pc];
 #pragma unroll
     for (int i = 1; i < KS; ++i)
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) dq[0][pc] += dq[i][pc];
-    const float n = half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[row]);
-    const float rho = qjl ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[row]) : 0.f;
+        for (int pc = 0; pc < 4; ++pc) R.dq[0][pc] += R.dq[i][pc];
     const int key = c.k0 + row;
     // pieces: sum_pc D[pc] 16^-pc, then the column scale 2^-e0
-    const float m = F.fm * fmaf(dm[0][3], 1.f / 4096.f, fmaf(dm[0][2], 1.f / 256.f, fmaf(dm[0][1], 1.f / 16.f, dm[0][0])));
+    const float m = F.fm * fmaf(R.dm[0][3], 1.f / 4096.f, fmaf(R.dm[0][2], 1.f / 256.f, fmaf(R.dm[0][1], 1.f / 16.f, R.dm[0][0])));
     float est = n * (F.cq + m);
     if (qjl) {
-        const float qv = F.fq * fmaf(dq[0][3], 1.f / 4096.f, fmaf(dq[0][2], 1.f / 256.f, fmaf(dq[0][1], 1.f / 16.f, dq[0][0])));
+        const float qv =
+            F.fq * fmaf(R.dq[0][3], 1.f / 4096.f, fmaf(R.dq[0][2], 1.f / 256.f, fmaf(R.dq[0][1], 1.f / 16.f, R.dq[0][0])));
         est = fmaf(rho, fmaf(2.f * a.prm.qjl_scale, qv, F.cu), est);
     }
     if (key < c.L && h < F.nh) a.logits[(F.qrow0 + h) * (size_t)a.k.cap + key] = a.scale * est;
 }
+
+// Position in a ring of N slots: slot and the parity of its current use.
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 struct Shared {
     uint64_t full[TcCfg<1>::kMaxStages], empty[TcCfg<1>::kMaxStages];
@@ -477,19 +508,24 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
     if (warp == kProducerWarp) {
         if (lane == 0) {
             Cursor c = seek(a, lo);
+            Ring<C::kStages> r;
             int64_t t = 0;
             for (; t < n && !aborted(S); ++t) {
-                const int s = (int)(t % C::kStages);
-                if (t >= C::kStages && !bar_wait(&S.empty[s], (uint32_t)(((t / C::kStages) - 1) & 1))) {
+                // a stage's previous tile must be finished (its empty phase) before the refill
+                if (t >= C::kStages && !bar_wait(&S.empty[r.slot], r.phase ^ 1u)) {
                     abort_all(S, a.err);
                     break;
                 }
-                issue_tile<P>(a, c, sm + s * C::kStageBytes, &S.full[s]);
+                issue_tile<P>(a, c, sm + r.slot * C::kStageBytes, &S.full[r.slot]);
                 next_tile(a, c);
+                r.advance();
             }
             // let every copy issued land before the CTA can leave (the last one of each stage)
-            for (int64_t u = t - C::kStages > 0 ? t - C::kStages : 0; u < t; ++u)
-                drained &= bar_wait(&S.full[u % C::kStages], (uint32_t)((u / C::kStages) & 1));
+            for (int k = 0; k < C::kStages && k < t; ++k) {
+                // stage r.slot - 1 - k holds tile t - 1 - k; its full phase is that tile's use
+                const int64_t u = t - 1 - k;
+                drained &= bar_wait(&S.full[(int)(u % C::kStages)], (uint32_t)((u / C::kStages) & 1));
+            }
         }
     } else if (warp > kProducerWarp) {
         const int w = warp - kProducerWarp - 1;   // mma warp: bit vector v, K share kh
@@ -501,8 +537,9 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
             const bool active = v < C::T || a.prm.qjl;
             uint64_t bd[4];
             b_descs<P>(v, kh, smem_u32(img_buf), bd);   // the B buffer is fixed; its contents follow the group
-            for (int64_t i = 0; i < n && !aborted(S); ++i) {
-                const int b = (int)(i % C::kNB);
+            Ring<C::kNB> rb;
+            for (int64_t i = 0; i < n && !aborted(S); ++i, rb.advance()) {
+                const int b = rb.slot;
                 if (c.g != cur_group) {
                     // every mma warp drains (its mma read the old B), the first one reloads B
                     bool ok = true;
@@ -525,7 +562,7 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
                     cur_group = c.g;
                     ++nswitch;
                 }
-                if (!bar_wait(&S.a_ready[b], (uint32_t)((i / C::kNB) & 1))) {
+                if (!bar_wait(&S.a_ready[b], rb.phase)) {
                     abort_all(S, a.err);
                     break;
                 }
@@ -549,42 +586,53 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
         Cursor ce = seek(a, lo), cf = ce;
         FinishGroup F;
         F.g = -1;
+        FinishRegs<P> R;
+        Ring<C::kStages> se, sf;   // stages of the expanded and of the finished tile
+        Ring<C::kNB> be, bf;       // TMEM buffers of the expanded and of the finished tile
         for (int64_t i = 0; i < n + C::kLag; ++i) {
             if (aborted(S)) break;
-            if (i < n) {
-                const int s = (int)(i % C::kStages), b = (int)(i % C::kNB);
-                bool okw = bar_wait(&S.full[s], (uint32_t)((i / C::kStages) & 1));
-                if (okw && i >= C::kNB) okw = bar_wait(&S.buf_free[b], (uint32_t)(((i / C::kNB) - 1) & 1));
+            const bool do_e = i < n, do_f = i >= C::kLag;
+            // expand tile i: loads, ALU and TMEM stores issued, completion awaited further down
+            if (do_e) {
+                bool okw = bar_wait(&S.full[se.slot], se.phase);
+                if (okw && i >= C::kNB) okw = bar_wait(&S.buf_free[be.slot], be.phase ^ 1u);
                 if (!okw) {
                     abort_all(S, a.err);
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;");
-                expand_tile<P>(a, sm + s * C::kStageBytes, tmem + lane_off + b * C::kBufCols, row, part);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;");
-                __syncwarp();
-                if (lane == 0) bar_arrive(&S.a_ready[b]);
-                next_tile(a, ce);
+                expand_tile<P>(a, sm + se.slot * C::kStageBytes, tmem + lane_off + be.slot * C::kBufCols, row, part);
             }
-            if (i >= C::kLag) {
-                const int64_t j = i - C::kLag;
-                const int s = (int)(j % C::kStages), b = (int)(j % C::kNB);
-                if (!bar_wait(&S.d_full[b], (uint32_t)((j / C::kNB) & 1))) {
+            // finish tile i - kLag: its TMEM loads go out while the stores above drain
+            if (do_f) {
+                if (!bar_wait(&S.d_full[bf.slot], bf.phase)) {
                     abort_all(S, a.err);
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;");
+                finish_load<P>(a, tmem + lane_off + bf.slot * C::kBufCols + C::kACols, part, R);
+            }
+            if (do_e) {
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;");
+                __syncwarp();
+                if (lane == 0) bar_arrive(&S.a_ready[be.slot]);
+                next_tile(a, ce);
+                se.advance();
+                be.advance();
+            }
+            if (do_f) {
                 if (cf.g != F.g) finish_group<P>(a, cf.g, part, F);
-                finish_tile<P>(a, sm + s * C::kStageBytes, tmem + lane_off + b * C::kBufCols + C::kACols, cf, F, row,
-                               part);
+                finish_store<P>(a, sm + sf.slot * C::kStageBytes, R, cf, F, row, part);
                 asm volatile("tcgen05.fence::before_thread_sync;");
                 __syncwarp();
                 if (lane == 0) {
-                    bar_arrive(&S.buf_free[b]);
-                    bar_arrive(&S.empty[s]);
+                    bar_arrive(&S.buf_free[bf.slot]);
+                    bar_arrive(&S.empty[sf.slot]);
                 }
                 next_tile(a, cf);
+                sf.advance();
+                bf.advance();
             }
         }
     }
