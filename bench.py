@@ -18,6 +18,7 @@ Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a bound
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -52,6 +53,29 @@ def set_batch(b: int) -> None:
     if b != B:
         WORKLOAD = WORKLOAD.replace("batch 8", f"batch {b}")
         B = b
+
+
+# DRAM traffic of the decode kernels from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum; batch 2 of the same workload, one launch each, scaled to a launch here by
+# the keys it scores).  A figure is reported only while the sources it was taken on are unchanged.
+NCU_SOURCES = ["k_attn.cu", "lut.cuh", "values.cuh", "tq_device.cuh", "tq_internal.h"]
+NCU_SOURCES_SHA = "0c95f55db90e1e6c"
+NCU_BYTES_PER_KEY = {
+    # values_coded128_kernel<3>: 138.434 MB read + 3.087 MB written, 2 x 8 x 131071 keys
+    "attn_values": (138.434304e6 + 3.087360e6) / (2 * 8 * 131071),
+    # logits_q8_kernel<2>: dram__bytes.sum.per_second x duration = 1.550616 TB/s x 80.096 us
+    "attn_logits": 1.550616e12 * 80.096e-6 / (2 * 8 * 131071),
+}
+
+
+def ncu_traffic(kernel: str, keys: float):
+    h = hashlib.sha256()
+    for f in NCU_SOURCES:
+        with open(os.path.join(ROOT, "compressed_kv_cache_02_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != NCU_SOURCES_SHA or kernel not in NCU_BYTES_PER_KEY:
+        return None
+    return NCU_BYTES_PER_KEY[kernel] * keys
 
 
 def peaks():
@@ -285,7 +309,10 @@ def run_tq(args, world, rank, local):
                    "kernel_path": args.kernel_path,
                    "l2": "inputs larger than L2 (cache codes ~0.9 GB)"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": dom_gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs", "traffic": None},
+                     "frac": dom_gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": (ncu_traffic(dominant, statistics.mean(lens_timed) * B * HKV)
+                                 if args.kernel_path == "auto" else None),
+                     "traffic_unit": "bytes per launch (ncu, scaled from batch 2)"},
         "kernels": {
             "attn_logits": {"ms": statistics.mean(t_logits) * 1e3, "GB_s": gbs_logits,
                             "bytes_per_key": LOGIT_BYTES, "frac_of_measured": gbs_logits / hbm,

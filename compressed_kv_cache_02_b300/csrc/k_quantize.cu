@@ -16,7 +16,6 @@ namespace tq {
 namespace {
 
 constexpr int kApplyRows = 8;     // input rows per CTA in apply_rows_kernel
-constexpr int kQuantRows = 16;    // vectors per CTA in quantize_kernel
 constexpr int kQuantThreads = 256;
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -73,10 +72,13 @@ struct QuantArgs {
     int* err;
 };
 
-// One CTA codes kQuantRows vectors.  Shared memory: the input tile and the residual tile,
-// both stored [coordinate][vector] so the matrix-vector loops read 16 vectors per j with
-// four 16-byte broadcasts.
+// One CTA codes kQuantRows vectors (16 for bulk inputs, 4 for the few vectors of a decode
+// append, which then spread over more SMs).  Shared memory: the input tile and the residual
+// tile, both stored [coordinate][vector] so the matrix-vector loops read kQuantRows vectors
+// per j with 16-byte broadcasts.
+template <int kQuantRows>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs a) {
+    static_assert(kQuantRows % 4 == 0, "rows are read four at a time");
     extern __shared__ float4 sm4[];
     const Params& prm = a.prm;
     const int d = prm.d, m = prm.m;
@@ -153,8 +155,11 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
         for (int v = 0; v < kQuantRows; ++v) {
             const float n = s_n[v];
             const float u = (n > 0.f) ? acc[v] / n : 0.f;
+            // #{k : t_k < u} by binary search over the sorted thresholds
             int idx = 0;
-            for (int k = 0; k < prm.L - 1; ++k) idx += (u > prm.thresholds[k]) ? 1 : 0;
+#pragma unroll
+            for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
+                if (b < prm.P && u > prm.thresholds[idx + (1 << b) - 1]) idx += 1 << b;
             if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * prm.centroids[idx];
             const long long row = s_row[v];
             for (int p = 0; p < prm.P; ++p) {
@@ -265,11 +270,16 @@ cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n
     a.norm = norm;
     a.rnorm = rnorm;
     a.err = c->derr;
-    const size_t smem = 2ull * c->d * kQuantRows * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // 16 rows per CTA once that fills the SMs twice over, else 4 (decode appends)
+    const bool bulk = n >= 2 * 148 * 16;
+    const int rows = bulk ? 16 : 4;
+    const size_t smem = 2ull * c->d * rows * sizeof(float);
+    cudaError_t e = bulk ? cudaFuncSetAttribute(quantize_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                         : cudaFuncSetAttribute(quantize_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned blocks = (unsigned)((n + kQuantRows - 1) / kQuantRows);
-    quantize_kernel<<<blocks, kQuantThreads, smem, s>>>(a);
+    const unsigned blocks = (unsigned)((n + rows - 1) / rows);
+    if (bulk) quantize_kernel<16><<<blocks, kQuantThreads, smem, s>>>(a);
+    else quantize_kernel<4><<<blocks, kQuantThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = s_tmem;
     const uint32_t tmem_row = tmem + ((uint32_t)(32 * q) << 16);
-    const int nthr = prm.L - 1;
     uint32_t phase = 0;
     bool ok = true;
 
@@ -220,10 +219,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         const float n16 = half_bits_to_float(float_to_half_bits(nrm));
         const int64_t grow = r0 + row;
         const bool valid = row < nvalid;
-        // idx = #{k : t_k < y / n}; compared as t_k n < y (n > 0), or all u = 0 when n = 0
-        float tn[kMaxLevels];
-#pragma unroll
-        for (int k = 0; k < kMaxLevels - 1; ++k) tn[k] = prm.thresholds[k] * nrm;
+        // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (P steps, the step
+        // for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
+        const float nv = nrm > 0.f ? nrm : 1.f;
         uint32_t pw[TQ_MAX_MSE_BITS] = {};
         float rs = 0.f;
 #pragma unroll
@@ -231,10 +229,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
             const float yc = nrm > 0.f ? y[c] : 0.f;
             int idx = 0;
 #pragma unroll
-            for (int k = 0; k < kMaxLevels - 1; ++k)
-                if (k < nthr) idx += (nrm > 0.f ? yc > tn[k] : 0.f > prm.thresholds[k]) ? 1 : 0;
-#pragma unroll
-            for (int p = 0; p < TQ_MAX_MSE_BITS; ++p) pw[p] |= (uint32_t)((idx >> p) & 1) << c;
+            for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
+                if (b < prm.P) {
+                    const bool up = yc > prm.thresholds[idx + (1 << b) - 1] * nv;
+                    idx += up ? (1 << b) : 0;
+                    pw[b] |= (up ? 1u : 0u) << c;
+                }
             const float r = y[c] - n16 * prm.centroids[idx];
             y[c] = r;
             rs = fmaf(r, r, rs);
