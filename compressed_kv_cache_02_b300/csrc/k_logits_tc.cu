@@ -21,21 +21,24 @@
 //   tc_image_kernel, with the epilogue constants, and copied into shared memory per CTA.
 // D (fp32, TMEM): 16 columns per mma warp; the MSE blocks sum, and so do the QJL ones.
 //
-// One CTA per SM owns a contiguous range of 128-key tiles and runs them through a pipeline of
-// specialised warps that meet only at mbarriers (all waits bounded; a timeout sets
-// TQ_DEVERR_TIMEOUT and stops every role):
-//   producer warp  bulk asynchronous copies of each tile's fields (planes, signs, norms,
-//                  residual norms; lengths rounded up to 8 keys, inside the cache since its
-//                  capacity is a multiple of 8) into a ring of shared-memory stages;
-//   16 worker warps warp w expands word w / 4 of every bit vector of keys 32 (w % 4) .. + 31
-//                  (its TMEM lanes) into the tile's A buffer, and kLag tiles later finishes
-//                  head w / 4 of those keys from D (fp32) into logits;
-//   mma warps      kSplit warps per bit vector, each issuing its share of the vector's 4
-//                  tcgen05.mma (K = 32 each) into its own 16 D columns and committing (a single
-//                  thread spends ~70 cycles per mma issue, so the issue is spread over warps); at a
-//                  group change they drain their mma and the first loads the group's B.
-// TMEM holds kNB tile buffers (A and D), so expansion, mma and the epilogue of different tiles
-// overlap.
+// One CTA per SM owns a contiguous range of 128-key tiles.  Tile i goes to worker group i % 4;
+// the groups run independently and meet the shared producer only at mbarriers (every wait is
+// bounded; a timeout sets TQ_DEVERR_TIMEOUT and stops every role):
+//   per group (128 TMEM columns: two 32-column A slots and two 32-column D buffers, and a
+//   ring of shared-memory stages)
+//     4 worker warps  warp q owns keys 32 q .. 32 q + 31 of the group's tiles (its TMEM lanes):
+//                  it expands the tile's bit vectors one at a time into the next free A slot,
+//                  then finishes the group's previous tile from its D buffer into logits;
+//     1 mma warp   bulk asynchronous copies of the group's tiles (one per field: planes, signs,
+//                  norms, residual norms; lengths rounded up to 8 keys, inside the cache since
+//                  its capacity is a multiple of 8) into the stage ring, refilling a stage once
+//                  the workers have released the tile two back (its D buffer, hence its stage);
+//                  per bit vector 4 tcgen05.mma (K = 32) from the slot into the tile's D (16
+//                  MSE columns, the T terms accumulating, and 16 QJL columns), a commit that
+//                  frees the slot when they complete, and per tile a commit that fills D.
+//                  Issue costs its thread ~70 cycles per mma, so four groups issue in parallel.
+//                  At a change of (batch, KV head, quad) it drains its mma and loads the
+//                  group's B image into its own buffer.
 #include "mma_e4m3.cuh"
 #include "tq_kernels.h"
 
@@ -43,8 +46,11 @@ namespace tq {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kWorkers = 16;                      // warps 0..15
-constexpr int kProducerWarp = kWorkers;           // then one mma warp per bit vector
+constexpr int kGroups = 4;                        // worker groups (tiles in flight x2)
+constexpr int kWorkerWarps = 4 * kGroups;         // warps 0..15: group w / 4, lanes 32 (w % 4)
+constexpr int kMmaWarp0 = kWorkerWarps;           // warps 16..19: the groups' mma (and copy) warps
+constexpr int kThreads = (kMmaWarp0 + kGroups) * 32;
+constexpr int kGroupCols = 128;                   // TMEM columns per group
 constexpr int kSuspendNs = 20000;     // suspend-time hint of one try_wait
 constexpr int kWaitLimit = 1 << 16;   // tries before a wait gives up (bounded by ~1.3 s)
 
@@ -52,32 +58,23 @@ template <int P>
 struct TcCfg {
     static constexpr int T = 1 << (P - 1);      // Walsh terms
     static constexpr int NV = T + 1;            // bit vectors per key (terms, then signs)
-    static constexpr int kSplit = 1;                // mma warps per bit vector (each its K share)
-    static constexpr int NI = NV * kSplit;          // mma warps
-    static constexpr int kThreads = (kWorkers + 1 + NI) * 32;
-    static constexpr int kACols = NV * 32;      // A: NV x 4 words x 8 columns (4 e4m3 each)
-    static constexpr int kDCols = NI * 16;      // D: 16 columns per mma warp
-    static constexpr int kBufCols = kACols + kDCols;
-    static constexpr int kNB = 512 / kBufCols >= 4 ? 4 : 512 / kBufCols;   // TMEM tile buffers
-    static constexpr int kLag = kNB - 1;        // tiles between a tile's expansion and its finish
     static constexpr int kSignOff = kTile * P * 16;
     static constexpr int kNormOff = kSignOff + kTile * 16;
     static constexpr int kRnormOff = kNormOff + kTile * 2;
     static constexpr int kStageBytes = kRnormOff + kTile * 2;
-    // enough stages to fill more than half of shared memory: one CTA (and its 512 TMEM
-    // columns) per SM
-    static constexpr int kStages = (120 * 1024 + kStageBytes - 1) / kStageBytes;
     static constexpr int kBmBytes = 16 * T * 128;   // MSE B: 16 columns x T*128 k
     static constexpr int kBqBytes = 16 * 128;       // QJL B: 16 columns x 128 k
     static constexpr int kConstOff = kBmBytes + kBqBytes;
     static constexpr int kImgBytes = (kConstOff + 64 + 127) / 128 * 128;
-    static constexpr int kImgOff = kStages * kStageBytes;
-    static constexpr int kSmem = kImgOff + kImgBytes;
+    static constexpr int kMaxStages = 8;        // per group
+    // each group's stage ring fills its share of what the images leave of ~200 KB (one CTA and
+    // its 512 TMEM columns per SM)
+    static constexpr int kStagesFit = (200 * 1024 - kGroups * kImgBytes) / (kGroups * kStageBytes);
+    static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
+    static constexpr int kImgOff = kGroups * kStages * kStageBytes;
+    static constexpr int kSmem = kImgOff + kGroups * kImgBytes;
     static_assert(kStageBytes % 128 == 0, "stage alignment");
-    static_assert(kNB >= 2 && kNB * kBufCols <= 512, "TMEM budget");
-    static_assert(kLag < kStages, "the producer must run ahead of the finish");
-    static constexpr int kMaxStages = 32;
-    static_assert(kStages <= kMaxStages, "barrier array");
+    static_assert(kStages >= 3, "the producer must run ahead of the finish");
 };
 
 struct TcArgs {
@@ -145,14 +142,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
-}
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-    uint32_t r[4];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(r[j]);
 }
 __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -317,143 +306,131 @@ __global__ void __launch_bounds__(128) tc_image_kernel(const TcArgs a) {
 
 // ------------------------------------------------------------------ scoring
 
-// Word wd of every bit vector of key `row` into A (the thread's TMEM lanes, column base a_tmem).
+// The tile's bit vectors of key `row`: the T Walsh terms (XOR of their planes), then the signs.
 template <int P>
-__device__ __forceinline__ void expand_tile(const TcArgs& a, const unsigned char* st, uint32_t a_tmem, int row,
-                                            int wd) {
+__device__ __forceinline__ void load_vectors(const unsigned char* st, int row, bool qjl, uint4 (&x)[TcCfg<P>::NV]) {
     using C = TcCfg<P>;
     constexpr int T = C::T;
-    uint32_t pw[P];
+    uint4 pl[P];
 #pragma unroll
-    for (int p = 0; p < P; ++p) pw[p] = *reinterpret_cast<const uint32_t*>(st + row * (P * 16) + p * 16 + wd * 4);
+    for (int p = 0; p < P; ++p) pl[p] = *reinterpret_cast<const uint4*>(st + row * (P * 16) + p * 16);
 #pragma unroll
     for (int v = 0; v < T; ++v) {
-        uint32_t x = 0u;
+        x[v] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int p = 0; p < P; ++p)
-            if ((odd_mask(v) >> p) & 1) x ^= pw[p];
-        uint32_t r[8];
-        expand_word(x, r);
-        tmem_st8(a_tmem + (v * 4 + wd) * 8, r);
+            if ((odd_mask(v) >> p) & 1) {
+                x[v].x ^= pl[p].x;
+                x[v].y ^= pl[p].y;
+                x[v].z ^= pl[p].z;
+                x[v].w ^= pl[p].w;
+            }
     }
-    if (a.prm.qjl) {
-        uint32_t r[8];
-        expand_word(*reinterpret_cast<const uint32_t*>(st + C::kSignOff + row * 16 + wd * 4), r);
-        tmem_st8(a_tmem + (T * 4 + wd) * 8, r);
-    }
+    x[T] = qjl ? *reinterpret_cast<const uint4*>(st + C::kSignOff + row * 16) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Shared-memory descriptors of the B blocks read by mma warp (v, kh): K-steps wd of its share.
-template <int P>
-__device__ __forceinline__ void b_descs(int v, int kh, uint32_t bimg, uint64_t (&bd)[4]) {
-    using C = TcCfg<P>;
-    constexpr int T = C::T;
-    const uint32_t bsrc = v < T ? bimg + v * 4 * 256 : bimg + C::kBmBytes;
-    const uint32_t sbo = v < T ? T * 128 * 8 : 128 * 8;
-#pragma unroll
-    for (int k = 0; k < 4 / C::kSplit; ++k) bd[k] = smem_desc(bsrc + (kh * (4 / C::kSplit) + k) * 256, sbo);
+// One bit vector into the 32 columns of an A slot: word wd -> columns 8 wd .. 8 wd + 7.
+__device__ __forceinline__ void expand_vector(const uint4& x, uint32_t slot_tmem) {
+    uint32_t r[8];
+    expand_word(x.x, r);
+    tmem_st8(slot_tmem, r);
+    expand_word(x.y, r);
+    tmem_st8(slot_tmem + 8, r);
+    expand_word(x.z, r);
+    tmem_st8(slot_tmem + 16, r);
+    expand_word(x.w, r);
+    tmem_st8(slot_tmem + 24, r);
 }
 
-// The mma of warp (v, kh) for one tile buffer: A columns of vector v, its D block.
-template <int P>
-__device__ __forceinline__ void issue_share(int v, int kh, uint32_t buf_tmem, const uint64_t (&bd)[4]) {
-    using C = TcCfg<P>;
-    constexpr int K = 4 / C::kSplit;
-    const uint32_t d = buf_tmem + C::kACols + 16 * (v * C::kSplit + kh);
-#pragma unroll
-    for (int k = 0; k < K; ++k) mma_ts(d, buf_tmem + (v * 4 + kh * K + k) * 8, bd[k], k ? 1u : 0u);
-}
-
-// Logit of key `row` for head h of the tile's quad, from D (column base d_tmem, this thread's lanes).
-// Per-group values a worker needs to finish tiles of head h.
+// Per-group values a worker needs to finish tiles.
 struct FinishGroup {
     int g, nh;
     size_t qrow0;
-    float fm, fq, cq, cu;   // 2^-e0 (MSE, QJL), c0 sum q', -kq sum u
+    const float4* c;   // 2^-e0 (MSE) x4, 2^-e0 (QJL) x4, c0 sum q' x4, -kq sum u x4 (shared memory)
 };
 
+// Called by a whole warp: the group's position and its 16 epilogue constants into the warp's
+// own shared-memory slot.
 template <int P>
-__device__ __forceinline__ void finish_group(const TcArgs& a, int g, int h, FinishGroup& F) {
+__device__ __forceinline__ void finish_group(const TcArgs& a, int g, float* warp_cst, FinishGroup& F) {
     using C = TcCfg<P>;
     const GroupPos gp = group_pos(a, g);
-    const float* cst = reinterpret_cast<const float*>(a.img + (size_t)g * C::kImgBytes + C::kConstOff);
     F.g = g;
     F.nh = gp.nh;
     F.qrow0 = gp.qrow0;
-    F.fm = __ldg(cst + h);
-    F.fq = __ldg(cst + 4 + h);
-    F.cq = __ldg(cst + 8 + h);
-    F.cu = __ldg(cst + 12 + h);
+    const int lane = threadIdx.x & 31;
+    __syncwarp();   // every lane is done with the previous group's constants
+    if (lane < 16) warp_cst[lane] = __ldg(reinterpret_cast<const float*>(a.img + (size_t)g * C::kImgBytes + C::kConstOff) + lane);
+    __syncwarp();
+    F.c = reinterpret_cast<const float4*>(warp_cst);
 }
 
-// Finishing a tile is split so that its TMEM loads overlap other work: finish_load issues the
-// loads of the D blocks (head h, this thread's lanes), finish_store waits for them and writes the
-// logit of key `row`.
-template <int P>
-struct FinishRegs {
-    float dm[TcCfg<P>::T * TcCfg<P>::kSplit][4];
-    float dq[TcCfg<P>::kSplit][4];
-};
-
-template <int P>
-__device__ __forceinline__ void finish_load(const TcArgs& a, uint32_t d_tmem, int h, FinishRegs<P>& R) {
-    using C = TcCfg<P>;
-    constexpr int T = C::T, KS = C::kSplit;
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < T * KS; ++i) tmem_ld4(d_tmem + 16 * i + 4 * h, R.dm[i]);
-#pragma unroll
-    for (int i = 0; i < KS; ++i) {
-        if (a.prm.qjl) tmem_ld4(d_tmem + 16 * (T * KS + i) + 4 * h, R.dq[i]);
-        else R.dq[i][0] = R.dq[i][1] = R.dq[i][2] = R.dq[i][3] = 0.f;
-    }
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Logits of key `row` for the 4 heads of the tile's quad from its D buffer.
 template <int P>
-__device__ __forceinline__ void finish_store(const TcArgs& a, const unsigned char* st, FinishRegs<P>& R,
-                                             const Cursor& c, const FinishGroup& F, int row, int h) {
+__device__ __forceinline__ void finish_tile(const TcArgs& a, const unsigned char* st, uint32_t d_tmem,
+                                            const Cursor& c, const FinishGroup& F, int row) {
     using C = TcCfg<P>;
-    constexpr int T = C::T, KS = C::kSplit;
     const bool qjl = a.prm.qjl != 0;
+    float dm[16], dq[16];
+    tmem_ld16(d_tmem, dm);
+    if (qjl) tmem_ld16(d_tmem + 16, dq);
     const float n = half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[row]);
     const float rho = qjl ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[row]) : 0.f;
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 1; i < T * KS; ++i)
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) R.dm[0][pc] += R.dm[i][pc];
-#pragma unroll
-    for (int i = 1; i < KS; ++i)
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) R.dq[0][pc] += R.dq[i][pc];
     const int key = c.k0 + row;
-    // pieces: sum_pc D[pc] 16^-pc, then the column scale 2^-e0
-    const float m = F.fm * fmaf(R.dm[0][3], 1.f / 4096.f, fmaf(R.dm[0][2], 1.f / 256.f, fmaf(R.dm[0][1], 1.f / 16.f, R.dm[0][0])));
-    float est = n * (F.cq + m);
-    if (qjl) {
-        const float qv =
-            F.fq * fmaf(R.dq[0][3], 1.f / 4096.f, fmaf(R.dq[0][2], 1.f / 256.f, fmaf(R.dq[0][1], 1.f / 16.f, R.dq[0][0])));
-        est = fmaf(rho, fmaf(2.f * a.prm.qjl_scale, qv, F.cu), est);
+    if (key >= c.L) return;
+    const float k2 = 2.f * a.prm.qjl_scale;
+    const float4 fm4 = F.c[0], fq4 = F.c[1], cq4 = F.c[2], cu4 = F.c[3];
+    const float fm[4] = {fm4.x, fm4.y, fm4.z, fm4.w}, fq[4] = {fq4.x, fq4.y, fq4.z, fq4.w};
+    const float cq[4] = {cq4.x, cq4.y, cq4.z, cq4.w}, cu[4] = {cu4.x, cu4.y, cu4.z, cu4.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        // pieces: sum_pc D[pc] 16^-pc, then the column scale 2^-e0
+        const float m = fm[h] * fmaf(dm[4 * h + 3], 1.f / 4096.f,
+                                     fmaf(dm[4 * h + 2], 1.f / 256.f, fmaf(dm[4 * h + 1], 1.f / 16.f, dm[4 * h])));
+        float est = n * (cq[h] + m);
+        if (qjl) {
+            const float qv = fq[h] * fmaf(dq[4 * h + 3], 1.f / 4096.f,
+                                          fmaf(dq[4 * h + 2], 1.f / 256.f, fmaf(dq[4 * h + 1], 1.f / 16.f, dq[4 * h])));
+            est = fmaf(rho, fmaf(k2, qv, cu[h]), est);
+        }
+        if (h < F.nh) a.logits[(F.qrow0 + h) * (size_t)a.k.cap + key] = a.scale * est;
     }
-    if (key < c.L && h < F.nh) a.logits[(F.qrow0 + h) * (size_t)a.k.cap + key] = a.scale * est;
 }
 
-// Position in a ring of N slots: slot and the parity of its current use.
+// Position in a ring of N slots: slot and the parity of its current use; `step` slots per move.
 template <int N>
 struct Ring {
     int slot = 0;
     uint32_t phase = 0;
-    __device__ __forceinline__ void advance() {
-        if (++slot == N) {
-            slot = 0;
+    __device__ __forceinline__ void advance(int step = 1) {
+        slot += step;
+        if (slot >= N) {
+            slot -= N;
             phase ^= 1u;
         }
     }
 };
 
+struct Group {
+    uint64_t full[8];   // the group's stage ring
+    uint64_t slot_ready[2], slot_free[2], d_full[2], d_free[2], img_bar, drain_bar;
+};
+
 struct Shared {
-    uint64_t full[TcCfg<1>::kMaxStages], empty[TcCfg<1>::kMaxStages];
-    uint64_t a_ready[4], d_full[4], buf_free[4];
-    uint64_t img_bar, drained, drain[16];
+    Group grp[kGroups];
+    float cst[kWorkerWarps][16];   // per worker warp: the epilogue constants of its current group
     uint32_t tmem;
     int abort;
 };
@@ -465,8 +442,9 @@ __device__ __forceinline__ void abort_all(Shared& S, int* err) {
 }
 
 template <int P>
-__global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(const TcArgs a) {
     using C = TcCfg<P>;
+    constexpr int T = C::T;
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ __align__(8) Shared S;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -477,25 +455,26 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
     for (int g = 0; g < a.ngroups; ++g) total += (group_len(a, g) + kTile - 1) / kTile;
     const int64_t lo = total * blockIdx.x / gridDim.x, hi = total * (blockIdx.x + 1) / gridDim.x, n = hi - lo;
     if (n <= 0) return;   // uniform over the CTA, before any allocation
+    const bool qjl = a.prm.qjl != 0;
+    const int nv = qjl ? C::NV : T;   // bit vectors scored per key
 
-    unsigned char* img_buf = sm + C::kImgOff;
     if (tid == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            bar_init_n(&S.full[s], 1);
-            bar_init_n(&S.empty[s], kWorkers);
+        for (int g = 0; g < kGroups; ++g) {
+            Group& G = S.grp[g];
+            for (int s = 0; s < C::kStages; ++s) bar_init_n(&G.full[s], 1);
+            for (int k = 0; k < 2; ++k) {
+                bar_init_n(&G.slot_ready[k], 4);
+                bar_init_n(&G.slot_free[k], 1);
+                bar_init_n(&G.d_full[k], 1);
+                bar_init_n(&G.d_free[k], 4);
+            }
+            bar_init_n(&G.img_bar, 1);
+            bar_init_n(&G.drain_bar, 1);
         }
-        for (int b = 0; b < C::kNB; ++b) {
-            bar_init_n(&S.a_ready[b], kWorkers);
-            bar_init_n(&S.d_full[b], C::NI);
-            bar_init_n(&S.buf_free[b], kWorkers);
-        }
-        bar_init_n(&S.img_bar, 1);
-        bar_init_n(&S.drained, C::NI);
-        for (int v = 0; v < C::NI; ++v) bar_init_n(&S.drain[v], 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kProducerWarp + 1) {
+    if (warp == kMmaWarp0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&S.tmem)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
@@ -505,134 +484,159 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
     const uint32_t tmem = S.tmem;
     bool drained = true;
 
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
-            Cursor c = seek(a, lo);
-            Ring<C::kStages> r;
-            int64_t t = 0;
-            for (; t < n && !aborted(S); ++t) {
-                // a stage's previous tile must be finished (its empty phase) before the refill
-                if (t >= C::kStages && !bar_wait(&S.empty[r.slot], r.phase ^ 1u)) {
-                    abort_all(S, a.err);
-                    break;
-                }
-                issue_tile<P>(a, c, sm + r.slot * C::kStageBytes, &S.full[r.slot]);
-                next_tile(a, c);
-                r.advance();
-            }
-            // let every copy issued land before the CTA can leave (the last one of each stage)
-            for (int k = 0; k < C::kStages && k < t; ++k) {
-                // stage r.slot - 1 - k holds tile t - 1 - k; its full phase is that tile's use
-                const int64_t u = t - 1 - k;
-                drained &= bar_wait(&S.full[(int)(u % C::kStages)], (uint32_t)((u / C::kStages) & 1));
-            }
-        }
-    } else if (warp > kProducerWarp) {
-        const int w = warp - kProducerWarp - 1;   // mma warp: bit vector v, K share kh
-        const int v = w / C::kSplit, kh = w % C::kSplit;
-        if (lane == 0) {
-            Cursor c = seek(a, lo);
-            int cur_group = -1, nswitch = 0, ndrain = 0;
+    if (warp >= kMmaWarp0) {
+        const int g = warp - kMmaWarp0;
+        Group& G = S.grp[g];
+        if (lane == 0 && g < n) {
+            Cursor c = seek(a, lo + g);
+            unsigned char* img = sm + C::kImgOff + g * C::kImgBytes;
+            const uint32_t bimg = smem_u32(img);
+            const uint32_t base = tmem + g * kGroupCols;
+            // B descriptors: the buffer is fixed (its contents follow the group); a K step of 32
+            // bytes is +256 B of start address, +16 in the descriptor's 16-byte address field
+            const uint64_t bm0 = smem_desc(bimg, T * 128 * 8), bq0 = smem_desc(bimg + C::kBmBytes, 128 * 8);
+            int cur_group = -1, nimg = 0, ndrain = 0;
             bool issued_any = false;
-            const bool active = v < C::T || a.prm.qjl;
-            uint64_t bd[4];
-            b_descs<P>(v, kh, smem_u32(img_buf), bd);   // the B buffer is fixed; its contents follow the group
-            Ring<C::kNB> rb;
-            for (int64_t i = 0; i < n && !aborted(S); ++i, rb.advance()) {
-                const int b = rb.slot;
-                if (c.g != cur_group) {
-                    // every mma warp drains (its mma read the old B), the first one reloads B
+            Ring<2> sa, db;
+            // copies: the group's first kStages tiles now, then one refill per tile
+            unsigned char* ring = sm + g * C::kStages * C::kStageBytes;
+            const int64_t ntiles = (n - g + kGroups - 1) / kGroups;
+            Cursor cp = c;
+            Ring<C::kStages> rp;
+            int64_t copied = 0;
+            for (; copied < ntiles && copied < C::kStages; ++copied) {
+                issue_tile<P>(a, cp, ring + rp.slot * C::kStageBytes, &G.full[rp.slot]);
+                for (int s = 0; s < kGroups; ++s) next_tile(a, cp);
+                rp.advance();
+            }
+            int64_t k = 0;   // the group's tile count
+            for (int64_t i = g; i < n && !aborted(S); i += kGroups, ++k) {
+                if (c.g != cur_group) {   // drain the mma that read the old B, then load this group's
                     bool ok = true;
-                    if (nswitch > 0) {
-                        if (issued_any) {
-                            mma_commit(&S.drain[w]);
-                            ok = bar_wait(&S.drain[w], (uint32_t)(ndrain++ & 1));
-                        }
-                        bar_arrive(&S.drained);
-                        if (ok && w == 0) ok = bar_wait(&S.drained, (uint32_t)((nswitch - 1) & 1));
+                    if (issued_any) {
+                        mma_commit(&G.drain_bar);
+                        ok = bar_wait(&G.drain_bar, (uint32_t)(ndrain++ & 1));
                     }
-                    if (ok && w == 0) {
-                        bar_expect_tx(&S.img_bar, C::kImgBytes);
-                        bulk_copy(img_buf, a.img + (size_t)c.g * C::kImgBytes, C::kImgBytes, &S.img_bar);
+                    if (ok) {
+                        bar_expect_tx(&G.img_bar, C::kImgBytes);
+                        bulk_copy(img, a.img + (size_t)c.g * C::kImgBytes, C::kImgBytes, &G.img_bar);
+                        ok = bar_wait(&G.img_bar, (uint32_t)(nimg++ & 1));
                     }
-                    if (!ok || !bar_wait(&S.img_bar, (uint32_t)(nswitch & 1))) {
+                    if (!ok) {
                         abort_all(S, a.err);
                         break;
                     }
                     cur_group = c.g;
-                    ++nswitch;
                 }
-                if (!bar_wait(&S.a_ready[b], rb.phase)) {
+                if (k >= 2) {
+                    if (!bar_wait(&G.d_free[db.slot], db.phase ^ 1u)) {
+                        abort_all(S, a.err);
+                        break;
+                    }
+                    // tile k - 2 is finished: its stage takes the next tile
+                    if (copied < ntiles) {
+                        issue_tile<P>(a, cp, ring + rp.slot * C::kStageBytes, &G.full[rp.slot]);
+                        for (int s = 0; s < kGroups; ++s) next_tile(a, cp);
+                        rp.advance();
+                        ++copied;
+                    }
+                }
+                const uint32_t d = base + 64 + 32 * db.slot;
+                bool ok = true;
+#pragma unroll
+                for (int v = 0; v < C::NV; ++v) {
+                    if (v == T && !qjl) break;
+                    if (!bar_wait(&G.slot_ready[sa.slot], sa.phase)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;");
+                    const uint32_t a_t = base + 32 * sa.slot;
+                    const uint32_t dd = v < T ? d : d + 16;
+                    const uint64_t b0 = v < T ? bm0 + (uint64_t)(v * 4 * 16) : bq0;
+#pragma unroll
+                    for (int wd = 0; wd < 4; ++wd)
+                        mma_ts(dd, a_t + 8 * wd, b0 + (uint64_t)(wd * 16), (wd == 0 && (v == 0 || v == T)) ? 0u : 1u);
+                    mma_commit(&G.slot_free[sa.slot]);
+                    issued_any = true;
+                    sa.advance();
+                }
+                if (!ok) {
                     abort_all(S, a.err);
                     break;
                 }
-                asm volatile("tcgen05.fence::after_thread_sync;");
-                if (active) {
-                    issue_share<P>(v, kh, tmem + b * C::kBufCols, bd);
-                    issued_any = true;
-                }
-                mma_commit(&S.d_full[b]);
-                next_tile(a, c);
+                mma_commit(&G.d_full[db.slot]);
+                db.advance();
+                for (int s = 0; s < kGroups; ++s) next_tile(a, c);
             }
             if (issued_any) {   // every mma issued has completed before the CTA can leave
-                mma_commit(&S.drain[w]);
-                drained &= bar_wait(&S.drain[w], (uint32_t)(ndrain++ & 1));
+                mma_commit(&G.drain_bar);
+                drained &= bar_wait(&G.drain_bar, (uint32_t)(ndrain++ & 1));
+            }
+            // and every copy issued has landed (the last use of each stage)
+            for (int j = 0; j < C::kStages && j < copied; ++j) {
+                const int64_t u = copied - 1 - j;
+                drained &= bar_wait(&G.full[(int)(u % C::kStages)], (uint32_t)((u / C::kStages) & 1));
             }
         }
     } else {
-        // workers: expand tile i, finish tile i - kLag
-        const int row = 32 * (warp & 3) + lane, part = warp >> 2;
-        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        Cursor ce = seek(a, lo), cf = ce;
-        FinishGroup F;
-        F.g = -1;
-        FinishRegs<P> R;
-        Ring<C::kStages> se, sf;   // stages of the expanded and of the finished tile
-        Ring<C::kNB> be, bf;       // TMEM buffers of the expanded and of the finished tile
-        for (int64_t i = 0; i < n + C::kLag; ++i) {
-            if (aborted(S)) break;
-            const bool do_e = i < n, do_f = i >= C::kLag;
-            // expand tile i: loads, ALU and TMEM stores issued, completion awaited further down
-            if (do_e) {
-                bool okw = bar_wait(&S.full[se.slot], se.phase);
-                if (okw && i >= C::kNB) okw = bar_wait(&S.buf_free[be.slot], be.phase ^ 1u);
-                if (!okw) {
-                    abort_all(S, a.err);
-                    break;
+        // worker warp: group g, keys (TMEM lanes) 32 q .. 32 q + 31
+        const int g = warp >> 2, q = warp & 3, row = 32 * q + lane;
+        Group& G = S.grp[g];
+        const unsigned char* ring = sm + g * C::kStages * C::kStageBytes;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const uint32_t base = tmem + lane_off + g * kGroupCols;
+        if (g < n) {
+            Cursor ce = seek(a, lo + g), cf = ce;
+            FinishGroup F;
+            F.g = -1;
+            Ring<C::kStages> se, sf;
+            Ring<2> sa, db;
+            int64_t u = 0;   // A slot uses so far
+            const int64_t ntiles = (n - g + kGroups - 1) / kGroups;   // this group's tiles
+            for (int64_t k = 0; k <= ntiles; ++k) {
+                if (aborted(S)) break;
+                if (k < ntiles) {   // expand tile k: one bit vector per A slot
+                    bool okw = bar_wait(&G.full[se.slot], se.phase);
+                    uint4 x[C::NV];
+                    if (okw) load_vectors<P>(ring + se.slot * C::kStageBytes, row, qjl, x);
+#pragma unroll
+                    for (int v = 0; v < C::NV; ++v) {
+                        if (!okw || (v == T && !qjl)) break;
+                        // the slot's previous vector must be consumed by its mma
+                        if (u >= 2) okw = bar_wait(&G.slot_free[sa.slot], sa.phase ^ 1u);
+                        if (!okw) break;
+                        asm volatile("tcgen05.fence::after_thread_sync;");
+                        expand_vector(x[v], base + 32 * sa.slot);
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                        asm volatile("tcgen05.fence::before_thread_sync;");
+                        __syncwarp();
+                        if (lane == 0) bar_arrive(&G.slot_ready[sa.slot]);
+                        sa.advance();
+                        ++u;
+                    }
+                    if (!okw) {
+                        abort_all(S, a.err);
+                        break;
+                    }
+                    for (int s = 0; s < kGroups; ++s) next_tile(a, ce);
+                    se.advance();
                 }
-                asm volatile("tcgen05.fence::after_thread_sync;");
-                expand_tile<P>(a, sm + se.slot * C::kStageBytes, tmem + lane_off + be.slot * C::kBufCols, row, part);
-            }
-            // finish tile i - kLag: its TMEM loads go out while the stores above drain
-            if (do_f) {
-                if (!bar_wait(&S.d_full[bf.slot], bf.phase)) {
-                    abort_all(S, a.err);
-                    break;
+                if (k >= 1) {   // finish tile k - 1
+                    if (!bar_wait(&G.d_full[db.slot], db.phase)) {
+                        abort_all(S, a.err);
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;");
+                    if (cf.g != F.g) finish_group<P>(a, cf.g, S.cst[warp], F);
+                    finish_tile<P>(a, ring + sf.slot * C::kStageBytes, base + 64 + 32 * db.slot, cf, F, row);
+                    asm volatile("tcgen05.fence::before_thread_sync;");
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(&G.d_free[db.slot]);   // frees D and the tile's stage
+                    db.advance();
+                    for (int s = 0; s < kGroups; ++s) next_tile(a, cf);
+                    sf.advance();
                 }
-                asm volatile("tcgen05.fence::after_thread_sync;");
-                finish_load<P>(a, tmem + lane_off + bf.slot * C::kBufCols + C::kACols, part, R);
-            }
-            if (do_e) {
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;");
-                __syncwarp();
-                if (lane == 0) bar_arrive(&S.a_ready[be.slot]);
-                next_tile(a, ce);
-                se.advance();
-                be.advance();
-            }
-            if (do_f) {
-                if (cf.g != F.g) finish_group<P>(a, cf.g, part, F);
-                finish_store<P>(a, sm + sf.slot * C::kStageBytes, R, cf, F, row, part);
-                asm volatile("tcgen05.fence::before_thread_sync;");
-                __syncwarp();
-                if (lane == 0) {
-                    bar_arrive(&S.buf_free[bf.slot]);
-                    bar_arrive(&S.empty[sf.slot]);
-                }
-                next_tile(a, cf);
-                sf.advance();
-                bf.advance();
             }
         }
     }
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(TcCfg<P>::kThreads, 1) logits_tc_kernel(const 
         if (!__syncthreads_and(drained)) return;   // something may still write TMEM or shared memory
     }
     asm volatile("tcgen05.fence::after_thread_sync;");
-    if (warp == kProducerWarp + 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    if (warp == kMmaWarp0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
 template <int P>
@@ -657,7 +661,7 @@ cudaError_t run_tc(const TcArgs& a, int device, cudaStream_t s) {
         grid = sms;   // one CTA per SM: each allocates all 512 TMEM columns
     }
     tc_image_kernel<P><<<a.ngroups, 128, 0, s>>>(a);
-    logits_tc_kernel<P><<<grid, C::kThreads, C::kSmem, s>>>(a);
+    logits_tc_kernel<P><<<grid, kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
 
