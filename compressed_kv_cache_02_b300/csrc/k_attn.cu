@@ -730,19 +730,21 @@ __global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const Value
         const uint32_t* tile = sV[buf];
         const ulonglong2* sW2 = reinterpret_cast<const ulonglong2*>(sW);
         const int sh = 4 * (lane & 7), wsel = lane >> 3;
+        const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv2);
 #pragma unroll 2
         for (int t = warp; t < ntile; t += kV2Threads / 32) {
             const uint32_t* row = tile + t * ROW;
+            // byte c of z = idx * 8 of coordinate 4 lane + c: the offset of its (c, c) pair
             uint32_t z = 0u;
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
                 const uint32_t nib = (row[pp * 4 + wsel] >> sh) & 15u;
-                z |= (nib * (0x00204081u << pp)) & (0x01010101u << pp);
+                z |= (nib * (0x00204081u << (pp + 3))) & (0x08080808u << pp);
             }
             const ulonglong2 w = sW2[t];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const u64 v = s_cv2[(z >> (8 * c)) & 15u];
+                const u64 v = *reinterpret_cast<const u64*>(cvb + __byte_perm(z, 0u, 0x4440 + c));
                 alo[c] = fma2(v, w.x, alo[c]);
                 ahi[c] = fma2(v, w.y, ahi[c]);
             }
