@@ -221,6 +221,8 @@ def run_tq(args, world, rank, local):
     vws = tq.values_workspace(D, B, HQ, HKV, cap, device=dev)
 
     def step(s, ev=None):
+        if ev:
+            ev[3].record()
         kctx.append(ks[s], kc, cap, length)
         vctx.append(vs[s], vc, cap, length)
         kctx.advance_len(length, cap)
@@ -239,7 +241,7 @@ def run_tq(args, world, rank, local):
     if kctx.sync_status() or vctx.sync_status():
         raise RuntimeError("device error flags after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     lens_timed = [N0 + s + 1 for s in range(args.steps)]    # cache length seen by step s
     barrier(world)
@@ -256,6 +258,7 @@ def run_tq(args, world, rank, local):
         raise RuntimeError("device error flags after the timed steps")
     t_logits = [e[0].elapsed_time(e[1]) / 1e3 for e in evs]
     t_output = [e[1].elapsed_time(e[2]) / 1e3 for e in evs]
+    t_append = [e[3].elapsed_time(e[0]) / 1e3 for e in evs]
     keys = sum(lens_timed) * B * HKV
     scores = keys * G
     value = scores * world / elapsed
@@ -320,6 +323,7 @@ def run_tq(args, world, rank, local):
             "attn_values": {"ms": statistics.mean(t_output) * 1e3, "GB_s": gbs_output,
                             "bytes_per_key": VALUES_BYTES, "frac_of_measured": gbs_output / hbm,
                             "frac_of_8TBs": gbs_output / 8000.0},
+            "append_K_V_and_advance": {"ms": statistics.mean(t_append) * 1e3},
             "step_GB_s": step_bytes / (elapsed / args.steps) / 1e9,
             "prefill_quantize": {"vectors": state["prefill_vectors"], "s": state["prefill_s"],
                                  "vectors_per_s": state["prefill_vectors"] / state["prefill_s"]},

@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
 #pragma unroll
         for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
         if (valid) {
+            // unrolled so that many loads of Pi^T are in flight (it is usually not in L2 for a
+            // decode append, which is latency-bound)
+#pragma unroll 32
             for (int j = 0; j < d; ++j) {
                 const float p = __ldg(a.PiT + (size_t)j * d + i);
 #pragma unroll
@@ -187,6 +190,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
 #pragma unroll
             for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
             if (valid) {
+#pragma unroll 32
                 for (int j = 0; j < d; ++j) {
                     const float st = __ldg(a.StT + (size_t)j * m + i);
 #pragma unroll
