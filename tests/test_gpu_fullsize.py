@@ -7,6 +7,9 @@ sampled outputs the oracle computes one by one.
   and recomputes the full attention output of two (batch, head) pairs.
 * Vector search: 10^6 database vectors (d=200, cone law) at 2 and 4 bits, 10^4 queries, top-100;
   the oracle scores the whole database for a few sampled queries.
+* One decode layer of an 8B-class GQA model: 8 KV heads x 32768 keys (d=128), keys 4 bits
+  (3 MSE + 1 QJL) quantized on the GPU, bf16 values, 32 query heads; the fused output and the
+  logits of sampled heads against the oracle.
 """
 from math import sqrt
 
@@ -123,3 +126,40 @@ def test_search_full_database_sampled_queries(bits):
         tol = max(1e-4, 1e-3 * abs(kth))
         for i in set(got.tolist()) ^ set(order.tolist()):
             assert abs(scores[i] - kth) <= tol, f"query {r}: item {i} differs away from a tie"
+
+
+def test_decode_layer_32k_bf16_values():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from compressed_kv_cache_02_b300 import tq
+    hkv, n, seed = 8, 32768, 2
+    kp = Pair(D, 4, seed=0)
+    kfac = inputs.anisotropic_factors(hkv, D, seed=seed, device="cuda")
+    vfac = inputs.anisotropic_factors(hkv, D, seed=seed + 1000, device="cuda")
+    K = inputs.anisotropic(1, hkv, n, D, kfac, seed=seed, device="cuda")
+    V = inputs.anisotropic(1, hkv, n, D, vfac, seed=seed + 1000, device="cuda")
+    q = inputs.anisotropic(1, hkv, G, D, kfac, seed=seed + 2000, device="cuda", dtype=torch.float32).reshape(1, hkv * G, D)
+    kc = kp.ctx.alloc_codes(1, hkv, n)
+    for h in range(hkv):
+        kp.ctx.quantize(K[0, h], out=tq.Codes(kc.planes[0, h], kc.norm[0, h], kc.signs[0, h], kc.rnorm[0, h]))
+    length = torch.tensor([n], dtype=torch.int32, device="cuda")
+    scale = 1.0 / sqrt(D)
+    out = kp.ctx.attn_output(q, kc, n, length, scale, V).cpu().numpy()
+    logits = kp.ctx.attn_logits(q, kc, n, length, scale).cpu().numpy()
+    torch.cuda.synchronize()
+    assert kp.ctx.sync_status() == 0
+    Kc, Vc, qc = K[0].float().cpu().numpy(), V[0].float().cpu().numpy(), q[0].cpu().numpy()
+    rng = np.random.default_rng(1)
+    for h in (0, 13, 31):
+        kvh = h // G
+        kz = kp.oquant(Kc[kvh])
+        ref_l = scale * oracle.estimate(qc[h], kz, kp.Pi, kp.cb, kp.S)
+        ref_o = oracle.turboquant.softmax(ref_l) @ Vc[kvh]
+        assert_close(out[0, h], ref_o, "decode-layer output")
+        rows = np.sort(rng.choice(n, size=2048, replace=False))
+        sel = torch.from_numpy(rows).cuda()
+        codes = tq.Codes(planes=kc.planes[0, kvh][sel], norm=kc.norm[0, kvh][sel], signs=kc.signs[0, kvh][sel],
+                         rnorm=kc.rnorm[0, kvh][sel])
+        same = check_codes(kp, Kc[kvh][rows], codes)
+        assert same.mean() > 0.99
+        assert_close(logits[0, h, rows][same], ref_l[rows][same], "decode-layer logits")
