@@ -524,9 +524,16 @@ __global__ void attn_combine_kernel(const float* __restrict__ partials, int nchu
     __syncthreads();
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         if (PiV) {
-            float s = 0.f;
-            for (int j = 0; j < d; ++j) s = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s);
-            o[i] = s;
+            // many loads of Pi_v in flight: the values pass has usually evicted it from L2
+            float s0 = 0.f, s1 = 0.f;
+            int j = 0;
+#pragma unroll 16
+            for (; j + 1 < d; j += 2) {
+                s0 = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s0);
+                s1 = fmaf(__ldg(PiV + (size_t)(j + 1) * d + i), orot[j + 1], s1);
+            }
+            if (j < d) s0 = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s0);
+            o[i] = s0 + s1;
         } else {
             o[i] = orot[i];
         }
@@ -620,6 +627,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::); }
 
 // Softmax + value sum for MSE-coded values at W == 4.  Tiles of 256 keys: each thread owns
 // one key of the tile for the softmax; the tile's value rows are copied to shared memory
@@ -629,14 +637,22 @@ __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_g
 // per plane: (nibble * 0x204081) & 0x01010101 moves bit c of the nibble to bit 8c.
 constexpr int kV2Threads = 256;
 
+// Coded values at d <= 128 as independent per-warp streams: warp w takes the 32-key blocks w,
+// w + 8, ... of the CTA's chunk, double-buffers their value rows with cp.async, keeps its own
+// online softmax (running max per head, per-lane partial sums, accumulators rescaled when the
+// max grows) and meets the other warps only once, at the end of the chunk (log-sum-exp merge of
+// the 8 warp partials).  Lanes own coordinates 4 lane .. 4 lane + 3 (a nibble of word lane / 8
+// of each plane); each 3-bit index is spread to idx * 8 in a byte so that a byte-permute and one
+// shared load fetch its (c, c) centroid pair for the packed FFMA2 over head pairs.
 template <int P>
-__global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const ValuesArgs a) {
-    constexpr int ROW = P * 4;                        // words per value row
-    constexpr int ROWS = ROW < 8 ? 8 : ROW;           // room for the final warp reduction too
-    __shared__ __align__(16) uint32_t sV[2][kV2Threads * ROWS];
-    __shared__ float4 sW[kV2Threads];
-    __shared__ float4 sRed[kV2Threads / 32];
-    __shared__ float4 s_m, s_l, s_alpha;
+__global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const ValuesArgs a) {
+    constexpr int NW = kV2Threads / 32;
+    constexpr int ROW = P * 4;                  // words per value row
+    constexpr int BUFW = 32 * ROW;              // words per 32-key buffer
+    constexpr int SVW = NW * 2 * BUFW > 4 * NW * 32 * 4 ? NW * 2 * BUFW : 4 * NW * 32 * 4;   // + room for the merge
+    __shared__ __align__(16) uint32_t sV[SVW];
+    __shared__ float4 sW[NW][32];
+    __shared__ float4 s_wm[NW], s_wl[NW];
     __shared__ u64 s_cv2[kMaxLevels];   // (c, c) pairs for the packed multiply
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
     const int L = checked_len(a.len, b, a.cap, a.err);
@@ -645,30 +661,28 @@ __global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const Value
     const int hbase = kvh * a.G + 4 * blockIdx.z;
     const int nh = min(4, kvh * a.G + a.G - hbase);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        s_l = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     if (threadIdx.x < kMaxLevels) s_cv2[threadIdx.x] = pk2(a.vprm.centroids[threadIdx.x], a.vprm.centroids[threadIdx.x]);
-    u64 alo[4], ahi[4];   // heads (0,1) and (2,3) of the 4 owned coordinates
-#pragma unroll
-    for (int c = 0; c < 4; ++c) alo[c] = ahi[c] = 0ull;
+    __syncthreads();
     const int64_t iend = min((int64_t)L, i0 + a.chunk);
+    const int nblk = (int)((iend - i0 + 31) / 32);
     const size_t rowbase = (size_t)bh * a.cap;
     const float* lg = a.logits + ((size_t)b * a.Hq + hbase) * a.cap;
     const uint32_t* vrows = static_cast<const uint32_t*>(a.v.values);
+    uint32_t* buf0 = sV + warp * 2 * BUFW;
+    const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv2);
 
-    auto issue_tile = [&](int64_t t0, int buf) {
-        const int n = (int)min((int64_t)kV2Threads, iend - t0);
-        const uint4* src = reinterpret_cast<const uint4*>(vrows + (rowbase + t0) * ROW);
-        uint4* dst = reinterpret_cast<uint4*>(sV[buf]);
-        for (int e = threadIdx.x; e < n * P; e += kV2Threads) cp_async16(dst + e, src + e);
+    auto issue_block = [&](int j, int buf) {   // the value rows of block j into buffer buf
+        const int64_t k0 = i0 + (int64_t)j * 32;
+        const int n = (int)min((int64_t)32, iend - k0);
+        const uint4* src = reinterpret_cast<const uint4*>(vrows + (rowbase + k0) * ROW);
+        uint4* dst = reinterpret_cast<uint4*>(buf0 + buf * BUFW);
+        for (int e = lane; e < n * P; e += 32) cp_async16(dst + e, src + e);
     };
-    auto load_logits = [&](int64_t t0, float4& l4, float& vn) {
-        const int64_t i = t0 + threadIdx.x;
+    auto load_logits = [&](int j, float4& l4, float& vn) {   // key k0 + lane of block j
+        const int64_t i = i0 + (int64_t)j * 32 + lane;
         l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         vn = 0.f;
-        if (i < iend) {
+        if (j < nblk && i < iend) {
             l4.x = __ldg(lg + i);
             if (nh > 1) l4.y = __ldg(lg + a.cap + i);
             if (nh > 2) l4.z = __ldg(lg + 2 * a.cap + i);
@@ -677,62 +691,44 @@ __global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const Value
         }
     };
 
-    float4 l4;
-    float vn;
-    load_logits(i0, l4, vn);
-    issue_tile(i0, 0);
+    u64 alo[4], ahi[4];   // heads (0,1) and (2,3) of the 4 owned coordinates
+#pragma unroll
+    for (int c = 0; c < 4; ++c) alo[c] = ahi[c] = 0ull;
+    float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 ls = make_float4(0.f, 0.f, 0.f, 0.f);   // this lane's share of the softmax sums
+    float4 l4, nl4;
+    float vn, nvn;
+    load_logits(warp, l4, vn);
+    if (warp < nblk) issue_block(warp, 0);
     cp_async_commit();
-    __syncthreads();
+    const int sh = 4 * (lane & 7), wsel = lane >> 3;
     int buf = 0;
-    for (int64_t t0 = i0; t0 < iend; t0 += kV2Threads, buf ^= 1) {
-        const int ntile = (int)min((int64_t)kV2Threads, iend - t0);
-        const int64_t tn = t0 + kV2Threads;
-        if (tn < iend) issue_tile(tn, buf ^ 1);
+    for (int j = warp; j < nblk; j += NW, buf ^= 1) {
+        const int jn = j + NW;
+        if (jn < nblk) issue_block(jn, buf ^ 1);
         cp_async_commit();
-        float4 nl4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        float nvn = 0.f;
-        if (tn < iend) load_logits(tn, nl4, nvn);
-
-        // online softmax over this tile (one key per thread)
-        const float4 wm = warp_max4(l4);
-        if (lane == 0) sRed[warp] = wm;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float4 mx = sRed[0];
-            for (int w = 1; w < kV2Threads / 32; ++w) mx = f4_max(mx, sRed[w]);
-            const float4 mo = s_m, mn = f4_max(mo, mx);
-            s_alpha = make_float4(rescale(mo.x, mn.x), rescale(mo.y, mn.y), rescale(mo.z, mn.z), rescale(mo.w, mn.w));
-            s_m = mn;
-        }
-        __syncthreads();
-        const float4 mn = s_m, alpha = s_alpha;
-        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z),
-                                     safe_exp(l4.w, mn.w));
-        sW[threadIdx.x] = f4_scale(vn, p);
-        const float4 ps = warp_sum4(p);
-        cp_async_wait1();   // this tile's value rows have landed
-        __syncthreads();
-        if (lane == 0) sRed[warp] = ps;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float4 sum = sRed[0];
-            for (int w = 1; w < kV2Threads / 32; ++w) sum = f4_add(sum, sRed[w]);
-            const float4 lo = s_l;
-            s_l = make_float4(fmaf(lo.x, alpha.x, sum.x), fmaf(lo.y, alpha.y, sum.y), fmaf(lo.z, alpha.z, sum.z),
-                              fmaf(lo.w, alpha.w, sum.w));
-        }
+        load_logits(jn, nl4, nvn);
+        // online softmax over this block (one key per lane)
+        const float4 bm = warp_max4(l4);
+        const float4 mn = f4_max(m4, bm);
+        const float4 alpha = make_float4(rescale(m4.x, mn.x), rescale(m4.y, mn.y), rescale(m4.z, mn.z), rescale(m4.w, mn.w));
+        m4 = mn;
+        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z), safe_exp(l4.w, mn.w));
+        ls = make_float4(fmaf(ls.x, alpha.x, p.x), fmaf(ls.y, alpha.y, p.y), fmaf(ls.z, alpha.z, p.z), fmaf(ls.w, alpha.w, p.w));
+        sW[warp][lane] = f4_scale(vn, p);
         const u64 al_lo = pk2(alpha.x, alpha.y), al_hi = pk2(alpha.z, alpha.w);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             alo[c] = mul2(alo[c], al_lo);
             ahi[c] = mul2(ahi[c], al_hi);
         }
-        const uint32_t* tile = sV[buf];
-        const ulonglong2* sW2 = reinterpret_cast<const ulonglong2*>(sW);
-        const int sh = 4 * (lane & 7), wsel = lane >> 3;
-        const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv2);
-#pragma unroll 2
-        for (int t = warp; t < ntile; t += kV2Threads / 32) {
+        cp_async_wait1();   // this block's value rows have landed
+        __syncwarp();
+        const uint32_t* tile = buf0 + buf * BUFW;
+        const ulonglong2* sW2 = reinterpret_cast<const ulonglong2*>(sW[warp]);
+        const int ntile = (int)min((int64_t)32, iend - (i0 + (int64_t)j * 32));
+#pragma unroll 4
+        for (int t = 0; t < ntile; ++t) {
             const uint32_t* row = tile + t * ROW;
             // byte c of z = idx * 8 of coordinate 4 lane + c: the offset of its (c, c) pair
             uint32_t z = 0u;
@@ -749,20 +745,55 @@ __global__ void __launch_bounds__(kV2Threads) values_coded128_kernel(const Value
                 ahi[c] = fma2(v, w.y, ahi[c]);
             }
         }
-        __syncthreads();   // sW, sRed and this buffer are reused
+        __syncwarp();   // sW and this buffer are reused
         l4 = nl4;
         vn = nvn;
     }
-    const size_t stride = (size_t)a.d + 2;
-    float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
-    float4 acc[4];
+    cp_async_wait0();
+    // merge the warps: M = max of their maxima, each warp's share scaled by exp(m_w - M)
+    ls = warp_sum4(ls);
+    if (lane == 0) {
+        s_wm[warp] = m4;
+        s_wl[warp] = ls;
+    }
+    __syncthreads();   // every warp's cp.async and reads of sV are done; sV becomes the merge buffer
+    float4 M = s_wm[0];
+    for (int w = 1; w < NW; ++w) M = f4_max(M, s_wm[w]);
+    const float4 sc = make_float4(rescale(m4.x, M.x), rescale(m4.y, M.y), rescale(m4.z, M.z), rescale(m4.w, M.w));
+    float4* red = reinterpret_cast<float4*>(sV);   // [NW][4][32]
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const float2 x = upk2(alo[c]), y = upk2(ahi[c]);
-        acc[c] = make_float4(x.x, x.y, y.x, y.y);
+        red[(warp * 4 + c) * 32 + lane] = make_float4(x.x * sc.x, x.y * sc.y, y.x * sc.z, y.y * sc.w);
     }
-    write_partial<4, true, kV2Threads>(acc, reinterpret_cast<float4*>(sV), s_m, s_l, pbase,
-                                       (size_t)a.nchunk * stride, nh, a.d);
+    __syncthreads();
+    const size_t stride = (size_t)a.d + 2;
+    const size_t hstride = (size_t)a.nchunk * stride;
+    float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
+    if (threadIdx.x < 128) {
+        const int c = threadIdx.x >> 5, l = threadIdx.x & 31, jc = 4 * l + c;
+        float4 sum = red[c * 32 + l];
+        for (int w = 1; w < NW; ++w) sum = f4_add(sum, red[(w * 4 + c) * 32 + l]);
+        if (jc < a.d) {
+            const float vv[4] = {sum.x, sum.y, sum.z, sum.w};
+            for (int h = 0; h < nh; ++h) pbase[h * hstride + 2 + jc] = vv[h];
+        }
+    }
+    if (threadIdx.x == 0) {
+        float4 lt = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < NW; ++w) {
+            const float4 mw = s_wm[w], lw = s_wl[w];
+            lt.x = fmaf(lw.x, rescale(mw.x, M.x), lt.x);
+            lt.y = fmaf(lw.y, rescale(mw.y, M.y), lt.y);
+            lt.z = fmaf(lw.z, rescale(mw.z, M.z), lt.z);
+            lt.w = fmaf(lw.w, rescale(mw.w, M.w), lt.w);
+        }
+        const float mv[4] = {M.x, M.y, M.z, M.w}, lv[4] = {lt.x, lt.y, lt.z, lt.w};
+        for (int h = 0; h < nh; ++h) {
+            pbase[h * hstride] = mv[h];
+            pbase[h * hstride + 1] = lv[h];
+        }
+    }
 }
 
 template <int P>
