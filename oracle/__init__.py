@@ -49,7 +49,8 @@ from .codebook import Codebook, sphere_codebook, sphere_marginal_pdf, sphere_cel
 from .turboquant import (
     Quantized, quantize, dequantize, qjl_signs, pack_planes, unpack_planes, pack_signs,
     unpack_signs, estimate, estimate_all, attention_logits, attention_values, attention_output,
-    search_topk, recall_at_1, fp16_round, QJL_CONST,
+    search_topk, recall_at_1, fp16_round, QJL_CONST, SplitCodebook, split_quantize, split_dequantize,
+    split_estimate, pack_split, unpack_split,
 )
 
 __all__ = [
@@ -58,5 +59,6 @@ __all__ = [
     "sphere_cell_first_moment", "Quantized", "quantize", "dequantize", "qjl_signs",
     "pack_planes", "unpack_planes", "pack_signs", "unpack_signs", "estimate", "estimate_all",
     "attention_logits", "attention_values", "attention_output", "search_topk", "recall_at_1", "fp16_round",
+    "SplitCodebook", "split_quantize", "split_dequantize", "split_estimate", "pack_split", "unpack_split",
     "QJL_CONST",
 ]

@@ -258,3 +258,89 @@ def recall_at_1(top_idx: np.ndarray, true_top1: np.ndarray) -> float:
     top_idx = np.asarray(top_idx)
     hits = [(true_top1[r] in top_idx[r]) for r in range(top_idx.shape[0])]
     return float(np.mean(hits))
+
+
+# ----------------------------------------------------------------------------- fractional bit widths
+
+@dataclass
+class SplitCodebook:
+    """Fractional bit width ([juejin §4]: KV quality at 3.5 and 2.5 bits per channel).
+
+    Reading (the pages give only the per-channel averages): the first ``d_hi``
+    rotated coordinates are coded with the (b+1)-bit table ``hi``, the other
+    d - d_hi with the b-bit table ``lo``; both are the Lloyd-Max tables of the
+    same one-coordinate law, which is exact because the rotated coordinates are
+    exchangeable.  Average MSE bits b + d_hi / d; the QJL stage adds 1 bit.
+    """
+
+    lo: Codebook
+    hi: Codebook
+    d_hi: int
+
+    def hi_mask(self, d: int) -> np.ndarray:
+        return np.arange(d) < self.d_hi
+
+    def codes(self, U: np.ndarray) -> np.ndarray:
+        """Per coordinate: the number of its table's thresholds strictly below u."""
+        hi = self.hi_mask(U.shape[-1])
+        return np.where(hi, scalar_codes(U, self.hi), scalar_codes(U, self.lo))
+
+    def centroid_values(self, idx: np.ndarray) -> np.ndarray:
+        """c_{g(j)}[idx_j] for every coordinate j."""
+        hi = self.hi_mask(idx.shape[-1])
+        return np.where(hi, self.hi.centroids[np.minimum(idx, len(self.hi.centroids) - 1)],
+                        self.lo.centroids[np.minimum(idx, len(self.lo.centroids) - 1)])
+
+
+def split_quantize(X: np.ndarray, Pi: np.ndarray, scb: SplitCodebook, S: Optional[np.ndarray] = None) -> Quantized:
+    """Steps 1 and 2 with the split table: as ``quantize`` coordinate by coordinate."""
+    X = np.asarray(X, dtype=np.float64)
+    n = np.linalg.norm(X, axis=-1)
+    norm16 = fp16_round(n)
+    Y = X @ Pi.T
+    safe = np.where(n > 0, n, 1.0)
+    U = np.where((n > 0)[..., None], Y / safe[..., None], 0.0)
+    idx = scb.codes(U)
+    if S is None:
+        return Quantized(idx=idx, norm16=norm16)
+    R = X - split_dequantize(idx, norm16, Pi, scb)
+    rnorm16 = fp16_round(np.linalg.norm(R, axis=-1))
+    return Quantized(idx=idx, norm16=norm16, signs=(R @ S.T) > 0.0, rnorm16=rnorm16)
+
+
+def split_dequantize(idx: np.ndarray, norm16: np.ndarray, Pi: np.ndarray, scb: SplitCodebook) -> np.ndarray:
+    """x_hat = n16 * Pi^T c_g[idx]."""
+    return norm16[..., None] * (scb.centroid_values(idx) @ Pi)
+
+
+def split_estimate(q: np.ndarray, z: Quantized, Pi: np.ndarray, scb: SplitCodebook,
+                   S: Optional[np.ndarray] = None) -> np.ndarray:
+    """The estimator of step 3 with the split table."""
+    q = np.asarray(q, dtype=np.float64)
+    mse = z.norm16 * (scb.centroid_values(z.idx) @ (Pi @ q))
+    if S is None:
+        return mse
+    m = S.shape[0]
+    sigma = 2.0 * z.signs.astype(np.float64) - 1.0
+    return mse + z.rnorm16 * (QJL_CONST / m) * (sigma @ (S @ q))
+
+
+def pack_split(idx: np.ndarray, b: int, d_hi: int) -> np.ndarray:
+    """Packed row of a split code (the library's layout): the b planes of all d coordinates
+    ([..., b * W] words, plane p = bit p of idx_j), then plane b of the first d_hi
+    coordinates ([..., ceil(d_hi / 32)] words)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    low = pack_planes(idx & ((1 << b) - 1), b)
+    low = low.reshape(low.shape[:-2] + (-1,))
+    top = pack_bits(((idx[..., :d_hi] >> b) & 1).astype(bool))
+    return np.concatenate([low, top], axis=-1)
+
+
+def unpack_split(words: np.ndarray, d: int, b: int, d_hi: int) -> np.ndarray:
+    words = np.asarray(words, dtype=np.uint32)
+    W = _words(d)
+    low = words[..., :b * W].reshape(words.shape[:-1] + (b, W))
+    idx = unpack_planes(low, d)
+    top = unpack_bits(words[..., b * W:], d_hi).astype(np.int64)
+    idx[..., :d_hi] |= top << b
+    return idx
