@@ -63,6 +63,7 @@ extern "C" int tq_attn_values_noalloc(const tq_ctx* vc, int d, const float* logi
         if (cudaGetDevice(&dev) != cudaSuccess || dev != vc->device)
             return fail(TQ_ERR_ARG, "the value context belongs to another device than the current one");
         if (vc->mode != TQ_MODE_MSE) return fail(TQ_ERR_ARG, "vctx must be an MSE-mode context");
+        if (vc->d_hi) return fail(TQ_ERR_UNSUPPORTED, "split (fractional bit width) value contexts are not supported");
         if (vc->d != d) return fail(TQ_ERR_ARG, "d must equal vctx's d");
         if (!v_norm || !aligned_to(v_norm, 2)) return fail(TQ_ERR_ARG, "coded values need v_norm");
     }

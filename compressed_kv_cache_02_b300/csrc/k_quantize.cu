@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
             }
         }
         const int word = (i0 >> 5) + warp;
+        // split contexts: coordinates below d_hi (whole words, as d_hi % 32 == 0) use the
+        // (P+1)-bit table, whose top bit goes to the partial plane after the P full ones
+        const bool hi = i < prm.d_hi;
+        const int nb = prm.P + (hi ? 1 : 0);
 #pragma unroll
         for (int v = 0; v < kQuantRows; ++v) {
             const float n = s_n[v];
@@ -162,13 +166,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
             int idx = 0;
 #pragma unroll
             for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
-                if (b < prm.P && u > prm.thresholds[idx + (1 << b) - 1]) idx += 1 << b;
-            if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * prm.centroids[idx];
+                if (b < nb) {
+                    const int k = idx + (1 << b) - 1;
+                    if (u > (hi ? prm.thresholds_hi[k] : prm.thresholds[k])) idx += 1 << b;
+                }
+            if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
             const long long row = s_row[v];
             for (int p = 0; p < prm.P; ++p) {
                 const unsigned bits = __ballot_sync(0xffffffffu, valid && ((idx >> p) & 1));
                 if (lane == 0 && word < prm.W && row >= 0)
-                    a.planes[(size_t)row * prm.P * prm.W + (size_t)p * prm.W + word] = bits;
+                    a.planes[(size_t)row * prm.row_words + (size_t)p * prm.W + word] = bits;
+            }
+            if (prm.d_hi) {
+                const unsigned bits = __ballot_sync(0xffffffffu, valid && hi && ((idx >> prm.P) & 1));
+                if (lane == 0 && word < prm.W_hi && row >= 0)
+                    a.planes[(size_t)row * prm.row_words + (size_t)prm.P * prm.W + word] = bits;
             }
         }
     }

@@ -95,8 +95,8 @@ int tq_host_matrices(uint64_t seed, int d, int m, float* Pi, float* S) {
     return TQ_OK;
 }
 
-int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, const float* Pi_host,
-               const float* S_host) {
+static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int mode, int m, const float* Pi_host,
+                    const float* S_host) {
     TQ_REQUIRE(out != nullptr, TQ_ERR_ARG, "out is NULL");
     *out = nullptr;
     TQ_REQUIRE(d >= 3 && d <= TQ_MAX_D, TQ_ERR_ARG, "d must be in [3, 1024]");
@@ -104,6 +104,8 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
     const int P = (mode == TQ_MODE_PROD) ? bits - 1 : bits;
     TQ_REQUIRE(P >= 1 && P <= TQ_MAX_MSE_BITS, TQ_ERR_ARG,
                mode == TQ_MODE_PROD ? "PROD mode needs bits in [2, 5]" : "MSE mode needs bits in [1, 4]");
+    TQ_REQUIRE(d_hi >= 0 && d_hi <= d && d_hi % 32 == 0, TQ_ERR_ARG, "d_hi must be a multiple of 32 in [0, d]");
+    if (d_hi) TQ_REQUIRE(P + 1 <= TQ_MAX_MSE_BITS, TQ_ERR_ARG, "the split table needs MSE bits + 1 <= 4");
     if (mode == TQ_MODE_PROD) TQ_REQUIRE(m >= 1 && m <= TQ_MAX_D, TQ_ERR_ARG, "m must be in [1, 1024]");
     else m = 0;
 
@@ -128,9 +130,19 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
     for (float v : c->S) if (!std::isfinite(v)) { delete c; return fail(TQ_ERR_ARG, "S has a non-finite entry"); }
 
     lloyd_max_codebook(d, P, c->centroids, c->thresholds);
+    c->d_hi = d_hi;
+    if (d_hi) lloyd_max_codebook(d, P + 1, c->centroids_hi, c->thresholds_hi);
 
     Params& p = c->prm;
     p.d = d; p.m = m; p.P = P; p.L = c->L; p.W = c->W; p.Ws = c->Ws;
+    p.d_hi = d_hi;
+    p.W_hi = (d_hi + 31) / 32;
+    p.row_words = P * c->W + p.W_hi;
+    for (int k = 0; k < kMaxLevels; ++k) {
+        const int Lh = 2 * c->L;
+        p.centroids_hi[k] = (d_hi && k < Lh) ? static_cast<float>(c->centroids_hi[k]) : 0.f;
+        p.thresholds_hi[k] = (d_hi && k < Lh - 1) ? static_cast<float>(c->thresholds_hi[k]) : INFINITY;
+    }
     p.qjl = m ? 1 : 0;
     p.qjl_scale = m ? static_cast<float>(std::sqrt(M_PI / 2.0) / m) : 0.f;
     for (int k = 0; k < kMaxLevels; ++k) {
@@ -173,7 +185,7 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
             }
         if ((rc = upload(&c->dST, ST)) != TQ_OK || (rc = upload(&c->dStT, StT)) != TQ_OK) { free_ctx(c); return rc; }
     }
-    if (d == 128 && (m == 0 || m == 128)) {   // tcgen05 operands for bulk quantization
+    if (d == 128 && (m == 0 || m == 128) && d_hi == 0) {   // tcgen05 operands for bulk quantization
         std::vector<float> St;
         if (m) {
             St.resize((size_t)128 * 128);
@@ -191,6 +203,23 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, co
     std::vector<int> zero(1, 0);
     if ((rc = upload(&c->derr, zero)) != TQ_OK) { free_ctx(c); return rc; }
     *out = c;
+    return TQ_OK;
+}
+
+int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m, const float* Pi_host,
+               const float* S_host) {
+    return init_ctx(out, seed, d, bits, 0, mode, m, Pi_host, S_host);
+}
+
+int tq_init_split(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int mode, int m, const float* Pi_host,
+                  const float* S_host) {
+    return init_ctx(out, seed, d, bits, d_hi, mode, m, Pi_host, S_host);
+}
+
+int tq_code_words(const tq_ctx* c, int* words, int* d_hi) {
+    TQ_REQUIRE(c != nullptr, TQ_ERR_ARG, "context is NULL");
+    if (words) *words = c->prm.row_words;
+    if (d_hi) *d_hi = c->d_hi;
     return TQ_OK;
 }
 
@@ -354,8 +383,10 @@ int tq_attn_logits(tq_ctx* c, const float* q, int B, int Hq, int Hkv, const uint
     float* qproj = c->m ? reinterpret_cast<float*>(base + w.qproj) : nullptr;
     if ((rc = tq_prep_queries(c, q, (int64_t)B * Hq, qrot, qproj, stream))) return rc;
     KeyCache k{kp, ks, kn, kr, cap, len};
-    cudaError_t e = launch_logits(c, qrot, qproj, B, Hq, Hkv, k, scale, logits, base + w.image,
-                                  static_cast<cudaStream_t>(stream));
+    cudaError_t e = c->d_hi ? launch_logits_split(c, qrot, qproj, B, Hq, Hkv, k, scale, logits,
+                                                  static_cast<cudaStream_t>(stream))
+                            : launch_logits(c, qrot, qproj, B, Hq, Hkv, k, scale, logits, base + w.image,
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_logits launch");
 }
 
@@ -366,6 +397,8 @@ int tq_attn_output(tq_ctx* c, const tq_ctx* vc, const float* q, int B, int Hq, i
     int rc = check_attn(c, q, B, Hq, Hkv, kp, ks, kn, kr, cap, len, ws, ws_bytes);
     if (rc) return rc;
     TQ_REQUIRE(c->d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_output supports d <= 512");
+    TQ_REQUIRE(c->d_hi == 0 && (!vc || vc->d_hi == 0), TQ_ERR_UNSUPPORTED,
+               "tq_attn_output does not take split (fractional bit width) contexts");
     TQ_REQUIRE(values && out && aligned(values, 16) && aligned(out, 4), TQ_ERR_ARG, "values and out must be non-NULL");
     if (vc) {
         if ((rc = check_ctx(vc))) return rc;
@@ -410,6 +443,7 @@ int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, 
         if (rc) return rc;
         TQ_REQUIRE(vc->mode == TQ_MODE_MSE, TQ_ERR_ARG, "vctx must be an MSE-mode context");
         TQ_REQUIRE(vc->d == d, TQ_ERR_ARG, "d must equal vctx's d");
+        TQ_REQUIRE(vc->d_hi == 0, TQ_ERR_UNSUPPORTED, "tq_attn_values does not take split (fractional bit width) contexts");
         TQ_REQUIRE(v_norm && aligned(v_norm, 2), TQ_ERR_ARG, "coded values need v_norm");
     }
     TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_values supports d <= 512");
@@ -459,6 +493,7 @@ int tq_search_topk(tq_ctx* c, const float* q, int64_t nq, const uint32_t* planes
     TQ_REQUIRE(nq >= 0 && n >= 1 && n < ((int64_t)1 << 31) && k >= 1 && k <= TQ_MAX_TOPK && k <= n, TQ_ERR_ARG,
                "need nq >= 0, 1 <= k <= min(n, 128), n < 2^31");
     if (nq == 0) return TQ_OK;
+    TQ_REQUIRE(c->d_hi == 0, TQ_ERR_UNSUPPORTED, "tq_search_topk does not take split (fractional bit width) contexts");
     TQ_REQUIRE(q && planes && norm && top_score && top_idx && ws, TQ_ERR_ARG, "a required pointer is NULL");
     TQ_REQUIRE(aligned(q, 16) && aligned(planes, 16) && aligned(norm, 2) && aligned(ws, 256) &&
                    aligned(top_score, 4) && aligned(top_idx, 4),

@@ -26,6 +26,13 @@ struct Params {
     int odd_walsh;   // 1 when the terms are exactly the odd-size subsets in increasing order
     int mask[kMaxTerms];
     float kappa[kMaxTerms];
+    // Split (fractional bit width) contexts: coordinates j < d_hi use the (P+1)-bit table below
+    // and store bit P of idx in a partial top plane of W_hi words after the P full planes.
+    int d_hi;        // 0: every coordinate uses the P-bit table
+    int W_hi;        // words of the top plane, ceil(d_hi / 32)
+    int row_words;   // words per code row: P * W + W_hi
+    float centroids_hi[kMaxLevels];
+    float thresholds_hi[kMaxLevels];
 };
 
 // Host-side set-up (host_setup.cpp).
@@ -46,6 +53,8 @@ struct tq_ctx {
     int d = 0, m = 0, bits = 0, mode = 0, P = 0, L = 0, W = 0, Ws = 0;
     std::vector<float> Pi, S;                 // float32 host copies, row-major
     std::vector<double> centroids, thresholds;
+    int d_hi = 0;                                   // split contexts: see Params
+    std::vector<double> centroids_hi, thresholds_hi;
     tq::Params prm{};
     float* dPiT = nullptr;    // [d][d]  PiT[j*d+i] = Pi[i][j]      (y = Pi x)
     float* dPi = nullptr;     // [d][d]  row-major Pi                (o = Pi^T a)

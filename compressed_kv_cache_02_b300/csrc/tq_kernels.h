@@ -54,6 +54,10 @@ size_t logits_tc_image_bytes(int B, int Hq, int Hkv);
 cudaError_t launch_logits_tc(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
                              const KeyCache& k, float scale, float* logits, void* image, cudaStream_t s);
 
+// Logits for split (fractional bit width) key contexts (prm.d_hi > 0), any d <= TQ_MAX_D.
+cudaError_t launch_logits_split(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq, int Hkv,
+                                const KeyCache& k, float scale, float* logits, cudaStream_t s);
+
 // Split-sequence attention output: per-chunk partials (max, sum, acc[d]) then the combine.
 cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* qrot,
                                const float* qproj, int B, int Hq, int Hkv, const KeyCache& k,

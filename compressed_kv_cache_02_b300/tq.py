@@ -39,6 +39,8 @@ _SIGS = {
     "tq_host_matrices": [_u64, _i, _i, _p, _p],
     "tq_init": [ctypes.POINTER(_p), _u64, _i, _i],
     "tq_init_ex": [ctypes.POINTER(_p), _u64, _i, _i, _i, _i, _p, _p],
+    "tq_init_split": [ctypes.POINTER(_p), _u64, _i, _i, _i, _i, _i, _p, _p],
+    "tq_code_words": [_p, _p, _p],
     "tq_info": [_p, _p, _p, _p, _p],
     "tq_layout": [_p, _p, _p, _p],
     "tq_export_matrices": [_p, _p, _p, _p, _p],
@@ -146,16 +148,17 @@ class Context:
     """A tq_ctx: seeded rotation, JL matrix and codebook on the current device."""
 
     def __init__(self, d: int, bits: int, seed: int = 0, mode: int = TQ_MODE_PROD, m: int | None = None,
-                 Pi=None, S=None):
+                 Pi=None, S=None, d_hi: int = 0):
+        """d_hi > 0: split (fractional bit width) context, see tq_init_split."""
         import numpy as np
         h = _p()
         Pi_a = None if Pi is None else np.ascontiguousarray(Pi, dtype=np.float32)
         S_a = None if S is None else np.ascontiguousarray(S, dtype=np.float32)
         if m is None:
             m = d
-        _check(lib.tq_init_ex(ctypes.byref(h), seed, d, bits, mode, m,
-                              None if Pi_a is None else Pi_a.ctypes.data,
-                              None if S_a is None else S_a.ctypes.data), "tq_init_ex")
+        _check(lib.tq_init_split(ctypes.byref(h), seed, d, bits, d_hi, mode, m,
+                                 None if Pi_a is None else Pi_a.ctypes.data,
+                                 None if S_a is None else S_a.ctypes.data), "tq_init_split")
         self.h = h
         d_, m_, p_, mode_ = _i(), _i(), _i(), _i()
         _check(lib.tq_info(h, ctypes.byref(d_), ctypes.byref(m_), ctypes.byref(p_), ctypes.byref(mode_)), "tq_info")
@@ -163,6 +166,9 @@ class Context:
         w, ws = _i(), _i()
         _check(lib.tq_layout(h, None, ctypes.byref(w), ctypes.byref(ws)), "tq_layout")
         self.W, self.Ws = w.value, ws.value
+        rw, dh = _i(), _i()
+        _check(lib.tq_code_words(h, ctypes.byref(rw), ctypes.byref(dh)), "tq_code_words")
+        self.row_words, self.d_hi = rw.value, dh.value
 
     def close(self):
         if getattr(self, "h", None):
@@ -193,8 +199,12 @@ class Context:
         return Pi, (S if self.m else None), c, t
 
     def alloc_codes(self, *shape, device="cuda") -> Codes:
-        """Zeroed code buffers for rows of the given leading shape."""
-        planes = torch.zeros(*shape, self.P, self.W, dtype=torch.int32, device=device)
+        """Zeroed code buffers for rows of the given leading shape (planes [..., P, W]; a split
+        context's rows are flat [..., row_words])."""
+        if self.d_hi:
+            planes = torch.zeros(*shape, self.row_words, dtype=torch.int32, device=device)
+        else:
+            planes = torch.zeros(*shape, self.P, self.W, dtype=torch.int32, device=device)
         norm = torch.zeros(*shape, dtype=torch.int16, device=device)
         if not self.qjl:
             return Codes(planes=planes, norm=norm)

@@ -130,6 +130,24 @@ int tq_init(tq_ctx** out, uint64_t seed, int d, int bits);
 int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m,
                const float* Pi_host, const float* S_host);
 
+/* Split (fractional bit width) context.  Pages: juejin.cn post, section 四 (KV quality at 3.5
+ * and 2.5 bits per channel).  Reading: the first d_hi rotated coordinates are coded with the
+ * (b+1)-bit Lloyd-Max table and the other d - d_hi with the b-bit one (b = MSE bits given by
+ * bits and mode as in tq_init_ex; the QJL stage is unchanged), i.e. b + d_hi / d MSE bits per
+ * coordinate on average: bits = 3, d_hi = d/2, PROD gives 3.5 bits per channel.
+ * d_hi must be a multiple of 32 in [0, d] and b + 1 <= TQ_MAX_MSE_BITS; d_hi = 0 is tq_init_ex.
+ * Code rows: the b full planes (W words each, as tq_layout) followed by the top plane of the
+ * first d_hi coordinates (ceil(d_hi / 32) words: bit j % 32 of word j / 32 holds bit b of
+ * idx_j); tq_code_words gives the row length.  tq_quantize, tq_append and tq_attn_logits
+ * accept split contexts (CUDA-core kernels); tq_attn_output, tq_attn_values and
+ * tq_search_topk return TQ_ERR_UNSUPPORTED for them.                                   */
+int tq_init_split(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int mode, int m,
+                  const float* Pi_host, const float* S_host);
+
+/* Words per code row (planes) of a context: MSE bits * W, plus ceil(d_hi / 32) for a split
+ * context; and its d_hi (0 when not split).  Any output may be NULL.                      */
+int tq_code_words(const tq_ctx* ctx, int* words, int* d_hi);
+
 void tq_destroy(tq_ctx* ctx);   /* frees the context's tables; NULL is a no-op */
 
 /* d, m (0 in MSE mode), MSE bits and mode of a context.  Any output may be NULL.       */
@@ -144,9 +162,11 @@ int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_wo
  * ld_x a multiple of 8, 16-byte aligned x), mma.sync tensor cores for tq_search_topk at d in
  * (96,128], (192,256] or d = 200-224, and the table kernels for tq_attn_logits.
  * TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere; TQ_PATH_TENSOR also
- * moves tq_attn_logits to its tensor-core kernel (mma.sync, e4m3 operands, fp32
- * accumulation; 96 < d <= 128, m <= 128 and 1-3 MSE bits, else the table kernels).
- * Both families compute the same estimator within the documented tolerance.              */
+ * moves tq_attn_logits to its tcgen05 kernel (kind::f8f6f4, key bits as e4m3 in tensor
+ * memory, fp32 accumulation; 96 < d <= 128, m <= 128, 1-3 MSE bits, a cache capacity that
+ * is a multiple of 8 and 16-byte aligned code arrays, else the table kernels).  Its waits
+ * are bounded: one that runs out sets TQ_DEVERR_TIMEOUT.  Both families compute the same
+ * estimator within the documented tolerance.                                            */
 enum tq_kernel_path { TQ_PATH_AUTO = 0, TQ_PATH_CUDA_CORE = 1, TQ_PATH_TENSOR = 2 };
 int tq_set_kernel_path(tq_ctx* ctx, int path);
 
