@@ -338,7 +338,8 @@ def run_tq(args, world, rank, local):
     if not args.no_extra:
         del logits, ws, vws, state, kc, vc
         torch.cuda.empty_cache()
-        res["other_workloads"] = {"search": measure_search(dev), "prefill": measure_prefill(dev)}
+        res["other_workloads"] = {"search": measure_search(dev), "prefill": measure_prefill(dev),
+                                  "fractional": measure_fractional(dev)}
     return res
 
 
@@ -443,6 +444,83 @@ def measure_prefill(dev):
     return {"workload": "32 layers x 8 KV heads x 16384 tokens x d=128 bf16", **res}
 
 
+def _decode_split(ctx, codes, Pi, cent_lo, cent_hi):
+    """x_hat of split codes (flat rows of ctx.row_words words), in torch (measurement only)."""
+    words = codes.planes.view(torch.int32).long() & 0xFFFFFFFF
+    n = words.shape[0]
+    W, P = ctx.W, ctx.P
+    j = torch.arange(ctx.d, device=words.device)
+    idx = torch.zeros(n, ctx.d, dtype=torch.long, device=words.device)
+    for p in range(P):
+        idx |= ((words[:, p * W + j // 32] >> (j % 32)) & 1) << p
+    hi = j < ctx.d_hi
+    jt = torch.clamp(j, max=max(ctx.d_hi - 1, 0))
+    top = ((words[:, P * W + jt // 32] >> (jt % 32)) & 1) * hi
+    idx |= top << P
+    c = torch.where(hi[None, :], cent_hi[idx.clamp(max=len(cent_hi) - 1)], cent_lo[idx.clamp(max=len(cent_lo) - 1)])
+    nrm = codes.norm.view(torch.float16).float()
+    return nrm[:, None] * (c @ Pi)
+
+
+def measure_fractional(dev):
+    """Fractional bit widths (split contexts): 3.5 and 2.5 bits per channel = 2 / 1 MSE bits with
+    the first half of the rotated coordinates one bit higher, plus 1 QJL bit.  Keys of the
+    decode-layer shape at batch 8 (8 x 8 KV heads x 32768 tokens, d=128, bf16 anisotropic)
+    quantized on the GPU, then one logits pass of 32 query heads; D_mse and D_prod as in the
+    prefill workload."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    Bf, Hf, Nf, Gf = 8, 8, 32768, 4
+    n = Bf * Hf * Nf
+    fac = inputs.anisotropic_factors(Hf, D, seed=2, device=dev)
+    X = inputs.anisotropic(Bf, Hf, Nf, D, fac, seed=2, device=dev)
+    q = inputs.anisotropic(Bf, Hf, Gf, D, fac, seed=2002, device=dev, dtype=torch.float32).reshape(Bf, Hf * Gf, D)
+    Qs = q.reshape(-1, D)
+    g = torch.Generator(device=dev)
+    g.manual_seed(8)
+    sample = torch.randperm(n, generator=g, device=dev)[: 1 << 16]
+    length = torch.full((Bf,), Nf, dtype=torch.int32, device=dev)
+    res = {}
+    for label, bits in (("3.5bit", 3), ("2.5bit", 2)):
+        ctx = tq.Context(D, bits, seed=0, d_hi=D // 2)
+        keys = ctx.alloc_codes(Bf, Hf, Nf, device=dev)
+        flat = tq.Codes(keys.planes.view(n, -1), keys.norm.view(n), keys.signs.view(n, -1), keys.rnorm.view(n))
+        ctx.quantize(X.reshape(n, D), out=flat)
+        tq_q, _ = _event_time(lambda: ctx.quantize(X.reshape(n, D), out=flat))
+        ws = ctx.attn_workspace(Bf, Hf * Gf, Hf, Nf, device=dev)
+        logits = torch.empty(Bf, Hf * Gf, Nf, device=dev)
+        scale = 1.0 / D ** 0.5
+        ctx.attn_logits(q, keys, Nf, length, scale, out=logits, workspace=ws)
+        t_l, _ = _event_time(lambda: ctx.attn_logits(q, keys, Nf, length, scale, out=logits, workspace=ws), reps=5)
+        if ctx.sync_status():
+            raise RuntimeError("device error flags in the fractional workload")
+        Pi, _, cent_lo, _ = ctx.export()
+        cent_hi, _ = tq.host_codebook(D, ctx.P + 1)
+        Pi_t = torch.from_numpy(Pi).to(dev)
+        xs = X.reshape(n, D)[sample].float()
+        sub = tq.Codes(flat.planes[sample], flat.norm[sample], flat.signs[sample], flat.rnorm[sample])
+        xh = _decode_split(ctx, sub, Pi_t, torch.from_numpy(cent_lo).float().to(dev),
+                           torch.from_numpy(cent_hi).float().to(dev))
+        d_mse = float(((xs - xh) ** 2).sum(1).div(xs.pow(2).sum(1)).mean())
+        ks = 1 << 14
+        sk = tq.Codes(sub.planes[:ks].reshape(1, 1, ks, -1), sub.norm[:ks].reshape(1, 1, ks),
+                      sub.signs[:ks].reshape(1, 1, ks, -1), sub.rnorm[:ks].reshape(1, 1, ks))
+        Q1 = Qs[:256]
+        est = ctx.attn_logits(Q1.reshape(1, 256, D), sk, ks, torch.tensor([ks], dtype=torch.int32, device=dev), 1.0)[0]
+        exact = Q1 @ xs[:ks].T
+        den = Q1.pow(2).sum(1)[:, None] * xs[:ks].pow(2).sum(1)[None, :]
+        d_prod = float(((est - exact) ** 2 / den).mean())
+        key_bytes = (ctx.row_words + ctx.Ws) * 4 + 4
+        logit_bytes = n * (key_bytes + Gf * 4)
+        hbm, _ = peaks()
+        res[label] = {"mse_bits": ctx.P + 0.5, "code_bytes_per_key": key_bytes, "quantize_ms": tq_q * 1e3,
+                      "vectors_per_s": n / tq_q, "logits_ms": t_l * 1e3, "logit_scores_per_s": n * Gf / t_l,
+                      "logits_GB_s": logit_bytes / t_l / 1e9, "logits_frac_of_measured_hbm": logit_bytes / t_l / 1e9 / hbm,
+                      "D_mse": d_mse, "D_prod": d_prod}
+        del keys, flat, logits, ws
+    return {"workload": "8 x 8 KV heads x 32768 keys d=128 bf16, 32 query heads; first 64 rotated coordinates +1 bit",
+            **res}
+
+
 # ----------------------------------------------------------------------------- the oracle arm
 
 def oracle_step_sample(n_keys: int, seed: int = SEED_DATA):
@@ -539,7 +617,7 @@ def main():
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     ap.add_argument("--kernel-path", choices=["auto", "cuda_core", "tensor"], default="auto",
                     help="kernel family of the decode step (tq_set_kernel_path)")
-    ap.add_argument("--only", choices=["search", "prefill"], default=None,
+    ap.add_argument("--only", choices=["search", "prefill", "fractional"], default=None,
                     help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()
     set_batch(args.batch)
@@ -548,7 +626,7 @@ def main():
     world, rank, local = dist_setup()
     if args.only:
         torch.cuda.set_device(local)
-        fn = measure_search if args.only == "search" else measure_prefill
+        fn = {"search": measure_search, "prefill": measure_prefill, "fractional": measure_fractional}[args.only]
         print(json.dumps({"only": args.only, **fn(torch.device("cuda", local))}), flush=True)
         return
     if args.impl == "reference":

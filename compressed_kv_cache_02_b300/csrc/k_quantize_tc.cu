@@ -222,6 +222,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (P steps, the step
         // for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
         const float nv = nrm > 0.f ? nrm : 1.f;
+        // split contexts: this thread's 32 coordinates (one word) are below d_hi or not as a whole
+        const bool hi = 32 * part < prm.d_hi;
+        const int nb = prm.P + (hi ? 1 : 0);
         uint32_t pw[TQ_MAX_MSE_BITS] = {};
         float rs = 0.f;
 #pragma unroll
@@ -230,17 +233,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
             int idx = 0;
 #pragma unroll
             for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
-                if (b < prm.P) {
-                    const bool up = yc > prm.thresholds[idx + (1 << b) - 1] * nv;
+                if (b < nb) {
+                    const int k = idx + (1 << b) - 1;
+                    const bool up = yc > (hi ? prm.thresholds_hi[k] : prm.thresholds[k]) * nv;
                     idx += up ? (1 << b) : 0;
                     pw[b] |= (up ? 1u : 0u) << c;
                 }
-            const float r = y[c] - n16 * prm.centroids[idx];
+            const float r = y[c] - n16 * (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
             y[c] = r;
             rs = fmaf(r, r, rs);
         }
-        if (valid)
-            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * (prm.P * 4) + p * 4 + part] = pw[p];
+        if (valid) {
+            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+            if (hi) {
+                const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
+                a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
+            }
+        }
         if (!prm.qjl) {   // MSE mode: no residual sketch
             if (valid && part == 0) {
                 const uint16_t nh = float_to_half_bits(nrm);

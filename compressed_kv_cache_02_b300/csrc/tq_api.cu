@@ -166,6 +166,25 @@ static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int 
         p.kappa[t] = t < p.nterms ? static_cast<float>(kappa[t]) : 0.f;
     }
 
+    if (d_hi) {
+        double c0h;
+        std::vector<int> mh;
+        std::vector<double> kh;
+        walsh_form(c->centroids_hi, P + 1, c0h, mh, kh);
+        std::vector<int> odd;
+        for (int S = 1; S < 2 * c->L; ++S)
+            if (__builtin_popcount(S) & 1) odd.push_back(S);
+        p.c0_hi = static_cast<float>(c0h);
+        p.split_walsh = (mh == odd && p.odd_walsh) ? 1 : 0;
+        for (int t = 0; t < kMaxTerms; ++t) {
+            p.kappa_hi[t] = t < (int)kh.size() ? static_cast<float>(kh[t]) : 0.f;
+            p.kappa_lo_x[t] = 0.f;
+            if (t < (int)odd.size() && !(odd[t] >> P & 1))
+                for (int u = 0; u < p.nterms; ++u)
+                    if (masks[u] == odd[t]) p.kappa_lo_x[t] = static_cast<float>(kappa[u]);
+        }
+    }
+
     // Device tables: Pi^T and Pi for the rotations, S^T for queries, (S Pi^T)^T for residuals.
     std::vector<float> PiT((size_t)d * d);
     for (int i = 0; i < d; ++i)
@@ -185,7 +204,7 @@ static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int 
             }
         if ((rc = upload(&c->dST, ST)) != TQ_OK || (rc = upload(&c->dStT, StT)) != TQ_OK) { free_ctx(c); return rc; }
     }
-    if (d == 128 && (m == 0 || m == 128) && d_hi == 0) {   // tcgen05 operands for bulk quantization
+    if (d == 128 && (m == 0 || m == 128)) {   // tcgen05 operands for bulk quantization
         std::vector<float> St;
         if (m) {
             St.resize((size_t)128 * 128);

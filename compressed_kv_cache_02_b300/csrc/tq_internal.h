@@ -33,6 +33,13 @@ struct Params {
     int row_words;   // words per code row: P * W + W_hi
     float centroids_hi[kMaxLevels];
     float thresholds_hi[kMaxLevels];
+    // Walsh forms over the P + 1 planes of a split row (the top plane read as 0 for coordinates
+    // >= d_hi): term t is the t-th odd subset of P + 1 bits; kappa_lo_x is the P-bit table's
+    // coefficient of that subset (0 when it contains bit P), kappa_hi the (P+1)-bit table's.
+    float c0_hi;
+    int split_walsh;   // 1 when both tables are odd (symmetric) in these terms
+    float kappa_hi[kMaxTerms];
+    float kappa_lo_x[kMaxTerms];
 };
 
 // Host-side set-up (host_setup.cpp).

@@ -105,6 +105,21 @@ def test_split_quantize(d, bits, d_hi, mode, dtype):
     assert same.mean() > 0.97
 
 
+@pytest.mark.parametrize("bits,d_hi,mode", [(3, 64, 0), (2, 64, 0), (4, 32, 0), (2, 96, 1)])
+@pytest.mark.parametrize("path", ["cuda_core", "tensor"])
+def test_split_quantize_bulk_bf16(bits, d_hi, mode, path):
+    """Bulk bf16 rows at d = 128: the tcgen05 quantize kernel (AUTO/TENSOR) and the CUDA-core one."""
+    tq = _tq()
+    pr = SplitPair(128, bits, d_hi, mode, seed=12)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if path == "tensor" else tq.TQ_PATH_CUDA_CORE)
+    fac = inputs.anisotropic_factors(1, 128, seed=13)
+    X = inputs.anisotropic(1, 1, 5003, 128, fac, seed=13)[0, 0]
+    codes = pr.ctx.quantize(X.cuda())
+    assert pr.ctx.sync_status() == 0
+    same = pr.check_codes(X.float().numpy(), codes)
+    assert same.mean() > 0.97
+
+
 @pytest.mark.parametrize("d,bits,d_hi,mode", CASES)
 def test_split_logits(d, bits, d_hi, mode):
     pr = SplitPair(d, bits, d_hi, mode, seed=3)
