@@ -138,7 +138,10 @@ __device__ __forceinline__ void rot_bytes(const uint32_t (&x)[4], int r, uint32_
     y[3] = __funnelshift_r(a3, a0, sh);
 }
 
+// 512 threads with two keys each per pass.  768 or 1024 threads with one key each (more warps
+// to hide the lookup latency) run no faster: the shared-memory pipe is what bounds the kernel.
 constexpr int kQ8Threads = 512;
+constexpr int kQ8Keys = 2;
 
 template <int P>
 __device__ __forceinline__ float4 score_key(const float4* __restrict__ Tq, const float4* __restrict__ Tu,
@@ -242,13 +245,15 @@ __global__ void __launch_bounds__(kQ8Threads, 1) logits_q8_kernel(const AttnArgs
         const size_t cap = a.k.cap;
         float* out = a.logits + qrow0 * cap;
         const int64_t kend = min((int64_t)L, b1 * 32);
-        for (int64_t k0 = b0 * 32 + threadIdx.x; k0 < kend; k0 += 2 * kQ8Threads) {
-            // two keys per thread per pass: both loads are in flight before either is scored
-            const int64_t kk[2] = {k0, k0 + kQ8Threads};
-            uint32_t pl[2][P][4], sg[2][4];
-            float n[2], rho[2];
+        for (int64_t k0 = b0 * 32 + threadIdx.x; k0 < kend; k0 += kQ8Keys * kQ8Threads) {
+            // kQ8Keys keys per thread per pass: their loads are in flight before any is scored
+            int64_t kk[kQ8Keys];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < kQ8Keys; ++u) kk[u] = k0 + (int64_t)u * kQ8Threads;
+            uint32_t pl[kQ8Keys][P][4], sg[kQ8Keys][4];
+            float n[kQ8Keys], rho[kQ8Keys];
+#pragma unroll
+            for (int u = 0; u < kQ8Keys; ++u) {
                 const bool valid = kk[u] < kend;
                 const size_t row = rowbase + (valid ? kk[u] : 0);
                 const uint4* pr = reinterpret_cast<const uint4*>(a.k.planes + row * (P * 4));
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) logits_q8_kernel(const AttnArgs
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < kQ8Keys; ++u) {
                 if (kk[u] < kend) {
                     const float4 e = score_key<P>(Tq, Tu, pl[u], sg[u], n[u], rho[u], r, kap, cq, cu, 2.f * kq, qjl);
                     const int64_t key = kk[u];
@@ -629,21 +634,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::); }
 
-// Softmax + value sum for MSE-coded values at W == 4.  Tiles of 256 keys: each thread owns
-// one key of the tile for the softmax; the tile's value rows are copied to shared memory
-// with cp.async one tile ahead, and the next tile's logits are prefetched into registers.
-// In the value sum a warp takes one key at a time; lane l owns coordinates 4l..4l+3 (a
-// nibble of word l/8 of every plane) and gathers their P-bit indices with one bit spread
-// per plane: (nibble * 0x204081) & 0x01010101 moves bit c of the nibble to bit 8c.
+// Threads per CTA of the coded-value kernel below (8 warps).
 constexpr int kV2Threads = 256;
 
 // Coded values at d <= 128 as independent per-warp streams: warp w takes the 32-key blocks w,
 // w + 8, ... of the CTA's chunk, double-buffers their value rows with cp.async, keeps its own
 // online softmax (running max per head, per-lane partial sums, accumulators rescaled when the
 // max grows) and meets the other warps only once, at the end of the chunk (log-sum-exp merge of
-// the 8 warp partials).  Lanes own coordinates 4 lane .. 4 lane + 3 (a nibble of word lane / 8
-// of each plane); each 3-bit index is spread to idx * 8 in a byte so that a byte-permute and one
-// shared load fetch its (c, c) centroid pair for the packed FFMA2 over head pairs.
+// the 8 warp partials).  Lane l owns the coordinates 32 (l / 8) + l % 8 + 8 c, c = 0..3: bits
+// l % 8 + 8 c of word l / 8 of each plane, so one rotate and one and-or per plane leave byte c of
+// z = 8 * index of coordinate c, and a byte-permute plus one shared load fetch its (c, c)
+// centroid pair for the packed FFMA2 over head pairs.
 template <int P>
 __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const ValuesArgs a) {
     constexpr int NW = kV2Threads / 32;
@@ -701,7 +702,10 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     load_logits(warp, l4, vn);
     if (warp < nblk) issue_block(warp, 0);
     cp_async_commit();
-    const int sh = 4 * (lane & 7), wsel = lane >> 3;
+    const int wsel = lane >> 3;
+    int rot[P];   // right-rotation moving bit lane % 8 + 8 c of plane pp to bit 8 c + pp + 3
+#pragma unroll
+    for (int pp = 0; pp < P; ++pp) rot[pp] = ((lane & 7) - pp - 3) & 31;
     int buf = 0;
     for (int j = warp; j < nblk; j += NW, buf ^= 1) {
         const int jn = j + NW;
@@ -730,12 +734,12 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
 #pragma unroll 4
         for (int t = 0; t < ntile; ++t) {
             const uint32_t* row = tile + t * ROW;
-            // byte c of z = idx * 8 of coordinate 4 lane + c: the offset of its (c, c) pair
+            // byte c of z = 8 * index of owned coordinate c: the offset of its (c, c) pair
             uint32_t z = 0u;
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
-                const uint32_t nib = (row[pp * 4 + wsel] >> sh) & 15u;
-                z |= (nib * (0x00204081u << (pp + 3))) & (0x08080808u << pp);
+                const uint32_t wd = row[pp * 4 + wsel];
+                z |= __funnelshift_r(wd, wd, rot[pp]) & (0x08080808u << pp);
             }
             const ulonglong2 w = sW2[t];
 #pragma unroll
@@ -771,7 +775,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const size_t hstride = (size_t)a.nchunk * stride;
     float* pbase = a.partials + (((size_t)b * a.Hq + hbase) * a.nchunk + blockIdx.x) * stride;
     if (threadIdx.x < 128) {
-        const int c = threadIdx.x >> 5, l = threadIdx.x & 31, jc = 4 * l + c;
+        const int c = threadIdx.x >> 5, l = threadIdx.x & 31, jc = 32 * (l >> 3) + (l & 7) + 8 * c;
         float4 sum = red[c * 32 + l];
         for (int w = 1; w < NW; ++w) sum = f4_add(sum, red[(w * 4 + c) * 32 + l]);
         if (jc < a.d) {

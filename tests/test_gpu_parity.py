@@ -121,7 +121,7 @@ def test_argument_errors_raise():
 
 # ------------------------------------------------------------------ attention
 
-def _kv_case(B, Hkv, G, N, d, kbits, vmode, seed, lens):
+def _kv_case(B, Hkv, G, N, d, kbits, vmode, seed, lens, vbits=3):
     """Oracle-coded keys (and values) on the device plus the oracle's reference pieces."""
     tq = _tq()
     kp = Pair(d, kbits, seed=seed)
@@ -134,7 +134,7 @@ def _kv_case(B, Hkv, G, N, d, kbits, vmode, seed, lens):
     keys = kp.to_device(kz, (B, Hkv, N))
     case = dict(kp=kp, K=K, V=V, q=q, kz=kz, keys=keys, lens=np.array(lens), B=B, Hkv=Hkv, Hq=Hkv * G, N=N, d=d)
     if vmode == "mse":
-        vp = Pair(d, 3, mode=tq.TQ_MODE_MSE, seed=seed + 7)
+        vp = Pair(d, vbits, mode=tq.TQ_MODE_MSE, seed=seed + 7)
         vz = vp.oquant(V.float().numpy())
         case.update(vp=vp, vz=vz, vcodes=vp.to_device(vz, (B, Hkv, N)))
     return case
@@ -240,6 +240,23 @@ def test_attention_values_from_logits(vmode, B, Hkv, G, N, lens):
         ref = oracle.attention_values(logits.cpu().numpy(), c["lens"], Hkv, values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
     torch.cuda.synchronize()
     assert_close(got.cpu().numpy(), ref, "softmax-weighted values")
+
+
+@pytest.mark.parametrize("vbits,d", [(1, 128), (2, 128), (3, 112), (4, 128), (4, 100)])
+def test_attention_values_code_widths(vbits, d):
+    """The value sum at every MSE width of the d <= 128 kernel (centroids from registers at 1-3
+    bits, from shared memory at 4) and at head dims below 128 (padded coordinates)."""
+    tq = _tq()
+    B, Hkv, G, N, lens = 2, 2, 4, 1500, [1500, 333]
+    c = _kv_case(B, Hkv, G, N, d, 3, "mse", seed=17, lens=lens, vbits=vbits)
+    kp, vp = c["kp"], c["vp"]
+    ref_l = oracle.attention_logits(c["q"].numpy(), c["kz"], c["lens"], kp.Pi, kp.S, kp.cb, 1.0 / sqrt(d))
+    logits = torch.from_numpy(np.nan_to_num(ref_l, nan=0.0).astype(np.float32)).cuda()
+    length = torch.tensor(lens, dtype=torch.int32).cuda()
+    got = tq.attn_values(logits, length, c["vcodes"], vctx=vp.ctx)
+    ref = oracle.attention_values(logits.cpu().numpy(), c["lens"], Hkv, values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
+    torch.cuda.synchronize()
+    assert_close(got.cpu().numpy(), ref, f"values at {vbits} bits, d = {d}")
 
 
 def test_decode_append_and_advance():
