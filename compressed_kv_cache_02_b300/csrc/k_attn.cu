@@ -310,6 +310,15 @@ __device__ __forceinline__ float4 warp_sum4(float4 v) {
     }
     return v;
 }
+// Warp max of each component with the f32 warp reduction (one instruction per component).
+__device__ __forceinline__ float4 warp_max4_redux(float4 v) {
+    float4 r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r.x) : "f"(v.x));
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r.y) : "f"(v.y));
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r.z) : "f"(v.z));
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r.w) : "f"(v.w));
+    return r;
+}
 // exp(l - m) with exp(-inf - anything) = 0 (no NaN when both are -inf).
 __device__ __forceinline__ float safe_exp(float l, float m) { return l == -INFINITY ? 0.f : __expf(l - m); }
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
@@ -652,9 +661,9 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     constexpr int BUFW = 32 * ROW;              // words per 32-key buffer
     constexpr int SVW = NW * 2 * BUFW > 4 * NW * 32 * 4 ? NW * 2 * BUFW : 4 * NW * 32 * 4;   // + room for the merge
     __shared__ __align__(16) uint32_t sV[SVW];
-    __shared__ float4 sW[NW][32];
+    __shared__ ulonglong2 sW[NW][32][2];
     __shared__ float4 s_wm[NW], s_wl[NW];
-    __shared__ u64 s_cv2[kMaxLevels];   // (c, c) pairs for the packed multiply
+    __shared__ float s_cv[kMaxLevels];
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
     const int L = checked_len(a.len, b, a.cap, a.err);
     const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
@@ -662,7 +671,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const int hbase = kvh * a.G + 4 * blockIdx.z;
     const int nh = min(4, kvh * a.G + a.G - hbase);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x < kMaxLevels) s_cv2[threadIdx.x] = pk2(a.vprm.centroids[threadIdx.x], a.vprm.centroids[threadIdx.x]);
+    if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
     __syncthreads();
     const int64_t iend = min((int64_t)L, i0 + a.chunk);
     const int nblk = (int)((iend - i0 + 31) / 32);
@@ -670,7 +679,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const float* lg = a.logits + ((size_t)b * a.Hq + hbase) * a.cap;
     const uint32_t* vrows = static_cast<const uint32_t*>(a.v.values);
     uint32_t* buf0 = sV + warp * 2 * BUFW;
-    const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv2);
+    const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv);
 
     auto issue_block = [&](int j, int buf) {   // the value rows of block j into buffer buf
         const int64_t k0 = i0 + (int64_t)j * 32;
@@ -705,7 +714,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const int wsel = lane >> 3;
     int rot[P];   // right-rotation moving bit lane % 8 + 8 c of plane pp to bit 8 c + pp + 3
 #pragma unroll
-    for (int pp = 0; pp < P; ++pp) rot[pp] = ((lane & 7) - pp - 3) & 31;
+    for (int pp = 0; pp < P; ++pp) rot[pp] = ((lane & 7) - pp - 2) & 31;
     int buf = 0;
     for (int j = warp; j < nblk; j += NW, buf ^= 1) {
         const int jn = j + NW;
@@ -713,41 +722,56 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
         cp_async_commit();
         load_logits(jn, nl4, nvn);
         // online softmax over this block (one key per lane)
-        const float4 bm = warp_max4(l4);
-        const float4 mn = f4_max(m4, bm);
-        const float4 alpha = make_float4(rescale(m4.x, mn.x), rescale(m4.y, mn.y), rescale(m4.z, mn.z), rescale(m4.w, mn.w));
-        m4 = mn;
-        const float4 p = make_float4(safe_exp(l4.x, mn.x), safe_exp(l4.y, mn.y), safe_exp(l4.z, mn.z), safe_exp(l4.w, mn.w));
-        ls = make_float4(fmaf(ls.x, alpha.x, p.x), fmaf(ls.y, alpha.y, p.y), fmaf(ls.z, alpha.z, p.z), fmaf(ls.w, alpha.w, p.w));
-        sW[warp][lane] = f4_scale(vn, p);
-        const u64 al_lo = pk2(alpha.x, alpha.y), al_hi = pk2(alpha.z, alpha.w);
+        const float4 mn = f4_max(m4, warp_max4_redux(l4));
+        if (mn.x != m4.x || mn.y != m4.y || mn.z != m4.z || mn.w != m4.w) {   // warp-uniform
+            // the running max grew: rescale the sums and accumulators by exp(old - new)
+            const float4 alpha = make_float4(rescale(m4.x, mn.x), rescale(m4.y, mn.y), rescale(m4.z, mn.z), rescale(m4.w, mn.w));
+            m4 = mn;
+            ls = make_float4(ls.x * alpha.x, ls.y * alpha.y, ls.z * alpha.z, ls.w * alpha.w);
+            const float av[4] = {alpha.x, alpha.y, alpha.z, alpha.w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            alo[c] = mul2(alo[c], al_lo);
-            ahi[c] = mul2(ahi[c], al_hi);
+            for (int h = 0; h < 4; ++h) {
+                const u64 al = pk2(av[h], av[h]);
+                alo[h] = mul2(alo[h], al);
+                ahi[h] = mul2(ahi[h], al);
+            }
+        }
+        const float4 p = make_float4(safe_exp(l4.x, m4.x), safe_exp(l4.y, m4.y), safe_exp(l4.z, m4.z), safe_exp(l4.w, m4.w));
+        ls = f4_add(ls, p);
+        {
+            const float4 w = f4_scale(vn, p);
+            sW[warp][lane][0] = make_ulonglong2(pk2(w.x, w.x), pk2(w.y, w.y));
+            sW[warp][lane][1] = make_ulonglong2(pk2(w.z, w.z), pk2(w.w, w.w));
         }
         cp_async_wait1();   // this block's value rows have landed
         __syncwarp();
         const uint32_t* tile = buf0 + buf * BUFW;
-        const ulonglong2* sW2 = reinterpret_cast<const ulonglong2*>(sW[warp]);
-        const int ntile = (int)min((int64_t)32, iend - (i0 + (int64_t)j * 32));
-#pragma unroll 4
-        for (int t = 0; t < ntile; ++t) {
+        const ulonglong2* sW2 = &sW[warp][0][0];
+        // All 32 rows, also in a partial block: a key past the end has weight exactly 0 (vn = 0,
+        // p = 0) and its stale row still selects finite centroids, so it adds nothing.
+#pragma unroll 8
+        for (int t = 0; t < 32; ++t) {
             const uint32_t* row = tile + t * ROW;
             // byte c of z = 8 * index of owned coordinate c: the offset of its (c, c) pair
             uint32_t z = 0u;
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
                 const uint32_t wd = row[pp * 4 + wsel];
-                z |= __funnelshift_r(wd, wd, rot[pp]) & (0x08080808u << pp);
+                z |= __funnelshift_r(wd, wd, rot[pp]) & (0x04040404u << pp);
             }
-            const ulonglong2 w = sW2[t];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const u64 v = *reinterpret_cast<const u64*>(cvb + __byte_perm(z, 0u, 0x4440 + c));
-                alo[c] = fma2(v, w.x, alo[c]);
-                ahi[c] = fma2(v, w.y, ahi[c]);
-            }
+            const u64 v01 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4440)),
+                                *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4441)));
+            const u64 v23 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4442)),
+                                *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4443)));
+            const ulonglong2 wa = sW2[2 * t], wb = sW2[2 * t + 1];
+            alo[0] = fma2(v01, wa.x, alo[0]);
+            ahi[0] = fma2(v23, wa.x, ahi[0]);
+            alo[1] = fma2(v01, wa.y, alo[1]);
+            ahi[1] = fma2(v23, wa.y, ahi[1]);
+            alo[2] = fma2(v01, wb.x, alo[2]);
+            ahi[2] = fma2(v23, wb.x, ahi[2]);
+            alo[3] = fma2(v01, wb.y, alo[3]);
+            ahi[3] = fma2(v23, wb.y, ahi[3]);
         }
         __syncwarp();   // sW and this buffer are reused
         l4 = nl4;
@@ -765,10 +789,13 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     for (int w = 1; w < NW; ++w) M = f4_max(M, s_wm[w]);
     const float4 sc = make_float4(rescale(m4.x, M.x), rescale(m4.y, M.y), rescale(m4.z, M.z), rescale(m4.w, M.w));
     float4* red = reinterpret_cast<float4*>(sV);   // [NW][4][32]
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const float2 x = upk2(alo[c]), y = upk2(ahi[c]);
-        red[(warp * 4 + c) * 32 + lane] = make_float4(x.x * sc.x, x.y * sc.y, y.x * sc.z, y.y * sc.w);
+    {
+        const float2 a0 = upk2(alo[0]), a1 = upk2(alo[1]), a2 = upk2(alo[2]), a3 = upk2(alo[3]);
+        const float2 b0 = upk2(ahi[0]), b1 = upk2(ahi[1]), b2 = upk2(ahi[2]), b3 = upk2(ahi[3]);
+        red[(warp * 4 + 0) * 32 + lane] = make_float4(a0.x * sc.x, a1.x * sc.y, a2.x * sc.z, a3.x * sc.w);
+        red[(warp * 4 + 1) * 32 + lane] = make_float4(a0.y * sc.x, a1.y * sc.y, a2.y * sc.z, a3.y * sc.w);
+        red[(warp * 4 + 2) * 32 + lane] = make_float4(b0.x * sc.x, b1.x * sc.y, b2.x * sc.z, b3.x * sc.w);
+        red[(warp * 4 + 3) * 32 + lane] = make_float4(b0.y * sc.x, b1.y * sc.y, b2.y * sc.z, b3.y * sc.w);
     }
     __syncthreads();
     const size_t stride = (size_t)a.d + 2;
