@@ -652,8 +652,9 @@ constexpr int kV2Threads = 256;
 // max grows) and meets the other warps only once, at the end of the chunk (log-sum-exp merge of
 // the 8 warp partials).  Lane l owns the coordinates 32 (l / 8) + l % 8 + 8 c, c = 0..3: bits
 // l % 8 + 8 c of word l / 8 of each plane, so one rotate and one and-or per plane leave byte c of
-// z = 8 * index of coordinate c, and a byte-permute plus one shared load fetch its (c, c)
-// centroid pair for the packed FFMA2 over head pairs.
+// z = 4 * index of coordinate c, and a byte-permute plus one shared load fetch its centroid.
+// The packed FFMA2 runs over coordinate pairs (0, 1), (2, 3) against each head's weight, which
+// shared memory holds duplicated as (w_h, w_h).
 template <int P>
 __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const ValuesArgs a) {
     constexpr int NW = kV2Threads / 32;
@@ -701,9 +702,9 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
         }
     };
 
-    u64 alo[4], ahi[4];   // heads (0,1) and (2,3) of the 4 owned coordinates
+    u64 alo[4], ahi[4];   // head h: owned coordinates (0, 1) in alo[h], (2, 3) in ahi[h]
 #pragma unroll
-    for (int c = 0; c < 4; ++c) alo[c] = ahi[c] = 0ull;
+    for (int h = 0; h < 4; ++h) alo[h] = ahi[h] = 0ull;
     float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4 ls = make_float4(0.f, 0.f, 0.f, 0.f);   // this lane's share of the softmax sums
     float4 l4, nl4;
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
 #pragma unroll 8
         for (int t = 0; t < 32; ++t) {
             const uint32_t* row = tile + t * ROW;
-            // byte c of z = 8 * index of owned coordinate c: the offset of its (c, c) pair
+            // byte c of z = 4 * index of owned coordinate c: the offset of its centroid
             uint32_t z = 0u;
 #pragma unroll
             for (int pp = 0; pp < P; ++pp) {
