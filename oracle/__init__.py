@@ -52,8 +52,17 @@ from .turboquant import (
     search_topk, recall_at_1, fp16_round, QJL_CONST, SplitCodebook, split_quantize, split_dequantize,
     split_estimate, pack_split, unpack_split,
 )
+from .polar import (
+    polar_forward, polar_inverse, angle_pdf, angle_cdf, angle_dof, AngleCodebook, angle_codebook,
+    PolarCodebook, polar_codebook, PolarQuantized, polar_codes, polar_rebuild, polar_dequantize,
+    polar_quantize, polar_estimate, polar_words, pack_polar, unpack_polar,
+)
 
 __all__ = [
+    "polar_forward", "polar_inverse", "angle_pdf", "angle_cdf", "angle_dof", "AngleCodebook",
+    "angle_codebook", "PolarCodebook", "polar_codebook", "PolarQuantized", "polar_codes",
+    "polar_rebuild", "polar_dequantize", "polar_quantize", "polar_estimate", "polar_words",
+    "pack_polar", "unpack_polar",
     "splitmix64_stream", "gaussian_stream", "haar_rotation", "jl_matrix", "method_matrices",
     "Codebook", "sphere_codebook", "sphere_marginal_pdf", "sphere_cell_prob",
     "sphere_cell_first_moment", "Quantized", "quantize", "dequantize", "qjl_signs",
