@@ -229,3 +229,73 @@ void walsh_form(const std::vector<double>& c, int bits, double& c0, std::vector<
 }
 
 }  // namespace tq
+
+namespace tq {
+
+// Lloyd-Max table of the level-`level` angles of the recursive polar transform.  Level 1 angles
+// are uniform on [0, 2 pi): the uniform table (cells [j D, (j+1) D), centroids (j + 1/2) D).
+// A level-l angle (l >= 2) is atan2 of two independent chi radii with k = 2^(l-1) degrees of
+// freedom, density proportional to (sin psi cos psi)^(k-1) on [0, pi/2], which is log-concave:
+// the Lloyd iteration (midpoint thresholds, cell means by composite Gauss-Legendre) has one fixed
+// point, symmetric about pi/4.
+void polar_angle_codebook(int level, int bits, std::vector<double>& c, std::vector<double>& t) {
+    const int L = 1 << bits;
+    c.resize(L);
+    t.resize(L - 1);
+    if (level == 1) {
+        const double D = 2.0 * M_PI / L;
+        for (int j = 0; j < L; ++j) c[j] = (j + 0.5) * D;
+        for (int j = 0; j + 1 < L; ++j) t[j] = (j + 1) * D;
+        return;
+    }
+    const double k = std::ldexp(1.0, level - 1);
+    const double q = M_PI / 4.0;
+    const double reach = std::min(q, 12.0 / std::sqrt(k));   // the density is negligible beyond
+    const double h = std::min(q / 4.0, 0.25 / std::sqrt(k));
+    GaussLegendre gl(32);
+    auto logf = [&](double psi) { return (k - 1.0) * std::log(std::sin(2.0 * psi)); };
+    const double logpeak = logf(q);
+    auto moments = [&](double a, double b, double& m0, double& m1) {
+        a = std::max(a, q - reach);
+        b = std::min(b, q + reach);
+        m0 = m1 = 0.0;
+        if (b <= a) return;
+        const int panels = std::max(1, (int)std::ceil((b - a) / h));
+        const double step = (b - a) / panels;
+        for (int p = 0; p < panels; ++p) {
+            const double mid = a + (p + 0.5) * step, half = 0.5 * step;
+            for (size_t i = 0; i < gl.x.size(); ++i) {
+                const double psi = mid + half * gl.x[i];
+                const double f = std::exp(logf(psi) - logpeak) * gl.w[i] * half;
+                m0 += f;
+                m1 += psi * f;
+            }
+        }
+    };
+    const double spread = std::min(q, 1.5 / std::sqrt(k));
+    for (int j = 0; j < L; ++j) c[j] = q + (2.0 * j + 1.0 - L) / L * spread;
+    std::vector<double> cn(L);
+    for (int it = 0; it < 200000; ++it) {
+        for (int j = 0; j + 1 < L; ++j) t[j] = 0.5 * (c[j] + c[j + 1]);
+        double moved = 0.0;
+        for (int j = 0; j < L; ++j) {
+            const double a = (j == 0) ? 0.0 : t[j - 1];
+            const double b = (j == L - 1) ? 2.0 * q : t[j];
+            double m0, m1;
+            moments(a, b, m0, m1);
+            cn[j] = m0 > 0.0 ? m1 / m0 : c[j];
+            moved = std::max(moved, std::fabs(cn[j] - c[j]));
+        }
+        c = cn;
+        if (moved < 1e-15) break;
+    }
+    for (int j = 0; j < L / 2; ++j) {   // symmetric about pi/4
+        const double s = 0.5 * ((c[L - 1 - j] - q) - (c[j] - q));
+        c[j] = q - s;
+        c[L - 1 - j] = q + s;
+    }
+    for (int j = 0; j + 1 < L; ++j) t[j] = 0.5 * (c[j] + c[j + 1]);
+    if (L % 2 == 0) t[L / 2 - 1] = q;
+}
+
+}  // namespace tq

@@ -49,6 +49,8 @@ void seeded_matrices(uint64_t seed, int d, int m, std::vector<double>& Pi,
                      std::vector<double>& S);
 void walsh_form(const std::vector<double>& centroids, int bits, double& c0,
                 std::vector<int>& masks, std::vector<double>& kappa);
+void polar_angle_codebook(int level, int bits, std::vector<double>& centroids,
+                          std::vector<double>& thresholds);
 
 // Thread-local error message (tq_api.cu).
 int fail(int code, const std::string& msg);

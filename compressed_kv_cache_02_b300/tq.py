@@ -58,6 +58,12 @@ _SIGS = {
     "tq_search_workspace_size": [_p, _i64, _i64, _i, ctypes.POINTER(_sz)],
     "tq_search_topk": [_p, _p, _i64, _p, _p, _p, _p, _i64, _i, _p, _p, _p, _sz, _p],
     "tq_sync_status": [_p, _p, _p],
+    "tq_host_polar_codebook": [_i, _i, _p, _p],
+    "tq_polar_init": [ctypes.POINTER(_p), _u64, _i, _i, _i, _p, _p],
+    "tq_polar_layout": [_p, _p, _p],
+    "tq_polar_quantize": [_p, _p, _i, _i64, _i64, _p, _p, _p, _p, _p],
+    "tq_polar_scores": [_p, _p, _i64, _p, _p, _p, _p, _i64, _f, _p, _p],
+    "tq_polar_sync_status": [_p, _p, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -65,6 +71,8 @@ for _name, _args in _SIGS.items():
     _fn.restype = _i
 lib.tq_destroy.argtypes = [_p]
 lib.tq_destroy.restype = None
+lib.tq_polar_destroy.argtypes = [_p]
+lib.tq_polar_destroy.restype = None
 lib.tq_last_error.argtypes = []
 lib.tq_last_error.restype = ctypes.c_char_p
 
@@ -299,4 +307,88 @@ class Context:
         code = lib.tq_sync_status(self.h, _stream(stream), ctypes.byref(flags))
         if code not in (TQ_OK, TQ_ERR_DEVICE):
             raise TQError(code, "tq_sync_status")
+        return flags.value
+
+
+# ---------------------------------------------------------------------------------- polar encoder
+
+def host_polar_codebook(level: int, bits: int):
+    import numpy as np
+    c = np.zeros(1 << bits)
+    t = np.zeros((1 << bits) - 1)
+    _check(lib.tq_host_polar_codebook(level, bits, c.ctypes.data, t.ctypes.data if t.size else None),
+           "tq_host_polar_codebook")
+    return c, t
+
+
+@dataclass
+class PolarCodes:
+    """Packed polar codes of a batch of vectors (device tensors, layout of include/tq.h)."""
+    codes: torch.Tensor
+    r16: torch.Tensor
+    signs: torch.Tensor | None = None
+    rnorm: torch.Tensor | None = None
+
+
+class PolarContext:
+    """A tq_polar: seeded rotation (and JL matrix), per-level angle tables on the current device."""
+
+    def __init__(self, d: int, bits: int, qjl: bool = True, seed: int = 0, Pi=None, S=None):
+        import numpy as np
+        h = _p()
+        Pi_a = None if Pi is None else np.ascontiguousarray(Pi, dtype=np.float32)
+        S_a = None if S is None else np.ascontiguousarray(S, dtype=np.float32)
+        _check(lib.tq_polar_init(ctypes.byref(h), seed, d, bits, int(qjl),
+                                 None if Pi_a is None else Pi_a.ctypes.data,
+                                 None if S_a is None else S_a.ctypes.data), "tq_polar_init")
+        self.h, self.d, self.bits, self.qjl = h, d, bits, bool(qjl)
+        cw, ws = _i(), _i()
+        _check(lib.tq_polar_layout(h, ctypes.byref(cw), ctypes.byref(ws)), "tq_polar_layout")
+        self.code_words, self.sign_words = cw.value, ws.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib.tq_polar_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc_codes(self, n: int, device="cuda") -> PolarCodes:
+        codes = torch.zeros(n, self.code_words, dtype=torch.int32, device=device)
+        r16 = torch.zeros(n, dtype=torch.int16, device=device)
+        if not self.qjl:
+            return PolarCodes(codes=codes, r16=r16)
+        return PolarCodes(codes=codes, r16=r16, signs=torch.zeros(n, self.sign_words, dtype=torch.int32, device=device),
+                          rnorm=torch.zeros(n, dtype=torch.int16, device=device))
+
+    def quantize(self, x: torch.Tensor, out: PolarCodes | None = None, stream=None) -> PolarCodes:
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("x must be float32 or bfloat16")
+        x2 = x.reshape(-1, self.d)
+        if out is None:
+            out = self.alloc_codes(x2.shape[0], device=x.device)
+        dtype = TQ_BF16 if x.dtype == torch.bfloat16 else TQ_F32
+        _check(lib.tq_polar_quantize(self.h, _ptr(x2), dtype, x2.shape[0], x2.stride(0), _ptr(out.codes),
+                                     _ptr(out.r16), _ptr(out.signs), _ptr(out.rnorm), _stream(stream)),
+               "tq_polar_quantize")
+        return out
+
+    def scores(self, q: torch.Tensor, keys: PolarCodes, scale: float = 1.0, out=None, stream=None) -> torch.Tensor:
+        q2 = q.reshape(-1, self.d).contiguous().float()
+        n = keys.codes.shape[0]
+        if out is None:
+            out = torch.empty(q2.shape[0], n, dtype=torch.float32, device=q.device)
+        _check(lib.tq_polar_scores(self.h, _ptr(q2), q2.shape[0], _ptr(keys.codes), _ptr(keys.r16), _ptr(keys.signs),
+                                   _ptr(keys.rnorm), n, scale, _ptr(out), _stream(stream)), "tq_polar_scores")
+        return out
+
+    def sync_status(self, stream=None) -> int:
+        flags = _i(0)
+        code = lib.tq_polar_sync_status(self.h, _stream(stream), ctypes.byref(flags))
+        if code not in (TQ_OK, TQ_ERR_DEVICE):
+            raise TQError(code, "tq_polar_sync_status")
         return flags.value

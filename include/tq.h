@@ -282,6 +282,55 @@ int tq_search_topk(tq_ctx* ctx, const float* q, int64_t nq, const uint32_t* plan
                    int64_t n, int k, float* top_score, int32_t* top_idx, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- polar-angle encoder
+ * The recursive polar representation of the pages: csdn tutorial, section 将笛卡尔积坐标转为
+ * 极坐标 (the length r kept at FP16 and d - 1 low-bit angles for the direction) and section
+ * TurboQuant原理剖析 (2 or 3 bits per angle, then 1 QJL bit per dimension); freelamp article,
+ * section 技术突破：极坐标量化 (rotation first; a recursive polar transform into one radius and
+ * a series of angles whose law is known in closed form).
+ * Readings: y = Pi x is transformed by pairing neighbours: level 1 maps (y_2i, y_2i+1) to a
+ * radius and an angle atan2(y_2i+1, y_2i) in [0, 2 pi); level l pairs the level-(l-1) radii into
+ * an angle atan2(right, left) in [0, pi/2]; d/2 + d/4 + ... + 1 = d - 1 angles.  Level 1 angles
+ * are uniform (table: cells of width 2 pi / 2^b, centroids at their centres); a level-l angle has
+ * density proportional to (sin psi cos psi)^(2^(l-1) - 1) and its own Lloyd-Max table.  Every
+ * angle takes b bits.  The QJL stage and the estimator are those of the PROD mode, on the
+ * residual x - Pi^T y_hat, y_hat rebuilt from the fp16 radius and the angle centroids.
+ * Code rows: the d - 1 codes (level 1 left to right, then level 2, ...) as consecutive b-bit
+ * fields of one little-endian bit stream (code a in stream bits a*b .. a*b + b - 1; stream bit
+ * t = bit t % 32 of word t / 32), tq_polar_layout words per vector.                        */
+#define TQ_POLAR_MAX_BITS 4
+typedef struct tq_polar tq_polar;
+
+/* The level-`level` angle table (1 <= level <= 8, 1 <= bits <= 4): 2^bits centroids ascending
+ * and 2^bits - 1 thresholds, float64, caller-owned arrays.  Host only.                     */
+int tq_host_polar_codebook(int level, int bits, double* centroids, double* thresholds);
+
+/* d in {16, 32, 64, 128, 256}; bits per angle 1..4; qjl 1 adds the QJL stage with m = d rows.
+ * Pi_host (d x d) and S_host (d x d) float32 row-major as in tq_init_ex (NULL: seeded).     */
+int tq_polar_init(tq_polar** out, uint64_t seed, int d, int bits, int qjl, const float* Pi_host,
+                  const float* S_host);
+void tq_polar_destroy(tq_polar* ctx);
+
+/* Words per vector of the code rows and of the sign rows (0 without QJL).                  */
+int tq_polar_layout(const tq_polar* ctx, int* code_words, int* sign_words);
+
+/* Encodes n rows of x (device, TQ_F32 or TQ_BF16, row stride ld_x >= d elements) into codes
+ * [n][code_words], r16 [n] (binary16 bits of |x|) and, with QJL, signs [n][sign_words] and
+ * rnorm16 [n] (binary16 bits of |x - x_hat|).  Device buffers, caller-owned; asynchronous on
+ * `stream`.  A radius rounding to binary16 infinity sets TQ_DEVERR_NORM_OVERFLOW.           */
+int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_t ld_x,
+                      uint32_t* codes, uint16_t* r16, uint32_t* signs, uint16_t* rnorm16,
+                      void* stream);
+
+/* out[i][k] = scale * est(q_i, x_k) for nq fp32 queries q [nq][d] against n coded rows
+ * (device buffers, out [nq][n] fp32 row-major).  Asynchronous on `stream`.                 */
+int tq_polar_scores(tq_polar* ctx, const float* q, int64_t nq, const uint32_t* codes,
+                    const uint16_t* r16, const uint32_t* signs, const uint16_t* rnorm16,
+                    int64_t n, float scale, float* out, void* stream);
+
+/* As tq_sync_status, for the polar context's device error word.                            */
+int tq_polar_sync_status(tq_polar* ctx, void* stream, int* flags);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronises `stream`, then reads and clears the context's device error word.  Returns

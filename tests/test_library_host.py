@@ -71,3 +71,28 @@ def test_context_calls_reject_null_context(tq):
     assert tq.lib.tq_quantize(None, None, 0, 1, 1, None, None, None, None, None) == tq.TQ_ERR_ARG
     assert tq.lib.tq_info(None, None, None, None, None) == tq.TQ_ERR_ARG
     tq.lib.tq_destroy(None)   # no-op
+
+
+@pytest.mark.parametrize("level", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_host_polar_codebook_matches_oracle(tq, level, bits):
+    c, t = tq.host_polar_codebook(level, bits)
+    ref = oracle.angle_codebook(level, bits)
+    assert np.max(np.abs(c - ref.centroids)) < 1e-11
+    assert np.max(np.abs(t - ref.thresholds)) < 1e-11
+
+
+def test_polar_calls_reject_bad_arguments(tq):
+    import ctypes
+    c, t = np.zeros(16), np.zeros(15)
+    assert tq.lib.tq_host_polar_codebook(0, 2, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_host_polar_codebook(2, 5, c.ctypes.data, t.ctypes.data) == tq.TQ_ERR_ARG
+    h = ctypes.c_void_p()
+    assert tq.lib.tq_polar_init(ctypes.byref(h), 0, 100, 3, 1, None, None) == tq.TQ_ERR_ARG   # not a power of two
+    assert tq.lib.tq_polar_init(ctypes.byref(h), 0, 8, 3, 1, None, None) == tq.TQ_ERR_ARG     # below 16
+    assert tq.lib.tq_polar_init(ctypes.byref(h), 0, 128, 5, 1, None, None) == tq.TQ_ERR_ARG   # bits
+    assert tq.lib.tq_polar_init(ctypes.byref(h), 0, 128, 3, 2, None, None) == tq.TQ_ERR_ARG   # qjl flag
+    assert tq.lib.tq_polar_quantize(None, None, 0, 1, 128, None, None, None, None, None) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_polar_scores(None, None, 1, None, None, None, None, 1, 1.0, None, None) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_polar_layout(None, None, None) == tq.TQ_ERR_ARG
+    tq.lib.tq_polar_destroy(None)   # no-op
