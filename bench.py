@@ -521,6 +521,82 @@ def measure_fractional(dev):
             **res}
 
 
+def _decode_polar(pc, d, bits, Pi_t, tables):
+    """x_hat of polar codes on the device (measurement only): unpack the b-bit fields, rebuild
+    y_hat top-down from r16 and the per-level angle centroids, rotate back."""
+    n = pc.codes.shape[0]
+    w = pc.codes.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+    bitsm = (w.unsqueeze(-1) >> torch.arange(32, device=w.device)) & 1
+    stream = bitsm.reshape(n, -1)[:, :(d - 1) * bits].reshape(n, d - 1, bits)
+    codes = (stream << torch.arange(bits, device=w.device)).sum(-1)
+    r = pc.r16.view(torch.float16).float()
+    levels, a, width = [], 0, d // 2
+    while width >= 1:
+        levels.append(codes[:, a:a + width])
+        a += width
+        width //= 2
+    cur = r[:, None]
+    for lev in range(len(levels), 0, -1):
+        ang = tables[lev - 1][levels[lev - 1]]
+        out = torch.empty(n, 2 * cur.shape[1], device=cur.device)
+        out[:, 0::2] = cur * torch.cos(ang)
+        out[:, 1::2] = cur * torch.sin(ang)
+        cur = out
+    return cur @ Pi_t
+
+
+def measure_polar(dev):
+    """Polar-angle encoder (r16 + d - 1 angles of b bits + 1 QJL bit): keys of the decode-layer
+    shape at batch 8 (8 x 8 KV heads x 32768 tokens, d=128, bf16 anisotropic) quantized on the
+    GPU; scores of one 4-query group against every key; D_mse on a 65536-key sample and D_prod
+    of 256 queries x 16384 keys, as in the prefill workload."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    Bf, Hf, Nf, Gf = 8, 8, 32768, 4
+    n = Bf * Hf * Nf
+    fac = inputs.anisotropic_factors(Hf, D, seed=2, device=dev)
+    X = inputs.anisotropic(Bf, Hf, Nf, D, fac, seed=2, device=dev).reshape(n, D)
+    q = inputs.anisotropic(Bf, Hf, Gf, D, fac, seed=2002, device=dev, dtype=torch.float32).reshape(-1, D)
+    g = torch.Generator(device=dev)
+    g.manual_seed(8)
+    sample = torch.randperm(n, generator=g, device=dev)[: 1 << 16]
+    Pi, _ = tq.host_matrices(0, D, D)
+    Pi_t = torch.from_numpy(Pi).to(dev)
+    hbm, _ = peaks()
+    res = {}
+    for label, bits in (("4bit_standard", 3), ("3bit_extreme", 2)):
+        ctx = tq.PolarContext(D, bits, qjl=True, seed=0)
+        pc = ctx.alloc_codes(n, device=dev)
+        ctx.quantize(X, out=pc)
+        t_q, _ = _event_time(lambda: ctx.quantize(X, out=pc))
+        out = torch.empty(Gf, n, device=dev)
+        ctx.scores(q[:Gf], pc, 1.0, out=out)
+        t_s, _ = _event_time(lambda: ctx.scores(q[:Gf], pc, 1.0, out=out), reps=5)
+        if ctx.sync_status():
+            raise RuntimeError("device error flags in the polar workload")
+        tables = [torch.from_numpy(tq.host_polar_codebook(lev, bits)[0]).float().to(dev) for lev in range(1, 8)]
+        xs = X[sample].float()
+        sub = tq.PolarCodes(pc.codes[sample], pc.r16[sample], pc.signs[sample], pc.rnorm[sample])
+        xh = _decode_polar(sub, D, bits, Pi_t, tables)
+        d_mse = float(((xs - xh) ** 2).sum(1).div(xs.pow(2).sum(1)).mean())
+        ks = 1 << 14
+        sk = tq.PolarCodes(sub.codes[:ks].contiguous(), sub.r16[:ks].contiguous(), sub.signs[:ks].contiguous(),
+                           sub.rnorm[:ks].contiguous())
+        Q1 = q[:256]
+        est = ctx.scores(Q1, sk, 1.0)
+        exact = Q1 @ xs[:ks].T
+        den = Q1.pow(2).sum(1)[:, None] * xs[:ks].pow(2).sum(1)[None, :]
+        d_prod = float(((est - exact) ** 2 / den).mean())
+        key_bytes = (ctx.code_words + ctx.sign_words) * 4 + 4
+        score_bytes = n * (key_bytes + Gf * 4)
+        res[label] = {"angle_bits": bits, "code_bytes_per_key": key_bytes, "quantize_ms": t_q * 1e3,
+                      "vectors_per_s": n / t_q, "scores_ms": t_s * 1e3, "scores_per_s": n * Gf / t_s,
+                      "scores_GB_s": score_bytes / t_s / 1e9, "scores_frac_of_measured_hbm": score_bytes / t_s / 1e9 / hbm,
+                      "D_mse": d_mse, "D_prod": d_prod}
+        del pc, out, ctx
+    return {"workload": "8 x 8 KV heads x 32768 keys d=128 bf16 (2.1M vectors); polar r16 + 127 angles + 128 QJL bits",
+            **res}
+
+
 # ----------------------------------------------------------------------------- the oracle arm
 
 def oracle_step_sample(n_keys: int, seed: int = SEED_DATA):
@@ -617,7 +693,7 @@ def main():
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     ap.add_argument("--kernel-path", choices=["auto", "cuda_core", "tensor"], default="auto",
                     help="kernel family of the decode step (tq_set_kernel_path)")
-    ap.add_argument("--only", choices=["search", "prefill", "fractional"], default=None,
+    ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar"], default=None,
                     help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()
     set_batch(args.batch)
@@ -626,7 +702,8 @@ def main():
     world, rank, local = dist_setup()
     if args.only:
         torch.cuda.set_device(local)
-        fn = {"search": measure_search, "prefill": measure_prefill, "fractional": measure_fractional}[args.only]
+        fn = {"search": measure_search, "prefill": measure_prefill, "fractional": measure_fractional,
+              "polar": measure_polar}[args.only]
         print(json.dumps({"only": args.only, **fn(torch.device("cuda", local))}), flush=True)
         return
     if args.impl == "reference":

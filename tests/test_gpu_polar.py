@@ -135,3 +135,31 @@ def test_polar_quantize_then_score():
     z = oracle.PolarQuantized(codes=codes, r16=r16, signs=signs, rnorm16=rn)
     for i in range(4):
         assert_close(got[i], oracle.polar_estimate(Q[i].numpy(), z, pr.Pi, pr.pcb, pr.S), "chained polar scores")
+
+
+@pytest.mark.parametrize("bits", [3, 2])
+def test_polar_full_size_sampled(bits):
+    """The measured workload (8 x 8 KV heads x 32768 keys, d=128, bf16 anisotropic) in the bench's
+    launch shapes: codes of 512 sampled rows against the oracle, and scores of one 4-query group
+    at 512 sampled keys against the oracle estimate from the GPU's own codes."""
+    pr = PolarPair(128, bits, True, seed=0)
+    Bf, Hf, Nf = 8, 8, 32768
+    n = Bf * Hf * Nf
+    fac = inputs.anisotropic_factors(Hf, 128, seed=2, device="cuda")
+    X = inputs.anisotropic(Bf, Hf, Nf, 128, fac, seed=2, device="cuda").reshape(n, 128)
+    q = inputs.anisotropic(Bf, Hf, 4, 128, fac, seed=2002, device="cuda", dtype=torch.float32).reshape(-1, 128)[:4]
+    pc = pr.ctx.quantize(X)
+    out = pr.ctx.scores(q, pc, 1.0)
+    assert pr.ctx.sync_status() == 0
+    g = np.random.default_rng(bits)
+    rows = np.sort(g.choice(n, size=512, replace=False))
+    ridx = torch.from_numpy(rows).cuda()
+    tq = _tq()
+    sub = tq.PolarCodes(pc.codes[ridx].cpu(), pc.r16[ridx].cpu(), pc.signs[ridx].cpu(), pc.rnorm[ridx].cpu())
+    same = pr.check_codes(X[ridx].float().cpu().numpy(), sub)
+    assert same.mean() > 0.97
+    codes, r16, signs, rn = pr.from_device(sub)
+    z = oracle.PolarQuantized(codes=codes, r16=r16, signs=signs, rnorm16=rn)
+    got = out[:, ridx].cpu().numpy()
+    for i in range(4):
+        assert_close(got[i], oracle.polar_estimate(q[i].cpu().numpy(), z, pr.Pi, pr.pcb, pr.S), "full-size polar scores")
