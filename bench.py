@@ -521,6 +521,79 @@ def measure_fractional(dev):
             **res}
 
 
+def measure_decode1(dev):
+    """One decode layer of an 8B-class GQA model at batch 1: 8 KV heads x 32768 tokens, d=128,
+    32 query heads; keys bf16 anisotropic coded at 4 bits (3 MSE + 1 QJL), values bf16.  All keys
+    are quantized, then the step (rotated queries, logits, softmax and the bf16 value sum:
+    tq_attn_output) runs 1000 times eagerly and 1000 times as one captured CUDA graph; the step
+    moves ~85 MB, so launch latency matters and the graph removes it."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    hkv, n, g, seed = 8, 32768, 4, 2
+    ctx = tq.Context(D, 4, seed=0)
+    kfac = inputs.anisotropic_factors(hkv, D, seed=seed, device=dev)
+    vfac = inputs.anisotropic_factors(hkv, D, seed=seed + 1000, device=dev)
+    K = inputs.anisotropic(1, hkv, n, D, kfac, seed=seed, device=dev)
+    V = inputs.anisotropic(1, hkv, n, D, vfac, seed=seed + 1000, device=dev)
+    q = inputs.anisotropic(1, hkv, g, D, kfac, seed=seed + 2000, device=dev, dtype=torch.float32).reshape(1, hkv * g, D)
+    kc = ctx.alloc_codes(1, hkv, n, device=dev)
+    flat = tq.Codes(kc.planes.view(hkv * n, ctx.P, -1), kc.norm.view(-1), kc.signs.view(hkv * n, -1), kc.rnorm.view(-1))
+    ctx.quantize(K.reshape(hkv * n, D), out=flat)
+    t_q, _ = _event_time(lambda: ctx.quantize(K.reshape(hkv * n, D), out=flat), reps=10)
+    length = torch.tensor([n], dtype=torch.int32, device=dev)
+    scale = 1.0 / D ** 0.5
+    ws = ctx.attn_workspace(1, hkv * g, hkv, n, device=dev)
+    out = torch.empty(1, hkv * g, D, device=dev)
+    logits = torch.empty(1, hkv * g, n, device=dev)
+
+    def step():
+        ctx.attn_output(q, kc, n, length, scale, V, out=out, workspace=ws)
+
+    for _ in range(20):
+        step()
+    reps = 1000
+    t_eager, _ = _event_time(step, reps=reps)
+    t_logits, _ = _event_time(lambda: ctx.attn_logits(q, kc, n, length, scale, out=logits, workspace=ws), reps=reps)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    t_graph, _ = _event_time(graph.replay, reps=reps)
+    # the step's 85 MB fit in L2: also time it cold, after writing a 256 MB buffer each time
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record()
+        graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    t_cold = sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs) / 1e3
+    del flush
+    if ctx.sync_status():
+        raise RuntimeError("device error flags in the batch-1 decode workload")
+    keys = hkv * n
+    key_bytes = (ctx.P * ctx.W + ctx.Ws) * 4 + 4
+    step_bytes = keys * (key_bytes + 2 * D)   # codes + bf16 values read once
+    logit_bytes = keys * (key_bytes + g * 4)
+    hbm, _ = peaks()
+    return {"workload": "batch 1, 8 KV heads x 32768 tokens, d=128, 32 query heads; keys 4-bit (3+1), values bf16",
+            "quantize_keys_ms": t_q * 1e3, "quantize_vectors_per_s": keys / t_q,
+            "l2": "step inputs (85 MB) fit in L2: step_ms_graph repeats L2-warm; step_ms_graph_cold after a 256 MB write",
+            "step_ms_eager": t_eager * 1e3, "step_ms_graph": t_graph * 1e3, "step_ms_graph_cold": t_cold * 1e3,
+            "step_GB_s_graph_cold": step_bytes / t_cold / 1e9,
+            "step_frac_of_measured_hbm_graph_cold": step_bytes / t_cold / 1e9 / hbm,
+            "logit_scores_per_s_graph": keys * g / t_graph, "step_GB_s_graph": step_bytes / t_graph / 1e9,
+            "step_frac_of_measured_hbm_graph": step_bytes / t_graph / 1e9 / hbm,
+            "logits_ms": t_logits * 1e3, "logits_GB_s": logit_bytes / t_logits / 1e9,
+            "bytes_per_step": step_bytes, "repeats": reps}
+
+
 def _decode_polar(pc, d, bits, Pi_t, tables):
     """x_hat of polar codes on the device (measurement only): unpack the b-bit fields, rebuild
     y_hat top-down from r16 and the per-level angle centroids, rotate back."""
@@ -693,7 +766,7 @@ def main():
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     ap.add_argument("--kernel-path", choices=["auto", "cuda_core", "tensor"], default="auto",
                     help="kernel family of the decode step (tq_set_kernel_path)")
-    ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar"], default=None,
+    ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar", "decode1"], default=None,
                     help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()
     set_batch(args.batch)
@@ -703,7 +776,7 @@ def main():
     if args.only:
         torch.cuda.set_device(local)
         fn = {"search": measure_search, "prefill": measure_prefill, "fractional": measure_fractional,
-              "polar": measure_polar}[args.only]
+              "polar": measure_polar, "decode1": measure_decode1}[args.only]
         print(json.dumps({"only": args.only, **fn(torch.device("cuda", local))}), flush=True)
         return
     if args.impl == "reference":
