@@ -52,6 +52,7 @@ from .turboquant import (
     search_topk, recall_at_1, fp16_round, QJL_CONST, SplitCodebook, split_quantize, split_dequantize,
     split_estimate, pack_split, unpack_split,
 )
+from . import paged
 from .polar import (
     polar_forward, polar_inverse, angle_pdf, angle_cdf, angle_dof, AngleCodebook, angle_codebook,
     PolarCodebook, polar_codebook, PolarQuantized, polar_codes, polar_rebuild, polar_dequantize,
@@ -59,6 +60,7 @@ from .polar import (
 )
 
 __all__ = [
+    "paged",
     "polar_forward", "polar_inverse", "angle_pdf", "angle_cdf", "angle_dof", "AngleCodebook",
     "angle_codebook", "PolarCodebook", "polar_codebook", "PolarQuantized", "polar_codes",
     "polar_rebuild", "polar_dequantize", "polar_quantize", "polar_estimate", "polar_words",
