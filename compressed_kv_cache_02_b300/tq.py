@@ -64,6 +64,9 @@ _SIGS = {
     "tq_polar_quantize": [_p, _p, _i, _i64, _i64, _p, _p, _p, _p, _p],
     "tq_polar_scores": [_p, _p, _i64, _p, _p, _p, _p, _i64, _f, _p, _p],
     "tq_polar_sync_status": [_p, _p, _p],
+    "tq_paged_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
+    "tq_paged_decode_step": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _f, _p,
+                             _p, _sz, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -392,3 +395,58 @@ class PolarContext:
         if code not in (TQ_OK, TQ_ERR_DEVICE):
             raise TQError(code, "tq_polar_sync_status")
         return flags.value
+
+
+# ---------------------------------------------------------------------------------- paged decode step
+
+@dataclass
+class PagedCache:
+    """Page pools of a compressed KV cache (layout of tq_paged_decode_step)."""
+    kplanes: torch.Tensor
+    ksigns: torch.Tensor
+    knorm: torch.Tensor
+    krnorm: torch.Tensor
+    vplanes: torch.Tensor
+    vnorm: torch.Tensor
+
+
+def alloc_paged_cache(kctx: "Context", vctx: "Context", num_pages: int, Hkv: int, page_size: int,
+                      device="cuda") -> PagedCache:
+    lead = (num_pages, Hkv, page_size)
+    return PagedCache(
+        kplanes=torch.zeros(*lead, kctx.P, kctx.W, dtype=torch.int32, device=device),
+        ksigns=torch.zeros(*lead, kctx.Ws, dtype=torch.int32, device=device),
+        knorm=torch.zeros(*lead, dtype=torch.int16, device=device),
+        krnorm=torch.zeros(*lead, dtype=torch.int16, device=device),
+        vplanes=torch.zeros(*lead, vctx.P, vctx.W, dtype=torch.int32, device=device),
+        vnorm=torch.zeros(*lead, dtype=torch.int16, device=device))
+
+
+def paged_workspace(B, Hq, Hkv, max_pages, page_size, device="cuda") -> torch.Tensor:
+    n = _sz()
+    _check(lib.tq_paged_workspace_size(B, Hq, Hkv, max_pages, page_size, ctypes.byref(n)), "tq_paged_workspace_size")
+    return torch.empty(n.value, dtype=torch.uint8, device=device)
+
+
+def paged_decode_step(kctx: "Context", vctx: "Context", q, k_new, v_new, cache: PagedCache, block_table, length,
+                      scale, out=None, workspace=None, stream=None):
+    """One fused decode step (tq_paged_decode_step): appends k_new / v_new [B, Hkv, 128] at
+    length[b], attends, advances length in place; returns out [B, Hq, 128]."""
+    B, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    num_pages, _, page_size = cache.knorm.shape
+    max_pages = block_table.shape[1]
+    if k_new.dtype != v_new.dtype or k_new.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k_new and v_new must both be float32 or bfloat16")
+    dtype = TQ_BF16 if k_new.dtype == torch.bfloat16 else TQ_F32
+    if out is None:
+        out = torch.empty(B, Hq, d, device=q.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = paged_workspace(B, Hq, Hkv, max_pages, page_size, device=q.device)
+    kn, vn = k_new.contiguous(), v_new.contiguous()
+    _check(lib.tq_paged_decode_step(kctx.h, vctx.h, _ptr(q.contiguous()), _ptr(kn), _ptr(vn), dtype, B, Hq, Hkv,
+                                    _ptr(block_table), max_pages, page_size, num_pages, _ptr(length),
+                                    _ptr(cache.kplanes), _ptr(cache.ksigns), _ptr(cache.knorm), _ptr(cache.krnorm),
+                                    _ptr(cache.vplanes), _ptr(cache.vnorm), float(scale), _ptr(out), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "tq_paged_decode_step")
+    return out

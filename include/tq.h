@@ -331,6 +331,32 @@ int tq_polar_scores(tq_polar* ctx, const float* q, int64_t nq, const uint32_t* c
 /* As tq_sync_status, for the polar context's device error word.                            */
 int tq_polar_sync_status(tq_polar* ctx, void* stream, int* flags);
 
+/* ---------------------------------------------------------------- fused paged decode step
+ * One decode step over a paged compressed KV cache in a single persistent (cooperative) launch.
+ * Pages: juejin.cn post, section 三 (attention logits over the compressed KV cache); csdn
+ * tutorial, section 背景 (every generated token joins the cache).  Readings: a page holds
+ * page_size consecutive token slots of one sequence for every KV head; the pools are
+ *   kplanes [num_pages][Hkv][page_size][P_k][4] u32, ksigns [..][4] u32, knorm, krnorm [..] fp16,
+ *   vplanes [num_pages][Hkv][page_size][P_v][4] u32, vnorm [..] fp16
+ * (rows in the layouts of tq_layout); block_table [B][max_pages] int32 gives the page of
+ * sequence b's tokens i*page_size .. (i+1)*page_size - 1.  The step quantizes k_new and v_new
+ * [B][Hkv][128] (TQ_F32 or TQ_BF16) into position len[b], then for every query head computes
+ *   out[b][h] = sum_{i <= len[b]} softmax_i(scale * est(q[b][h], key_i)) * v_hat_i
+ * (q [B][Hq][128] fp32, GQA groups of Hq / Hkv heads; out [B][Hq][128] fp32), and sets
+ * len[b] += 1.  Keys: a PROD context with d = m = 128 and 1..3 MSE bits; values: an MSE context
+ * with d = 128.  page_size is a positive multiple of 32; the page of position len[b] must be in
+ * the table (an entry outside 0..num_pages-1 or len[b] >= max_pages * page_size sets
+ * TQ_DEVERR_LEN_RANGE in kctx's error word and skips that append).  Device buffers are
+ * caller-owned; planes, signs and the workspace 16-byte aligned; asynchronous on `stream`.
+ * The launch's grid barriers are bounded: one that gives up sets TQ_DEVERR_TIMEOUT.        */
+int tq_paged_workspace_size(int B, int Hq, int Hkv, int max_pages, int page_size, size_t* bytes);
+int tq_paged_decode_step(tq_ctx* kctx, const tq_ctx* vctx, const float* q, const void* k_new,
+                         const void* v_new, int dtype, int B, int Hq, int Hkv,
+                         const int32_t* block_table, int max_pages, int page_size, int num_pages,
+                         int32_t* len, uint32_t* kplanes, uint32_t* ksigns, uint16_t* knorm,
+                         uint16_t* krnorm, uint32_t* vplanes, uint16_t* vnorm, float scale,
+                         float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronises `stream`, then reads and clears the context's device error word.  Returns
