@@ -104,5 +104,5 @@ def test_paged_calls_reject_bad_arguments(tq):
     assert tq.lib.tq_paged_workspace_size(2, 8, 2, 4, 48, ctypes.byref(n)) == tq.TQ_ERR_ARG   # page_size % 32
     assert tq.lib.tq_paged_workspace_size(2, 7, 2, 4, 64, ctypes.byref(n)) == tq.TQ_ERR_ARG   # Hq % Hkv
     assert tq.lib.tq_paged_workspace_size(2, 8, 2, 4, 64, ctypes.byref(n)) == tq.TQ_OK and n.value > 0
-    assert tq.lib.tq_paged_decode_step(None, None, *([None] * 4), 0, 1, 4, 1, None, 1, 32, 1, None,
+    assert tq.lib.tq_paged_decode_step(None, None, *([None] * 3), 0, 1, 4, 1, None, 1, 32, 1, None,
                                        *([None] * 6), 1.0, None, None, 0, None) == tq.TQ_ERR_ARG
