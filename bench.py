@@ -594,6 +594,59 @@ def measure_decode1(dev):
             "bytes_per_step": step_bytes, "repeats": reps}
 
 
+def measure_paged(dev, steps=16, warmup=3):
+    """The headline decode workload (batch 8, 8 KV heads x 131072 cached tokens, keys 2+1 bits,
+    values 3-bit MSE) over a paged cache: pages of 256 tokens placed at random in the pools
+    through the block table, each step one fused persistent launch (append + logits + softmax +
+    values + merge + advance: tq_paged_decode_step).  Inputs (~0.9 GB of pools) exceed L2."""
+    from compressed_kv_cache_02_b300 import tq
+    st = build_state(dev)
+    kctx, vctx, kc, vc, cap = st["kctx"], st["vctx"], st["kc"], st["vc"], st["cap"]
+    ps = 256
+    npp = cap // ps
+    num_pages = B * npp
+    g = torch.Generator(device="cpu")
+    g.manual_seed(11)
+    perm = torch.randperm(num_pages, generator=g).to(dev)
+
+    def pool(x):   # [B, Hkv, cap, ...] -> [num_pages, Hkv, ps, ...], page (b, i) at perm[b * npp + i]
+        rest = x.shape[3:]
+        ordered = x.reshape(B, HKV, npp, ps, *rest).transpose(1, 2).reshape(num_pages, HKV, ps, *rest)
+        out = torch.empty_like(ordered)
+        out[perm] = ordered
+        return out
+
+    cache = tq.PagedCache(kplanes=pool(kc.planes), ksigns=pool(kc.signs), knorm=pool(kc.norm),
+                          krnorm=pool(kc.rnorm), vplanes=pool(vc.planes), vnorm=pool(vc.norm))
+    del kc, vc, st["kc"], st["vc"]
+    table = perm.reshape(B, npp).to(torch.int32).contiguous()
+    length = torch.full((B,), N0, dtype=torch.int32, device=dev)
+    ks, vs, qs = step_inputs(st, warmup + steps, dev)
+    scale = 1.0 / D ** 0.5
+    ws = tq.paged_workspace(B, HQ, HKV, npp, ps, device=dev)
+    out = torch.empty(B, HQ, D, device=dev)
+    for s_ in range(warmup):
+        tq.paged_decode_step(kctx, vctx, qs[s_], ks[s_], vs[s_], cache, table, length, scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s_ in range(warmup, warmup + steps):
+        tq.paged_decode_step(kctx, vctx, qs[s_], ks[s_], vs[s_], cache, table, length, scale, out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    flags = kctx.sync_status()
+    if flags:
+        raise RuntimeError(f"device error flags {flags} in the paged workload")
+    keys = B * HKV * (N0 + warmup + steps / 2)
+    step_bytes = keys * (K_BYTES + V_BYTES)
+    hbm, _ = peaks()
+    return {"workload": WORKLOAD + "; paged cache (256-token pages, random placement), one fused launch per step",
+            "steps": steps, "ms_per_step": t * 1e3, "logit_scores_per_s": keys * G / t,
+            "step_GB_s": step_bytes / t / 1e9, "step_frac_of_measured_hbm": step_bytes / t / 1e9 / hbm,
+            "bytes_per_key": K_BYTES + V_BYTES, "launches_per_step": 1}
+
+
 def _decode_polar(pc, d, bits, Pi_t, tables):
     """x_hat of polar codes on the device (measurement only): unpack the b-bit fields, rebuild
     y_hat top-down from r16 and the per-level angle centroids, rotate back."""
@@ -766,7 +819,7 @@ def main():
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     ap.add_argument("--kernel-path", choices=["auto", "cuda_core", "tensor"], default="auto",
                     help="kernel family of the decode step (tq_set_kernel_path)")
-    ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar", "decode1"], default=None,
+    ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar", "decode1", "paged"], default=None,
                     help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()
     set_batch(args.batch)
@@ -776,7 +829,7 @@ def main():
     if args.only:
         torch.cuda.set_device(local)
         fn = {"search": measure_search, "prefill": measure_prefill, "fractional": measure_fractional,
-              "polar": measure_polar, "decode1": measure_decode1}[args.only]
+              "polar": measure_polar, "decode1": measure_decode1, "paged": measure_paged}[args.only]
         print(json.dumps({"only": args.only, **fn(torch.device("cuda", local))}), flush=True)
         return
     if args.impl == "reference":

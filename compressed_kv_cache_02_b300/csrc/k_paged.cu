@@ -31,9 +31,24 @@
 namespace tq {
 namespace {
 
-constexpr int kPThreads = 256;
+constexpr int kPThreads = 512;
 constexpr int kPWarps = kPThreads / 32;
 constexpr int kBarrierSpins = 1 << 22;   // x ~200 ns: a barrier gives up after about a second
+
+__device__ __forceinline__ void cpa16(void* smem, const void* gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cpa_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
+__device__ __forceinline__ void cpa_wait0() { asm volatile("cp.async.wait_group 0;\n" ::); }
+
+template <int PK>
+struct KeyRow {
+    uint32_t pl[PK][4], sg[4];
+    float n, rho, vn;
+    bool valid;
+};
 
 struct PagedArgs {
     Params kp, vp;
@@ -70,6 +85,7 @@ struct PagedShared {
     float us[4 * 128];
     float x[128], y[128], r[128];
     ulonglong2 sW[kPWarps][32][2];
+    uint4 vbuf[kPWarps][2][32 * 4];   // per warp, double-buffered value rows (up to 4 planes)
     float4 s_wm[kPWarps], s_wl[kPWarps];
     float red[kPWarps];
     float cv[kMaxLevels];
@@ -226,29 +242,50 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
     float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4 ls = make_float4(0.f, 0.f, 0.f, 0.f);
     const int nblk = (k_hi - k_lo + 31) / 32;
-    for (int j = warp; j < nblk; j += kPWarps) {
-        const int key = k_lo + j * 32 + lane;
+    // block jj's value rows (one page: page_size is a multiple of 32) into buffer buf, by cp.async
+    auto issue_vals = [&](int jj, int buf) {
+        size_t r0 = 0;
+        if (jj >= nblk || !slot_of(a, b, k_lo + jj * 32, kvh, r0)) return;
+        const int nk = min(32, k_hi - (k_lo + jj * 32));
+        const uint4* src = reinterpret_cast<const uint4*>(a.vplanes + r0 * (PV * 4));
+        for (int e = lane; e < nk * PV; e += 32) cpa16(&s.vbuf[warp][buf][e], src + e);
+    };
+    // this lane's key of block jj into registers
+    auto load_key = [&](int jj, KeyRow<PK>& kr) {
+        const int key = k_lo + jj * 32 + lane;
         size_t row = 0;
-        const bool valid = key < k_hi && slot_of(a, b, key, kvh, row);
+        kr.valid = jj < nblk && key < k_hi && slot_of(a, b, key, kvh, row);
+        if (!kr.valid) return;
+#pragma unroll
+        for (int p = 0; p < PK; ++p) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.kplanes + row * (PK * 4)) + p);
+            kr.pl[p][0] = v.x; kr.pl[p][1] = v.y; kr.pl[p][2] = v.z; kr.pl[p][3] = v.w;
+        }
+        const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(a.ksigns + row * 4));
+        kr.sg[0] = sv.x; kr.sg[1] = sv.y; kr.sg[2] = sv.z; kr.sg[3] = sv.w;
+        kr.n = half_bits_to_float(__ldcg(a.knorm + row));
+        kr.rho = half_bits_to_float(__ldcg(a.krnorm + row));
+        kr.vn = half_bits_to_float(__ldcg(a.vnorm + row));
+    };
+    KeyRow<PK> cur, nxt;
+    load_key(warp, cur);
+    issue_vals(warp, 0);
+    cpa_commit();
+    int buf = 0;
+    for (int j = warp; j < nblk; j += kPWarps, buf ^= 1) {
+        const int jn = j + kPWarps;
+        issue_vals(jn, buf ^ 1);   // the next block's rows and key are in flight while this one runs
+        cpa_commit();
+        load_key(jn, nxt);
         float4 l4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         float vn = 0.f;
-        if (valid) {
-            uint32_t pl[PK][4], sg[4];
-#pragma unroll
-            for (int p = 0; p < PK; ++p) {
-                const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.kplanes + row * (PK * 4)) + p);
-                pl[p][0] = v.x; pl[p][1] = v.y; pl[p][2] = v.z; pl[p][3] = v.w;
-            }
-            const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(a.ksigns + row * 4));
-            sg[0] = sv.x; sg[1] = sv.y; sg[2] = sv.z; sg[3] = sv.w;
-            const float n = half_bits_to_float(__ldcg(a.knorm + row));
-            const float rho = half_bits_to_float(__ldcg(a.krnorm + row));
-            const float4 e = score_key<PK>(s.Tq, s.Tu, pl, sg, n, rho, r8, kap, cq, cu, 2.f * kq, true);
+        if (cur.valid) {
+            const float4 e = score_key<PK>(s.Tq, s.Tu, cur.pl, cur.sg, cur.n, cur.rho, r8, kap, cq, cu, 2.f * kq, true);
             l4.x = a.scale * e.x;
             l4.y = nh > 1 ? a.scale * e.y : -INFINITY;
             l4.z = nh > 2 ? a.scale * e.z : -INFINITY;
             l4.w = nh > 3 ? a.scale * e.w : -INFINITY;
-            vn = half_bits_to_float(__ldcg(a.vnorm + row));
+            vn = cur.vn;
         }
         // online softmax over the block (one key per lane)
         const float4 mn = f4_max(m4, warp_max4_redux(l4));
@@ -269,18 +306,19 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
         const float4 w = f4_scale(vn, pr);
         s.sW[warp][lane][0] = make_ulonglong2(pk2(w.x, w.x), pk2(w.y, w.y));
         s.sW[warp][lane][1] = make_ulonglong2(pk2(w.z, w.z), pk2(w.w, w.w));
-        // the block's rows for the value sum (all in one page: page_size is a multiple of 32)
         size_t row0 = 0;
         const bool have = slot_of(a, b, k_lo + j * 32, kvh, row0);
         const int nk = min(32, k_hi - (k_lo + j * 32));
+        cpa_wait1();   // this block's value rows have landed
         __syncwarp();
         if (have) {
+            const uint32_t* vb = reinterpret_cast<const uint32_t*>(&s.vbuf[warp][buf][0]);
             for (int t = 0; t < nk; ++t) {
-                const uint32_t* vr = a.vplanes + (row0 + t) * (PV * 4);
+                const uint32_t* vr = vb + t * (PV * 4);
                 uint32_t z = 0u;
 #pragma unroll
                 for (int pp = 0; pp < PV; ++pp) {
-                    const uint32_t wd = __ldcg(vr + pp * 4 + wsel);
+                    const uint32_t wd = vr[pp * 4 + wsel];
                     z |= __funnelshift_r(wd, wd, rot[pp]) & (0x04040404u << pp);
                 }
                 const u64 v01 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4440)),
@@ -298,8 +336,10 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
                 ahi[3] = fma2(v23, wb.y, ahi[3]);
             }
         }
-        __syncwarp();
+        __syncwarp();   // sW and this buffer are reused
+        cur = nxt;
     }
+    cpa_wait0();
     // merge the warps of the CTA
     ls = warp_sum4(ls);
     if (lane == 0) {
@@ -511,8 +551,8 @@ int tq_paged_decode_step(tq_ctx* kctx, const tq_ctx* vctx, const float* q, const
         return tq::fail(TQ_ERR_ARG, "tq_paged_decode_step: NULL buffer");
     if (workspace_bytes < need) return tq::fail(TQ_ERR_ARG, "tq_paged_decode_step: workspace too small");
     if ((reinterpret_cast<uintptr_t>(kplanes) | reinterpret_cast<uintptr_t>(ksigns) |
-         reinterpret_cast<uintptr_t>(workspace)) % 16)
-        return tq::fail(TQ_ERR_ARG, "tq_paged_decode_step: key planes, signs and workspace must be 16-byte aligned");
+         reinterpret_cast<uintptr_t>(vplanes) | reinterpret_cast<uintptr_t>(workspace)) % 16)
+        return tq::fail(TQ_ERR_ARG, "tq_paged_decode_step: planes, signs and workspace must be 16-byte aligned");
     tq::PagedArgs a{};
     a.kp = kctx->prm;
     a.vp = vctx->prm;
