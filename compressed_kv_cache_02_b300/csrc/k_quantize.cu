@@ -129,30 +129,51 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
     }
     __syncthreads();
 
-    // y = Pi x; idx_j = #(thresholds < y_j / n); planes by warp ballots; r' = y - n16 c[idx]
+    // y = Pi x; idx_j = #(thresholds < y_j / n); planes by warp ballots; r' = y - n16 c[idx].
+    // For d <= 128 every output coordinate's sum over j is split between S = 2 (d <= 64: 4)
+    // threads, whose partial sums meet in shared memory: all threads load the matrix, and each
+    // runs half (a quarter) of the dependent loads, which is what a decode append waits on.
+    const int S = d <= 64 ? 4 : (d <= 128 ? 2 : 1);
+    const int span = kQuantThreads / S, part = tid / span, ii = tid - part * span;
+    float* red = rT + (size_t)d * kQuantRows;   // [S - 1][span][kQuantRows] partial sums
     const float4* xT4 = reinterpret_cast<const float4*>(xT);
-    for (int i0 = 0; i0 < d; i0 += kQuantThreads) {
-        const int i = i0 + tid;
+    for (int i0 = 0; i0 < d; i0 += span) {
+        const int i = i0 + ii;
         const bool valid = i < d;
+        const int j0 = part * d / S, j1 = (part + 1) * d / S;
         float acc[kQuantRows];
 #pragma unroll
         for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
         if (valid) {
-            // unrolled so that many loads of Pi^T are in flight (it is usually not in L2 for a
-            // decode append, which is latency-bound)
-#pragma unroll 32
-            for (int j = 0; j < d; ++j) {
-                const float p = __ldg(a.PiT + (size_t)j * d + i);
+            // 32 loads of Pi^T issued before their FMAs (it is usually not in L2 for a decode
+            // append, which waits on these rounds of latency)
+            for (int jb = j0; jb < j1; jb += 32) {
+                float pv[32];
 #pragma unroll
-                for (int q = 0; q < kQuantRows / 4; ++q) {
-                    const float4 xv = xT4[j * (kQuantRows / 4) + q];
-                    acc[4 * q] = fmaf(p, xv.x, acc[4 * q]);
-                    acc[4 * q + 1] = fmaf(p, xv.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(p, xv.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(p, xv.w, acc[4 * q + 3]);
+                for (int u = 0; u < 32; ++u) pv[u] = jb + u < j1 ? __ldg(a.PiT + (size_t)(jb + u) * d + i) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    if (jb + u >= j1) break;
+#pragma unroll
+                    for (int q = 0; q < kQuantRows / 4; ++q) {
+                        const float4 xv = xT4[(jb + u) * (kQuantRows / 4) + q];
+                        acc[4 * q] = fmaf(pv[u], xv.x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(pv[u], xv.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(pv[u], xv.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(pv[u], xv.w, acc[4 * q + 3]);
+                    }
                 }
             }
         }
+        if (S > 1) {   // one pass (span >= d): fold the parts into part 0
+            if (part > 0 && valid)
+                for (int v = 0; v < kQuantRows; ++v) red[((part - 1) * span + ii) * kQuantRows + v] = acc[v];
+            __syncthreads();
+            if (part == 0 && valid)
+                for (int q = 1; q < S; ++q)
+                    for (int v = 0; v < kQuantRows; ++v) acc[v] += red[((q - 1) * span + ii) * kQuantRows + v];
+        }
+        if (part > 0) continue;   // whole warps: span is a multiple of 32
         const int word = (i0 >> 5) + warp;
         // split contexts: coordinates below d_hi (whole words, as d_hi % 32 == 0) use the
         // (P+1)-bit table, whose top bit goes to the partial plane after the P full ones
@@ -193,28 +214,46 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
             s = warp_sum(s);
             if (lane == 0) s_r[v] = sqrtf(s);
         }
-        // sign_j = [((S Pi^T) r')_j > 0]
+        // sign_j = [((S Pi^T) r')_j > 0], the sum over j split as for y
         const float4* rT4 = reinterpret_cast<const float4*>(rT);
-        for (int i0 = 0; i0 < m; i0 += kQuantThreads) {
-            const int i = i0 + tid;
+        const int Sm = m <= 64 ? 4 : (m <= 128 ? 2 : 1);
+        const int spm = kQuantThreads / Sm, pm = tid / spm, im = tid - pm * spm;
+        for (int i0 = 0; i0 < m; i0 += spm) {
+            const int i = i0 + im;
             const bool valid = i < m;
+            const int j0 = pm * d / Sm, j1 = (pm + 1) * d / Sm;
             float acc[kQuantRows];
 #pragma unroll
             for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
             if (valid) {
-#pragma unroll 32
-                for (int j = 0; j < d; ++j) {
-                    const float st = __ldg(a.StT + (size_t)j * m + i);
+                for (int jb = j0; jb < j1; jb += 32) {
+                    float sv[32];
 #pragma unroll
-                    for (int q = 0; q < kQuantRows / 4; ++q) {
-                        const float4 rv = rT4[j * (kQuantRows / 4) + q];
-                        acc[4 * q] = fmaf(st, rv.x, acc[4 * q]);
-                        acc[4 * q + 1] = fmaf(st, rv.y, acc[4 * q + 1]);
-                        acc[4 * q + 2] = fmaf(st, rv.z, acc[4 * q + 2]);
-                        acc[4 * q + 3] = fmaf(st, rv.w, acc[4 * q + 3]);
+                    for (int u = 0; u < 32; ++u) sv[u] = jb + u < j1 ? __ldg(a.StT + (size_t)(jb + u) * m + i) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        if (jb + u >= j1) break;
+#pragma unroll
+                        for (int q = 0; q < kQuantRows / 4; ++q) {
+                            const float4 rv = rT4[(jb + u) * (kQuantRows / 4) + q];
+                            acc[4 * q] = fmaf(sv[u], rv.x, acc[4 * q]);
+                            acc[4 * q + 1] = fmaf(sv[u], rv.y, acc[4 * q + 1]);
+                            acc[4 * q + 2] = fmaf(sv[u], rv.z, acc[4 * q + 2]);
+                            acc[4 * q + 3] = fmaf(sv[u], rv.w, acc[4 * q + 3]);
+                        }
                     }
                 }
             }
+            if (Sm > 1) {
+                __syncthreads();   // the y pass's partial sums are no longer read
+                if (pm > 0 && valid)
+                    for (int v = 0; v < kQuantRows; ++v) red[((pm - 1) * spm + im) * kQuantRows + v] = acc[v];
+                __syncthreads();
+                if (pm == 0 && valid)
+                    for (int q = 1; q < Sm; ++q)
+                        for (int v = 0; v < kQuantRows; ++v) acc[v] += red[((q - 1) * spm + im) * kQuantRows + v];
+            }
+            if (pm > 0) continue;
             const int word = (i0 >> 5) + warp;
 #pragma unroll
             for (int v = 0; v < kQuantRows; ++v) {
@@ -289,7 +328,7 @@ cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n
     // 16 rows per CTA once that fills the SMs twice over, else 4 (decode appends)
     const bool bulk = n >= 2 * 148 * 16;
     const int rows = bulk ? 16 : 4;
-    const size_t smem = 2ull * c->d * rows * sizeof(float);
+    const size_t smem = (2ull * c->d + 3 * 64) * rows * sizeof(float);   // + the split partial sums
     cudaError_t e = bulk ? cudaFuncSetAttribute(quantize_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                          : cudaFuncSetAttribute(quantize_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
