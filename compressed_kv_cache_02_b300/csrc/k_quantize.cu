@@ -16,7 +16,9 @@ namespace tq {
 namespace {
 
 constexpr int kApplyRows = 8;     // input rows per CTA in apply_rows_kernel
-constexpr int kQuantThreads = 256;
+constexpr int kQuantThreads = 256;    // bulk inputs (16 vectors per CTA)
+constexpr int kAppendThreads = 1024;  // decode appends (4 vectors per CTA, sums split 8 ways)
+constexpr int kQuantBatch = 16;       // matrix loads issued before their FMAs
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -76,8 +78,14 @@ struct QuantArgs {
 // append, which then spread over more SMs).  Shared memory: the input tile and the residual
 // tile, both stored [coordinate][vector] so the matrix-vector loops read kQuantRows vectors
 // per j with 16-byte broadcasts.
-template <int kQuantRows>
-__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs a) {
+// Ways the sum over j of one output coordinate is split between threads (T threads per CTA):
+// as many as leave one pass over the outputs, at most 8; 1 for d > T / 2.
+__host__ __device__ constexpr int quant_split(int d, int T) {
+    return d <= T / 8 ? 8 : (d <= T / 4 ? 4 : (d <= T / 2 ? 2 : 1));
+}
+
+template <int kQuantRows, int kT>
+__global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
     static_assert(kQuantRows % 4 == 0, "rows are read four at a time");
     extern __shared__ float4 sm4[];
     const Params& prm = a.prm;
@@ -104,7 +112,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
         }
         s_row[tid] = row;
     }
-    for (int e = tid; e < kQuantRows * d; e += kQuantThreads) {
+    for (int e = tid; e < kQuantRows * d; e += kT) {
         const int v = e / d, j = e - v * d;
         float val = 0.f;
         if (v0 + v < a.n) {
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
     __syncthreads();
 
     // n = ||x||, n16 = fp16(n)
-    for (int v = warp; v < kQuantRows; v += kQuantThreads / 32) {
+    for (int v = warp; v < kQuantRows; v += kT / 32) {
         float s = 0.f;
         for (int j = lane; j < d; j += 32) { const float t = xT[j * kQuantRows + v]; s = fmaf(t, t, s); }
         s = warp_sum(s);
@@ -133,8 +141,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
     // For d <= 128 every output coordinate's sum over j is split between S = 2 (d <= 64: 4)
     // threads, whose partial sums meet in shared memory: all threads load the matrix, and each
     // runs half (a quarter) of the dependent loads, which is what a decode append waits on.
-    const int S = d <= 64 ? 4 : (d <= 128 ? 2 : 1);
-    const int span = kQuantThreads / S, part = tid / span, ii = tid - part * span;
+    const int S = quant_split(d, kT);
+    const int span = kT / S, part = tid / span, ii = tid - part * span;
     float* red = rT + (size_t)d * kQuantRows;   // [S - 1][span][kQuantRows] partial sums
     const float4* xT4 = reinterpret_cast<const float4*>(xT);
     for (int i0 = 0; i0 < d; i0 += span) {
@@ -145,14 +153,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
 #pragma unroll
         for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
         if (valid) {
-            // 32 loads of Pi^T issued before their FMAs (it is usually not in L2 for a decode
+            // kQuantBatch loads of Pi^T issued before their FMAs (it is usually not in L2 for a decode
             // append, which waits on these rounds of latency)
-            for (int jb = j0; jb < j1; jb += 32) {
-                float pv[32];
+            for (int jb = j0; jb < j1; jb += kQuantBatch) {
+                float pv[kQuantBatch];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) pv[u] = jb + u < j1 ? __ldg(a.PiT + (size_t)(jb + u) * d + i) : 0.f;
+                for (int u = 0; u < kQuantBatch; ++u) pv[u] = jb + u < j1 ? __ldg(a.PiT + (size_t)(jb + u) * d + i) : 0.f;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
+                for (int u = 0; u < kQuantBatch; ++u) {
                     if (jb + u >= j1) break;
 #pragma unroll
                     for (int q = 0; q < kQuantRows / 4; ++q) {
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
 
     if (prm.qjl) {
         __syncthreads();
-        for (int v = warp; v < kQuantRows; v += kQuantThreads / 32) {
+        for (int v = warp; v < kQuantRows; v += kT / 32) {
             float s = 0.f;
             for (int j = lane; j < d; j += 32) { const float t = rT[j * kQuantRows + v]; s = fmaf(t, t, s); }
             s = warp_sum(s);
@@ -216,8 +224,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
         }
         // sign_j = [((S Pi^T) r')_j > 0], the sum over j split as for y
         const float4* rT4 = reinterpret_cast<const float4*>(rT);
-        const int Sm = m <= 64 ? 4 : (m <= 128 ? 2 : 1);
-        const int spm = kQuantThreads / Sm, pm = tid / spm, im = tid - pm * spm;
+        const int Sm = quant_split(m, kT);
+        const int spm = kT / Sm, pm = tid / spm, im = tid - pm * spm;
         for (int i0 = 0; i0 < m; i0 += spm) {
             const int i = i0 + im;
             const bool valid = i < m;
@@ -226,12 +234,12 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantArgs
 #pragma unroll
             for (int v = 0; v < kQuantRows; ++v) acc[v] = 0.f;
             if (valid) {
-                for (int jb = j0; jb < j1; jb += 32) {
-                    float sv[32];
+                for (int jb = j0; jb < j1; jb += kQuantBatch) {
+                    float sv[kQuantBatch];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) sv[u] = jb + u < j1 ? __ldg(a.StT + (size_t)(jb + u) * m + i) : 0.f;
+                    for (int u = 0; u < kQuantBatch; ++u) sv[u] = jb + u < j1 ? __ldg(a.StT + (size_t)(jb + u) * m + i) : 0.f;
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
+                    for (int u = 0; u < kQuantBatch; ++u) {
                         if (jb + u >= j1) break;
 #pragma unroll
                         for (int q = 0; q < kQuantRows / 4; ++q) {
@@ -325,16 +333,20 @@ cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n
     a.norm = norm;
     a.rnorm = rnorm;
     a.err = c->derr;
-    // 16 rows per CTA once that fills the SMs twice over, else 4 (decode appends)
+    // 16 rows per CTA once that fills the SMs twice over, else 4 (decode appends) with 1024
+    // threads, which split every sum 8 ways: an append is a chain of dependent loads
     const bool bulk = n >= 2 * 148 * 16;
     const int rows = bulk ? 16 : 4;
-    const size_t smem = (2ull * c->d + 3 * 64) * rows * sizeof(float);   // + the split partial sums
-    cudaError_t e = bulk ? cudaFuncSetAttribute(quantize_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                         : cudaFuncSetAttribute(quantize_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int T = bulk ? kQuantThreads : kAppendThreads;
+    const int S = quant_split(c->d, T), Sm = c->m ? quant_split(c->m, T) : 1;
+    const int extra = std::max((S - 1) * (T / S), (Sm - 1) * (T / Sm));
+    const size_t smem = (2ull * c->d + extra) * rows * sizeof(float);   // + the split partial sums
+    cudaError_t e = bulk ? cudaFuncSetAttribute(quantize_kernel<16, kQuantThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                         : cudaFuncSetAttribute(quantize_kernel<4, kAppendThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((n + rows - 1) / rows);
-    if (bulk) quantize_kernel<16><<<blocks, kQuantThreads, smem, s>>>(a);
-    else quantize_kernel<4><<<blocks, kQuantThreads, smem, s>>>(a);
+    if (bulk) quantize_kernel<16, kQuantThreads><<<blocks, kQuantThreads, smem, s>>>(a);
+    else quantize_kernel<4, kAppendThreads><<<blocks, kAppendThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
