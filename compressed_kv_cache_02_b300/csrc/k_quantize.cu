@@ -26,34 +26,68 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// out[v][i] = sum_j MT[j][i] in[v][j] for kApplyRows rows per CTA: MT is read coalesced
-// along i, each value reused for all rows staged in shared memory.
-__global__ void apply_rows_kernel(const float* __restrict__ MT, int din, int dout,
-                                  const float* __restrict__ in, size_t ldi, int64_t nv,
-                                  float* __restrict__ out, size_t ldo) {
-    extern __shared__ float4 xs4[];   // [din][kApplyRows] floats
+// out[v][i] = sum_j MT[j][i] in[v][j] for kApplyRows rows per CTA: MT is read coalesced along i,
+// each value reused for all rows staged in shared memory.  The sum over j of an output is split
+// between S threads (quant_split below: 8 ways at dout <= 128 with 1024 threads), each issuing
+// its loads kQuantBatch at a time, and the parts meet in shared memory.
+__host__ __device__ constexpr int apply_split(int dout, int T) {
+    return dout <= T / 8 ? 8 : (dout <= T / 4 ? 4 : (dout <= T / 2 ? 2 : 1));
+}
+
+constexpr int kApplyThreads = 1024;
+
+__global__ void __launch_bounds__(kApplyThreads) apply_rows_kernel(const float* __restrict__ MT, int din, int dout,
+                                                                   const float* __restrict__ in, size_t ldi, int64_t nv,
+                                                                   float* __restrict__ out, size_t ldo) {
+    extern __shared__ float4 xs4[];   // [din][kApplyRows] floats, then the partial sums
     float* xs = reinterpret_cast<float*>(xs4);
+    const int S = apply_split(dout, kApplyThreads);
+    const int span = kApplyThreads / S, part = threadIdx.x / span, ii = threadIdx.x - part * span;
+    float* red = xs + (size_t)din * kApplyRows;   // [S - 1][span][kApplyRows]
     const int64_t v0 = (int64_t)blockIdx.x * kApplyRows;
     for (int e = threadIdx.x; e < din * kApplyRows; e += blockDim.x) {
         const int v = e / din, j = e - v * din;
         xs[j * kApplyRows + v] = (v0 + v < nv) ? in[(size_t)(v0 + v) * ldi + j] : 0.f;
     }
     __syncthreads();
-    for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < dout; i += gridDim.y * blockDim.x) {
+    const int j0 = part * din / S, j1 = (part + 1) * din / S;
+    for (int i0 = blockIdx.y * span; i0 < dout; i0 += gridDim.y * span) {
+        const int i = i0 + ii;
+        const bool valid = i < dout;
         float acc[kApplyRows];
 #pragma unroll
         for (int v = 0; v < kApplyRows; ++v) acc[v] = 0.f;
-        for (int j = 0; j < din; ++j) {
-            const float mv = __ldg(MT + (size_t)j * dout + i);
-            const float4 a = xs4[j * 2], b = xs4[j * 2 + 1];
-            acc[0] = fmaf(mv, a.x, acc[0]); acc[1] = fmaf(mv, a.y, acc[1]);
-            acc[2] = fmaf(mv, a.z, acc[2]); acc[3] = fmaf(mv, a.w, acc[3]);
-            acc[4] = fmaf(mv, b.x, acc[4]); acc[5] = fmaf(mv, b.y, acc[5]);
-            acc[6] = fmaf(mv, b.z, acc[6]); acc[7] = fmaf(mv, b.w, acc[7]);
-        }
+        if (valid) {
+            for (int jb = j0; jb < j1; jb += 16) {
+                float mv[16];
 #pragma unroll
-        for (int v = 0; v < kApplyRows; ++v)
-            if (v0 + v < nv) out[(size_t)(v0 + v) * ldo + i] = acc[v];
+                for (int u = 0; u < 16; ++u) mv[u] = jb + u < j1 ? __ldg(MT + (size_t)(jb + u) * dout + i) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (jb + u >= j1) break;
+                    const float4 a = xs4[(jb + u) * 2], b = xs4[(jb + u) * 2 + 1];
+                    acc[0] = fmaf(mv[u], a.x, acc[0]); acc[1] = fmaf(mv[u], a.y, acc[1]);
+                    acc[2] = fmaf(mv[u], a.z, acc[2]); acc[3] = fmaf(mv[u], a.w, acc[3]);
+                    acc[4] = fmaf(mv[u], b.x, acc[4]); acc[5] = fmaf(mv[u], b.y, acc[5]);
+                    acc[6] = fmaf(mv[u], b.z, acc[6]); acc[7] = fmaf(mv[u], b.w, acc[7]);
+                }
+            }
+        }
+        if (S > 1) {   // uniform: the loop runs once (span >= dout)
+            if (part > 0 && valid)
+#pragma unroll
+                for (int v = 0; v < kApplyRows; ++v) red[((part - 1) * span + ii) * kApplyRows + v] = acc[v];
+            __syncthreads();
+            if (part == 0 && valid)
+                for (int q = 1; q < S; ++q)
+#pragma unroll
+                    for (int v = 0; v < kApplyRows; ++v) acc[v] += red[((q - 1) * span + ii) * kApplyRows + v];
+        }
+        if (part == 0 && valid) {
+#pragma unroll
+            for (int v = 0; v < kApplyRows; ++v)
+                if (v0 + v < nv) out[(size_t)(v0 + v) * ldo + i] = acc[v];
+        }
     }
 }
 
@@ -74,16 +108,16 @@ struct QuantArgs {
     int* err;
 };
 
-// One CTA codes kQuantRows vectors (16 for bulk inputs, 4 for the few vectors of a decode
-// append, which then spread over more SMs).  Shared memory: the input tile and the residual
-// tile, both stored [coordinate][vector] so the matrix-vector loops read kQuantRows vectors
-// per j with 16-byte broadcasts.
 // Ways the sum over j of one output coordinate is split between threads (T threads per CTA):
 // as many as leave one pass over the outputs, at most 8; 1 for d > T / 2.
 __host__ __device__ constexpr int quant_split(int d, int T) {
     return d <= T / 8 ? 8 : (d <= T / 4 ? 4 : (d <= T / 2 ? 2 : 1));
 }
 
+// One CTA codes kQuantRows vectors with kT threads (16 vectors and 256 threads for bulk inputs,
+// 4 vectors and 1024 threads for the few vectors of a decode append).  Shared memory: the input
+// tile and the residual tile, both stored [coordinate][vector] so the matrix-vector loops read
+// kQuantRows vectors per j with 16-byte broadcasts, then the split partial sums.
 template <int kQuantRows, int kT>
 __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
     static_assert(kQuantRows % 4 == 0, "rows are read four at a time");
@@ -302,14 +336,14 @@ __global__ void advance_len_kernel(int32_t* len, int B, int64_t cap, int step, i
 cudaError_t launch_apply_rows(const float* MT, int din, int dout, const float* in, size_t ldi,
                               int64_t nv, float* out, size_t ldo, cudaStream_t s) {
     if (nv <= 0) return cudaSuccess;
-    const int threads = dout >= 256 ? 256 : ((dout + 31) / 32) * 32;
-    const size_t smem = (size_t)din * kApplyRows * sizeof(float);
+    const int S = apply_split(dout, kApplyThreads), span = kApplyThreads / S;
+    const size_t smem = ((size_t)din + (size_t)(S - 1) * span) * kApplyRows * sizeof(float);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(apply_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid((unsigned)((nv + kApplyRows - 1) / kApplyRows), (dout + threads - 1) / threads);
-    apply_rows_kernel<<<grid, threads, smem, s>>>(MT, din, dout, in, ldi, nv, out, ldo);
+    dim3 grid((unsigned)((nv + kApplyRows - 1) / kApplyRows), (unsigned)((dout + span - 1) / span));
+    apply_rows_kernel<<<grid, kApplyThreads, smem, s>>>(MT, din, dout, in, ldi, nv, out, ldo);
     return cudaGetLastError();
 }
 
