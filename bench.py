@@ -59,7 +59,7 @@ def set_batch(b: int) -> None:
 # dram__bytes_write.sum; batch 2 of the same workload, one launch each, scaled to a launch here by
 # the keys it scores).  A figure is reported only while the sources it was taken on are unchanged.
 NCU_SOURCES = ["k_attn.cu", "attn_q8.cuh", "lut.cuh", "values.cuh", "tq_device.cuh", "tq_internal.h"]
-NCU_SOURCES_SHA = "a96d59828308ea81"
+NCU_SOURCES_SHA = "9c4a7b59cb9c1b2c"
 NCU_BYTES_PER_KEY = {
     # values_coded128_kernel<3>: 138.455 MB read + 0.036 MB written, 2 x 8 x 131071 keys
     "attn_values": (138.455296e6 + 0.036352e6) / (2 * 8 * 131071),

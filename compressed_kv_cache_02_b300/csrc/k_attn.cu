@@ -395,21 +395,37 @@ __global__ void attn_combine_kernel(const float* __restrict__ partials, int nchu
         orot[j] = s * inv;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        if (PiV) {
-            // many loads of Pi_v in flight: the values pass has usually evicted it from L2
-            float s0 = 0.f, s1 = 0.f;
-            int j = 0;
-#pragma unroll 16
-            for (; j + 1 < d; j += 2) {
-                s0 = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s0);
-                s1 = fmaf(__ldg(PiV + (size_t)(j + 1) * d + i), orot[j + 1], s1);
+    if (!PiV) {
+        for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = orot[i];
+        return;
+    }
+    // o = Pi_v^T orot: each output's sum over j split between S = blockDim / span threads, loads
+    // issued 16 at a time (the values pass has usually evicted Pi_v from L2)
+    const int span = d < (int)blockDim.x ? ((d + 31) / 32) * 32 : (int)blockDim.x;
+    const int S = blockDim.x / span, part = threadIdx.x / span, ii = threadIdx.x - part * span;
+    const bool active = part < S;   // blockDim need not be a multiple of span
+    float* red = orot + d;   // [S - 1][span]
+    const int j0 = part * d / S, j1 = (part + 1) * d / S;
+    for (int i0 = 0; i0 < d; i0 += span) {   // one pass when S > 1
+        const int i = i0 + ii;
+        float acc = 0.f;
+        if (active && i < d) {
+            for (int jb = j0; jb < j1; jb += 16) {
+                float pv[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pv[u] = jb + u < j1 ? __ldg(PiV + (size_t)(jb + u) * d + i) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (jb + u < j1) acc = fmaf(pv[u], orot[jb + u], acc);
             }
-            if (j < d) s0 = fmaf(__ldg(PiV + (size_t)j * d + i), orot[j], s0);
-            o[i] = s0 + s1;
-        } else {
-            o[i] = orot[i];
         }
+        if (S > 1) {
+            if (active && part > 0 && i < d) red[(part - 1) * span + ii] = acc;
+            __syncthreads();
+            if (part == 0 && i < d)
+                for (int q = 1; q < S; ++q) acc += red[(q - 1) * span + ii];
+        }
+        if (part == 0 && i < d) o[i] = acc;
     }
 }
 
@@ -781,9 +797,12 @@ cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int
     else if (W <= 8) e = vc ? run_values<8, true, false>(a, grid, s) : run_values<8, false, false>(a, grid, s);
     else e = vc ? run_values<16, true, false>(a, grid, s) : run_values<16, false, false>(a, grid, s);
     if (e != cudaSuccess) return e;
-    const int threads = d >= 256 ? 256 : ((d + 31) / 32) * 32;
-    attn_combine_kernel<<<B * Hq, threads, d * sizeof(float), s>>>(partials, a.nchunk, a.chunk, d, Hq, len, cap,
-                                                                  vc ? vc->dPi : nullptr, out);
+    // 512 threads: the back-rotation's sums split 4 ways at d <= 128 (2 at d <= 256)
+    const int threads = vc ? 512 : (d >= 256 ? 256 : ((d + 31) / 32) * 32);
+    const int span = d < threads ? ((d + 31) / 32) * 32 : threads;
+    const size_t csmem = ((size_t)d + (size_t)(threads / span - 1) * span) * sizeof(float);
+    attn_combine_kernel<<<B * Hq, threads, csmem, s>>>(partials, a.nchunk, a.chunk, d, Hq, len, cap,
+                                                       vc ? vc->dPi : nullptr, out);
     return cudaGetLastError();
 }
 
