@@ -659,10 +659,81 @@ def measure_paged(dev, steps=16, warmup=3):
     keys = B * HKV * (N0 + warmup + steps / 2)
     step_bytes = keys * (K_BYTES + V_BYTES)
     hbm, _ = peaks()
+    del cache, ks, vs, qs, st
+    torch.cuda.empty_cache()
     return {"workload": WORKLOAD + "; paged cache (256-token pages, random placement), one fused launch per step",
             "steps": steps, "ms_per_step": t * 1e3, "logit_scores_per_s": keys * G / t,
             "step_GB_s": step_bytes / t / 1e9, "step_frac_of_measured_hbm": step_bytes / t / 1e9 / hbm,
-            "bytes_per_key": K_BYTES + V_BYTES, "launches_per_step": 1}
+            "bytes_per_key": K_BYTES + V_BYTES, "launches_per_step": 1,
+            "batch1": measure_paged_small(dev)}
+
+
+def measure_paged_small(dev, reps=200):
+    """Latency-bound size for the fused step: batch 1, 8 KV heads x 32768 cached tokens, keys 2+1
+    bits, values 3-bit MSE.  The fused paged step (one launch) against the unfused step on the
+    same codes (key and value appends, advance, logits, values + combine: 8 launches), each
+    repeated `reps` times back to back (the cache, ~27 MB, stays in L2 in both)."""
+    from compressed_kv_cache_02_b300 import inputs, tq
+    b1, n0, ps = 1, 32768, 256
+    kctx = tq.Context(D, KBITS, seed=SEED_ROT)
+    vctx = tq.Context(D, VBITS, seed=SEED_ROT + 1, mode=tq.TQ_MODE_MSE)
+    cap = n0 + 2 * reps + 1024
+    cap = ((cap + ps - 1) // ps) * ps
+    kfac = inputs.anisotropic_factors(HKV, D, seed=SEED_DATA, device=dev)
+    vfac = inputs.anisotropic_factors(HKV, D, seed=SEED_DATA + 1000, device=dev)
+    K = inputs.anisotropic(b1, HKV, n0, D, kfac, seed=SEED_DATA * 100, device=dev)
+    V = inputs.anisotropic(b1, HKV, n0, D, vfac, seed=SEED_DATA * 100 + 1000, device=dev)
+    kc = kctx.alloc_codes(b1, HKV, cap, device=dev)
+    vc = vctx.alloc_codes(b1, HKV, cap, device=dev)
+    for h in range(HKV):
+        kctx.quantize(K[0, h], out=tq.Codes(kc.planes[0, h, :n0], kc.norm[0, h, :n0], kc.signs[0, h, :n0],
+                                            kc.rnorm[0, h, :n0]))
+        vctx.quantize(V[0, h], out=tq.Codes(vc.planes[0, h, :n0], vc.norm[0, h, :n0]))
+    kn = inputs.anisotropic(b1, HKV, 1, D, kfac, seed=10_001, device=dev)[:, :, 0].contiguous()
+    vn = inputs.anisotropic(b1, HKV, 1, D, vfac, seed=20_001, device=dev)[:, :, 0].contiguous()
+    q = inputs.anisotropic(b1, HKV, G, D, kfac, seed=30_001, device=dev, dtype=torch.float32).reshape(b1, HQ, D)
+    scale = 1.0 / D ** 0.5
+    # unfused: the headline step's calls on this cache
+    length = torch.full((b1,), n0, dtype=torch.int32, device=dev)
+    logits = torch.empty(b1, HQ, cap, device=dev)
+    out = torch.empty(b1, HQ, D, device=dev)
+    ws = kctx.attn_workspace(b1, HQ, HKV, cap, device=dev)
+    vws = tq.values_workspace(D, b1, HQ, HKV, cap, device=dev)
+
+    def unfused():
+        kctx.append(kn, kc, cap, length)
+        vctx.append(vn, vc, cap, length)
+        kctx.advance_len(length, cap)
+        kctx.attn_logits(q, kc, cap, length, scale, out=logits, workspace=ws)
+        tq.attn_values(logits, length, vc, vctx=vctx, out=out, workspace=vws)
+
+    for _ in range(5):
+        unfused()
+    t_unf, _ = _event_time(unfused, reps=reps)
+    # fused: the same codes in pages (identity placement)
+    npp = cap // ps
+
+    def pool(x):
+        rest = x.shape[3:]
+        return x.reshape(b1, HKV, npp, ps, *rest).transpose(1, 2).reshape(b1 * npp, HKV, ps, *rest).contiguous()
+
+    cache = tq.PagedCache(kplanes=pool(kc.planes), ksigns=pool(kc.signs), knorm=pool(kc.norm), krnorm=pool(kc.rnorm),
+                          vplanes=pool(vc.planes), vnorm=pool(vc.norm))
+    table = torch.arange(npp, dtype=torch.int32, device=dev).reshape(b1, npp)
+    plen = torch.full((b1,), n0, dtype=torch.int32, device=dev)
+    pws = tq.paged_workspace(b1, HQ, HKV, npp, ps, device=dev)
+
+    def fused():
+        tq.paged_decode_step(kctx, vctx, q, kn, vn, cache, table, plen, scale, out=out, workspace=pws)
+
+    for _ in range(5):
+        fused()
+    t_fus, _ = _event_time(fused, reps=reps)
+    if kctx.sync_status() or vctx.sync_status():
+        raise RuntimeError("device error flags in the small paged workload")
+    return {"workload": "batch 1, 8 KV heads x 32768 tokens, d=128, 32 query heads; keys 2+1 bits, values 3-bit MSE",
+            "step_ms_unfused": t_unf * 1e3, "launches_unfused": 8, "step_ms_fused_paged": t_fus * 1e3,
+            "launches_fused": 1, "repeats": reps, "l2": "cache ~27 MB, L2-resident in both arms"}
 
 
 def _decode_polar(pc, d, bits, Pi_t, tables):
