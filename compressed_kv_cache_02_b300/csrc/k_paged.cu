@@ -485,14 +485,22 @@ cudaError_t launch_paged_v(const PagedArgs& a, int device, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-// Tokens per chunk: ~2 items per SM over all (batch, KV head, quad) groups at the given capacity,
-// a multiple of 32, at least 256.
+// Tokens per chunk (a multiple of 32).  Phase 2 runs ceil(items / CTAs) rounds of items, items =
+// groups x chunks, and each item pays for its table set-up (~2048 keys' worth of time), so the
+// chunk count minimises rounds x (keys per chunk + 2048) for one CTA per SM of a B300 (148).
 int paged_chunk(int B, int Hkv, int quads, int64_t cap) {
-    int64_t c = ((int64_t)B * Hkv * quads * cap + 2 * 148 - 1) / (2 * 148);
-    c = ((c + 31) / 32) * 32;
-    if (c < 256) c = 256;
-    if (c > cap) c = ((cap + 31) / 32) * 32;
-    return (int)std::max<int64_t>(c, 32);
+    const int64_t groups = (int64_t)B * Hkv * quads, ctas = 148;
+    int64_t best_cost = -1, best = 32;
+    for (int64_t nc = 1; nc <= 64; ++nc) {
+        const int64_t chunk = ((cap + nc - 1) / nc + 31) / 32 * 32;
+        const int64_t rounds = (groups * nc + ctas - 1) / ctas;
+        const int64_t cost = rounds * (chunk + 2048);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = chunk;
+        }
+    }
+    return (int)std::max<int64_t>(best, 32);
 }
 
 }  // namespace

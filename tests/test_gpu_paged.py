@@ -66,7 +66,7 @@ def _prefill(cache, kp, vp, table, lens, ps, K, V):
         getattr(cache, k).copy_(torch.from_numpy(v))
 
 
-@pytest.mark.parametrize("kbits,vbits,G,dtype", [(3, 3, 4, "f32"), (4, 2, 8, "bf16"), (2, 4, 4, "f32")])
+@pytest.mark.parametrize("kbits,vbits,G,dtype", [(3, 3, 4, "f32"), (4, 2, 8, "bf16"), (2, 4, 4, "f32"), (3, 3, 6, "f32")])
 def test_paged_decode_steps(kbits, vbits, G, dtype):
     tq = _tq()
     B, Hkv, ps, num_pages, max_pages, steps = 3, 2, 64, 24, 6, 3
