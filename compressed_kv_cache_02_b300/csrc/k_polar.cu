@@ -53,11 +53,13 @@ constexpr int kPolarQThreads = 128;
 __device__ __forceinline__ int level_offset(int d, int l) { return d - (d >> (l - 1)); }
 
 // Shared memory of the quantize kernel (floats): x, y, radii per level (d - 1 in all), codes.
+// All four arrays are [coordinate or node][vector], so a thread's loop over the vectors of one
+// coordinate is two 16-byte loads and consecutive threads of the tree steps hit consecutive words.
 struct QuantSmem {
-    float x[kPolarVecs][256];
-    float y[kPolarVecs][256];     // rotated rows, then the rebuilt y_hat
-    float rad[kPolarVecs][256];   // radii of every tree node (level-1 nodes first)
-    unsigned char code[kPolarVecs][256];
+    float x[256 * kPolarVecs];
+    float y[256 * kPolarVecs];     // rotated rows, then the rebuilt y_hat
+    float rad[256 * kPolarVecs];   // radii of every tree node (level-1 nodes first)
+    unsigned char code[256 * kPolarVecs];
     float red[kPolarVecs][kPolarQThreads / 32];
     float nrm[kPolarVecs];
 };
@@ -102,7 +104,7 @@ struct PolarQuantArgs {
 };
 
 __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const PolarQuantArgs a) {
-    __shared__ QuantSmem s;
+    __shared__ __align__(16) QuantSmem s;
     const PolarParams& p = a.prm;
     const int d = p.d, nthr = (1 << p.bits) - 1;
     for (int64_t v0 = (int64_t)blockIdx.x * kPolarVecs; v0 < a.n; v0 += (int64_t)gridDim.x * kPolarVecs) {
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
                     xv = a.dtype == TQ_BF16 ? bf16_bits_to_float(static_cast<const uint16_t*>(a.x)[row * a.ld + j])
                                             : static_cast<const float*>(a.x)[row * a.ld + j];
                 }
-                s.x[r][j] = xv;
+                s.x[(j) * kPolarVecs + (r)] = xv;
                 sq[r] = fmaf(xv, xv, sq[r]);
             }
         }
@@ -133,29 +135,35 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
             for (int j = 0; j < d; ++j) {
                 const float w = __ldg(a.PiT + (size_t)j * d + i);
 #pragma unroll
-                for (int r = 0; r < kPolarVecs; ++r) acc[r] = fmaf(w, s.x[r][j], acc[r]);
+                for (int q = 0; q < kPolarVecs / 4; ++q) {
+                    const float4 v = reinterpret_cast<const float4*>(&s.x[j * kPolarVecs])[q];
+                    acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+                }
             }
 #pragma unroll
-            for (int r = 0; r < kPolarVecs; ++r) s.y[r][i] = acc[r];
+            for (int r = 0; r < kPolarVecs; ++r) s.y[(i) * kPolarVecs + (r)] = acc[r];
         }
         __syncthreads();
         // 3. polar transform level by level: node radii into rad, angle codes into code
         for (int l = 1; l <= p.L; ++l) {
             const int nodes = d >> l, off = level_offset(d, l), poff = l > 1 ? level_offset(d, l - 1) : 0;
             for (int e = threadIdx.x; e < nodes * kPolarVecs; e += blockDim.x) {
-                const int r = e / nodes, i = e - r * nodes;
+                const int i = e / kPolarVecs, r = e - i * kPolarVecs;
                 float lo, hi;
                 if (l == 1) {
-                    lo = s.y[r][2 * i];
-                    hi = s.y[r][2 * i + 1];
+                    lo = s.y[(2 * i) * kPolarVecs + (r)];
+                    hi = s.y[(2 * i + 1) * kPolarVecs + (r)];
                 } else {
-                    lo = s.rad[r][poff + 2 * i];
-                    hi = s.rad[r][poff + 2 * i + 1];
+                    lo = s.rad[(poff + 2 * i) * kPolarVecs + (r)];
+                    hi = s.rad[(poff + 2 * i + 1) * kPolarVecs + (r)];
                 }
                 float psi = atan2f(hi, lo);
                 if (l == 1 && psi < 0.f) psi += 6.28318530717958647692f;
-                s.rad[r][off + i] = sqrtf(fmaf(lo, lo, hi * hi));
-                s.code[r][off + i] = (unsigned char)angle_code(psi, p.thr[l - 1], nthr);
+                s.rad[(off + i) * kPolarVecs + (r)] = sqrtf(fmaf(lo, lo, hi * hi));
+                s.code[(off + i) * kPolarVecs + (r)] = (unsigned char)angle_code(psi, p.thr[l - 1], nthr);
             }
             __syncthreads();
         }
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
             uint32_t word = 0u;
             for (int b = 0; b < 32; ++b) {
                 const int t = 32 * w + b, an = t / p.bits;
-                if (an < d - 1) word |= (uint32_t)((s.code[r][an] >> (t - an * p.bits)) & 1) << b;
+                if (an < d - 1) word |= (uint32_t)((s.code[(an) * kPolarVecs + (r)] >> (t - an * p.bits)) & 1) << b;
             }
             a.codes[(v0 + r) * p.cw + w] = word;
         }
@@ -180,21 +188,21 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
         }
         // 5. rebuild y_hat top-down from the stored radius and the angle centroids
         if (threadIdx.x < kPolarVecs)   // the root radius: the stored fp16 norm
-            s.rad[threadIdx.x][d - 2] = half_bits_to_float(float_to_half_bits(sqrtf(s.nrm[threadIdx.x])));
+            s.rad[(d - 2) * kPolarVecs + (threadIdx.x)] = half_bits_to_float(float_to_half_bits(sqrtf(s.nrm[threadIdx.x])));
         __syncthreads();
         for (int l = p.L; l >= 1; --l) {
             const int nodes = d >> l, off = level_offset(d, l), coff = l > 1 ? level_offset(d, l - 1) : 0;
             for (int e = threadIdx.x; e < nodes * kPolarVecs; e += blockDim.x) {
-                const int r = e / nodes, i = e - r * nodes;
-                const float rho = s.rad[r][off + i];
-                const int c = s.code[r][off + i];
+                const int i = e / kPolarVecs, r = e - i * kPolarVecs;
+                const float rho = s.rad[(off + i) * kPolarVecs + (r)];
+                const int c = s.code[(off + i) * kPolarVecs + (r)];
                 const float lo = rho * p.ccos[l - 1][c], hi = rho * p.csin[l - 1][c];
                 if (l == 1) {
-                    s.y[r][2 * i] = lo;
-                    s.y[r][2 * i + 1] = hi;
+                    s.y[(2 * i) * kPolarVecs + (r)] = lo;
+                    s.y[(2 * i + 1) * kPolarVecs + (r)] = hi;
                 } else {
-                    s.rad[r][coff + 2 * i] = lo;
-                    s.rad[r][coff + 2 * i + 1] = hi;
+                    s.rad[(coff + 2 * i) * kPolarVecs + (r)] = lo;
+                    s.rad[(coff + 2 * i + 1) * kPolarVecs + (r)] = hi;
                 }
             }
             __syncthreads();
@@ -210,16 +218,22 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
             for (int i = 0; i < d; ++i) {
                 const float w = __ldg(a.Pi + (size_t)i * d + j);
 #pragma unroll
-                for (int r = 0; r < kPolarVecs; ++r) acc[r] = fmaf(w, s.y[r][i], acc[r]);
+                for (int q = 0; q < kPolarVecs / 4; ++q) {
+                    const float4 v = reinterpret_cast<const float4*>(&s.y[i * kPolarVecs])[q];
+                    acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+                }
             }
 #pragma unroll
             for (int r = 0; r < kPolarVecs; ++r) {
-                const float res = s.x[r][j] - acc[r];
+                const float res = s.x[(j) * kPolarVecs + (r)] - acc[r];
                 rq[r] = fmaf(res, res, rq[r]);
                 acc[r] = res;
             }
 #pragma unroll
-            for (int r = 0; r < kPolarVecs; ++r) s.rad[r][j] = acc[r];   // the residual rows
+            for (int r = 0; r < kPolarVecs; ++r) s.rad[(j) * kPolarVecs + (r)] = acc[r];   // the residual rows
         }
         block_sums(s, rq);
         // 7. signs of S r (thread i: row i of S), one ballot word per warp
@@ -232,7 +246,13 @@ __global__ void __launch_bounds__(kPolarQThreads) polar_quantize_kernel(const Po
                 for (int j = 0; j < d; ++j) {
                     const float w = __ldg(a.ST + (size_t)j * p.m + i);
 #pragma unroll
-                    for (int r = 0; r < kPolarVecs; ++r) acc[r] = fmaf(w, s.rad[r][j], acc[r]);
+                    for (int q = 0; q < kPolarVecs / 4; ++q) {
+                        const float4 v = reinterpret_cast<const float4*>(&s.rad[j * kPolarVecs])[q];
+                        acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                        acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                        acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                        acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+                    }
                 }
             }
 #pragma unroll
