@@ -93,24 +93,36 @@ struct PagedShared {
     int flag;
 };
 
+// Waits until *counter >= target, at most kBarrierSpins polls; on giving up it sets
+// TQ_DEVERR_TIMEOUT and returns false.
+__device__ bool bounded_wait(const int* counter, int target, int* err) {
+    int spins = 0;
+    while (*((const volatile int*)counter) < target) {
+        if (++spins > kBarrierSpins) {
+            set_error(err, TQ_DEVERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(200);
+    }
+    return true;
+}
+
 __device__ bool grid_barrier(int* counter, int* err, int& abort_flag) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(counter, 1);
-        int spins = 0;
-        while (*((volatile int*)counter) < (int)gridDim.x) {
-            if (++spins > kBarrierSpins) {
-                set_error(err, TQ_DEVERR_TIMEOUT);
-                abort_flag = 1;
-                break;
-            }
-            __nanosleep(200);
-        }
+        if (!bounded_wait(counter, (int)gridDim.x, err)) abort_flag = 1;
         __threadfence();
     }
     __syncthreads();
     return abort_flag == 0;
+}
+
+// Self-test of the bounded wait: one thread arrives at a two-party barrier nobody else joins.
+__global__ void wait_selftest_kernel(int* counter, int* err) {
+    atomicAdd(counter, 1);
+    bounded_wait(counter, 2, err);
 }
 
 __device__ __forceinline__ float block_sum(float v, PagedShared& s) {
@@ -612,3 +624,19 @@ int tq_paged_decode_step(tq_ctx* kctx, const tq_ctx* vctx, const float* q, const
 }
 
 }  // extern "C"
+
+extern "C" int tq_selftest_wait_timeout(tq_ctx* ctx, void* stream) {
+    if (!ctx) return tq::fail(TQ_ERR_ARG, "tq_selftest_wait_timeout: context is NULL");
+    int* counter = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&counter), sizeof(int));
+    if (e != cudaSuccess) return tq::fail(TQ_ERR_CUDA, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(counter, 0, sizeof(int), st);
+    if (e == cudaSuccess) {
+        tq::wait_selftest_kernel<<<1, 1, 0, st>>>(counter, ctx->derr);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(counter);
+    return e == cudaSuccess ? TQ_OK : tq::fail(TQ_ERR_CUDA, std::string("wait self-test: ") + cudaGetErrorString(e));
+}

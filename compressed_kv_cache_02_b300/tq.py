@@ -24,7 +24,7 @@ TQ_OK, TQ_ERR_ARG, TQ_ERR_CUDA, TQ_ERR_OOM, TQ_ERR_UNSUPPORTED, TQ_ERR_DEVICE = 
 TQ_F32, TQ_BF16 = 0, 1
 TQ_MODE_PROD, TQ_MODE_MSE = 0, 1
 TQ_MAX_TOPK = 128
-TQ_DEVERR_NORM_OVERFLOW, TQ_DEVERR_LEN_RANGE = 1, 2
+TQ_DEVERR_NORM_OVERFLOW, TQ_DEVERR_LEN_RANGE, TQ_DEVERR_TIMEOUT = 1, 2, 4
 TQ_PATH_AUTO, TQ_PATH_CUDA_CORE, TQ_PATH_TENSOR = 0, 1, 2
 
 _p = ctypes.c_void_p
@@ -65,6 +65,7 @@ _SIGS = {
     "tq_polar_scores": [_p, _p, _i64, _p, _p, _p, _p, _i64, _f, _p, _p],
     "tq_polar_sync_status": [_p, _p, _p],
     "tq_paged_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
+    "tq_selftest_wait_timeout": [_p, _p],
     "tq_paged_decode_step": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _f, _p,
                              _p, _sz, _p],
 }

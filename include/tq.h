@@ -357,6 +357,13 @@ int tq_paged_decode_step(tq_ctx* kctx, const tq_ctx* vctx, const float* q, const
                          uint16_t* krnorm, uint32_t* vplanes, uint16_t* vnorm, float scale,
                          float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Self-test of the bounded device waits (the grid barriers of tq_paged_decode_step use the same
+ * code): launches one thread that arrives at a two-party counter nobody else joins, so its wait
+ * gives up after its poll limit (about a second) and sets TQ_DEVERR_TIMEOUT in ctx's error word;
+ * the kernel then returns and the context stays usable.  Synchronous on `stream`.  Returns
+ * TQ_OK when the launch ran (read the flag with tq_sync_status).                           */
+int tq_selftest_wait_timeout(tq_ctx* ctx, void* stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronises `stream`, then reads and clears the context's device error word.  Returns

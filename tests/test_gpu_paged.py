@@ -137,3 +137,16 @@ def test_paged_step_flags_a_missing_page():
     flags = kp.ctx.sync_status()
     assert flags & tq.TQ_DEVERR_LEN_RANGE
     assert int(length[0]) == 32   # no append, no advance
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """A wait that nothing completes (the self-test kernel) ends with TQ_DEVERR_TIMEOUT instead
+    of hanging; the same context then quantizes normally."""
+    tq = _tq()
+    kp = Pair(D, 3, seed=0)
+    assert tq.lib.tq_selftest_wait_timeout(kp.ctx.h, None) == tq.TQ_OK
+    assert kp.ctx.sync_status() & tq.TQ_DEVERR_TIMEOUT
+    x = torch.randn(8, D).cuda()
+    codes = kp.ctx.quantize(x)
+    assert kp.ctx.sync_status() == 0
+    check_codes(kp, x.cpu().numpy(), codes)
