@@ -1,6 +1,7 @@
 // The C-ABI of libtq (include/tq.h): argument checks, context set-up and the launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -42,8 +43,19 @@ int check_ctx(const tq_ctx* c) {
     return TQ_OK;
 }
 
+// Fault injection for the allocation-failure tests: when >= 0, the table allocation after that
+// many more successful ones fails as if the device were out of memory (then the hook disarms).
+std::atomic<int> g_fail_alloc_after{-1};
+
 template <typename T>
 int upload(T** dst, const std::vector<T>& src) {
+    int armed = g_fail_alloc_after.load();
+    while (armed >= 0 && !g_fail_alloc_after.compare_exchange_weak(armed, armed - 1)) {
+    }
+    if (armed == 0) {
+        *dst = nullptr;
+        return fail(TQ_ERR_OOM, "cudaMalloc of context tables failed: simulated by tq_debug_fail_alloc_after");
+    }
     cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
     if (e != cudaSuccess) {
         *dst = nullptr;
@@ -247,6 +259,12 @@ int tq_init(tq_ctx** out, uint64_t seed, int d, int bits) {
 }
 
 void tq_destroy(tq_ctx* ctx) { free_ctx(ctx); }
+
+int tq_debug_fail_alloc_after(int n) {
+    if (n < -1) return fail(TQ_ERR_ARG, "tq_debug_fail_alloc_after: n >= -1");
+    g_fail_alloc_after.store(n);
+    return TQ_OK;
+}
 
 int tq_info(const tq_ctx* c, int* d, int* m, int* mse_bits, int* mode) {
     TQ_REQUIRE(c != nullptr, TQ_ERR_ARG, "context is NULL");

@@ -66,6 +66,7 @@ _SIGS = {
     "tq_polar_sync_status": [_p, _p, _p],
     "tq_paged_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
     "tq_selftest_wait_timeout": [_p, _p],
+    "tq_debug_fail_alloc_after": [_i],
     "tq_paged_decode_step": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _f, _p,
                              _p, _sz, _p],
 }

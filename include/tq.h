@@ -150,6 +150,12 @@ int tq_code_words(const tq_ctx* ctx, int* words, int* d_hi);
 
 void tq_destroy(tq_ctx* ctx);   /* frees the context's tables; NULL is a no-op */
 
+/* Fault injection for tests: after n more successful table allocations of tq_init* (process-
+ * wide), the next one fails as if the device were out of memory — the init call returns
+ * TQ_ERR_OOM, frees what it had allocated and leaves *out NULL — and the hook disarms.  n = -1
+ * disarms it.  Off by default.                                                             */
+int tq_debug_fail_alloc_after(int n);
+
 /* d, m (0 in MSE mode), MSE bits and mode of a context.  Any output may be NULL.       */
 int tq_info(const tq_ctx* ctx, int* d, int* m, int* mse_bits, int* mode);
 

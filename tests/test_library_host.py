@@ -106,3 +106,8 @@ def test_paged_calls_reject_bad_arguments(tq):
     assert tq.lib.tq_paged_workspace_size(2, 8, 2, 4, 64, ctypes.byref(n)) == tq.TQ_OK and n.value > 0
     assert tq.lib.tq_paged_decode_step(None, None, *([None] * 3), 0, 1, 4, 1, None, 1, 32, 1, None,
                                        *([None] * 6), 1.0, None, None, 0, None) == tq.TQ_ERR_ARG
+
+
+def test_alloc_fault_hook_rejects_bad_values(tq):
+    assert tq.lib.tq_debug_fail_alloc_after(-2) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_debug_fail_alloc_after(-1) == tq.TQ_OK
