@@ -514,6 +514,10 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
 }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::); }
@@ -530,16 +534,16 @@ constexpr int kV2Threads = 256;
 // z = 4 * index of coordinate c, and a byte-permute plus one shared load fetch its centroid.
 // The packed FFMA2 runs over coordinate pairs (0, 1), (2, 3) against each head's weight, which
 // shared memory holds duplicated as (w_h, w_h).
-template <int P>
+template <int P, bool SPLIT>
 __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const ValuesArgs a) {
     constexpr int NW = kV2Threads / 32;
-    constexpr int ROW = P * 4;                  // words per value row
-    constexpr int BUFW = 32 * ROW;              // words per 32-key buffer
+    constexpr int ROW = P * 4;                  // words per value row (split rows: row_words)
+    constexpr int BUFW = 32 * (SPLIT ? ROW + 4 : ROW);   // words per 32-key buffer
     constexpr int SVW = NW * 2 * BUFW > 4 * NW * 32 * 4 ? NW * 2 * BUFW : 4 * NW * 32 * 4;   // + room for the merge
     __shared__ __align__(16) uint32_t sV[SVW];
     __shared__ ulonglong2 sW[NW][32][2];
     __shared__ float4 s_wm[NW], s_wl[NW];
-    __shared__ float s_cv[kMaxLevels];
+    __shared__ float s_cv[kMaxLevels], s_cv_hi[kMaxLevels];
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
     const int L = checked_len(a.len, b, a.cap, a.err);
     const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
@@ -548,7 +552,10 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const int nh = min(4, kvh * a.G + a.G - hbase);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
+    if (SPLIT && threadIdx.x < kMaxLevels) s_cv_hi[threadIdx.x] = a.vprm.centroids_hi[threadIdx.x];
     __syncthreads();
+    // split rows: P full planes, then the top plane of the first d_hi coordinates (W_hi words)
+    const int rw = SPLIT ? a.vprm.row_words : ROW;
     const int64_t iend = min((int64_t)L, i0 + a.chunk);
     const int nblk = (int)((iend - i0 + 31) / 32);
     const size_t rowbase = (size_t)bh * a.cap;
@@ -560,9 +567,15 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     auto issue_block = [&](int j, int buf) {   // the value rows of block j into buffer buf
         const int64_t k0 = i0 + (int64_t)j * 32;
         const int n = (int)min((int64_t)32, iend - k0);
-        const uint4* src = reinterpret_cast<const uint4*>(vrows + (rowbase + k0) * ROW);
-        uint4* dst = reinterpret_cast<uint4*>(buf0 + buf * BUFW);
-        for (int e = lane; e < n * P; e += 32) cp_async16(dst + e, src + e);
+        if constexpr (SPLIT) {   // rows of row_words words need not start on 16 bytes
+            const uint32_t* src = vrows + (rowbase + k0) * rw;
+            uint32_t* dst = buf0 + buf * BUFW;
+            for (int e = lane; e < n * rw; e += 32) cp_async4(dst + e, src + e);
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(vrows + (rowbase + k0) * ROW);
+            uint4* dst = reinterpret_cast<uint4*>(buf0 + buf * BUFW);
+            for (int e = lane; e < n * P; e += 32) cp_async16(dst + e, src + e);
+        }
     };
     auto load_logits = [&](int j, float4& l4, float& vn) {   // key k0 + lane of block j
         const int64_t i = i0 + (int64_t)j * 32 + lane;
@@ -591,6 +604,10 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     int rot[P];   // right-rotation moving bit lane % 8 + 8 c of plane pp to bit 8 c + pp + 3
 #pragma unroll
     for (int pp = 0; pp < P; ++pp) rot[pp] = ((lane & 7) - pp - 2) & 31;
+    // split contexts: a lane's coordinates share word wsel, so the (P+1)-bit table is per lane
+    const bool hi = SPLIT && 32 * wsel < a.vprm.d_hi;
+    const int rot_top = ((lane & 7) - P - 2) & 31;
+    const unsigned char* cvl = hi ? reinterpret_cast<const unsigned char*>(s_cv_hi) : cvb;
     int buf = 0;
     for (int j = warp; j < nblk; j += NW, buf ^= 1) {
         const int jn = j + NW;
@@ -627,7 +644,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
         // p = 0) and its stale row still selects finite centroids, so it adds nothing.
 #pragma unroll 8
         for (int t = 0; t < 32; ++t) {
-            const uint32_t* row = tile + t * ROW;
+            const uint32_t* row = tile + t * (SPLIT ? rw : ROW);
             // byte c of z = 4 * index of owned coordinate c: the offset of its centroid
             uint32_t z = 0u;
 #pragma unroll
@@ -635,10 +652,14 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
                 const uint32_t wd = row[pp * 4 + wsel];
                 z |= __funnelshift_r(wd, wd, rot[pp]) & (0x04040404u << pp);
             }
-            const u64 v01 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4440)),
-                                *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4441)));
-            const u64 v23 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4442)),
-                                *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4443)));
+            if (SPLIT && hi) {
+                const uint32_t wd = row[P * 4 + wsel];
+                z |= __funnelshift_r(wd, wd, rot_top) & (0x04040404u << P);
+            }
+            const u64 v01 = pk2(*reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4440)),
+                                *reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4441)));
+            const u64 v23 = pk2(*reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4442)),
+                                *reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4443)));
             const ulonglong2 wa = sW2[2 * t], wb = sW2[2 * t + 1];
             alo[0] = fma2(v01, wa.x, alo[0]);
             ahi[0] = fma2(v23, wa.x, ahi[0]);
@@ -705,7 +726,13 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
 
 template <int P>
 cudaError_t run_values_coded128(const ValuesArgs& a, dim3 grid, cudaStream_t s) {
-    values_coded128_kernel<P><<<grid, kV2Threads, 0, s>>>(a);
+    if constexpr (P < TQ_MAX_MSE_BITS) {
+        if (a.vprm.d_hi) {
+            values_coded128_kernel<P, true><<<grid, kV2Threads, 0, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
+    values_coded128_kernel<P, false><<<grid, kV2Threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -480,7 +480,8 @@ int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, 
         if (rc) return rc;
         TQ_REQUIRE(vc->mode == TQ_MODE_MSE, TQ_ERR_ARG, "vctx must be an MSE-mode context");
         TQ_REQUIRE(vc->d == d, TQ_ERR_ARG, "d must equal vctx's d");
-        TQ_REQUIRE(vc->d_hi == 0, TQ_ERR_UNSUPPORTED, "tq_attn_values does not take split (fractional bit width) contexts");
+        TQ_REQUIRE(vc->d_hi == 0 || (d > 96 && d <= 128), TQ_ERR_UNSUPPORTED,
+                   "tq_attn_values takes split (fractional bit width) value contexts at 96 < d <= 128 only");
         TQ_REQUIRE(v_norm && aligned(v_norm, 2), TQ_ERR_ARG, "coded values need v_norm");
     }
     TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_values supports d <= 512");

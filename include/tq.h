@@ -139,8 +139,8 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m,
  * Code rows: the b full planes (W words each, as tq_layout) followed by the top plane of the
  * first d_hi coordinates (ceil(d_hi / 32) words: bit j % 32 of word j / 32 holds bit b of
  * idx_j); tq_code_words gives the row length.  tq_quantize, tq_append and tq_attn_logits
- * accept split contexts (CUDA-core kernels); tq_attn_output, tq_attn_values and
- * tq_search_topk return TQ_ERR_UNSUPPORTED for them.                                   */
+ * accept split contexts (CUDA-core kernels), and tq_attn_values split MSE value contexts at
+ * 96 < d <= 128; tq_attn_output and tq_search_topk return TQ_ERR_UNSUPPORTED for them.  */
 int tq_init_split(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int mode, int m,
                   const float* Pi_host, const float* S_host);
 

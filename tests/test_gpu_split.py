@@ -179,3 +179,33 @@ def test_split_contexts_are_refused_where_unsupported():
     with pytest.raises(tq.TQError) as e:
         pr.ctx.attn_output(q, keys, 64, length, 1.0, torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device="cuda"))
     assert e.value.code == tq.TQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("vbits,d_hi,lens", [(3, 64, [1500, 333]), (2, 64, [1500, 1]), (1, 96, [700, 1500]),
+                                            (2, 32, [0, 1500])])
+def test_split_values(vbits, d_hi, lens):
+    """Softmax + value sum over split (fractional bit width) MSE value codes: 2.5 MSE bits per
+    value channel = 2 bits with half the rotated coordinates at 3, and so on."""
+    tq = _tq()
+    d, B, Hkv, G, N = 128, 2, 2, 4, 1500
+    pr = SplitPair(d, vbits, d_hi, mode=tq.TQ_MODE_MSE, seed=31)
+    fac = inputs.anisotropic_factors(Hkv, d, seed=32)
+    V = inputs.anisotropic(B, Hkv, N, d, fac, seed=32)
+    z = pr.oquant(V.float().numpy().reshape(-1, d))
+    vcodes = pr.to_device(z, (B, Hkv, N))
+    g = np.random.default_rng(33)
+    logits = g.normal(0, 2.0, size=(B, Hkv * G, N)).astype(np.float32)
+    length = torch.tensor(lens, dtype=torch.int32).cuda()
+    got = tq.attn_values(torch.from_numpy(logits).cuda(), length, vcodes, vctx=pr.ctx).cpu().numpy()
+    assert pr.ctx.sync_status() == 0
+    idx = z.idx.reshape(B, Hkv, N, d)
+    n16 = z.norm16.reshape(B, Hkv, N)
+    for b in range(B):
+        for h in range(Hkv * G):
+            L = lens[b]
+            if L == 0:
+                assert np.all(got[b, h] == 0)
+                continue
+            p = oracle.turboquant.softmax(logits[b, h, :L].astype(np.float64))
+            Vh = oracle.split_dequantize(idx[b, h // G, :L], n16[b, h // G, :L], pr.Pi, pr.scb)
+            assert_close(got[b, h], p @ Vh, "split values")
