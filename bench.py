@@ -530,11 +530,27 @@ def measure_fractional(dev):
         key_bytes = (ctx.row_words + ctx.Ws) * 4 + 4
         logit_bytes = n * (key_bytes + Gf * 4)
         hbm, _ = peaks()
+        # values at the same fractional width (MSE: bits + 0.5 per channel), softmax + value sum
+        vbits = bits   # the same width as the keys: 3.5 (2.5) bits per value channel
+        vctx = tq.Context(D, vbits, seed=1, mode=tq.TQ_MODE_MSE, d_hi=D // 2)
+        vals = vctx.alloc_codes(Bf, Hf, Nf, device=dev)
+        Vx = inputs.anisotropic(Bf, Hf, Nf, D, inputs.anisotropic_factors(Hf, D, seed=1002, device=dev), seed=1002,
+                                device=dev)
+        vctx.quantize(Vx.reshape(n, D), out=tq.Codes(vals.planes.view(n, -1), vals.norm.view(n)))
+        del Vx
+        vws = tq.values_workspace(D, Bf, Hf * Gf, Hf, Nf, device=dev)
+        vout = torch.empty(Bf, Hf * Gf, D, device=dev)
+        tq.attn_values(logits, length, vals, vctx=vctx, out=vout, workspace=vws)
+        t_v, _ = _event_time(lambda: tq.attn_values(logits, length, vals, vctx=vctx, out=vout, workspace=vws), reps=5)
+        if vctx.sync_status():
+            raise RuntimeError("device error flags in the fractional values")
         res[label] = {"mse_bits": ctx.P + 0.5, "code_bytes_per_key": key_bytes, "quantize_ms": tq_q * 1e3,
                       "vectors_per_s": n / tq_q, "logits_ms": t_l * 1e3, "logit_scores_per_s": n * Gf / t_l,
                       "logits_GB_s": logit_bytes / t_l / 1e9, "logits_frac_of_measured_hbm": logit_bytes / t_l / 1e9 / hbm,
-                      "D_mse": d_mse, "D_prod": d_prod}
-        del keys, flat, logits, ws
+                      "D_mse": d_mse, "D_prod": d_prod,
+                      "values_mse_bits": vbits + 0.5, "values_ms": t_v * 1e3,
+                      "attention_ms": (t_l + t_v) * 1e3}
+        del keys, flat, logits, ws, vals, vws, vout
     return {"workload": "8 x 8 KV heads x 32768 keys d=128 bf16, 32 query heads; first 64 rotated coordinates +1 bit",
             **res}
 
