@@ -163,3 +163,17 @@ def test_polar_full_size_sampled(bits):
     got = out[:, ridx].cpu().numpy()
     for i in range(4):
         assert_close(got[i], oracle.polar_estimate(q[i].cpu().numpy(), z, pr.Pi, pr.pcb, pr.S), "full-size polar scores")
+
+
+def test_polar_empty_calls():
+    """n = 0 rows to quantize and n = 0 keys (or no queries) to score: nothing launches, OK."""
+    tq = _tq()
+    pr = PolarPair(64, 2, True, seed=3)
+    empty = torch.zeros(0, 64, device="cuda")
+    pc = pr.ctx.quantize(empty)
+    assert pc.codes.shape == (0, pr.ctx.code_words)
+    out = pr.ctx.scores(torch.randn(4, 64, device="cuda"), pc, 1.0)
+    assert out.shape == (4, 0)
+    keys = pr.ctx.quantize(torch.randn(10, 64, device="cuda"))
+    assert pr.ctx.scores(torch.zeros(0, 64, device="cuda"), keys, 1.0).shape == (0, 10)
+    assert pr.ctx.sync_status() == 0
