@@ -143,6 +143,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char* sB = sm;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         // for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
         const float nv = nrm > 0.f ? nrm : 1.f;
         // split contexts: this thread's 32 coordinates (one word) are below d_hi or not as a whole
-        const bool hi = 32 * part < prm.d_hi;
+        const bool hi = SPLIT && 32 * part < prm.d_hi;   // ordinary contexts: false at compile time
         const int nb = prm.P + (hi ? 1 : 0);
         uint32_t pw[TQ_MAX_MSE_BITS] = {};
         float rs = 0.f;
@@ -365,13 +366,16 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     a.norm = norm;
     a.rnorm = rnorm;
     a.err = c->derr;
-    cudaError_t e = cudaFuncSetAttribute(quantize_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+    const bool split = c->prm.d_hi > 0;
+    cudaError_t e = split ? cudaFuncSetAttribute(quantize_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal)
+                          : cudaFuncSetAttribute(quantize_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
     if (e != cudaSuccess) return e;
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
     const int64_t ntiles = (n + kTile - 1) / kTile;
     const int grid = (int)(ntiles < sms ? ntiles : sms);
-    quantize_tc_kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
+    if (split) quantize_tc_kernel<true><<<grid, kTcThreads, kSmemTotal, s>>>(a);
+    else quantize_tc_kernel<false><<<grid, kTcThreads, kSmemTotal, s>>>(a);
     return cudaGetLastError();
 }
 
