@@ -33,7 +33,8 @@ from dataclasses import dataclass
 from math import lgamma, log, exp, pi, sqrt
 
 import numpy as np
-from scipy.special import betaincc, ndtri
+from scipy.linalg import solve_banded
+from scipy.special import betaincc, betainccinv, ndtri
 
 
 def _log_norm_const(d: int) -> float:
@@ -111,33 +112,93 @@ class Codebook:
         return float(1.0 - self.d * np.sum(self.cell_prob * self.centroids ** 2))
 
 
-def sphere_codebook(d: int, bits: int, tol: float = 4e-16, max_iter: int = 200000) -> Codebook:
-    """Lloyd-Max quantizer with 2**bits levels for the density f_d.
+# Stop rule of the Newton solve: a further Lloyd step moves no centroid by more than this.  It is
+# the rounding floor of the step itself: a cell's probability is a difference of incomplete-beta
+# values of size ~1/2 (absolute error ~1e-16), i.e. ~1e-14 relative for a cell of probability
+# 1/256, and the cell mean inherits that.
+NEWTON_TOL = 5e-14
 
-    Start: the levels of the N(0, 1/d) quantiles at (k + 1/2) / L (a start only).
-    Step:  thresholds t_k = (c_k + c_{k+1}) / 2; centroids c_k = E[T | t_{k-1} < T < t_k]
-           with t_{-1} = -1 and t_{L-1} = 1.
-    Stop:  when no centroid moves by more than ``tol`` (rounding level: the fixed point is
-           reached to ~1e-16, not just slowed down); then symmetrise (f_d is even).
+
+def _cells(c: np.ndarray, d: float):
+    """Midpoint thresholds of the centroids c and, per cell, (lo, hi, P_k, E[T | cell])."""
+    t = 0.5 * (c[:-1] + c[1:])
+    lo = np.concatenate(([-1.0], t))
+    hi = np.concatenate((t, [1.0]))
+    p = sphere_cell_prob(lo, hi, d)
+    return t, lo, hi, p, sphere_cell_first_moment(lo, hi, d) / p
+
+
+def _sphere_quantiles(probs: np.ndarray, d: float) -> np.ndarray:
+    """t with P(T < t) = prob for the density proportional to (1 - t^2)^((d-3)/2), d > 1 real:
+    T^2 ~ Beta(1/2, (d-1)/2), so the inverse of the regularised incomplete beta gives |t|."""
+    probs = np.asarray(probs, dtype=np.float64)
+    upper = np.where(probs < 0.5, probs, 1.0 - probs)          # P(T > |t|) = upper
+    a = np.sqrt(betainccinv(0.5, 0.5 * (d - 1), 2.0 * upper))
+    return np.where(probs < 0.5, -a, a)
+
+
+def _newton_lloyd(c: np.ndarray, d: int, tol: float, max_iter: int = 200) -> np.ndarray:
+    """Solves the Lloyd-Max conditions c_k = E[T | t_(k-1) < T < t_k], t_k = (c_k + c_(k+1))/2
+    by Newton's method on F(c) = g(c) - c, g one Lloyd step, until one more Lloyd step would move
+    no centroid by more than ``tol`` (the rounding level of the step itself).  With
+    A_k = f(lo_k)(g_k - lo_k)/P_k and B_k = f(hi_k)(hi_k - g_k)/P_k (the derivatives of the cell
+    mean in its edges, which move by 1/2 with each neighbouring centroid), the Jacobian of c - g is
+    tridiagonal:
+        row k:  -A_k/2 at c_(k-1),  1 - (A_k + B_k)/2 at c_k,  -B_k/2 at c_(k+1).
+    A step that would break the ordering of the centroids is halved."""
+    L = len(c)
+    for _ in range(max_iter):
+        _, lo, hi, p, g = _cells(c, d)
+        if np.max(np.abs(g - c)) <= tol:
+            return c
+        A = np.where(np.arange(L) > 0, sphere_marginal_pdf(lo, d) * (g - lo) / p, 0.0)
+        B = np.where(np.arange(L) < L - 1, sphere_marginal_pdf(hi, d) * (hi - g) / p, 0.0)
+        ab = np.zeros((3, L))
+        ab[0, 1:] = -0.5 * B[:-1]          # upper diagonal: row k, column k + 1
+        ab[1] = 1.0 - 0.5 * (A + B)
+        ab[2, :-1] = -0.5 * A[1:]          # lower diagonal: row k, column k - 1
+        step = solve_banded((1, 1), ab, g - c)
+        while True:
+            c_new = c + step
+            if np.all(np.diff(c_new) > 0) and -1.0 < c_new[0] and c_new[-1] < 1.0:
+                break
+            step = 0.5 * step
+        c = c_new
+    raise RuntimeError("Newton iteration on the Lloyd-Max conditions did not converge")
+
+
+def sphere_codebook(d: int, bits: int, tol: float = 4e-16, max_iter: int = 200000) -> Codebook:
+    """Lloyd-Max quantizer with 2**bits levels for the density f_d: the fixed point of
+    thresholds t_k = (c_k + c_{k+1}) / 2 and centroids c_k = E[T | t_{k-1} < T < t_k]
+    (t_{-1} = -1, t_{L-1} = 1), which is unique since f_d is log-concave.
+
+    1 to 4 bits: the Lloyd iteration itself, started at the levels of the N(0, 1/d) quantiles
+    at (k + 1/2) / L, stopped when no centroid moves by more than ``tol`` (rounding level: the
+    fixed point is reached to ~1e-16, not just slowed down).
+    5 to 8 bits: one Lloyd step contracts the error by only ~1 - O(1/L^2) there, so the same
+    fixed point is solved for by Newton's method (``_newton_lloyd``), started at the
+    high-resolution optimum (centroid density proportional to f_d^(1/3), i.e. the quantiles at
+    (k + 1/2) / L of the same family with (d - 3)/2 replaced by (d - 3)/6) and stopped on the
+    residual rule at the rounding floor of a Lloyd step (``NEWTON_TOL``).
+    Finally the table is symmetrised (f_d is even).
     """
     if d < 3:
         raise ValueError("the sphere-marginal codebook needs d >= 3")
     if not 1 <= bits <= 8:
         raise ValueError("bits must be in 1..8")
     L = 1 << bits
-    c = ndtri((np.arange(L) + 0.5) / L) / sqrt(d)
-    for _ in range(max_iter):
-        t = 0.5 * (c[:-1] + c[1:])
-        lo = np.concatenate(([-1.0], t))
-        hi = np.concatenate((t, [1.0]))
-        p = sphere_cell_prob(lo, hi, d)
-        c_new = sphere_cell_first_moment(lo, hi, d) / p
-        moved = np.max(np.abs(c_new - c))
-        c = c_new
-        if moved < tol:
-            break
+    if bits <= 4:
+        c = ndtri((np.arange(L) + 0.5) / L) / sqrt(d)
+        for _ in range(max_iter):
+            _, _, _, _, c_new = _cells(c, d)
+            moved = np.max(np.abs(c_new - c))
+            c = c_new
+            if moved < tol:
+                break
+        else:
+            raise RuntimeError("Lloyd iteration did not converge")
     else:
-        raise RuntimeError("Lloyd iteration did not converge")
+        c = _newton_lloyd(_sphere_quantiles((np.arange(L) + 0.5) / L, (d + 6.0) / 3.0), d, NEWTON_TOL)
     c = 0.5 * (c - c[::-1])
     t = 0.5 * (c[:-1] + c[1:])
     if L % 2 == 0:

@@ -36,7 +36,7 @@ def test_one_bit_closed_form(d, c1, D1):
 
 
 @pytest.mark.parametrize("d", [16, 128, 200])
-@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 8])
 def test_lloyd_conditions_by_independent_quadrature(d, bits):
     cb = sphere_codebook(d, bits)
     c, t = cb.centroids, cb.thresholds
@@ -68,10 +68,22 @@ def test_gaussian_limit_matches_max_1960(bits):
 
 @pytest.mark.parametrize("d", [16, 128])
 def test_distortion_falls_with_bits(d):
-    D = [sphere_codebook(d, b).distortion() for b in (1, 2, 3, 4)]
-    assert all(D[i + 1] < D[i] for i in range(3))
-    # rate-distortion sanity: each extra bit buys at least a factor ~3 (the Gaussian limit is ~3.1-3.6)
-    assert all(D[i] / D[i + 1] > 2.9 for i in range(3))
+    D = [sphere_codebook(d, b).distortion() for b in range(1, 9)]
+    assert all(D[i + 1] < D[i] for i in range(7))
+    # rate-distortion sanity: each extra bit buys at least a factor ~3 (the Gaussian limit is ~3.1-3.6,
+    # tending to 4 at high rate)
+    assert all(4.0 > D[i] / D[i + 1] > 2.9 for i in range(7))
+
+
+def test_high_rate_limit_panter_dite():
+    # High-resolution theory (Panter and Dite, 1951): the b-bit Lloyd-Max distortion of a unit
+    # Gaussian behaves as (pi sqrt(3) / 2) 4^-b.  In the d -> infinity limit of the sphere marginal
+    # (sqrt(d) T -> N(0, 1)) the solved tables approach that constant from below as b grows.
+    C = pi * sqrt(3.0) / 2.0
+    d = 10 ** 6
+    r = [sphere_codebook(d, b).distortion() * 4 ** b for b in (5, 6, 7, 8)]
+    assert all(r[i] < r[i + 1] < C for i in range(3))
+    assert abs(r[-1] / C - 1.0) < 0.015
 
 
 def test_cell_probabilities_sum_to_one():

@@ -14,7 +14,7 @@ def _unit_rows(n, d, seed):
     return g / np.linalg.norm(g, axis=1, keepdims=True)
 
 
-@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 6, 8])
 def test_threshold_count_is_brute_force_nearest(bits):
     cb = sphere_codebook(12, bits)
     u = rng.gaussian_stream(5, 5000) / np.sqrt(12)
@@ -27,7 +27,7 @@ def test_value_on_threshold_takes_lower_index():
     assert np.array_equal(scalar_codes(cb.thresholds, cb), np.arange(len(cb.thresholds)))
 
 
-@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_centroids_round_trip(bits):
     # Each centroid lies inside its own cell: coding a codebook value returns its index,
     # so dequantize-then-code is the identity on the codes.
@@ -42,14 +42,38 @@ def test_mse_matches_table_and_falls_with_bits():
     Pi, _ = rng.method_matrices(1, d, 1)
     X = rng.gaussian_stream(2, n * d).reshape(n, d)
     emp = []
-    for bits in (1, 2, 3, 4):
+    for bits in range(1, 9):
         cb = sphere_codebook(d, bits)
         z = oracle.quantize(X, Pi, cb)
         U = (X @ Pi.T) / np.linalg.norm(X, axis=1, keepdims=True)
         err = np.sum((U - cb.centroids[z.idx]) ** 2, axis=1)
         assert abs(err.mean() - cb.distortion()) < 3 * err.std() / np.sqrt(n)
         emp.append(err.mean())
-    assert all(emp[i + 1] < emp[i] for i in range(3))
+    assert all(emp[i + 1] < emp[i] for i in range(7))
+
+
+@pytest.mark.parametrize("d", [128, 200])
+def test_round_trip_at_eight_bits(d):
+    # "Exact round trip at high bit width" (juejin.cn post, section 四, read at b_m = 8 MSE bits):
+    # coding the reconstruction x_hat = n16 Pi^T c[idx] again returns the same codes wherever the
+    # new rotated direction is not within 1e-5 of a threshold, and the relative reconstruction
+    # error is the table's distortion: mean ||x - x_hat||^2 / ||x||^2 = D(8) within 3 SE (plus the
+    # fp16 norm's at most 2^-22 relative square error), every vector within 3 sqrt(D(8)).
+    n = 2000
+    Pi, _ = rng.method_matrices(3, d, 1)
+    cb = sphere_codebook(d, 8)
+    X = 5.0 * rng.gaussian_stream(11, n * d).reshape(n, d)
+    z = oracle.quantize(X, Pi, cb)
+    Xh = oracle.dequantize(z.idx, z.norm16, Pi, cb)
+    z2 = oracle.quantize(Xh, Pi, cb)
+    U2 = (Xh @ Pi.T) / np.linalg.norm(Xh, axis=1, keepdims=True)
+    near = np.min(np.abs(U2[..., None] - cb.thresholds[None, None, :]), axis=-1) < 1e-5
+    diff = z2.idx != z.idx
+    assert not (diff & ~near).any()
+    assert diff.mean() < 1e-3
+    rel = np.sum((X - Xh) ** 2, axis=1) / np.sum(X ** 2, axis=1)
+    assert abs(rel.mean() - cb.distortion()) < 3 * rel.std() / np.sqrt(n) + 2.0 ** -22
+    assert np.sqrt(rel).max() < 3 * np.sqrt(cb.distortion())
 
 
 def test_reconstruction_error_and_norm():
