@@ -260,24 +260,35 @@ def test_attention_values_code_widths(vbits, d):
 
 
 def test_decode_append_and_advance():
+    """Decode-step append: every appended row lands at position len[b] + s of its (batch, head)
+    and passes the quantize parity rules there (codes by the threshold band, signs on the GPU's
+    own codes, norm and residual norm within one fp16 ulp); every other slot keeps the zeros of
+    the freshly allocated cache."""
     tq = _tq()
     d, B, H, cap = 128, 2, 3, 40
+    L0 = [5, 17]
     pr = Pair(d, 3, seed=2)
     cache = pr.ctx.alloc_codes(B, H, cap)
-    length = torch.tensor([5, 17], dtype=torch.int32).cuda()
+    length = torch.tensor(L0, dtype=torch.int32).cuda()
     steps = [inputs.gaussian(B * H, d, seed=100 + s).reshape(B, H, d) for s in range(3)]
     for x in steps:
         pr.ctx.append(x.cuda(), cache, cap, length)
         pr.ctx.advance_len(length, cap)
     assert pr.ctx.sync_status() == 0
-    assert length.cpu().tolist() == [8, 20]
-    idx, n16, signs, r16 = pr.from_device(cache)
-    idx = idx.reshape(B, H, cap, d)
+    assert length.cpu().tolist() == [L + len(steps) for L in L0]
+    written = torch.zeros(B, H, cap, dtype=torch.bool)
     for s, x in enumerate(steps):
-        z = pr.oquant(x.numpy())
-        for b, L0 in enumerate([5, 17]):
-            rows = idx[b, :, L0 + s]
-            assert (rows == z.idx[b]).mean() > 0.999
+        pos = [L + s for L in L0]
+        rows = tq.Codes(planes=torch.stack([cache.planes[b, :, pos[b]] for b in range(B)]).reshape(B * H, pr.P, -1),
+                        norm=torch.stack([cache.norm[b, :, pos[b]] for b in range(B)]).reshape(B * H),
+                        signs=torch.stack([cache.signs[b, :, pos[b]] for b in range(B)]).reshape(B * H, -1),
+                        rnorm=torch.stack([cache.rnorm[b, :, pos[b]] for b in range(B)]).reshape(B * H))
+        check_codes(pr, x.numpy().reshape(B * H, d), rows)
+        for b in range(B):
+            written[b, :, pos[b]] = True
+    for field in (cache.planes, cache.signs, cache.norm, cache.rnorm):
+        f = field.cpu()
+        assert not f[~written].any(), "a slot other than len[b] + step was written"
     # an out-of-range length is flagged and skipped, not written
     bad = torch.tensor([cap, 0], dtype=torch.int32).cuda()
     before = cache.planes.clone()
