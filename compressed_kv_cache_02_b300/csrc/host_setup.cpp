@@ -164,29 +164,117 @@ void seeded_matrices(uint64_t seed, int d, int m, std::vector<double>& Pi, std::
     Pi = haar_from_gaussian(std::move(G), d);
 }
 
+// One Lloyd step from centroids c: thresholds t at the midpoints, and per cell its probability
+// m0, first moment m1 and mean g = m1 / m0 (the new centroid).
+static void lloyd_cells(const SphereMarginal& f, const std::vector<double>& c, std::vector<double>& t,
+                        std::vector<double>& m0, std::vector<double>& g) {
+    const int L = (int)c.size();
+    t.resize(L - 1);
+    m0.resize(L);
+    g.resize(L);
+    for (int k = 0; k + 1 < L; ++k) t[k] = 0.5 * (c[k] + c[k + 1]);
+    for (int k = 0; k < L; ++k) {
+        const double a = (k == 0) ? -1.0 : t[k - 1];
+        const double b = (k == L - 1) ? 1.0 : t[k];
+        double p0, p1;
+        f.moments(a, b, p0, p1);
+        m0[k] = p0;
+        g[k] = p0 > 0.0 ? p1 / p0 : c[k];
+    }
+}
+
+// Start for many levels: the high-resolution optimum, whose centroid density is proportional to
+// f^(1/3) = (1 - t^2)^((d-3)/6) (up to a constant): its quantiles at (k + 1/2) / L, from the
+// cumulative integral of f^(1/3) on a fine grid (composite Gauss-Legendre), linearly interpolated.
+static std::vector<double> high_rate_start(int d, int L) {
+    const double reach = std::min(1.0, 40.0 / std::sqrt((double)d));
+    const int panels = 8192;
+    const double step = 2.0 * reach / panels;
+    GaussLegendre gl(16);
+    std::vector<double> edge(panels + 1), cum(panels + 1, 0.0);
+    for (int i = 0; i <= panels; ++i) edge[i] = -reach + i * step;
+    for (int i = 0; i < panels; ++i) {
+        const double mid = edge[i] + 0.5 * step, half = 0.5 * step;
+        double acc = 0.0;
+        for (size_t n = 0; n < gl.x.size(); ++n) {
+            const double x = mid + half * gl.x[n];
+            acc += gl.w[n] * half * std::exp((d - 3) / 6.0 * std::log1p(-x * x));
+        }
+        cum[i + 1] = cum[i] + acc;
+    }
+    std::vector<double> c(L);
+    int i = 0;
+    for (int k = 0; k < L; ++k) {
+        const double target = (k + 0.5) / L * cum[panels];
+        while (i + 1 < panels && cum[i + 1] < target) ++i;
+        const double w = cum[i + 1] - cum[i];
+        c[k] = edge[i] + (w > 0.0 ? (target - cum[i]) / w : 0.5) * step;
+    }
+    return c;
+}
+
 // Lloyd-Max: thresholds at midpoints of adjacent centroids, centroids at the conditional
-// means of their cells; repeated to a fixed point (unique: f_d is log-concave for d >= 3).
+// means of their cells; the fixed point is unique (f_d is log-concave for d >= 3).
+// Up to 4 bits it is reached by repeating the Lloyd step.  From 5 bits on one step contracts the
+// error by only ~1 - O(1/L^2), so the same conditions are solved by Newton's method on
+// F(c) = g(c) - c from the high-rate start: with A_k = f(lo_k)(g_k - lo_k)/m0_k and
+// B_k = f(hi_k)(hi_k - g_k)/m0_k (the cell mean's derivatives in its edges, each edge moving by
+// 1/2 with its two centroids) the Jacobian of c - g is tridiagonal, row k being
+// (-A_k/2, 1 - (A_k + B_k)/2, -B_k/2); it is solved by the Thomas algorithm, a step that would
+// break the ordering is halved, and the solve stops once a further Lloyd step would move no
+// centroid by more than 5e-14 (the rounding level of the step's quadrature).
 void lloyd_max_codebook(int d, int bits, std::vector<double>& c, std::vector<double>& t) {
     const int L = 1 << bits;
     SphereMarginal f(d);
     c.resize(L);
     t.resize(L - 1);
-    const double spread = std::min(1.0, 2.0 / std::sqrt((double)d));   // start inside (-1, 1)
-    for (int k = 0; k < L; ++k) c[k] = (2.0 * k + 1.0 - L) / L * spread;
-    std::vector<double> cn(L);
-    for (int it = 0; it < 200000; ++it) {
-        for (int k = 0; k + 1 < L; ++k) t[k] = 0.5 * (c[k] + c[k + 1]);
-        double moved = 0.0;
-        for (int k = 0; k < L; ++k) {
-            double a = (k == 0) ? -1.0 : t[k - 1];
-            double b = (k == L - 1) ? 1.0 : t[k];
-            double m0, m1;
-            f.moments(a, b, m0, m1);
-            cn[k] = m0 > 0.0 ? m1 / m0 : c[k];
-            moved = std::max(moved, std::fabs(cn[k] - c[k]));
+    std::vector<double> m0, g;
+    if (bits <= 4) {
+        const double spread = std::min(1.0, 2.0 / std::sqrt((double)d));   // start inside (-1, 1)
+        for (int k = 0; k < L; ++k) c[k] = (2.0 * k + 1.0 - L) / L * spread;
+        for (int it = 0; it < 200000; ++it) {
+            lloyd_cells(f, c, t, m0, g);
+            double moved = 0.0;
+            for (int k = 0; k < L; ++k) moved = std::max(moved, std::fabs(g[k] - c[k]));
+            c = g;
+            if (moved < 4e-16) break;   // at the fixed point up to rounding
         }
-        c = cn;
-        if (moved < 4e-16) break;   // at the fixed point up to rounding
+    } else {
+        c = high_rate_start(d, L);
+        std::vector<double> lo(L), di(L), up(L), rhs(L), step(L), cn(L);
+        for (int it = 0; it < 200; ++it) {
+            lloyd_cells(f, c, t, m0, g);
+            double res = 0.0;
+            for (int k = 0; k < L; ++k) res = std::max(res, std::fabs(g[k] - c[k]));
+            if (res <= 5e-14) break;
+            for (int k = 0; k < L; ++k) {
+                const double a = (k == 0) ? -1.0 : t[k - 1];
+                const double b = (k == L - 1) ? 1.0 : t[k];
+                const double A = (k == 0) ? 0.0 : f.pdf(a) * (g[k] - a) / m0[k];
+                const double B = (k == L - 1) ? 0.0 : f.pdf(b) * (b - g[k]) / m0[k];
+                lo[k] = -0.5 * A;
+                di[k] = 1.0 - 0.5 * (A + B);
+                up[k] = -0.5 * B;
+                rhs[k] = g[k] - c[k];
+            }
+            // Thomas algorithm: forward elimination, back substitution
+            for (int k = 1; k < L; ++k) {
+                const double w = lo[k] / di[k - 1];
+                di[k] -= w * up[k - 1];
+                rhs[k] -= w * rhs[k - 1];
+            }
+            step[L - 1] = rhs[L - 1] / di[L - 1];
+            for (int k = L - 2; k >= 0; --k) step[k] = (rhs[k] - up[k] * step[k + 1]) / di[k];
+            for (int halvings = 0; halvings < 60; ++halvings) {
+                bool ok = true;
+                for (int k = 0; k < L; ++k) cn[k] = c[k] + step[k];
+                if (!(cn[0] > -1.0 && cn[L - 1] < 1.0)) ok = false;
+                for (int k = 0; ok && k + 1 < L; ++k) ok = cn[k] < cn[k + 1];
+                if (ok) break;
+                for (double& v : step) v *= 0.5;
+            }
+            c = cn;
+        }
     }
     for (int k = 0; k < L / 2; ++k) {   // the density is even: symmetrise
         double s = 0.5 * (c[L - 1 - k] - c[k]);

@@ -275,12 +275,12 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
     float4* sW = sm + Scorer<W, P>::smem_bytes(prm) / sizeof(float4);   // [kThreads]
     float4* sRed = sW + kThreads;                                        // [kThreads / 32]
     __shared__ float4 s_m, s_l, s_alpha;
-    __shared__ float s_cv[kMaxLevels];
+    __shared__ float s_cv[kMaxCodeLevels];   // the value table (coded values; any MSE width)
     if (threadIdx.x == 0) {
         s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         s_l = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
+    for (int k = threadIdx.x; k < a.vprm.L; k += blockDim.x) s_cv[k] = a.vprm.tab[k];
     const ValueSrc v{a.values, a.vnorm, a.vprm.P, a.vprm.W, prm.d};
     float4 acc[C];
 #pragma unroll
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kValThreads) values_kernel(const ValuesArgs a)
     __shared__ float4 sRed[kValThreads / 32];
     extern __shared__ float4 red[];   // [kValThreads / 32][C][32]
     __shared__ float4 s_m, s_l, s_alpha;
-    __shared__ float s_cv[kMaxLevels];
+    __shared__ float s_cv[kMaxCodeLevels];   // the value table (coded values; any MSE width)
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
     const int L = checked_len(a.len, b, a.cap, a.err);
     const int64_t i0 = (int64_t)blockIdx.x * a.chunk;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kValThreads) values_kernel(const ValuesArgs a)
         s_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         s_l = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (threadIdx.x < kMaxLevels) s_cv[threadIdx.x] = a.vprm.centroids[threadIdx.x];
+    for (int k = threadIdx.x; k < a.vprm.L; k += blockDim.x) s_cv[k] = a.vprm.tab[k];
     float4 acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
 
 template <int P>
 cudaError_t run_values_coded128(const ValuesArgs& a, dim3 grid, cudaStream_t s) {
-    if constexpr (P < TQ_MAX_MSE_BITS) {
+    if constexpr (P < kFastBits) {
         if (a.vprm.d_hi) {
             values_coded128_kernel<P, true><<<grid, kV2Threads, 0, s>>>(a);
             return cudaGetLastError();
@@ -812,7 +812,7 @@ cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int
     dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
     const int W = (d + 31) / 32;
     cudaError_t e;
-    if (vc && W == 4) {
+    if (vc && W == 4 && vc->P <= kFastBits) {
         switch (vc->P) {
             case 1: e = run_values_coded128<1>(a, grid, s); break;
             case 2: e = run_values_coded128<2>(a, grid, s); break;

@@ -83,16 +83,16 @@ __global__ void __launch_bounds__(kSplitThreads) logits_split_kernel(const Split
         const uint32_t* cr = a.k.planes + row * prm.row_words;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int w = 0; w < prm.W; ++w) {
-            uint32_t pw[TQ_MAX_MSE_BITS];
+            uint32_t pw[kFastBits];
 #pragma unroll
-            for (int p = 0; p < TQ_MAX_MSE_BITS; ++p) pw[p] = p < prm.P ? __ldg(cr + p * prm.W + w) : 0u;
+            for (int p = 0; p < kFastBits; ++p) pw[p] = p < prm.P ? __ldg(cr + p * prm.W + w) : 0u;
             const bool hi = 32 * w < prm.d_hi;   // whole words: d_hi % 32 == 0
             const uint32_t top = hi ? __ldg(cr + prm.P * prm.W + w) : 0u;
             const int nj = min(32, d - 32 * w);
             for (int t = 0; t < nj; ++t) {
                 int idx = 0;
 #pragma unroll
-                for (int p = 0; p < TQ_MAX_MSE_BITS; ++p) idx |= (int)((pw[p] >> t) & 1u) << p;
+                for (int p = 0; p < kFastBits; ++p) idx |= (int)((pw[p] >> t) & 1u) << p;
                 idx |= (int)((top >> t) & 1u) << prm.P;
                 const float c = hi ? s_chi[idx] : s_clo[idx];
                 acc = f4_fma(c, sq4[32 * w + t], acc);

@@ -558,8 +558,9 @@ int tq_paged_decode_step(tq_ctx* kctx, const tq_ctx* vctx, const float* q, const
     if (kctx->mode != TQ_MODE_PROD || kctx->d != 128 || kctx->m != 128 || kctx->d_hi || !kctx->prm.odd_walsh)
         return tq::fail(TQ_ERR_UNSUPPORTED, "tq_paged_decode_step: keys need a PROD context with d = m = 128 "
                                             "(not split)");
-    if (vctx->mode != TQ_MODE_MSE || vctx->d != 128 || vctx->d_hi)
-        return tq::fail(TQ_ERR_UNSUPPORTED, "tq_paged_decode_step: values need an MSE context with d = 128");
+    if (vctx->mode != TQ_MODE_MSE || vctx->d != 128 || vctx->d_hi || vctx->P > tq::kFastBits)
+        return tq::fail(TQ_ERR_UNSUPPORTED, "tq_paged_decode_step: values need an MSE context with d = 128 "
+                                            "and 1..4 bits (not split)");
     if (dtype != TQ_F32 && dtype != TQ_BF16) return tq::fail(TQ_ERR_ARG, "tq_paged_decode_step: dtype");
     size_t need = 0;
     int rc = tq_paged_workspace_size(B, Hq, Hkv, max_pages, page_size, &need);

@@ -118,7 +118,9 @@ __host__ __device__ constexpr int quant_split(int d, int T) {
 // 4 vectors and 1024 threads for the few vectors of a decode append).  Shared memory: the input
 // tile and the residual tile, both stored [coordinate][vector] so the matrix-vector loops read
 // kQuantRows vectors per j with 16-byte broadcasts, then the split partial sums.
-template <int kQuantRows, int kT>
+// WIDE (more than kFastBits MSE bits, MSE mode): the table is read from prm.tab into shared
+// memory instead of the kernel parameters.
+template <int kQuantRows, int kT, bool WIDE>
 __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
     static_assert(kQuantRows % 4 == 0, "rows are read four at a time");
     extern __shared__ float4 sm4[];
@@ -128,6 +130,14 @@ __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
     float* rT = xT + (size_t)d * kQuantRows;      // [d][kQuantRows]
     __shared__ float s_n[kQuantRows], s_n16[kQuantRows], s_r[kQuantRows];
     __shared__ long long s_row[kQuantRows];
+    constexpr int kTab = WIDE ? kMaxCodeLevels : 1;
+    __shared__ float s_cen[kTab], s_thr[kTab];
+    if constexpr (WIDE) {
+        for (int k = threadIdx.x; k < kMaxCodeLevels; k += kT) {
+            s_cen[k] = k < prm.L ? prm.tab[k] : 0.f;
+            s_thr[k] = k < prm.L - 1 ? prm.tab[prm.L + k] : INFINITY;
+        }
+    }
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t v0 = (int64_t)blockIdx.x * kQuantRows;
@@ -227,13 +237,23 @@ __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
             const float u = (n > 0.f) ? acc[v] / n : 0.f;
             // #{k : t_k < u} by binary search over the sorted thresholds
             int idx = 0;
+            if constexpr (WIDE) {
 #pragma unroll
-            for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
-                if (b < nb) {
-                    const int k = idx + (1 << b) - 1;
-                    if (u > (hi ? prm.thresholds_hi[k] : prm.thresholds[k])) idx += 1 << b;
-                }
-            if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
+                for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
+                    if (b < nb) {
+                        const int k = idx + (1 << b) - 1;
+                        if (u > s_thr[k]) idx += 1 << b;
+                    }
+            } else {
+#pragma unroll
+                for (int b = kFastBits - 1; b >= 0; --b)
+                    if (b < nb) {
+                        const int k = idx + (1 << b) - 1;
+                        if (u > (hi ? prm.thresholds_hi[k] : prm.thresholds[k])) idx += 1 << b;
+                    }
+            }
+            const float cval = WIDE ? s_cen[idx] : (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
+            if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * cval;
             const long long row = s_row[v];
             for (int p = 0; p < prm.P; ++p) {
                 const unsigned bits = __ballot_sync(0xffffffffu, valid && ((idx >> p) & 1));
@@ -375,13 +395,18 @@ cudaError_t launch_quantize(const tq_ctx* c, const void* x, int dtype, int64_t n
     const int S = quant_split(c->d, T), Sm = c->m ? quant_split(c->m, T) : 1;
     const int extra = std::max((S - 1) * (T / S), (Sm - 1) * (T / Sm));
     const size_t smem = (2ull * c->d + extra) * rows * sizeof(float);   // + the split partial sums
-    cudaError_t e = bulk ? cudaFuncSetAttribute(quantize_kernel<16, kQuantThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                         : cudaFuncSetAttribute(quantize_kernel<4, kAppendThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((n + rows - 1) / rows);
-    if (bulk) quantize_kernel<16, kQuantThreads><<<blocks, kQuantThreads, smem, s>>>(a);
-    else quantize_kernel<4, kAppendThreads><<<blocks, kAppendThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    auto run = [&](auto kernel, int threads) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kernel<<<blocks, threads, smem, s>>>(a);
+        return cudaGetLastError();
+    };
+    if (c->P > kFastBits)
+        return bulk ? run(quantize_kernel<16, kQuantThreads, true>, kQuantThreads)
+                    : run(quantize_kernel<4, kAppendThreads, true>, kAppendThreads);
+    return bulk ? run(quantize_kernel<16, kQuantThreads, false>, kQuantThreads)
+                : run(quantize_kernel<4, kAppendThreads, false>, kAppendThreads);
 }
 
 cudaError_t launch_advance_len(int32_t* len, int B, int64_t cap, int step, int* err, cudaStream_t s) {

@@ -33,7 +33,8 @@ constexpr uint32_t kMatBytes = 128 * 128 * 2;   // one 128 x 128 bf16 operand
 constexpr uint32_t kSmemB = 6 * kMatBytes;      // Pi pieces then S Pi^T pieces
 constexpr uint32_t kSmemA = kMatBytes;          // the tile (x, then r' hi, then r' lo)
 constexpr uint32_t kSmemTotal = kSmemB + kSmemA + 4 * kTile * sizeof(float);   // + norm partials [4][128]
-constexpr long kWaitLimit = 1L << 26;
+constexpr uint64_t kWaitNs = 1000000000ull;   // a wait gives up after one second
+constexpr int kSuspendNs = 20000;             // suspend-time hint of one try_wait
 
 __host__ __device__ constexpr uint32_t kmajor_off(int r, int k) {
     return (uint32_t)(((r >> 3) * 16 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
@@ -73,17 +74,27 @@ __device__ __forceinline__ void commit(uint64_t* mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar)));
 }
 
-// Waits for the given phase parity; false after kWaitLimit polls.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the given phase parity; false once kWaitNs of wall-clock time (the GPU's global
+// nanosecond timer) have passed.  Each try_wait may suspend the thread for up to kSuspendNs and
+// resumes as soon as the phase completes.
 __device__ __forceinline__ bool wait_phase(uint64_t* mbar, uint32_t parity) {
-    for (long it = 0; it < kWaitLimit; ++it) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
         uint32_t done;
         asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(done)
-            : "r"(smem_u32(mbar)), "r"(parity));
+            : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs)
+            : "memory");
         if (done) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
@@ -226,14 +237,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         // split contexts: this thread's 32 coordinates (one word) are below d_hi or not as a whole
         const bool hi = SPLIT && 32 * part < prm.d_hi;   // ordinary contexts: false at compile time
         const int nb = prm.P + (hi ? 1 : 0);
-        uint32_t pw[TQ_MAX_MSE_BITS] = {};
+        uint32_t pw[kFastBits] = {};
         float rs = 0.f;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
             const float yc = nrm > 0.f ? y[c] : 0.f;
             int idx = 0;
 #pragma unroll
-            for (int b = TQ_MAX_MSE_BITS - 1; b >= 0; --b)
+            for (int b = kFastBits - 1; b >= 0; --b)
                 if (b < nb) {
                     const int k = idx + (1 << b) - 1;
                     const bool up = yc > (hi ? prm.thresholds_hi[k] : prm.thresholds[k]) * nv;
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
 }  // namespace
 
 bool quantize_tc_supported(const tq_ctx* c, int dtype, const void* x, int64_t n, int64_t ld_x) {
-    return c->bops != nullptr && c->kernel_path != TQ_PATH_CUDA_CORE && dtype == TQ_BF16 && n >= 4096 &&
+    return c->bops != nullptr && c->P <= kFastBits && c->kernel_path != TQ_PATH_CUDA_CORE && dtype == TQ_BF16 && n >= 4096 &&
            (ld_x % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
 }
 

@@ -202,15 +202,17 @@ template <>
 struct Scorer<0, 0> {
     const float4* qg;   // [d] : the 4 staged rotated queries per coordinate
     const float4* ug;   // [m]
+    const float* cv;    // [L] : the centroid table (from the context's device table, any P)
 
     static __host__ __device__ size_t smem_bytes(const Params& prm) {
-        return (size_t)(prm.d + (prm.qjl ? prm.m : 0)) * sizeof(float4);
+        return (size_t)(prm.d + (prm.qjl ? prm.m : 0)) * sizeof(float4) + (size_t)kMaxCodeLevels * sizeof(float);
     }
 
     __device__ void setup(float4* sm, const Params& prm, const float* qrot, const float* qproj,
                           size_t qrow0, int nh) {
         float4* q4 = sm;
         float4* u4 = sm + prm.d;
+        float* c = reinterpret_cast<float*>(u4 + (prm.qjl ? prm.m : 0));
         for (int j = threadIdx.x; j < prm.d; j += blockDim.x) {
             float v[4];
 #pragma unroll
@@ -225,9 +227,11 @@ struct Scorer<0, 0> {
                 u4[j] = make_float4(v[0], v[1], v[2], v[3]);
             }
         }
+        for (int k = threadIdx.x; k < prm.L; k += blockDim.x) c[k] = prm.tab[k];
         __syncthreads();
         qg = q4;
         ug = u4;
+        cv = c;
     }
 
     __device__ float4 operator()(const Params& prm, const uint32_t* planes, const uint32_t* signs,
@@ -235,13 +239,13 @@ struct Scorer<0, 0> {
         const uint32_t* pr = planes + row * (size_t)(prm.P * prm.W);
         float4 mse = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int w = 0; w < prm.W; ++w) {
-            uint32_t pw[kMaxLevels > 0 ? TQ_MAX_MSE_BITS : 1];
+            uint32_t pw[TQ_MAX_MSE_BITS];
             for (int p = 0; p < prm.P; ++p) pw[p] = __ldg(pr + p * prm.W + w);
             const int jend = min(32, prm.d - 32 * w);
             for (int bit = 0; bit < jend; ++bit) {
                 int idx = 0;
                 for (int p = 0; p < prm.P; ++p) idx |= ((pw[p] >> bit) & 1u) << p;
-                mse = f4_fma(prm.centroids[idx], qg[32 * w + bit], mse);
+                mse = f4_fma(cv[idx], qg[32 * w + bit], mse);
             }
         }
         float4 e = f4_scale(half_bits_to_float(__ldg(norm + row)), mse);
@@ -264,7 +268,7 @@ struct Scorer<0, 0> {
 // Whether the table path applies to a context (and its shared memory fits one CTA).
 __host__ __device__ inline bool lut_path_ok(const Params& prm, size_t extra_smem, size_t smem_limit) {
     const int W = prm.W;
-    if (W < 1 || W > 7 || prm.P < 1 || prm.P > 4) return false;
+    if (W < 1 || W > 7 || prm.P < 1 || prm.P > kFastBits) return false;
     if (prm.qjl && prm.Ws != W) return false;
     const int nbq = (prm.d + 7) / 8, nbu = prm.qjl ? (prm.m + 7) / 8 : 0;
     const size_t need = (size_t)(nbq + nbu) * 256 * 16 + 4ull * 8 * (nbq + nbu) * 4 + 32 + extra_smem;

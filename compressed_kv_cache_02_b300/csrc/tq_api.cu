@@ -75,6 +75,7 @@ void free_ctx(tq_ctx* c) {
     cudaFree(c->dStT);
     cudaFree(c->derr);
     cudaFree(c->bops);
+    cudaFree(c->dtab);
     delete c;
 }
 
@@ -89,7 +90,7 @@ const char* tq_last_error(void) { return g_err.c_str(); }
 
 int tq_host_codebook(int d, int mse_bits, double* centroids, double* thresholds) {
     TQ_REQUIRE(d >= 3 && d <= TQ_MAX_D, TQ_ERR_ARG, "d must be in [3, 1024]");
-    TQ_REQUIRE(mse_bits >= 1 && mse_bits <= TQ_MAX_MSE_BITS, TQ_ERR_ARG, "mse_bits must be in [1, 4]");
+    TQ_REQUIRE(mse_bits >= 1 && mse_bits <= TQ_MAX_MSE_BITS, TQ_ERR_ARG, "mse_bits must be in [1, 8]");
     std::vector<double> c, t;
     lloyd_max_codebook(d, mse_bits, c, t);
     if (centroids) std::memcpy(centroids, c.data(), c.size() * sizeof(double));
@@ -114,10 +115,12 @@ static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int 
     TQ_REQUIRE(d >= 3 && d <= TQ_MAX_D, TQ_ERR_ARG, "d must be in [3, 1024]");
     TQ_REQUIRE(mode == TQ_MODE_PROD || mode == TQ_MODE_MSE, TQ_ERR_ARG, "mode must be TQ_MODE_PROD or TQ_MODE_MSE");
     const int P = (mode == TQ_MODE_PROD) ? bits - 1 : bits;
-    TQ_REQUIRE(P >= 1 && P <= TQ_MAX_MSE_BITS, TQ_ERR_ARG,
-               mode == TQ_MODE_PROD ? "PROD mode needs bits in [2, 5]" : "MSE mode needs bits in [1, 4]");
+    if (mode == TQ_MODE_PROD)
+        TQ_REQUIRE(P >= 1 && P <= kFastBits, TQ_ERR_ARG, "PROD mode needs bits in [2, 5]");
+    else
+        TQ_REQUIRE(P >= 1 && P <= TQ_MAX_MSE_BITS, TQ_ERR_ARG, "MSE mode needs bits in [1, 8]");
     TQ_REQUIRE(d_hi >= 0 && d_hi <= d && d_hi % 32 == 0, TQ_ERR_ARG, "d_hi must be a multiple of 32 in [0, d]");
-    if (d_hi) TQ_REQUIRE(P + 1 <= TQ_MAX_MSE_BITS, TQ_ERR_ARG, "the split table needs MSE bits + 1 <= 4");
+    if (d_hi) TQ_REQUIRE(P + 1 <= kFastBits, TQ_ERR_ARG, "the split table needs MSE bits + 1 <= 4");
     if (mode == TQ_MODE_PROD) TQ_REQUIRE(m >= 1 && m <= TQ_MAX_D, TQ_ERR_ARG, "m must be in [1, 1024]");
     else m = 0;
 
@@ -161,10 +164,10 @@ static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int 
         p.centroids[k] = k < c->L ? static_cast<float>(c->centroids[k]) : 0.f;
         p.thresholds[k] = k < c->L - 1 ? static_cast<float>(c->thresholds[k]) : INFINITY;
     }
-    double c0;
+    double c0 = c->centroids[0];
     std::vector<int> masks;
     std::vector<double> kappa;
-    walsh_form(c->centroids, P, c0, masks, kappa);
+    if (P <= kFastBits) walsh_form(c->centroids, P, c0, masks, kappa);
     p.c0 = static_cast<float>(c0);
     p.nterms = static_cast<int>(masks.size());
     {
@@ -231,6 +234,11 @@ static int init_ctx(tq_ctx** out, uint64_t seed, int d, int bits, int d_hi, int 
         build_tc_operands(c->Pi.data(), m ? St.data() : nullptr, ops);
         if ((rc = upload(&c->bops, ops)) != TQ_OK) { free_ctx(c); return rc; }
     }
+    std::vector<float> tab(2 * c->L - 1);
+    for (int k = 0; k < c->L; ++k) tab[k] = static_cast<float>(c->centroids[k]);
+    for (int k = 0; k + 1 < c->L; ++k) tab[c->L + k] = static_cast<float>(c->thresholds[k]);
+    if ((rc = upload(&c->dtab, tab)) != TQ_OK) { free_ctx(c); return rc; }
+    p.tab = c->dtab;
     std::vector<int> zero(1, 0);
     if ((rc = upload(&c->derr, zero)) != TQ_OK) { free_ctx(c); return rc; }
     *out = c;

@@ -9,17 +9,23 @@
 
 namespace tq {
 
-constexpr int kMaxLevels = 1 << TQ_MAX_MSE_BITS;   // 16 centroids at most
-constexpr int kMaxTerms = kMaxLevels - 1;          // nonzero subsets of the bit planes
+// The table kernels (byte tables, Walsh form, tensor-core logits, the tcgen05 quantizer) and the
+// tables carried in the kernel parameters cover up to kFastBits MSE bits; wider MSE-mode tables
+// (up to TQ_MAX_MSE_BITS) live in device memory (Params::tab) and take the generic kernels.
+constexpr int kFastBits = 4;
+constexpr int kMaxLevels = 1 << kFastBits;           // 16 centroids in the parameter tables
+constexpr int kMaxTerms = kMaxLevels - 1;            // nonzero subsets of the bit planes
+constexpr int kMaxCodeLevels = 1 << TQ_MAX_MSE_BITS; // 256: the widest table
 
 // Everything a kernel needs about a context, passed by value as a kernel parameter.
 struct Params {
     int d, m, P, L, W, Ws;   // dimension, JL rows (0 in MSE mode), planes, levels, words
+    const float* tab;        // device: the L centroids then the L - 1 thresholds (float32), any P
     int qjl;                 // 1 in PROD mode
     float qjl_scale;         // sqrt(pi/2) / m
-    float centroids[kMaxLevels];
+    float centroids[kMaxLevels];    // the first min(L, 16) entries of tab (P <= kFastBits: all)
     float thresholds[kMaxLevels];
-    // Walsh form of the table (see host_setup.cpp): c(idx) = c0 + sum_t kappa[t] * x_t(idx),
+    // Walsh form (P <= kFastBits only; nterms = 0 and odd_walsh = 0 above) of the table (see host_setup.cpp): c(idx) = c0 + sum_t kappa[t] * x_t(idx),
     // where x_t(idx) = parity of the idx bits selected by mask[t].
     float c0;
     int nterms;
@@ -70,6 +76,7 @@ struct tq_ctx {
     float* dST = nullptr;     // [d][m]  ST[j*m+i] = S[i][j]        (u = S q)
     float* dStT = nullptr;    // [d][m]  StT[j*m+i] = (S Pi^T)[i][j] (S r = (S Pi^T)(Pi x - n c))
     uint16_t* bops = nullptr; // d = 128: tcgen05 B operands (3 bf16 pieces of Pi, of S Pi^T)
+    float* dtab = nullptr;    // [L centroids | L - 1 thresholds] float32 (Params::tab)
     int* derr = nullptr;      // device error word
     int kernel_path = TQ_PATH_AUTO;   // logits kernel family (tq_set_kernel_path)
 };

@@ -90,7 +90,7 @@ enum tq_device_error {
 };
 
 #define TQ_MAX_D 1024
-#define TQ_MAX_MSE_BITS 4
+#define TQ_MAX_MSE_BITS 8   /* MSE mode; PROD mode takes 1..4 MSE bits (bits 2..5) */
 #define TQ_MAX_TOPK 128
 
 typedef struct tq_ctx tq_ctx;
@@ -103,7 +103,9 @@ typedef struct tq_ctx tq_ctx;
  * float64, computed by the Lloyd iteration with Gauss-Legendre quadrature of the density
  * Gamma(d/2)/(sqrt(pi)Gamma((d-1)/2)) (1-t^2)^((d-3)/2).  Pages: nonndazone.ru essay,
  * sections 3.2 (centroids where probability is higher) and 3.4 (precomputed once);
- * freelamp article, section 技术突破 (predictable law after rotation).
+ * freelamp article, section 技术突破 (predictable law after rotation).  The table is the fixed
+ * point of the Lloyd-Max conditions (midpoint thresholds, centroids at the cell means): up to 4
+ * bits reached by the Lloyd iteration, from 5 bits by Newton's method on the same conditions.
  * 3 <= d <= TQ_MAX_D, 1 <= mse_bits <= TQ_MAX_MSE_BITS.  Arrays are caller-owned.     */
 int tq_host_codebook(int d, int mse_bits, double* centroids, double* thresholds);
 
@@ -117,13 +119,17 @@ int tq_host_matrices(uint64_t seed, int d, int m, float* Pi, float* S);
 
 /* ---------------------------------------------------------------- contexts */
 
-/* PROD-mode context: bits = MSE bits + 1 QJL bit (2..TQ_MAX_MSE_BITS+1), m = d, matrices
+/* PROD-mode context: bits = MSE bits + 1 QJL bit (2..5), m = d, matrices
  * from tq_host_matrices(seed, d, d).  Allocates the context's device tables on the
  * current device.  Pages: csdn tutorial, section TurboQuant原理剖析 (2+1 and 3+1 bits).   */
 int tq_init(tq_ctx** out, uint64_t seed, int d, int bits);
 
-/* General context.  mode TQ_MODE_PROD: bits = MSE bits + 1, m = JL rows (1..TQ_MAX_D);
+/* General context.  mode TQ_MODE_PROD: bits = MSE bits + 1 (2..5), m = JL rows (1..TQ_MAX_D);
  * mode TQ_MODE_MSE: bits = MSE bits (1..TQ_MAX_MSE_BITS), m ignored (no QJL stage).
+ * Contexts of 1..4 MSE bits take the table and tensor-core kernels; MSE contexts of 5..8 bits
+ * take the generic CUDA-core kernels of every call (tq_quantize, tq_append, tq_attn_logits,
+ * tq_attn_output, tq_attn_values, tq_search_topk) with the same results' contract;
+ * tq_paged_decode_step takes 1..4-bit value contexts only (TQ_ERR_UNSUPPORTED otherwise).
  * Pi_host (d x d) and S_host (m x d, PROD only) are float32 row-major host arrays used as
  * given (copied); NULL means "generate from seed" as tq_host_matrices does.  Pi_host must
  * be orthogonal to float32 precision (not checked beyond finiteness).                  */
@@ -135,7 +141,7 @@ int tq_init_ex(tq_ctx** out, uint64_t seed, int d, int bits, int mode, int m,
  * (b+1)-bit Lloyd-Max table and the other d - d_hi with the b-bit one (b = MSE bits given by
  * bits and mode as in tq_init_ex; the QJL stage is unchanged), i.e. b + d_hi / d MSE bits per
  * coordinate on average: bits = 3, d_hi = d/2, PROD gives 3.5 bits per channel.
- * d_hi must be a multiple of 32 in [0, d] and b + 1 <= TQ_MAX_MSE_BITS; d_hi = 0 is tq_init_ex.
+ * d_hi must be a multiple of 32 in [0, d] and b + 1 <= 4; d_hi = 0 is tq_init_ex.
  * Code rows: the b full planes (W words each, as tq_layout) followed by the top plane of the
  * first d_hi coordinates (ceil(d_hi / 32) words: bit j % 32 of word j / 32 holds bit b of
  * idx_j); tq_code_words gives the row length.  tq_quantize, tq_append and tq_attn_logits

@@ -68,14 +68,41 @@ def test_quantize_bulk_bf16(mode, bits, n, ld, kernel_path):
     assert same.mean() > 0.99
 
 
-@pytest.mark.parametrize("bits", [1, 3, 4])
-def test_quantize_mse_mode(bits):
+@pytest.mark.parametrize("bits,d,n", [(1, 128, 700), (3, 128, 700), (4, 128, 700), (5, 128, 700), (6, 200, 300),
+                                      (8, 128, 700), (8, 128, 5000), (7, 33, 250), (8, 300, 90)])
+def test_quantize_mse_mode(bits, d, n):
+    """MSE-mode codes at every width 1..8 (5..8 bits: the table read from device memory), the
+    decode-append (small n) and bulk (n >= 4736) variants of the CUDA-core kernel."""
     tq = _tq()
-    pr = Pair(128, bits, mode=tq.TQ_MODE_MSE, seed=1)
-    X = inputs.gaussian(700, 128, seed=5).cuda()
+    pr = Pair(d, bits, mode=tq.TQ_MODE_MSE, seed=1)
+    X = inputs.gaussian(n, d, seed=5).cuda()
     codes = pr.ctx.quantize(X)
     assert codes.signs is None
-    check_codes(pr, X.cpu().numpy(), codes)
+    assert pr.ctx.sync_status() == 0
+    same = check_codes(pr, X.cpu().numpy(), codes)
+    assert same.mean() > 0.9
+
+
+@pytest.mark.parametrize("d", [128, 200])
+def test_round_trip_at_eight_bits_on_gpu(d):
+    """The high-bit-width round trip through the library: codes of x at 8 MSE bits, the oracle's
+    reconstruction of those codes, coded again by the library, give the same codes wherever the
+    reconstruction's rotated direction is not within 1e-5 of a threshold."""
+    tq = _tq()
+    pr = Pair(d, 8, mode=tq.TQ_MODE_MSE, seed=3)
+    X = 5.0 * inputs.gaussian(1000, d, seed=11)
+    c1 = pr.ctx.quantize(X.cuda())
+    idx1, n1, _, _ = pr.from_device(c1)
+    Xh = oracle.dequantize(idx1, n1, pr.Pi, pr.cb)
+    c2 = pr.ctx.quantize(torch.from_numpy(Xh.astype(np.float32)).cuda())
+    assert pr.ctx.sync_status() == 0
+    idx2, _, _, _ = pr.from_device(c2)
+    U2 = (Xh @ pr.Pi.T) / np.linalg.norm(Xh, axis=1, keepdims=True)
+    near = np.min(np.abs(U2[..., None] - pr.cb.thresholds[None, None, :]), axis=-1) < 1e-5
+    diff = idx1 != idx2
+    assert not (diff & ~near).any()
+    rel = np.sum((X.numpy() - Xh) ** 2, axis=1) / np.sum(X.numpy().astype(np.float64) ** 2, axis=1)
+    assert abs(rel.mean() - pr.cb.distortion()) < 3 * rel.std() / np.sqrt(len(rel)) + 2.0 ** -22
 
 
 def test_quantize_strided_rows_zero_rows_and_empty():
@@ -116,7 +143,9 @@ def test_argument_errors_raise():
                               out.norm.data_ptr(), None, None)
     assert code == tq.TQ_ERR_ARG                                   # PROD needs signs
     with pytest.raises(tq.TQError):
-        tq.Context(16, 6)                                          # 5 MSE bits unsupported
+        tq.Context(16, 6)                                          # PROD mode: at most 4 MSE bits
+    with pytest.raises(tq.TQError):
+        tq.Context(16, 9, mode=tq.TQ_MODE_MSE)                     # MSE mode: at most 8 bits
 
 
 # ------------------------------------------------------------------ attention
@@ -180,10 +209,11 @@ def test_logits(B, Hkv, G, N, d, bits, lens, kernel_path):
         assert_close(got[b, :, :L], ref[b, :, :L], "logits")
 
 
-def test_logits_mse_keys(kernel_path):
+@pytest.mark.parametrize("bits", [3, 6, 8])
+def test_logits_mse_keys(kernel_path, bits):
     tq = _tq()
     d, N = 128, 600
-    kp = Pair(d, 3, mode=tq.TQ_MODE_MSE, seed=9)
+    kp = Pair(d, bits, mode=tq.TQ_MODE_MSE, seed=9)
     kp.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     K = inputs.gaussian(2 * N, d, seed=9).reshape(1, 2, N, d)
     q = inputs.gaussian(8, d, seed=10).reshape(1, 8, d)
@@ -194,7 +224,7 @@ def test_logits_mse_keys(kernel_path):
     assert_close(got, ref, "mse-key logits")
 
 
-@pytest.mark.parametrize("vmode", ["bf16", "mse"])
+@pytest.mark.parametrize("vmode", ["bf16", "mse", "mse8"])
 @pytest.mark.parametrize("B,Hkv,G,N,bits,lens", [
     (1, 8, 4, 1100, 4, [1100]),
     (2, 2, 4, 2600, 3, [2600, 1]),
@@ -202,7 +232,8 @@ def test_logits_mse_keys(kernel_path):
 ])
 def test_attention_output(vmode, B, Hkv, G, N, bits, lens):
     d = 128
-    c = _kv_case(B, Hkv, G, N, d, bits, vmode, seed=11, lens=lens)
+    c = _kv_case(B, Hkv, G, N, d, bits, "mse" if vmode == "mse8" else vmode, seed=11, lens=lens,
+                 vbits=8 if vmode == "mse8" else 3)
     scale = 1.0 / sqrt(d)
     length = torch.tensor(lens, dtype=torch.int32).cuda()
     kp = c["kp"]
@@ -242,10 +273,12 @@ def test_attention_values_from_logits(vmode, B, Hkv, G, N, lens):
     assert_close(got.cpu().numpy(), ref, "softmax-weighted values")
 
 
-@pytest.mark.parametrize("vbits,d", [(1, 128), (2, 128), (3, 112), (4, 128), (4, 100)])
+@pytest.mark.parametrize("vbits,d", [(1, 128), (2, 128), (3, 112), (4, 128), (4, 100), (5, 128), (8, 128), (8, 100),
+                                     (6, 200)])
 def test_attention_values_code_widths(vbits, d):
-    """The value sum at every MSE width of the d <= 128 kernel (centroids from registers at 1-3
-    bits, from shared memory at 4) and at head dims below 128 (padded coordinates)."""
+    """The value sum at every MSE width: 1-4 bits on the d <= 128 coded-value kernel, 5-8 bits (and
+    d = 200) on the generic one with the table from device memory; head dims below 128 (padded
+    coordinates)."""
     tq = _tq()
     B, Hkv, G, N, lens = 2, 2, 4, 1500, [1500, 333]
     c = _kv_case(B, Hkv, G, N, d, 3, "mse", seed=17, lens=lens, vbits=vbits)
@@ -342,6 +375,23 @@ def test_search_topk(d, bits, n, nq, k, kernel_path):
     assert pr.ctx.sync_status() == 0
     ref_s, ref_i = oracle.search_topk(Q.numpy(), z, pr.Pi, pr.cb, pr.S, k)
     scores = oracle.estimate_all(Q.numpy(), z, pr.Pi, pr.cb, pr.S)
+    _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
+
+
+@pytest.mark.parametrize("bits,d", [(8, 200), (6, 64)])
+def test_search_topk_wide_mse(bits, d):
+    """Search over MSE-mode codes of 6 and 8 bits (generic scorer, table from device memory)."""
+    tq = _tq()
+    n, nq, k = 2000, 6, 20
+    pr = Pair(d, bits, mode=tq.TQ_MODE_MSE, seed=5)
+    X = inputs.cone(n, d, seed=5, mu_seed=77)
+    Q = inputs.cone(nq, d, seed=6, mu_seed=77)
+    z = pr.oquant(X.numpy())
+    db = pr.to_device(z, (n,))
+    s, i = pr.ctx.search_topk(Q.cuda(), db, k)
+    assert pr.ctx.sync_status() == 0
+    ref_s, ref_i = oracle.search_topk(Q.numpy(), z, pr.Pi, pr.cb, None, k)
+    scores = oracle.estimate_all(Q.numpy(), z, pr.Pi, pr.cb, None)
     _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
 
 

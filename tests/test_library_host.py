@@ -49,6 +49,26 @@ def test_host_codebook_matches_oracle(tq, d, bits):
     assert np.max(np.abs(t - ref.thresholds)) < 1e-12
 
 
+@pytest.mark.parametrize("d", [3, 16, 128, 200, 1024])
+@pytest.mark.parametrize("bits", [5, 6, 7, 8])
+def test_host_codebook_wide_matches_oracle(tq, d, bits):
+    # From 5 bits both sides solve the Lloyd-Max conditions by Newton's method, each with its own
+    # quadrature (library: composite Gauss-Legendre; oracle: incomplete beta).  The fixed point is
+    # then determined only to ~L^2 times the rounding of one Lloyd step (the smallest eigenvalue of
+    # the step's Jacobian is ~(pi/L)^2), so the two tables agree to that level, far below the
+    # float32 rounding the kernels apply, and the library's table passes the oracle's own Lloyd
+    # step to that step's rounding floor.
+    from oracle import codebook as cbm
+    c, t = tq.host_codebook(d, bits)
+    ref = sphere_codebook(d, bits)
+    tol = 2e-12 * 4.0 ** (bits - 4)
+    assert np.max(np.abs(c - ref.centroids)) < tol
+    assert np.max(np.abs(t - ref.thresholds)) < tol
+    _, _, _, _, g = cbm._cells(c, d)
+    assert np.max(np.abs(g - c)) < 2e-13
+    assert np.array_equal(c, -c[::-1]) and np.all(np.diff(c) > 0)
+
+
 @pytest.mark.parametrize("d,m", [(4, 4), (16, 16), (128, 128), (200, 200), (40, 24)])
 def test_host_matrices_match_oracle_generator(tq, d, m):
     Pi, S = tq.host_matrices(7, d, m)
@@ -62,7 +82,7 @@ def test_host_matrices_match_oracle_generator(tq, d, m):
 def test_host_argument_errors(tq):
     c = np.zeros(2)
     assert tq.lib.tq_host_codebook(2, 1, c.ctypes.data, None) == tq.TQ_ERR_ARG
-    assert tq.lib.tq_host_codebook(128, 5, c.ctypes.data, None) == tq.TQ_ERR_ARG
+    assert tq.lib.tq_host_codebook(128, 9, c.ctypes.data, None) == tq.TQ_ERR_ARG
     assert b"mse_bits" in tq.lib.tq_last_error()
     assert tq.lib.tq_host_matrices(0, 2000, 4, None, None) == tq.TQ_ERR_ARG
 
