@@ -367,6 +367,43 @@ __global__ void __launch_bounds__(kValThreads) values_kernel(const ValuesArgs a)
     write_partial<C, NIB, kValThreads>(acc, red, s_m, s_l, pbase, (size_t)a.nchunk * stride, nh, a.d);
 }
 
+// o = Pi_v^T orot (orot in shared memory, d values followed by room for the split sums), or a copy
+// when Pi_v is NULL (bf16 values: no rotation).  Each output's sum over j is split between
+// S = blockDim / span threads, loads issued 16 at a time (the values pass has usually evicted Pi_v
+// from L2).  Every thread of the block calls it after orot is written and visible.
+__device__ void back_rotate_store(float* orot, int d, const float* __restrict__ PiV, float* __restrict__ o) {
+    if (!PiV) {
+        for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = orot[i];
+        return;
+    }
+    const int span = d < (int)blockDim.x ? ((d + 31) / 32) * 32 : (int)blockDim.x;
+    const int S = blockDim.x / span, part = threadIdx.x / span, ii = threadIdx.x - part * span;
+    const bool active = part < S;   // blockDim need not be a multiple of span
+    float* red = orot + d;   // [S - 1][span]
+    const int j0 = part * d / S, j1 = (part + 1) * d / S;
+    for (int i0 = 0; i0 < d; i0 += span) {   // one pass when S > 1
+        const int i = i0 + ii;
+        float acc = 0.f;
+        if (active && i < d) {
+            for (int jb = j0; jb < j1; jb += 16) {
+                float pv[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pv[u] = jb + u < j1 ? __ldg(PiV + (size_t)(jb + u) * d + i) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (jb + u < j1) acc = fmaf(pv[u], orot[jb + u], acc);
+            }
+        }
+        if (S > 1) {
+            if (active && part > 0 && i < d) red[(part - 1) * span + ii] = acc;
+            __syncthreads();
+            if (part == 0 && i < d)
+                for (int q = 1; q < S; ++q) acc += red[(q - 1) * span + ii];
+        }
+        if (part == 0 && i < d) o[i] = acc;
+    }
+}
+
 // out[b][h] = Pi_v^T (sum_c e^{m_c - M} a_c) / (sum_c e^{m_c - M} l_c) over the chunks that
 // hold keys; Pi_v NULL for bf16 values (no rotation).
 __global__ void attn_combine_kernel(const float* __restrict__ partials, int nchunk, int chunk, int d,
@@ -395,38 +432,67 @@ __global__ void attn_combine_kernel(const float* __restrict__ partials, int nchu
         orot[j] = s * inv;
     }
     __syncthreads();
-    if (!PiV) {
-        for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = orot[i];
+    back_rotate_store(orot, d, PiV, o);
+}
+
+// The state of a whole (batch, query head) over this call's keys, for a merge with other shards
+// of the sequence: part[bh] = (M, sum_c e^{m_c - M} l_c, sum_c e^{m_c - M} a_c[0..d)) over the chunks
+// that hold keys, unnormalised and in the value context's rotated basis; (-inf, 0, 0...) when the
+// sequence holds no keys here.
+__global__ void chunks_to_partial_kernel(const float* __restrict__ partials, int nchunk, int chunk, int d, int Hq,
+                                         const int32_t* len, int64_t cap, float* __restrict__ part) {
+    const int bh = blockIdx.x, b = bh / Hq;
+    int L = len[b];
+    L = L < 0 ? 0 : (L > cap ? (int)cap : L);
+    const int nc = (L + chunk - 1) / chunk;
+    const size_t stride = (size_t)d + 2;
+    float* o = part + (size_t)bh * stride;
+    const float* p = partials + (size_t)bh * nchunk * stride;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, p[c * stride]);
+    float tot = 0.f;
+    for (int c = 0; c < nc; ++c) tot += p[c * stride + 1] * rescale(p[c * stride], M);
+    if (threadIdx.x == 0) {
+        o[0] = M;
+        o[1] = tot;
+    }
+    for (int j = threadIdx.x; j < d; j += blockDim.x) {
+        float s = 0.f;
+        for (int c = 0; c < nc; ++c) s = fmaf(p[c * stride + 2 + j], rescale(p[c * stride], M), s);
+        o[2 + j] = s;
+    }
+}
+
+// out[bh] = Pi_v^T (sum_r e^{m_r - M} a_r) / (sum_r e^{m_r - M} l_r) over R shards' partial states
+// parts[r][bh] = (m_r, l_r, a_r[0..d)); zeros when every shard is empty (all l_r = 0).
+__global__ void merge_partials_kernel(const float* __restrict__ parts, int R, int64_t BH, int d, const float* PiV,
+                                      float* __restrict__ out) {
+    extern __shared__ float orot[];
+    const int64_t bh = blockIdx.x;
+    const size_t stride = (size_t)d + 2;
+    float* o = out + (size_t)bh * d;
+    float M = -INFINITY;
+    for (int r = 0; r < R; ++r) M = fmaxf(M, parts[((size_t)r * BH + bh) * stride]);
+    float tot = 0.f;
+    for (int r = 0; r < R; ++r) {
+        const float* p = parts + ((size_t)r * BH + bh) * stride;
+        tot += p[1] * rescale(p[0], M);
+    }
+    if (!(tot > 0.f)) {
+        for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = 0.f;
         return;
     }
-    // o = Pi_v^T orot: each output's sum over j split between S = blockDim / span threads, loads
-    // issued 16 at a time (the values pass has usually evicted Pi_v from L2)
-    const int span = d < (int)blockDim.x ? ((d + 31) / 32) * 32 : (int)blockDim.x;
-    const int S = blockDim.x / span, part = threadIdx.x / span, ii = threadIdx.x - part * span;
-    const bool active = part < S;   // blockDim need not be a multiple of span
-    float* red = orot + d;   // [S - 1][span]
-    const int j0 = part * d / S, j1 = (part + 1) * d / S;
-    for (int i0 = 0; i0 < d; i0 += span) {   // one pass when S > 1
-        const int i = i0 + ii;
+    const float inv = 1.f / tot;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) {
         float acc = 0.f;
-        if (active && i < d) {
-            for (int jb = j0; jb < j1; jb += 16) {
-                float pv[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) pv[u] = jb + u < j1 ? __ldg(PiV + (size_t)(jb + u) * d + i) : 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (jb + u < j1) acc = fmaf(pv[u], orot[jb + u], acc);
-            }
+        for (int r = 0; r < R; ++r) {
+            const float* p = parts + ((size_t)r * BH + bh) * stride;
+            acc = fmaf(p[2 + j], rescale(p[0], M), acc);
         }
-        if (S > 1) {
-            if (active && part > 0 && i < d) red[(part - 1) * span + ii] = acc;
-            __syncthreads();
-            if (part == 0 && i < d)
-                for (int q = 1; q < S; ++q) acc += red[(q - 1) * span + ii];
-        }
-        if (part == 0 && i < d) o[i] = acc;
+        orot[j] = acc * inv;
     }
+    __syncthreads();
+    back_rotate_store(orot, d, PiV, o);
 }
 
 template <typename K>
@@ -794,7 +860,7 @@ cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qpro
 
 cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
                                const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
-                               float* partials, float* out, cudaStream_t s) {
+                               float* partials, float* out, cudaStream_t s, float* part_out) {
     ValuesArgs a{};
     a.logits = logits;
     a.B = B;
@@ -824,12 +890,27 @@ cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int
     else if (W <= 8) e = vc ? run_values<8, true, false>(a, grid, s) : run_values<8, false, false>(a, grid, s);
     else e = vc ? run_values<16, true, false>(a, grid, s) : run_values<16, false, false>(a, grid, s);
     if (e != cudaSuccess) return e;
+    if (part_out) {   // this call's shard of the sequence: per (batch, head) state, no normalisation
+        const int pt = d >= 256 ? 256 : ((d + 31) / 32) * 32;
+        chunks_to_partial_kernel<<<B * Hq, pt, 0, s>>>(partials, a.nchunk, a.chunk, d, Hq, len, cap, part_out);
+        return cudaGetLastError();
+    }
     // 512 threads: the back-rotation's sums split 4 ways at d <= 128 (2 at d <= 256)
     const int threads = vc ? 512 : (d >= 256 ? 256 : ((d + 31) / 32) * 32);
     const int span = d < threads ? ((d + 31) / 32) * 32 : threads;
     const size_t csmem = ((size_t)d + (size_t)(threads / span - 1) * span) * sizeof(float);
     attn_combine_kernel<<<B * Hq, threads, csmem, s>>>(partials, a.nchunk, a.chunk, d, Hq, len, cap,
                                                        vc ? vc->dPi : nullptr, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_partials(const tq_ctx* vc, int d, const float* parts, int R, int64_t BH, float* out,
+                                  cudaStream_t s) {
+    if (BH <= 0) return cudaSuccess;
+    const int threads = vc ? 512 : (d >= 256 ? 256 : ((d + 31) / 32) * 32);
+    const int span = d < threads ? ((d + 31) / 32) * 32 : threads;
+    const size_t smem = ((size_t)d + (size_t)(threads / span - 1) * span) * sizeof(float);
+    merge_partials_kernel<<<(unsigned)BH, threads, smem, s>>>(parts, R, BH, d, vc ? vc->dPi : nullptr, out);
     return cudaGetLastError();
 }
 

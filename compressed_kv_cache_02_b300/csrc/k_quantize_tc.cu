@@ -4,18 +4,22 @@
 // Pages: juejin.cn post section 二 and csdn tutorial sections PolarQuant / QJL (rotate, code,
 // residual, signs); the arithmetic is that of quantize_kernel (k_quantize.cu), only the two
 // d x d products move to tensor cores:
-//   phase 1  Y = X Pi^T          A = the tile's x rows (bf16, exact), B = Pi as 3 bf16 pieces
-//                                (hi + mid + lo = the float32 Pi exactly), one TMEM
-//                                accumulator of 128 columns per piece; y = (lo + mid) + hi.
+//   phase 1  Y = X Pi^T          A = the tile's x rows (bf16, exact), B = Pi as 2 bf16 pieces
+//                                (hi + mid; what they leave is below 2^-18 of each entry, so u
+//                                moves by ~3e-7, far inside the 1e-5 band of the code parity
+//                                rule), both accumulated into one TMEM accumulator (128 columns).
 //   epilogue n = ||x||, n16, u = y / n, idx, bit planes, r' = y - n16 c[idx], ||r'||.
-//   phase 2  Z = r' (S Pi^T)^T   A = r' split into bf16 hi and lo (two passes into the same
-//                                accumulators), B = S Pi^T as 3 bf16 pieces; sign_j = [z_j > 0].
-// Pi and S Pi^T stay resident in shared memory (6 x 32 KB), so one CTA per SM walks the
-// tiles of 128 rows.  Operands use the K-major no-swizzle core-matrix layout (8 rows x 16
-// bytes per core matrix; LBO = 128 B between core matrices along K, SBO = 2048 B between
-// 8-row groups).  Warps w, w+4, w+8, w+12 share TMEM lanes 32(w%4)..+31 (rows) and split
-// each row's 128 coordinates in quarters of 32, one bit-plane word each.  One thread issues the MMAs; tcgen05.commit signals an mbarrier
-// whose waits are bounded (TQ_DEVERR_TIMEOUT).
+//   phase 2  Z = r' (S Pi^T)^T   A = r' split into bf16 hi and lo (two passes into one
+//                                accumulator), B = S Pi^T as 2 bf16 pieces (z moves by ~2e-6 of
+//                                ||x||, inside the 1e-5 band of the sign rule); sign_j = [z_j > 0].
+// Pi and S Pi^T stay resident in shared memory (4 x 32 KB), so one CTA per SM walks the tiles of
+// 128 rows.  The next tile's x rows are copied (cp.async) into the second of two x buffers while
+// the current tile runs, so the copy overlaps the MMAs and the epilogues.  Operands use the
+// K-major no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix; LBO = 128 B between
+// core matrices along K, SBO = 2048 B between 8-row groups).  Warps w, w+4, w+8, w+12 share TMEM
+// lanes 32(w%4)..+31 (rows) and split each row's 128 coordinates in quarters of 32, one bit-plane
+// word each.  One thread issues the MMAs; tcgen05.commit signals an mbarrier whose waits are
+// bounded in time (TQ_DEVERR_TIMEOUT).
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -30,9 +34,12 @@ namespace {
 constexpr int kTcThreads = 512;   // 4 threads per row, 32 coordinates each
 constexpr int kTile = 128;
 constexpr uint32_t kMatBytes = 128 * 128 * 2;   // one 128 x 128 bf16 operand
-constexpr uint32_t kSmemB = 6 * kMatBytes;      // Pi pieces then S Pi^T pieces
-constexpr uint32_t kSmemA = kMatBytes;          // the tile (x, then r' hi, then r' lo)
-constexpr uint32_t kSmemTotal = kSmemB + kSmemA + 4 * kTile * sizeof(float);   // + norm partials [4][128]
+constexpr int kPieces = 2;                      // bf16 pieces of Pi and of S Pi^T
+constexpr uint32_t kSmemB = 2 * kPieces * kMatBytes;   // Pi pieces then S Pi^T pieces (128 KB)
+constexpr uint32_t kSmemX = 2 * kMatBytes;             // two x tiles (the current one, the next)
+constexpr uint32_t kSmemR = kMatBytes;                 // r' hi, then r' lo
+constexpr uint32_t kSmemTotal = kSmemB + kSmemX + kSmemR + 4 * kTile * sizeof(float);   // + norm partials [4][128]
+constexpr uint32_t kTmemCols = 256;                    // D1 (Y) in columns 0..127, D2 (Z) in 128..255
 constexpr uint64_t kWaitNs = 1000000000ull;   // a wait gives up after one second
 constexpr int kSuspendNs = 20000;             // suspend-time hint of one try_wait
 
@@ -57,17 +64,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t da, uint64_t db
         "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
 }
 
-// D[p] (+)= A B_p^T for the three B pieces p: 8 K-steps of 16 per piece.  The descriptors of
-// later K-steps and pieces differ only in the start-address field (16-byte units), which
-// stays below 2^14 for any shared-memory offset.
+// D (+)= A (B_0 + B_1)^T: 8 K-steps of 16 per piece, every step into the same accumulator.  The
+// descriptors of later K-steps and pieces differ only in the start-address field (16-byte units),
+// which stays below 2^14 for any shared-memory offset.
 __device__ __forceinline__ void issue_pieces(uint32_t tmem, uint32_t a_saddr, uint32_t b_saddr, bool accumulate) {
     const uint64_t da = smem_desc(a_saddr), db = smem_desc(b_saddr);
 #pragma unroll 1
-    for (int p = 0; p < 3; ++p)
+    for (int p = 0; p < kPieces; ++p)
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            mma_bf16(tmem + p * 128, da + (uint64_t)(s * 16), db + (uint64_t)((p * kMatBytes + s * 256) >> 4),
-                     (accumulate || s > 0) ? 1u : 0u);
+            mma_bf16(tmem, da + (uint64_t)(s * 16), db + (uint64_t)((p * kMatBytes + s * 256) >> 4),
+                     (accumulate || p > 0 || s > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void commit(uint64_t* mbar) {
@@ -108,19 +115,16 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// The 32 coordinates [32 part, 32 part + 32) of this thread's row from the 3 piece
-// accumulators (columns p*128 + ...), summed small pieces first.
+// The 32 coordinates [32 part, 32 part + 32) of this thread's row from the accumulator at tmem_row.
 __device__ __forceinline__ void load_row_part(uint32_t tmem_row, int part, float (&y)[32]) {
+    float v0[16], v1[16];
+    ld16(tmem_row + 32 * part, v0);
+    ld16(tmem_row + 32 * part + 16, v1);
+    asm volatile("tcgen05.wait::ld.sync.aligned;");
 #pragma unroll
-    for (int p = 2; p >= 0; --p) {
-#pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-            float v[16];
-            ld16(tmem_row + p * 128 + 32 * part + c0, v);
-            asm volatile("tcgen05.wait::ld.sync.aligned;");
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[c0 + j] = (p == 2) ? v[j] : y[c0 + j] + v[j];
-        }
+    for (int j = 0; j < 16; ++j) {
+        y[j] = v0[j];
+        y[16 + j] = v1[j];
     }
 }
 
@@ -154,12 +158,26 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 
+// The x rows of tile `tile` into buffer sX (cp.async, zeros beyond n), one commit group.
+__device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char* sX) {
+    const int64_t r0 = (int64_t)tile * kTile;
+    const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+    for (int e = threadIdx.x; e < kTile * 16; e += kTcThreads) {
+        const int r = e >> 4, kc = e & 15;
+        unsigned char* dst = sX + kmajor_off(r, 8 * kc);
+        if (r < nvalid) cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;");
+}
+
 template <bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs a) {
-    extern __shared__ __align__(1024) unsigned char sm[];
+    extern __shared__ __align__(128) unsigned char sm[];   // no-swizzle operands need 16-byte alignment
     unsigned char* sB = sm;
-    unsigned char* sA = sm + kSmemB;
-    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemA);   // [4][128] x-norm, then r-norm parts
+    unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]
+    unsigned char* sR = sm + kSmemB + kSmemX;
+    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128] x-norm, then r-norm parts
     __shared__ __align__(8) uint64_t mbar;
     __shared__ uint32_t s_tmem;
     const Params& prm = a.prm;
@@ -170,48 +188,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
 
     for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) cp_async16(sB + 16 * e, a.bops + e);
     asm volatile("cp.async.commit_group;");
+    stage_x(a, blockIdx.x, sX);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar)));
         asm volatile("fence.mbarrier_init.release.cluster;");
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem)));
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "n"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = s_tmem;
-    const uint32_t tmem_row = tmem + ((uint32_t)(32 * q) << 16);
+    const uint32_t d1_row = tmem + ((uint32_t)(32 * q) << 16);
+    const uint32_t d2_row = d1_row + 128;
     uint32_t phase = 0;
     bool ok = true;
+    int buf = 0;
 
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, buf ^= 1) {
         const int64_t r0 = (int64_t)tile * kTile;
         const int nvalid = (int)min((int64_t)kTile, a.n - r0);
-        // stage the tile's x rows (zeros beyond n)
-        for (int e = tid; e < kTile * 16; e += kTcThreads) {
-            const int r = e >> 4, kc = e & 15;
-            unsigned char* dst = sA + kmajor_off(r, 8 * kc);
-            if (r < nvalid) cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("cp.async.commit_group;");
-        asm volatile("cp.async.wait_all;");
+        unsigned char* sXc = sX + buf * kMatBytes;
+        asm volatile("cp.async.wait_group 0;");          // this tile's rows (and, at first, Pi) have landed
         asm volatile("fence.proxy.async.shared::cta;");
         asm volatile("tcgen05.fence::before_thread_sync;");
         __syncthreads();
         asm volatile("tcgen05.fence::after_thread_sync;");
-        // phase 1: Y = X Pi^T (3 pieces)
+        // phase 1: Y = X Pi^T
         if (tid == 0) {
-            issue_pieces(tmem, smem_u32(sA), smem_u32(sB), false);
+            issue_pieces(tmem, smem_u32(sXc), smem_u32(sB), false);
             commit(&mbar);
         }
+        // the next tile's rows into the other buffer (its last readers, the previous tile's phase 1
+        // and norms, are done) while this tile computes
+        const int next = tile + gridDim.x;
+        if (next < ntiles) stage_x(a, next, sX + (buf ^ 1) * kMatBytes);
         // ||x|| partial from the staged tile while the MMAs run
         float xs = 0.f;
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc) {
-            const uint4 w = *reinterpret_cast<const uint4*>(sA + kmajor_off(row, 32 * part + 8 * kc));
+            const uint4 w = *reinterpret_cast<const uint4*>(sXc + kmajor_off(row, 32 * part + 8 * kc));
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -226,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         float y[32];
-        load_row_part(tmem_row, part, y);
+        load_row_part(d1_row, part, y);
         const float nrm = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
         const float n16 = half_bits_to_float(float_to_half_bits(nrm));
         const int64_t grow = r0 + row;
@@ -269,10 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
                 if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
             }
             asm volatile("tcgen05.fence::before_thread_sync;");
-            __syncthreads();   // TMEM reads and x reads done before the next tile
+            __syncthreads();   // TMEM reads and x-norm reads done before the next tile
             continue;
         }
-        store_row_part(sA, row, part, y);   // r' hi (rounded to bf16 by the store)
+        store_row_part(sR, row, part, y);   // r' hi (rounded to bf16 by the store)
         asm volatile("tcgen05.fence::before_thread_sync;");
         asm volatile("fence.proxy.async.shared::cta;");
         __syncthreads();   // everyone has read its x-norm partials and written r' hi
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
         // phase 2a: Z = r'_hi (S Pi^T)^T
         if (tid == 0) {
-            issue_pieces(tmem, smem_u32(sA), smem_u32(sB) + 3 * kMatBytes, false);
+            issue_pieces(tmem + 128, smem_u32(sR), smem_u32(sB) + kPieces * kMatBytes, false);
             commit(&mbar);
         }
         ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
@@ -288,14 +307,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
-        store_row_part(sA, row, part, y);   // r' lo = r' - bf16(r')
+        store_row_part(sR, row, part, y);   // r' lo = r' - bf16(r')
         asm volatile("fence.proxy.async.shared::cta;");
         asm volatile("tcgen05.fence::before_thread_sync;");
         __syncthreads();
         asm volatile("tcgen05.fence::after_thread_sync;");
         // phase 2b: Z += r'_lo (S Pi^T)^T
         if (tid == 0) {
-            issue_pieces(tmem, smem_u32(sA), smem_u32(sB) + 3 * kMatBytes, true);
+            issue_pieces(tmem + 128, smem_u32(sR), smem_u32(sB) + kPieces * kMatBytes, true);
             commit(&mbar);
         }
         ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
@@ -303,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         float z[32];
-        load_row_part(tmem_row, part, z);
+        load_row_part(d2_row, part, z);
         uint32_t sw = 0u;
 #pragma unroll
         for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
@@ -319,12 +338,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         asm volatile("tcgen05.fence::before_thread_sync;");
         __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
     }
+    asm volatile("cp.async.wait_all;");   // a prefetch still in flight lands before the CTA leaves
     if (!ok) {
         if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
         return;   // an MMA may still be in flight: leave the TMEM allocation to the context teardown
     }
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
 }
 
 }  // namespace
@@ -334,10 +354,10 @@ bool quantize_tc_supported(const tq_ctx* c, int dtype, const void* x, int64_t n,
            (ld_x % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
 }
 
-// Host layout of the six B operands (Pi pieces hi, mid, lo, then S Pi^T pieces): element (i, j)
-// of each 128 x 128 matrix at kmajor_off(i, j); St NULL leaves the last three zero.
+// Host layout of the four B operands (Pi pieces hi, mid, then S Pi^T pieces hi, mid): element
+// (i, j) of each 128 x 128 matrix at kmajor_off(i, j); St NULL leaves the last two zero.
 void build_tc_operands(const float* Pi, const float* St, std::vector<uint16_t>& out) {
-    out.assign(6 * 128 * 128, 0);
+    out.assign(2 * kPieces * 128 * 128, 0);
     auto bf16_rne = [](float v) -> uint16_t {
         uint32_t u;
         std::memcpy(&u, &v, 4);
@@ -355,12 +375,10 @@ void build_tc_operands(const float* Pi, const float* St, std::vector<uint16_t>& 
             for (int j = 0; j < 128; ++j) {
                 const float v = which == 0 ? Pi[i * 128 + j] : St[i * 128 + j];
                 const uint16_t h = bf16_rne(v);
-                const float r1 = v - bf16_val(h);
-                const uint16_t m = bf16_rne(r1);
-                const uint16_t l = bf16_rne(r1 - bf16_val(m));
-                const uint16_t piece[3] = {h, m, l};
-                for (int p = 0; p < 3; ++p)
-                    out[((size_t)(3 * which + p) * 128 * 128 * 2 + kmajor_off(i, j)) / 2] = piece[p];
+                const uint16_t m = bf16_rne(v - bf16_val(h));
+                const uint16_t piece[kPieces] = {h, m};
+                for (int p = 0; p < kPieces; ++p)
+                    out[((size_t)(kPieces * which + p) * 128 * 128 * 2 + kmajor_off(i, j)) / 2] = piece[p];
             }
 }
 

@@ -186,6 +186,39 @@ __global__ void __launch_bounds__(kThreads) search_merge_kernel(const float* __r
     }
 }
 
+// Per query: the R shards' k candidates each (rows shifted to global numbers by the shard's
+// offset; INT_MAX marks padding and keeps a score of -inf), sorted best first, the first k kept.
+__global__ void __launch_bounds__(kThreads) shard_topk_merge_kernel(const float* __restrict__ cand_s,
+                                                                   const int32_t* __restrict__ cand_i, int R,
+                                                                   int64_t nq, int k, int npow, const ShardOffsets offs,
+                                                                   float* top_s, int32_t* top_i) {
+    extern __shared__ float msm[];
+    float* s = msm;
+    int* id = reinterpret_cast<int*>(msm + npow);
+    const size_t q = blockIdx.x;
+    for (int t = threadIdx.x; t < npow; t += blockDim.x) {
+        float sc = -INFINITY;
+        int ix = INT_MAX;
+        if (t < R * k) {
+            const int r = t / k, j = t - r * k;
+            const size_t at = ((size_t)r * nq + q) * k + j;
+            const int32_t li = cand_i[at];
+            if (li != INT_MAX) {
+                sc = cand_s[at];
+                ix = (int)(li + offs.off[r]);
+            }
+        }
+        s[t] = sc;
+        id[t] = ix;
+    }
+    __syncthreads();
+    bitonic_sort(s, id, npow);
+    for (int t = threadIdx.x; t < k; t += blockDim.x) {
+        top_s[q * k + t] = s[t];
+        top_i[q * k + t] = id[t];
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Tensor-core scoring (mma.sync m16n8k32, e4m3, fp32 accumulate) for d <= 256: a CTA takes 8
 // queries and a database chunk, streamed in tiles of 128 vectors staged in shared memory.
@@ -469,6 +502,18 @@ void search_chunking(int64_t n, int k, int* chunk, int* nchunk) {
     int64_t c = ((tiles + nc - 1) / nc) * kThreads;
     *chunk = (int)c;
     *nchunk = (int)((n + c - 1) / c);
+}
+
+cudaError_t launch_topk_merge(const float* cand_s, const int32_t* cand_i, int R, int64_t nq, int k,
+                              const ShardOffsets& offs, float* top_s, int32_t* top_i, cudaStream_t s) {
+    if (nq <= 0) return cudaSuccess;
+    int npow = 1;
+    while (npow < R * k) npow <<= 1;
+    const size_t smem = (size_t)npow * (sizeof(float) + sizeof(int));
+    cudaError_t e = cudaFuncSetAttribute(shard_topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    shard_topk_merge_kernel<<<(unsigned)nq, kThreads, smem, s>>>(cand_s, cand_i, R, nq, k, npow, offs, top_s, top_i);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_search(const tq_ctx* c, const float* qrot, const float* qproj, int64_t nq,

@@ -477,9 +477,9 @@ int tq_attn_values_workspace_size(int d, int B, int Hq, int Hkv, int64_t cap, si
     return TQ_OK;
 }
 
-int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
-                   const int32_t* len, const void* values, const uint16_t* v_norm, float* out, void* ws,
-                   size_t ws_bytes, void* stream) {
+static int values_call(const char* name, const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv,
+                       int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm, float* out,
+                       void* ws, size_t ws_bytes, void* stream, float* part_out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -489,10 +489,10 @@ int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, 
         TQ_REQUIRE(vc->mode == TQ_MODE_MSE, TQ_ERR_ARG, "vctx must be an MSE-mode context");
         TQ_REQUIRE(vc->d == d, TQ_ERR_ARG, "d must equal vctx's d");
         TQ_REQUIRE(vc->d_hi == 0 || (d > 96 && d <= 128), TQ_ERR_UNSUPPORTED,
-                   "tq_attn_values takes split (fractional bit width) value contexts at 96 < d <= 128 only");
+                   std::string(name) + " takes split (fractional bit width) value contexts at 96 < d <= 128 only");
         TQ_REQUIRE(v_norm && aligned(v_norm, 2), TQ_ERR_ARG, "coded values need v_norm");
     }
-    TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_values supports d <= 512");
+    TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, std::string(name) + " supports d <= 512");
     TQ_REQUIRE(B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0, TQ_ERR_ARG, "need B >= 1 and Hq a positive multiple of Hkv");
     TQ_REQUIRE(cap >= 1 && cap < (int64_t)1 << 31, TQ_ERR_ARG, "cap must be in [1, 2^31)");
     TQ_REQUIRE(logits && len && values && out && ws, TQ_ERR_ARG, "a required pointer is NULL");
@@ -502,9 +502,59 @@ int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, 
                "workspace too small (see tq_attn_values_workspace_size)");
     // without a context (bf16 values) there is no error word: out-of-range lengths are clamped
     int* err = vc ? vc->derr : nullptr;
-    e = launch_attn_values(vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, err, static_cast<float*>(ws), out,
-                           static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_values launch");
+    e = launch_attn_values(vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, err, static_cast<float*>(ws),
+                           part_out ? nullptr : out, static_cast<cudaStream_t>(stream), part_out);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, (std::string(name) + " launch").c_str());
+}
+
+int tq_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                   const int32_t* len, const void* values, const uint16_t* v_norm, float* out, void* ws,
+                   size_t ws_bytes, void* stream) {
+    return values_call("tq_attn_values", vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, out, ws, ws_bytes,
+                       stream, nullptr);
+}
+
+int tq_attn_values_partial(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                           const int32_t* len, const void* values, const uint16_t* v_norm, float* part, void* ws,
+                           size_t ws_bytes, void* stream) {
+    return values_call("tq_attn_values_partial", vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, part, ws,
+                       ws_bytes, stream, part);
+}
+
+int tq_attn_merge_partials(const tq_ctx* vc, int d, const float* parts, int R, int B, int Hq, float* out,
+                           void* stream) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (vc) {
+        int rc = check_ctx(vc);
+        if (rc) return rc;
+        TQ_REQUIRE(vc->mode == TQ_MODE_MSE && vc->d == d, TQ_ERR_ARG, "vctx must be an MSE-mode context of dimension d");
+    }
+    TQ_REQUIRE(d >= 1 && d <= 512, TQ_ERR_UNSUPPORTED, "tq_attn_merge_partials supports d <= 512");
+    TQ_REQUIRE(R >= 1 && B >= 1 && Hq >= 1, TQ_ERR_ARG, "need R >= 1, B >= 1, Hq >= 1");
+    TQ_REQUIRE(parts && out && aligned(parts, 4) && aligned(out, 4), TQ_ERR_ARG, "parts and out must be non-NULL, 4-byte aligned");
+    e = launch_merge_partials(vc, d, parts, R, (int64_t)B * Hq, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_attn_merge_partials launch");
+}
+
+int tq_topk_merge(const float* cand_s, const int32_t* cand_i, int R, int64_t nq, int k, const int64_t* row_offsets,
+                  float* top_s, int32_t* top_i, void* stream) {
+    TQ_REQUIRE(R >= 1 && R <= kMaxShards, TQ_ERR_ARG, "R must be in [1, 64]");
+    TQ_REQUIRE(k >= 1 && k <= TQ_MAX_TOPK && nq >= 0 && nq < ((int64_t)1 << 31), TQ_ERR_ARG,
+               "need 1 <= k <= 128 and 0 <= nq < 2^31");
+    if (nq == 0) return TQ_OK;
+    TQ_REQUIRE(cand_s && cand_i && row_offsets && top_s && top_i, TQ_ERR_ARG, "a required pointer is NULL");
+    TQ_REQUIRE(aligned(cand_s, 4) && aligned(cand_i, 4) && aligned(top_s, 4) && aligned(top_i, 4), TQ_ERR_ARG,
+               "misaligned pointer");
+    ShardOffsets offs{};
+    for (int r = 0; r < R; ++r) {
+        TQ_REQUIRE(row_offsets[r] >= 0 && row_offsets[r] < ((int64_t)1 << 31), TQ_ERR_ARG,
+                   "row offsets must be in [0, 2^31)");
+        offs.off[r] = row_offsets[r];
+    }
+    cudaError_t e = launch_topk_merge(cand_s, cand_i, R, nq, k, offs, top_s, top_i, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e, "tq_topk_merge launch");
 }
 
 struct SearchWs {

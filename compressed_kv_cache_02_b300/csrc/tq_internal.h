@@ -75,7 +75,7 @@ struct tq_ctx {
     float* dPi = nullptr;     // [d][d]  row-major Pi                (o = Pi^T a)
     float* dST = nullptr;     // [d][m]  ST[j*m+i] = S[i][j]        (u = S q)
     float* dStT = nullptr;    // [d][m]  StT[j*m+i] = (S Pi^T)[i][j] (S r = (S Pi^T)(Pi x - n c))
-    uint16_t* bops = nullptr; // d = 128: tcgen05 B operands (3 bf16 pieces of Pi, of S Pi^T)
+    uint16_t* bops = nullptr; // d = 128: tcgen05 B operands (2 bf16 pieces of Pi, of S Pi^T)
     float* dtab = nullptr;    // [L centroids | L - 1 thresholds] float32 (Params::tab)
     int* derr = nullptr;      // device error word
     int kernel_path = TQ_PATH_AUTO;   // logits kernel family (tq_set_kernel_path)

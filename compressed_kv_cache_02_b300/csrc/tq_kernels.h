@@ -65,9 +65,24 @@ cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* 
                                float* partials, float* out, cudaStream_t s);
 
 // Softmax + value sum from precomputed logits, then the combine (vc NULL: bf16 values of dim d).
+// part_out non-NULL: instead of the combine, one unnormalised partial state per (batch, head),
+// [B*Hq][d + 2] = (max, sum of weights, weighted sum in the rotated basis), for a shard merge.
 cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
                                const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
-                               float* partials, float* out, cudaStream_t s);
+                               float* partials, float* out, cudaStream_t s, float* part_out = nullptr);
+
+// out[bh] from R shards' partial states parts [R][BH][d + 2] (log-sum-exp merge, then Pi_v^T).
+cudaError_t launch_merge_partials(const tq_ctx* vc, int d, const float* parts, int R, int64_t BH, float* out,
+                                  cudaStream_t s);
+
+// Global top-k from R shards' lists cand [R][nq][k] (row numbers local to each shard, shifted by
+// offsets[r]; an entry with index INT_MAX is padding).
+constexpr int kMaxShards = 64;
+struct ShardOffsets {
+    long long off[kMaxShards];
+};
+cudaError_t launch_topk_merge(const float* cand_s, const int32_t* cand_i, int R, int64_t nq, int k,
+                              const ShardOffsets& offs, float* top_s, int32_t* top_i, cudaStream_t s);
 
 // Search: per-chunk top-k candidates into cand (score, index pairs), then the merge.
 void search_chunking(int64_t n, int k, int* chunk, int* nchunk);

@@ -55,6 +55,9 @@ _SIGS = {
     "tq_attn_values_workspace_size": [_i, _i, _i, _i, _i64, ctypes.POINTER(_sz)],
     "tq_attn_values": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _sz, _p],
     "tq_attn_values_noalloc": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p],
+    "tq_attn_values_partial": [_p, _i, _p, _i, _i, _i, _i64, _p, _p, _p, _p, _p, _sz, _p],
+    "tq_attn_merge_partials": [_p, _i, _p, _i, _i, _i, _p, _p],
+    "tq_topk_merge": [_p, _p, _i, _i64, _i, _p, _p, _p, _p],
     "tq_search_workspace_size": [_p, _i64, _i64, _i, ctypes.POINTER(_sz)],
     "tq_search_topk": [_p, _p, _i64, _p, _p, _p, _p, _i64, _i, _p, _p, _p, _sz, _p],
     "tq_sync_status": [_p, _p, _p],
@@ -155,6 +158,50 @@ def attn_values(logits, length, values, vctx=None, d=None, Hkv=None, out=None, w
     _check(lib.tq_attn_values(vh, d, _ptr(logits), B, Hq, Hkv, cap, _ptr(length), vptr, vnorm, _ptr(out),
                               _ptr(workspace), workspace.numel(), _stream(stream)), "tq_attn_values")
     return out
+
+
+def attn_values_partial(logits, length, values, vctx=None, out=None, workspace=None, stream=None):
+    """tq_attn_values_partial: this block's partial states [B, Hq, d + 2] = (max, weight sum,
+    weighted value sum) over logits [B, Hq, cap] and its values (bf16 [B, Hkv, cap, d] or Codes)."""
+    B, Hq, cap = logits.shape
+    if vctx is None:
+        Hkv, d = values.shape[1], values.shape[3]
+        vptr, vnorm, vh = _ptr(values), None, None
+    else:
+        Hkv, d = values.planes.shape[1], vctx.d
+        vptr, vnorm, vh = _ptr(values.planes), _ptr(values.norm), vctx.h
+    if out is None:
+        out = torch.empty(B, Hq, d + 2, device=logits.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = values_workspace(d, B, Hq, Hkv, cap, device=logits.device)
+    _check(lib.tq_attn_values_partial(vh, d, _ptr(logits), B, Hq, Hkv, cap, _ptr(length), vptr, vnorm, _ptr(out),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)), "tq_attn_values_partial")
+    return out
+
+
+def attn_merge_partials(parts, vctx=None, out=None, stream=None):
+    """tq_attn_merge_partials: parts [R, B, Hq, d + 2] of R blocks -> out [B, Hq, d]."""
+    R, B, Hq, d2 = parts.shape
+    d = d2 - 2
+    parts = parts.contiguous()
+    if out is None:
+        out = torch.empty(B, Hq, d, device=parts.device, dtype=torch.float32)
+    _check(lib.tq_attn_merge_partials(None if vctx is None else vctx.h, d, _ptr(parts), R, B, Hq, _ptr(out),
+                                      _stream(stream)), "tq_attn_merge_partials")
+    return out
+
+
+def topk_merge(cand_s, cand_i, row_offsets, stream=None):
+    """tq_topk_merge: R blocks' lists cand_s / cand_i [R, nq, k] (block-local rows, INT32_MAX =
+    padding) and their first global rows -> global top_s, top_i [nq, k]."""
+    import numpy as np
+    R, nq, k = cand_s.shape
+    offs = np.ascontiguousarray(np.asarray(row_offsets, dtype=np.int64))
+    top_s = torch.empty(nq, k, device=cand_s.device, dtype=torch.float32)
+    top_i = torch.empty(nq, k, device=cand_s.device, dtype=torch.int32)
+    _check(lib.tq_topk_merge(_ptr(cand_s.contiguous()), _ptr(cand_i.contiguous()), R, nq, k, offs.ctypes.data,
+                             _ptr(top_s), _ptr(top_i), _stream(stream)), "tq_topk_merge")
+    return top_s, top_i
 
 
 class Context:

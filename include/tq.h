@@ -261,6 +261,39 @@ int tq_attn_values(const tq_ctx* vctx, int d, const float* logits, int B, int Hq
                    int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
                    float* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- sharded attention and search
+ * A sequence (or a database) cut into R contiguous blocks held by R processes, one GPU each.  The
+ * pages time both operations on one GPU (juejin.cn post, section 三); the reading for R blocks is
+ * the exact split of the softmax: each block contributes its partial state, and the states are
+ * merged by their maxima (log-sum-exp).  The exchange between processes (an all-gather of the
+ * partial states, or of the per-block top-k lists) is the caller's: these calls compute on one
+ * device and take device buffers.                                                            */
+
+/* As tq_attn_values over this call's block of the sequence (len[b] = the number of positions the
+ * block holds for batch b), but instead of the output it writes one partial state per (batch,
+ * query head): part float32 [B][Hq][d + 2] = (m, l, a[0..d)) with m the largest logit, l = sum_i
+ * exp(logit_i - m) and a = sum_i exp(logit_i - m) v_i; for coded values a is in the value
+ * context's rotated basis (v_i = n16 c_v[idx_i], before Pi_v^T).  A sequence with no positions in
+ * the block gets m = -inf, l = 0, a = 0.  Workspace: tq_attn_values_workspace_size.          */
+int tq_attn_values_partial(const tq_ctx* vctx, int d, const float* logits, int B, int Hq, int Hkv,
+                           int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
+                           float* part, void* workspace, size_t ws_bytes, void* stream);
+
+/* out[b][h] (float32 [B][Hq][d]) from the partial states of R blocks, parts float32
+ * [R][B][Hq][d + 2] as tq_attn_values_partial writes them:  with M = max_r m_r,
+ *   out = Pi_v^T (sum_r exp(m_r - M) a_r) / sum_r exp(m_r - M) l_r
+ * (no rotation for bf16 values: vctx NULL); zeros where every block is empty.                */
+int tq_attn_merge_partials(const tq_ctx* vctx, int d, const float* parts, int R, int B, int Hq,
+                           float* out, void* stream);
+
+/* Global top-k from R blocks' lists: cand_s float32 [R][nq][k] and cand_i int32 [R][nq][k] (row
+ * numbers within block r, as tq_search_topk returns them; an entry whose index is INT32_MAX is
+ * padding, for a block with fewer than k rows); row_offsets host int64 [R] (block r's first global
+ * row, each in [0, 2^31)).  top_s / top_i [nq][k]: the k best of all blocks' candidates by score
+ * descending, equal scores by global row ascending.  1 <= R <= 64, 1 <= k <= TQ_MAX_TOPK.     */
+int tq_topk_merge(const float* cand_s, const int32_t* cand_i, int R, int64_t nq, int k,
+                  const int64_t* row_offsets, float* top_s, int32_t* top_i, void* stream);
+
 /* Size of the static scratch array behind tq_attn_values_noalloc (8 MiB per device).     */
 #define TQ_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -271,10 +304,13 @@ int tq_attn_values(const tq_ctx* vctx, int d, const float* logits, int B, int Hq
  * have no counterpart: this is an interface variant, the arithmetic is tq_attn_values'.
  * Scratch: a file-scope device array of TQ_NOALLOC_SCRATCH_BYTES that every GPU loading the
  * library keeps until exit.  Shapes needing more than that (B*Hq*nchunk*(d+2)*4 bytes, as
- * tq_attn_values_workspace_size reports) are rejected with TQ_ERR_UNSUPPORTED.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  No call allocates or
- * frees memory.  All calls on a device share the array: calls that overlap on the GPU race. */
+ * tq_attn_values_workspace_size reports) are rejected with TQ_ERR_UNSUPPORTED, and so are
+ * split (fractional bit width) value contexts, which tq_attn_values takes.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that device current
+ * and keeps it for the life of the process; make that first call before any stream capture.
+ * A cudaDeviceReset (or any teardown of the device's primary context) invalidates the kept
+ * address: do not call this entry point on that device afterwards.  No call allocates or frees
+ * memory.  All calls on a device share the array: calls that overlap on the GPU race.       */
 int tq_attn_values_noalloc(const tq_ctx* vctx, int d, const float* logits, int B, int Hq, int Hkv,
                            int64_t cap, const int32_t* len, const void* values, const uint16_t* v_norm,
                            float* out, void* stream);

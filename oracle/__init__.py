@@ -73,3 +73,4 @@ __all__ = [
     "SplitCodebook", "split_quantize", "split_dequantize", "split_estimate", "pack_split", "unpack_split",
     "QJL_CONST",
 ]
+from . import sharded

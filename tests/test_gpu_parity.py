@@ -85,23 +85,26 @@ def test_quantize_mse_mode(bits, d, n):
 
 @pytest.mark.parametrize("d", [128, 200])
 def test_round_trip_at_eight_bits_on_gpu(d):
-    """The high-bit-width round trip through the library: codes of x at 8 MSE bits, the oracle's
-    reconstruction of those codes, coded again by the library, give the same codes wherever the
-    reconstruction's rotated direction is not within 1e-5 of a threshold."""
+    """The high-bit-width round trip through the library: the codes of x at 8 MSE bits, the
+    reconstruction of those codes (oracle), coded again by the library.  The second coding passes
+    the quantize parity rules against the oracle's coding of the same reconstruction, and returns
+    the first codes on every row whose centroid vector has unit norm to within 5e-3 (the rows
+    where the renormalisation of re-coding keeps every value in its cell; over 99 % of them)."""
     tq = _tq()
     pr = Pair(d, 8, mode=tq.TQ_MODE_MSE, seed=3)
     X = 5.0 * inputs.gaussian(1000, d, seed=11)
     c1 = pr.ctx.quantize(X.cuda())
     idx1, n1, _, _ = pr.from_device(c1)
-    Xh = oracle.dequantize(idx1, n1, pr.Pi, pr.cb)
-    c2 = pr.ctx.quantize(torch.from_numpy(Xh.astype(np.float32)).cuda())
+    Xh = oracle.dequantize(idx1, n1, pr.Pi, pr.cb).astype(np.float32)
+    c2 = pr.ctx.quantize(torch.from_numpy(Xh).cuda())
     assert pr.ctx.sync_status() == 0
+    check_codes(pr, Xh, c2)
     idx2, _, _, _ = pr.from_device(c2)
-    U2 = (Xh @ pr.Pi.T) / np.linalg.norm(Xh, axis=1, keepdims=True)
-    near = np.min(np.abs(U2[..., None] - pr.cb.thresholds[None, None, :]), axis=-1) < 1e-5
-    diff = idx1 != idx2
-    assert not (diff & ~near).any()
-    rel = np.sum((X.numpy() - Xh) ** 2, axis=1) / np.sum(X.numpy().astype(np.float64) ** 2, axis=1)
+    unit = np.abs(np.linalg.norm(pr.cb.centroids[idx1], axis=1) - 1.0) < 5e-3
+    assert unit.mean() > 0.99
+    assert np.array_equal(idx2[unit], idx1[unit])
+    Xd = X.numpy().astype(np.float64)
+    rel = np.sum((Xd - Xh) ** 2, axis=1) / np.sum(Xd ** 2, axis=1)
     assert abs(rel.mean() - pr.cb.distortion()) < 3 * rel.std() / np.sqrt(len(rel)) + 2.0 ** -22
 
 
