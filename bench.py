@@ -205,9 +205,9 @@ def run_tq(args, world, rank, local):
     dev = torch.device("cuda", local)
     state = build_state(dev)
     kctx, vctx, kc, vc, cap = state["kctx"], state["vctx"], state["kc"], state["vc"], state["cap"]
-    path = {"auto": tq.TQ_PATH_AUTO, "cuda_core": tq.TQ_PATH_CUDA_CORE, "tensor": tq.TQ_PATH_TENSOR}[args.kernel_path]
-    kctx.set_kernel_path(path)
-    vctx.set_kernel_path(path)
+    paths = {"auto": tq.TQ_PATH_AUTO, "cuda_core": tq.TQ_PATH_CUDA_CORE, "tensor": tq.TQ_PATH_TENSOR}
+    kctx.set_kernel_path(paths[args.kernel_path])
+    vctx.set_kernel_path(paths[args.values_path or args.kernel_path])
     total = args.warmup + args.steps
     assert N0 - args.warmup >= 1 and N0 + args.steps <= cap
     ks, vs, qs = step_inputs(state, total, dev)
@@ -325,7 +325,7 @@ def run_tq(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "kv_heads": HKV, "query_heads": HQ, "head_dim": D,
                    "cached_tokens": N0, "key_bits": KBITS, "value_bits": VBITS, "parallelism": f"replicas x{world}",
-                   "kernel_path": args.kernel_path,
+                   "kernel_path": args.kernel_path, "values_path": args.values_path or args.kernel_path,
                    "l2": "inputs larger than L2 (cache codes ~0.9 GB)"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": dom_gbs / hbm, "peak_source": f"{peak_kind} hbm_gbs",
@@ -990,6 +990,8 @@ def main():
     ap.add_argument("--batch", type=int, default=B, help="smaller batch for profiling captures (default 8)")
     ap.add_argument("--kernel-path", choices=["auto", "cuda_core", "tensor"], default="auto",
                     help="kernel family of the decode step (tq_set_kernel_path)")
+    ap.add_argument("--values-path", choices=["auto", "cuda_core", "tensor"], default=None,
+                    help="kernel family of the value sum (default: --kernel-path)")
     ap.add_argument("--only", choices=["search", "prefill", "fractional", "polar", "decode1", "paged"], default=None,
                     help="run only one secondary workload and print its measurements (profiling captures)")
     args = ap.parse_args()

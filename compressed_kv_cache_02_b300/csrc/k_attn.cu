@@ -838,7 +838,11 @@ cudaError_t run_logits_q8(const AttnArgs& a, dim3 grid, cudaStream_t s) {
 
 cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qproj, int B, int Hq,
                           int Hkv, const KeyCache& k, float scale, float* logits, void* image, cudaStream_t s) {
-    if (kc->kernel_path == TQ_PATH_TENSOR && logits_tc_ok(kc, k))
+    // AUTO takes the tensor-core kernel where it measured faster than the byte tables: keys of
+    // 2 MSE bits + QJL (at 1 or 3 MSE bits, and below ~2^18 keys x head quads, the byte tables win)
+    const int64_t quad_keys = (int64_t)B * Hkv * ((Hq / Hkv + 3) / 4) * k.cap;
+    const bool tc_auto = kc->kernel_path == TQ_PATH_AUTO && kc->prm.qjl && kc->prm.P == 2 && quad_keys >= (1 << 18);
+    if ((kc->kernel_path == TQ_PATH_TENSOR || tc_auto) && logits_tc_ok(kc, k))
         return launch_logits_tc(kc, qrot, qproj, B, Hq, Hkv, k, scale, logits, image, s);
     AttnArgs a = make_args(kc, qrot, qproj, B, Hq, Hkv, k, scale);
     a.logits = logits;
@@ -860,7 +864,7 @@ cudaError_t launch_logits(const tq_ctx* kc, const float* qrot, const float* qpro
 
 cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
                                const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
-                               float* partials, float* out, cudaStream_t s, float* part_out) {
+                               float* partials, float* out, cudaStream_t s, float* part_out, bool allow_tc) {
     ValuesArgs a{};
     a.logits = logits;
     a.B = B;
@@ -875,10 +879,20 @@ cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int
     a.v = ValueSrc{values, vnorm, vc ? vc->P : 0, vc ? vc->W : 0, d};
     a.partials = partials;
     attn_chunking(nullptr, B, Hq, Hkv, cap, &a.chunk, &a.nchunk);
+    // the tensor-core kernel copies the norms as 4-byte pairs: an even capacity and a 4-byte
+    // aligned norm array keep every pair aligned and inside its sequence's rows
+    const bool tc = allow_tc && vc && vc->kernel_path == TQ_PATH_TENSOR && values_tc_supported(vc, d) &&
+                    cap % 2 == 0 && (reinterpret_cast<uintptr_t>(vnorm) & 3u) == 0;
+    if (tc) {
+        a.chunk = values_tc_chunk(B, Hq, Hkv, cap);
+        a.nchunk = (int)((cap + a.chunk - 1) / a.chunk);
+    }
     dim3 grid(a.nchunk, B * Hkv, (a.G + 3) / 4);
     const int W = (d + 31) / 32;
     cudaError_t e;
-    if (vc && W == 4 && vc->P <= kFastBits) {
+    if (tc) {
+        e = launch_values_tc(vc, d, logits, B, Hq, Hkv, cap, len, values, vnorm, err, partials, a.chunk, a.nchunk, s);
+    } else if (vc && W == 4 && vc->P <= kFastBits) {
         switch (vc->P) {
             case 1: e = run_values_coded128<1>(a, grid, s); break;
             case 2: e = run_values_coded128<2>(a, grid, s); break;

@@ -14,31 +14,23 @@
 //   shifted copy of a 32-bit word with 0x04040404 or 0x08080808 yields 4 coordinates at once:
 //   register c of word x is ((x >> s_c) & mask_c), byte i holding coordinate 8 i + ((c + 2) & 7)
 //   of the word with value 2^-7 (c even) or 2^-6 (c odd).  Eleven ALU operations per 32
-//   coordinates; tcgen05.st writes the registers as TMEM columns (4 k per 32-bit column).
+//   coordinates; one 32-column tcgen05.st writes a bit vector (4 k per 32-bit column).
 // B (K x 16 columns, shared memory, K-major no-swizzle core matrices): column 4 h + pc is piece
 //   pc of query head h, value x 2^(e0_h) x (2^7 or 2^6, undoing the A scale); four e4m3 pieces
 //   x = b0 + b1/16 + b2/256 + b3/4096 carry ~16 bits.  Built once per group by
 //   tc_image_kernel, with the epilogue constants, and copied into shared memory per CTA.
-// D (fp32, TMEM): 16 columns per mma warp; the MSE blocks sum, and so do the QJL ones.
+// D (fp32, TMEM): 16 MSE columns (the T terms accumulate) and 16 QJL columns.
 //
-// One CTA per SM owns a contiguous range of 128-key tiles.  Tile i goes to worker group i % 4;
-// the groups run independently and meet the shared producer only at mbarriers (every wait is
-// bounded; a timeout sets TQ_DEVERR_TIMEOUT and stops every role):
-//   per group (128 TMEM columns: two 32-column A slots and two 32-column D buffers, and a
-//   ring of shared-memory stages)
-//     4 worker warps  warp q owns keys 32 q .. 32 q + 31 of the group's tiles (its TMEM lanes):
-//                  it expands the tile's bit vectors one at a time into the next free A slot,
-//                  then finishes the group's previous tile from its D buffer into logits;
-//     1 mma warp   bulk asynchronous copies of the group's tiles (one per field: planes, signs,
-//                  norms, residual norms; lengths rounded up to 8 keys, inside the cache since
-//                  its capacity is a multiple of 8) into the stage ring, refilling a stage once
-//                  the workers have released the tile two back (its D buffer, hence its stage);
-//                  per bit vector 4 tcgen05.mma (K = 32) from the slot into the tile's D (16
-//                  MSE columns, the T terms accumulating, and 16 QJL columns), a commit that
-//                  frees the slot when they complete, and per tile a commit that fills D.
-//                  Issue costs its thread ~70 cycles per mma, so four groups issue in parallel.
-//                  At a change of (batch, KV head, quad) it drains its mma and loads the
-//                  group's B image into its own buffer.
+// logits_tc_kernel: a CTA of 4 warps owns a chunk of keys of one (batch, KV head, head quad) and
+// walks it in tiles of 128 keys, one key per thread (= TMEM lane).  Per tile: the next tile's codes
+// are copied (cp.async) into the other of two stages; each thread builds its key's bit vectors,
+// waits until the previous tile's MMAs are done, finishes that tile from D (its previous key's
+// logits), expands the new vectors into A and, after one CTA barrier, one thread issues the tile's
+// mma (4 per bit vector) and a commit.  A (32 columns per vector) and D (32 columns) fit 128 TMEM
+// columns (256 at 3 MSE bits), so up to 4 (2) CTAs share an SM and interleave their tiles on the
+// tensor pipe: the small mma (N = 16) are bound by the issue rate of the tensor pipe (about one
+// per 32 cycles per SM measured), not by its arithmetic.  Every wait is bounded in time; one that
+// runs out sets TQ_DEVERR_TIMEOUT.
 #include "mma_e4m3.cuh"
 #include "tq_kernels.h"
 
@@ -46,13 +38,8 @@ namespace tq {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kGroups = 4;                        // worker groups (tiles in flight x2)
-constexpr int kWorkerWarps = 4 * kGroups;         // warps 0..15: group w / 4, lanes 32 (w % 4)
-constexpr int kMmaWarp0 = kWorkerWarps;           // warps 16..19: the groups' mma (and copy) warps
-constexpr int kThreads = (kMmaWarp0 + kGroups) * 32;
-constexpr int kGroupCols = 128;                   // TMEM columns per group
-constexpr int kSuspendNs = 20000;     // suspend-time hint of one try_wait
-constexpr int kWaitLimit = 1 << 16;   // tries before a wait gives up (bounded by ~1.3 s)
+constexpr int kSuspendNs = 20000;                 // suspend-time hint of one try_wait
+constexpr uint64_t kWaitNs = 1000000000ull;       // a wait gives up after one second
 
 template <int P>
 struct TcCfg {
@@ -66,15 +53,7 @@ struct TcCfg {
     static constexpr int kBqBytes = 16 * 128;       // QJL B: 16 columns x 128 k
     static constexpr int kConstOff = kBmBytes + kBqBytes;
     static constexpr int kImgBytes = (kConstOff + 64 + 127) / 128 * 128;
-    static constexpr int kMaxStages = 8;        // per group
-    // each group's stage ring fills its share of what the images leave of ~200 KB (one CTA and
-    // its 512 TMEM columns per SM)
-    static constexpr int kStagesFit = (200 * 1024 - kGroups * kImgBytes) / (kGroups * kStageBytes);
-    static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
-    static constexpr int kImgOff = kGroups * kStages * kStageBytes;
-    static constexpr int kSmem = kImgOff + kGroups * kImgBytes;
     static_assert(kStageBytes % 128 == 0, "stage alignment");
-    static_assert(kStages >= 3, "the producer must run ahead of the finish");
 };
 
 struct TcArgs {
@@ -91,20 +70,17 @@ struct TcArgs {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-__device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 // Waits for the phase with the given parity to complete.  Each try_wait may suspend the thread
-// for up to kSuspendNs (it resumes as soon as the phase completes), so waiting warps do not
-// spin on the issue slots; false after kWaitLimit tries (~1 s).
+// for up to kSuspendNs (it resumes as soon as the phase completes); false once kWaitNs of
+// wall-clock time (the GPU's global timer) have passed.
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-    for (int it = 0; it < kWaitLimit; ++it) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
@@ -112,8 +88,8 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
             : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
             : "memory");
         if (done) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 // K-major no-swizzle operand: core matrices of 8 rows x 16 bytes, LBO = 128 B along K,
@@ -139,13 +115,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)));
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
-}
-__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void bar_init_n(uint64_t* bar, int n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(n));
 }
@@ -161,55 +130,6 @@ __device__ __forceinline__ void expand_word(uint32_t x, uint32_t (&r)[8]) {
     r[5] = z & 0x08080808u;
     r[6] = u & 0x04040404u;
     r[7] = u & 0x08080808u;
-}
-
-__device__ __forceinline__ int group_len(const TcArgs& a, int g) {
-    const int L = a.k.len[g / (a.Hkv * a.quads)];
-    return L < 0 ? 0 : (L > a.k.cap ? (int)a.k.cap : L);
-}
-
-struct Cursor {
-    int g, L, k0;
-};
-
-__device__ Cursor seek(const TcArgs& a, int64_t u) {
-    Cursor c{0, 0, 0};
-    for (; c.g < a.ngroups; ++c.g) {
-        c.L = group_len(a, c.g);
-        const int64_t n = (c.L + kTile - 1) / kTile;
-        if (u < n) {
-            c.k0 = (int)(u * kTile);
-            return c;
-        }
-        u -= n;
-    }
-    c.L = 0;
-    return c;
-}
-
-__device__ __forceinline__ void next_tile(const TcArgs& a, Cursor& c) {
-    c.k0 += kTile;
-    while (c.k0 >= c.L && c.g < a.ngroups) {
-        ++c.g;
-        c.k0 = 0;
-        c.L = c.g < a.ngroups ? group_len(a, c.g) : 0;
-    }
-}
-
-template <int P>
-__device__ void issue_tile(const TcArgs& a, const Cursor& c, unsigned char* st, uint64_t* bar) {
-    using C = TcCfg<P>;
-    const int b = c.g / (a.Hkv * a.quads), kvh = (c.g / a.quads) % a.Hkv;
-    const size_t row = ((size_t)b * a.Hkv + kvh) * (size_t)a.k.cap + (size_t)c.k0;
-    const int nk = min(kTile, c.L - c.k0);
-    const uint32_t nc = (uint32_t)((nk + 7) & ~7);
-    const bool qjl = a.prm.qjl != 0;
-    const uint32_t bp = nc * P * 16, bs = qjl ? nc * 16 : 0u, bn = nc * 2, br = qjl ? nc * 2 : 0u;
-    bar_expect_tx(bar, bp + bs + bn + br);
-    bulk_copy(st, a.k.planes + row * (P * 4), bp, bar);
-    if (qjl) bulk_copy(st + C::kSignOff, a.k.signs + row * 4, bs, bar);
-    bulk_copy(st + C::kNormOff, a.k.norm + row, bn, bar);
-    if (qjl) bulk_copy(st + C::kRnormOff, a.k.rnorm + row, br, bar);
 }
 
 struct GroupPos {
@@ -329,42 +249,6 @@ __device__ __forceinline__ void load_vectors(const unsigned char* st, int row, b
     x[T] = qjl ? *reinterpret_cast<const uint4*>(st + C::kSignOff + row * 16) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// One bit vector into the 32 columns of an A slot: word wd -> columns 8 wd .. 8 wd + 7.
-__device__ __forceinline__ void expand_vector(const uint4& x, uint32_t slot_tmem) {
-    uint32_t r[8];
-    expand_word(x.x, r);
-    tmem_st8(slot_tmem, r);
-    expand_word(x.y, r);
-    tmem_st8(slot_tmem + 8, r);
-    expand_word(x.z, r);
-    tmem_st8(slot_tmem + 16, r);
-    expand_word(x.w, r);
-    tmem_st8(slot_tmem + 24, r);
-}
-
-// Per-group values a worker needs to finish tiles.
-struct FinishGroup {
-    int g, nh;
-    size_t qrow0;
-    const float4* c;   // 2^-e0 (MSE) x4, 2^-e0 (QJL) x4, c0 sum q' x4, -kq sum u x4 (shared memory)
-};
-
-// Called by a whole warp: the group's position and its 16 epilogue constants into the warp's
-// own shared-memory slot.
-template <int P>
-__device__ __forceinline__ void finish_group(const TcArgs& a, int g, float* warp_cst, FinishGroup& F) {
-    using C = TcCfg<P>;
-    const GroupPos gp = group_pos(a, g);
-    F.g = g;
-    F.nh = gp.nh;
-    F.qrow0 = gp.qrow0;
-    const int lane = threadIdx.x & 31;
-    __syncwarp();   // every lane is done with the previous group's constants
-    if (lane < 16) warp_cst[lane] = __ldg(reinterpret_cast<const float*>(a.img + (size_t)g * C::kImgBytes + C::kConstOff) + lane);
-    __syncwarp();
-    F.c = reinterpret_cast<const float4*>(warp_cst);
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -376,292 +260,245 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// Logits of key `row` for the 4 heads of the tile's quad from its D buffer.
+// ------------------------------------------------------------------ scoring, one CTA per chunk
+
+constexpr int kT2Threads = 128;
+constexpr int kT2ChunkMax = 2048;
+
+#ifndef TQ_LOGITS_TC_BUFFERS
+#define TQ_LOGITS_TC_BUFFERS 1
+#endif
+
 template <int P>
-__device__ __forceinline__ void finish_tile(const TcArgs& a, const unsigned char* st, uint32_t d_tmem,
-                                            const Cursor& c, const FinishGroup& F, int row) {
+struct Tc2Cfg {
     using C = TcCfg<P>;
-    const bool qjl = a.prm.qjl != 0;
-    float dm[16], dq[16];
-    tmem_ld16(d_tmem, dm);
-    if (qjl) tmem_ld16(d_tmem + 16, dq);
-    const float n = half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[row]);
-    const float rho = qjl ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[row]) : 0.f;
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    const int key = c.k0 + row;
-    if (key >= c.L) return;
-    const float k2 = 2.f * a.prm.qjl_scale;
-    const float4 fm4 = F.c[0], fq4 = F.c[1], cq4 = F.c[2], cu4 = F.c[3];
-    const float fm[4] = {fm4.x, fm4.y, fm4.z, fm4.w}, fq[4] = {fq4.x, fq4.y, fq4.z, fq4.w};
-    const float cq[4] = {cq4.x, cq4.y, cq4.z, cq4.w}, cu[4] = {cu4.x, cu4.y, cu4.z, cu4.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        // pieces: sum_pc D[pc] 16^-pc, then the column scale 2^-e0
-        const float m = fm[h] * fmaf(dm[4 * h + 3], 1.f / 4096.f,
-                                     fmaf(dm[4 * h + 2], 1.f / 256.f, fmaf(dm[4 * h + 1], 1.f / 16.f, dm[4 * h])));
-        float est = n * (cq[h] + m);
-        if (qjl) {
-            const float qv = fq[h] * fmaf(dq[4 * h + 3], 1.f / 4096.f,
-                                          fmaf(dq[4 * h + 2], 1.f / 256.f, fmaf(dq[4 * h + 1], 1.f / 16.f, dq[4 * h])));
-            est = fmaf(rho, fmaf(k2, qv, cu[h]), est);
-        }
-        if (h < F.nh) a.logits[(F.qrow0 + h) * (size_t)a.k.cap + key] = a.scale * est;
-    }
+    static constexpr int kACols = 32 * C::NV;                       // A: one 32-column slot per vector
+    static constexpr int kBufCols = kACols + 32;                    // A and D (16 MSE + 16 QJL columns)
+    // two A + D buffers where they fit 256 columns (the MMAs of one tile then overlap the next
+    // tile's expansion and the finish of the one before), else one
+    static constexpr int NB = (TQ_LOGITS_TC_BUFFERS >= 2 && 2 * kBufCols <= 256) ? 2 : 1;
+    static constexpr int kTmemCols = (NB * kBufCols <= 128) ? 128 : 256;
+    static constexpr int kStageOff = C::kImgBytes;                  // B image, then two code stages
+    static constexpr int kSmemUsed = kStageOff + 2 * C::kStageBytes;
+    // dynamic shared memory requested: caps the CTAs per SM at 512 / kTmemCols
+    static constexpr int kSmem = kTmemCols == 128 ? 52 * 1024 : 100 * 1024;
+    static_assert(kSmemUsed <= kSmem, "shared memory layout");
+};
+
+__device__ __forceinline__ void cp_async16_tc(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 
-// Position in a ring of N slots: slot and the parity of its current use; `step` slots per move.
-template <int N>
-struct Ring {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void advance(int step = 1) {
-        slot += step;
-        if (slot >= N) {
-            slot -= N;
-            phase ^= 1u;
-        }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
+// Codes of the keys [k0, k0 + nk) of the cache rows starting at `row` into a stage (TcCfg
+// lays them out), 16-byte cp.async pieces, one commit group.  The norm fields are copied in whole
+// 16-byte pieces (8 keys), which stay inside the cache because its capacity is a multiple of 8.
+template <int P>
+__device__ __forceinline__ void stage_codes(const TcArgs& a, size_t row, int nk, unsigned char* st, bool qjl) {
+    using C = TcCfg<P>;
+    const int npl = nk * P, nsg = qjl ? nk : 0, nn = (nk + 7) / 8, nr = qjl ? nn : 0;
+    const uint4* pl = reinterpret_cast<const uint4*>(a.k.planes + row * (P * 4));
+    const uint4* sg = reinterpret_cast<const uint4*>(a.k.signs + row * 4);
+    const uint4* nm = reinterpret_cast<const uint4*>(a.k.norm + row);
+    const uint4* rn = reinterpret_cast<const uint4*>(a.k.rnorm + row);
+    for (int e = threadIdx.x; e < npl + nsg + nn + nr; e += kT2Threads) {
+        if (e < npl) cp_async16_tc(st + 16 * e, pl + e);
+        else if (e < npl + nsg) cp_async16_tc(st + C::kSignOff + 16 * (e - npl), sg + (e - npl));
+        else if (e < npl + nsg + nn) cp_async16_tc(st + C::kNormOff + 16 * (e - npl - nsg), nm + (e - npl - nsg));
+        else cp_async16_tc(st + C::kRnormOff + 16 * (e - npl - nsg - nn), rn + (e - npl - nsg - nn));
     }
-};
-
-struct Group {
-    uint64_t full[8];   // the group's stage ring
-    uint64_t slot_ready[2], slot_free[2], d_full[2], d_free[2], img_bar, drain_bar;
-};
-
-struct Shared {
-    Group grp[kGroups];
-    float cst[kWorkerWarps][16];   // per worker warp: the epilogue constants of its current group
-    uint32_t tmem;
-    int abort;
-};
-
-__device__ __forceinline__ bool aborted(const Shared& S) { return *(volatile const int*)&S.abort != 0; }
-__device__ __forceinline__ void abort_all(Shared& S, int* err) {
-    *(volatile int*)&S.abort = 1;
-    set_error(err, TQ_DEVERR_TIMEOUT);
+    asm volatile("cp.async.commit_group;");
 }
 
 template <int P>
-__global__ void __launch_bounds__(kThreads, 1) logits_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, int chunk) {
     using C = TcCfg<P>;
+    using K2 = Tc2Cfg<P>;
     constexpr int T = C::T;
-    extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ __align__(8) Shared S;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (blockIdx.x == 0 && tid == 0)
-        for (int b = 0; b < a.B; ++b)
-            if (a.k.len[b] < 0 || a.k.len[b] > a.k.cap) set_error(a.err, TQ_DEVERR_LEN_RANGE);
-    int64_t total = 0;
-    for (int g = 0; g < a.ngroups; ++g) total += (group_len(a, g) + kTile - 1) / kTile;
-    const int64_t lo = total * blockIdx.x / gridDim.x, hi = total * (blockIdx.x + 1) / gridDim.x, n = hi - lo;
-    if (n <= 0) return;   // uniform over the CTA, before any allocation
+    constexpr int NB = K2::NB;
+    extern __shared__ __align__(128) unsigned char sm[];
+    unsigned char* img = sm;
+    unsigned char* stages = sm + K2::kStageOff;
+    __shared__ __align__(8) uint64_t s_mma[NB];   // buffer u: the MMAs of its latest tile are done
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.y, b = bh / a.Hkv;
+    const int g = bh * a.quads + blockIdx.z;   // (batch, KV head, quad) as group_pos numbers them
+    const int L = checked_len(a.k.len, b, a.k.cap, a.err);
+    const int64_t i0 = (int64_t)blockIdx.x * chunk;
+    if (i0 >= L) return;
+    const int nkeys = (int)(min((int64_t)L, i0 + chunk) - i0);
+    const int ntile = (nkeys + kTile - 1) / kTile;
+    const GroupPos gp = group_pos(a, g);
     const bool qjl = a.prm.qjl != 0;
-    const int nv = qjl ? C::NV : T;   // bit vectors scored per key
+    const size_t row0 = (size_t)bh * a.k.cap + (size_t)i0;
 
+    for (int e = tid; e < C::kImgBytes / 16; e += kT2Threads)
+        cp_async16_tc(img + 16 * e, a.img + (size_t)g * C::kImgBytes + 16 * e);
+    stage_codes<P>(a, row0, min(kTile, nkeys), stages, qjl);
     if (tid == 0) {
-        for (int g = 0; g < kGroups; ++g) {
-            Group& G = S.grp[g];
-            for (int s = 0; s < C::kStages; ++s) bar_init_n(&G.full[s], 1);
-            for (int k = 0; k < 2; ++k) {
-                bar_init_n(&G.slot_ready[k], 4);
-                bar_init_n(&G.slot_free[k], 1);
-                bar_init_n(&G.d_full[k], 1);
-                bar_init_n(&G.d_free[k], 4);
-            }
-            bar_init_n(&G.img_bar, 1);
-            bar_init_n(&G.drain_bar, 1);
-        }
-        S.abort = 0;
+        for (int u = 0; u < NB; ++u) bar_init_n(&s_mma[u], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kMmaWarp0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&S.tmem)));
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "n"(K2::kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
-    const uint32_t tmem = S.tmem;
-    bool drained = true;
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t bimg = smem_u32(img);
+    const uint64_t bm0 = smem_desc(bimg, T * 128 * 8), bq0 = smem_desc(bimg + C::kBmBytes, 128 * 8);
+    const float k2 = 2.f * a.prm.qjl_scale;
+    float cst[16];
+    // this thread's key of the tiles in flight: norm, residual norm, index (-1: none); `newer` is
+    // the latest tile's, `older` the one before (two buffers)
+    struct KeyState {
+        float n, rho;
+        int key;
+    };
+    KeyState older{0.f, 0.f, -1}, newer{0.f, 0.f, -1};
+    bool ok = true;
 
-    if (warp >= kMmaWarp0) {
-        const int g = warp - kMmaWarp0;
-        Group& G = S.grp[g];
-        if (lane == 0 && g < n) {
-            Cursor c = seek(a, lo + g);
-            unsigned char* img = sm + C::kImgOff + g * C::kImgBytes;
-            const uint32_t bimg = smem_u32(img);
-            const uint32_t base = tmem + g * kGroupCols;
-            // B descriptors: the buffer is fixed (its contents follow the group); a K step of 32
-            // bytes is +256 B of start address, +16 in the descriptor's 16-byte address field
-            const uint64_t bm0 = smem_desc(bimg, T * 128 * 8), bq0 = smem_desc(bimg + C::kBmBytes, 128 * 8);
-            int cur_group = -1, nimg = 0, ndrain = 0;
-            bool issued_any = false;
-            Ring<2> sa, db;
-            // copies: the group's first kStages tiles now, then one refill per tile
-            unsigned char* ring = sm + g * C::kStages * C::kStageBytes;
-            const int64_t ntiles = (n - g + kGroups - 1) / kGroups;
-            Cursor cp = c;
-            Ring<C::kStages> rp;
-            int64_t copied = 0;
-            for (; copied < ntiles && copied < C::kStages; ++copied) {
-                issue_tile<P>(a, cp, ring + rp.slot * C::kStageBytes, &G.full[rp.slot]);
-                for (int s = 0; s < kGroups; ++s) next_tile(a, cp);
-                rp.advance();
-            }
-            int64_t k = 0;   // the group's tile count
-            for (int64_t i = g; i < n && !aborted(S); i += kGroups, ++k) {
-                if (c.g != cur_group) {   // drain the mma that read the old B, then load this group's
-                    bool ok = true;
-                    if (issued_any) {
-                        mma_commit(&G.drain_bar);
-                        ok = bar_wait(&G.drain_bar, (uint32_t)(ndrain++ & 1));
-                    }
-                    if (ok) {
-                        bar_expect_tx(&G.img_bar, C::kImgBytes);
-                        bulk_copy(img, a.img + (size_t)c.g * C::kImgBytes, C::kImgBytes, &G.img_bar);
-                        ok = bar_wait(&G.img_bar, (uint32_t)(nimg++ & 1));
-                    }
-                    if (!ok) {
-                        abort_all(S, a.err);
-                        break;
-                    }
-                    cur_group = c.g;
-                }
-                if (k >= 2) {
-                    if (!bar_wait(&G.d_free[db.slot], db.phase ^ 1u)) {
-                        abort_all(S, a.err);
-                        break;
-                    }
-                    // tile k - 2 is finished: its stage takes the next tile
-                    if (copied < ntiles) {
-                        issue_tile<P>(a, cp, ring + rp.slot * C::kStageBytes, &G.full[rp.slot]);
-                        for (int s = 0; s < kGroups; ++s) next_tile(a, cp);
-                        rp.advance();
-                        ++copied;
-                    }
-                }
-                const uint32_t d = base + 64 + 32 * db.slot;
-                bool ok = true;
+    // logits of this thread's key of a tile whose MMAs (on buffer u) are done
+    auto finish = [&](int u, const KeyState& ks) {
+        const uint32_t d = lane_tmem + (uint32_t)(u * K2::kBufCols + K2::kACols);
+        float dm[16], dq[16];
+        tmem_ld16(d, dm);
+        if (qjl) tmem_ld16(d + 16, dq);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (ks.key < 0) return;
 #pragma unroll
-                for (int v = 0; v < C::NV; ++v) {
-                    if (v == T && !qjl) break;
-                    if (!bar_wait(&G.slot_ready[sa.slot], sa.phase)) {
-                        ok = false;
-                        break;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;");
-                    const uint32_t a_t = base + 32 * sa.slot;
-                    const uint32_t dd = v < T ? d : d + 16;
-                    const uint64_t b0 = v < T ? bm0 + (uint64_t)(v * 4 * 16) : bq0;
-#pragma unroll
-                    for (int wd = 0; wd < 4; ++wd)
-                        mma_ts(dd, a_t + 8 * wd, b0 + (uint64_t)(wd * 16), (wd == 0 && (v == 0 || v == T)) ? 0u : 1u);
-                    mma_commit(&G.slot_free[sa.slot]);
-                    issued_any = true;
-                    sa.advance();
-                }
-                if (!ok) {
-                    abort_all(S, a.err);
-                    break;
-                }
-                mma_commit(&G.d_full[db.slot]);
-                db.advance();
-                for (int s = 0; s < kGroups; ++s) next_tile(a, c);
+        for (int h = 0; h < 4; ++h) {
+            const float m = cst[h] * fmaf(dm[4 * h + 3], 1.f / 4096.f,
+                                          fmaf(dm[4 * h + 2], 1.f / 256.f, fmaf(dm[4 * h + 1], 1.f / 16.f, dm[4 * h])));
+            float est = ks.n * (cst[8 + h] + m);
+            if (qjl) {
+                const float qv = cst[4 + h] * fmaf(dq[4 * h + 3], 1.f / 4096.f,
+                                                   fmaf(dq[4 * h + 2], 1.f / 256.f, fmaf(dq[4 * h + 1], 1.f / 16.f, dq[4 * h])));
+                est = fmaf(ks.rho, fmaf(k2, qv, cst[12 + h]), est);
             }
-            if (issued_any) {   // every mma issued has completed before the CTA can leave
-                mma_commit(&G.drain_bar);
-                drained &= bar_wait(&G.drain_bar, (uint32_t)(ndrain++ & 1));
-            }
-            // and every copy issued has landed (the last use of each stage)
-            for (int j = 0; j < C::kStages && j < copied; ++j) {
-                const int64_t u = copied - 1 - j;
-                drained &= bar_wait(&G.full[(int)(u % C::kStages)], (uint32_t)((u / C::kStages) & 1));
-            }
+            if (h < gp.nh) a.logits[(gp.qrow0 + h) * (size_t)a.k.cap + (size_t)(i0 + ks.key)] = a.scale * est;
         }
-    } else {
-        // worker warp: group g, keys (TMEM lanes) 32 q .. 32 q + 31
-        const int g = warp >> 2, q = warp & 3, row = 32 * q + lane;
-        Group& G = S.grp[g];
-        const unsigned char* ring = sm + g * C::kStages * C::kStageBytes;
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const uint32_t base = tmem + lane_off + g * kGroupCols;
-        if (g < n) {
-            Cursor ce = seek(a, lo + g), cf = ce;
-            FinishGroup F;
-            F.g = -1;
-            Ring<C::kStages> se, sf;
-            Ring<2> sa, db;
-            int64_t u = 0;   // A slot uses so far
-            const int64_t ntiles = (n - g + kGroups - 1) / kGroups;   // this group's tiles
-            for (int64_t k = 0; k <= ntiles; ++k) {
-                if (aborted(S)) break;
-                if (k < ntiles) {   // expand tile k: one bit vector per A slot
-                    bool okw = bar_wait(&G.full[se.slot], se.phase);
-                    uint4 x[C::NV];
-                    if (okw) load_vectors<P>(ring + se.slot * C::kStageBytes, row, qjl, x);
+    };
+    // waits (every thread, CTA-uniform outcome) for the MMAs of the tile that used buffer u last
+    auto wait_buffer = [&](int u, int tile) -> bool {
+        const bool w = bar_wait(&s_mma[u], (uint32_t)((tile / NB) & 1));
+        if (!__syncthreads_and(w)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        return true;
+    };
+
+    for (int t = 0; t < ntile && ok; ++t) {
+        const int u = t % NB;
+        unsigned char* st = stages + (t & 1) * C::kStageBytes;
+        if (t + 1 < ntile)
+            stage_codes<P>(a, row0 + (size_t)(t + 1) * kTile, min(kTile, nkeys - (t + 1) * kTile),
+                           stages + ((t + 1) & 1) * C::kStageBytes, qjl);
+        else
+            asm volatile("cp.async.commit_group;");
+        asm volatile("cp.async.wait_group 1;");
+        asm volatile("fence.proxy.async.shared::cta;");   // the image is read by the tensor cores
+        __syncthreads();
+        if (t == 0) {
 #pragma unroll
-                    for (int v = 0; v < C::NV; ++v) {
-                        if (!okw || (v == T && !qjl)) break;
-                        // the slot's previous vector must be consumed by its mma
-                        if (u >= 2) okw = bar_wait(&G.slot_free[sa.slot], sa.phase ^ 1u);
-                        if (!okw) break;
-                        asm volatile("tcgen05.fence::after_thread_sync;");
-                        expand_vector(x[v], base + 32 * sa.slot);
-                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                        asm volatile("tcgen05.fence::before_thread_sync;");
-                        __syncwarp();
-                        if (lane == 0) bar_arrive(&G.slot_ready[sa.slot]);
-                        sa.advance();
-                        ++u;
-                    }
-                    if (!okw) {
-                        abort_all(S, a.err);
-                        break;
-                    }
-                    for (int s = 0; s < kGroups; ++s) next_tile(a, ce);
-                    se.advance();
-                }
-                if (k >= 1) {   // finish tile k - 1
-                    if (!bar_wait(&G.d_full[db.slot], db.phase)) {
-                        abort_all(S, a.err);
-                        break;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;");
-                    if (cf.g != F.g) finish_group<P>(a, cf.g, S.cst[warp], F);
-                    finish_tile<P>(a, ring + sf.slot * C::kStageBytes, base + 64 + 32 * db.slot, cf, F, row);
-                    asm volatile("tcgen05.fence::before_thread_sync;");
-                    __syncwarp();
-                    if (lane == 0) bar_arrive(&G.d_free[db.slot]);   // frees D and the tile's stage
-                    db.advance();
-                    for (int s = 0; s < kGroups; ++s) next_tile(a, cf);
-                    sf.advance();
-                }
-            }
+            for (int i = 0; i < 16; ++i) cst[i] = reinterpret_cast<const float*>(img + C::kConstOff)[i];
         }
+        // this thread's key of tile t: its bit vectors and norms
+        const int key = t * kTile + tid;
+        const bool valid = key < nkeys;
+        uint4 x[C::NV];
+        load_vectors<P>(st, tid, qjl, x);
+        const float n = valid ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[tid]) : 0.f;
+        const float rho = (valid && qjl) ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[tid]) : 0.f;
+        // buffer u was last used by tile t - NB: wait for its MMAs, finish it
+        if (t >= NB) {
+            if (!wait_buffer(u, t - NB)) {
+                ok = false;
+                break;
+            }
+            finish(u, NB == 2 ? older : newer);
+        }
+        const uint32_t abuf = (uint32_t)(u * K2::kBufCols);
+#pragma unroll
+        for (int v = 0; v < C::NV; ++v) {
+            if (v == T && !qjl) break;
+            uint32_t r[32];
+            const uint32_t w4[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+                uint32_t e8[8];
+                expand_word(w4[wd], e8);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) r[8 * wd + c] = e8[c];
+            }
+            tmem_st32(lane_tmem + abuf + 32 * v, r);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            const uint32_t dm_t = tmem + abuf + K2::kACols, dq_t = dm_t + 16;
+#pragma unroll
+            for (int v = 0; v < T; ++v)
+#pragma unroll
+                for (int wd = 0; wd < 4; ++wd)
+                    mma_ts(dm_t, tmem + abuf + 32 * v + 8 * wd, bm0 + (uint64_t)((v * 4 + wd) * 16),
+                           (v == 0 && wd == 0) ? 0u : 1u);
+            if (qjl) {
+#pragma unroll
+                for (int wd = 0; wd < 4; ++wd)
+                    mma_ts(dq_t, tmem + abuf + 32 * T + 8 * wd, bq0 + (uint64_t)(wd * 16), wd == 0 ? 0u : 1u);
+            }
+            mma_commit(&s_mma[u]);
+        }
+        older = newer;
+        newer = KeyState{n, rho, valid ? key : -1};
+    }
+    asm volatile("cp.async.wait_all;");
+    // the tiles still in flight, oldest first
+    if (ok && NB == 2 && ntile >= 2) {
+        ok = wait_buffer((ntile - 2) % NB, ntile - 2);
+        if (ok) finish((ntile - 2) % NB, older);
+    }
+    if (ok) {
+        ok = wait_buffer((ntile - 1) % NB, ntile - 1);
+        if (ok) finish((ntile - 1) % NB, newer);
+    }
+    if (!ok) {
+        if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
+        return;   // an MMA may still be in flight: the TMEM allocation is left to the context teardown
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
-    const bool ok = __syncthreads_and(drained && !aborted(S)) != 0;
-    if (!ok) {
-        if (!__syncthreads_and(drained)) return;   // something may still write TMEM or shared memory
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;");
-    if (warp == kMmaWarp0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(K2::kTmemCols));
 }
 
 template <int P>
-cudaError_t run_tc(const TcArgs& a, int device, cudaStream_t s) {
-    using C = TcCfg<P>;
-    static int grid = 0;
-    if (!grid) {
-        cudaError_t e = cudaFuncSetAttribute(logits_tc_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        int sms = 148;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-        grid = sms;   // one CTA per SM: each allocates all 512 TMEM columns
-    }
+cudaError_t run_tc(const TcArgs& a, cudaStream_t s) {
+    using K2 = Tc2Cfg<P>;
+    cudaError_t e = cudaFuncSetAttribute(logits_tc_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, K2::kSmem);
+    if (e != cudaSuccess) return e;
+    // keys per CTA: the largest power of two in [256, kT2ChunkMax] giving two rounds of CTAs
+    int chunk = kT2ChunkMax;
+    while (chunk > 256 && (int64_t)a.ngroups * ((a.k.cap + chunk - 1) / chunk) < 148 * 8) chunk >>= 1;
+    const int nchunk = (int)((a.k.cap + chunk - 1) / chunk);
     tc_image_kernel<P><<<a.ngroups, 128, 0, s>>>(a);
-    logits_tc_kernel<P><<<grid, kThreads, C::kSmem, s>>>(a);
+    dim3 grid(nchunk, a.B * a.Hkv, a.quads);
+    logits_tc_kernel<P><<<grid, kT2Threads, K2::kSmem, s>>>(a, chunk);
     return cudaGetLastError();
 }
 
@@ -703,9 +540,9 @@ cudaError_t launch_logits_tc(const tq_ctx* kc, const float* qrot, const float* q
     a.img = static_cast<unsigned char*>(image);
     a.err = kc->derr;
     switch (kc->prm.P) {
-        case 1: return run_tc<1>(a, kc->device, s);
-        case 2: return run_tc<2>(a, kc->device, s);
-        case 3: return run_tc<3>(a, kc->device, s);
+        case 1: return run_tc<1>(a, s);
+        case 2: return run_tc<2>(a, s);
+        case 3: return run_tc<3>(a, s);
     }
     return cudaErrorInvalidValue;
 }

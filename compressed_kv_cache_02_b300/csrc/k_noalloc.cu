@@ -85,7 +85,8 @@ extern "C" int tq_attn_values_noalloc(const tq_ctx* vc, int d, const float* logi
     int rc = scratch_for_current_device(&scratch);
     if (rc != TQ_OK) return rc;
     cudaError_t e = launch_attn_values(vc, d, logits, B, Hq, Hkv, cap, len, values, v_norm, vc ? vc->derr : nullptr,
-                                       static_cast<float*>(scratch), out, static_cast<cudaStream_t>(stream));
+                                       static_cast<float*>(scratch), out, static_cast<cudaStream_t>(stream), nullptr,
+                                       false);
     if (e != cudaSuccess)
         return fail(TQ_ERR_CUDA, std::string("tq_attn_values_noalloc launch: ") + cudaGetErrorString(e));
     return TQ_OK;

@@ -130,13 +130,20 @@ __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
     float* rT = xT + (size_t)d * kQuantRows;      // [d][kQuantRows]
     __shared__ float s_n[kQuantRows], s_n16[kQuantRows], s_r[kQuantRows];
     __shared__ long long s_row[kQuantRows];
-    constexpr int kTab = WIDE ? kMaxCodeLevels : 1;
-    __shared__ float s_cen[kTab], s_thr[kTab];
+    // The tables in shared memory (the binary search indexes them per lane, which the kernel-
+    // parameter space would serialise); WIDE: read from prm.tab, up to 256 levels.
+    constexpr int kTab = WIDE ? kMaxCodeLevels : kMaxLevels;
+    __shared__ float s_cen[kTab], s_thr[kTab], s_cen_hi[kMaxLevels], s_thr_hi[kMaxLevels];
     if constexpr (WIDE) {
         for (int k = threadIdx.x; k < kMaxCodeLevels; k += kT) {
             s_cen[k] = k < prm.L ? prm.tab[k] : 0.f;
             s_thr[k] = k < prm.L - 1 ? prm.tab[prm.L + k] : INFINITY;
         }
+    } else if (threadIdx.x < kMaxLevels) {
+        s_cen[threadIdx.x] = prm.centroids[threadIdx.x];
+        s_thr[threadIdx.x] = prm.thresholds[threadIdx.x];
+        s_cen_hi[threadIdx.x] = prm.centroids_hi[threadIdx.x];
+        s_thr_hi[threadIdx.x] = prm.thresholds_hi[threadIdx.x];
     }
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -249,10 +256,10 @@ __global__ void __launch_bounds__(kT) quantize_kernel(const QuantArgs a) {
                 for (int b = kFastBits - 1; b >= 0; --b)
                     if (b < nb) {
                         const int k = idx + (1 << b) - 1;
-                        if (u > (hi ? prm.thresholds_hi[k] : prm.thresholds[k])) idx += 1 << b;
+                        if (u > (hi ? s_thr_hi[k] : s_thr[k])) idx += 1 << b;
                     }
             }
-            const float cval = WIDE ? s_cen[idx] : (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
+            const float cval = WIDE ? s_cen[idx] : (hi ? s_cen_hi[idx] : s_cen[idx]);
             if (valid) rT[i * kQuantRows + v] = acc[v] - s_n16[v] * cval;
             const long long row = s_row[v];
             for (int p = 0; p < prm.P; ++p) {

@@ -180,11 +180,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
     float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128] x-norm, then r-norm parts
     __shared__ __align__(8) uint64_t mbar;
     __shared__ uint32_t s_tmem;
+    // the tables in shared memory: the binary search indexes them per lane, which the kernel-
+    // parameter (constant) space would serialise
+    __shared__ float s_thr[kMaxLevels], s_cen[kMaxLevels], s_thr_hi[kMaxLevels], s_cen_hi[kMaxLevels];
     const Params& prm = a.prm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, part = warp >> 2, row = 32 * q + lane;
     const int ntiles = (int)((a.n + kTile - 1) / kTile);
     if (blockIdx.x >= ntiles) return;
+    if (tid < kMaxLevels) {
+        s_thr[tid] = prm.thresholds[tid];
+        s_cen[tid] = prm.centroids[tid];
+        s_thr_hi[tid] = prm.thresholds_hi[tid];
+        s_cen_hi[tid] = prm.centroids_hi[tid];
+    }
 
     for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) cp_async16(sB + 16 * e, a.bops + e);
     asm volatile("cp.async.commit_group;");
@@ -266,11 +275,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
             for (int b = kFastBits - 1; b >= 0; --b)
                 if (b < nb) {
                     const int k = idx + (1 << b) - 1;
-                    const bool up = yc > (hi ? prm.thresholds_hi[k] : prm.thresholds[k]) * nv;
+                    const bool up = yc > (hi ? s_thr_hi[k] : s_thr[k]) * nv;
                     idx += up ? (1 << b) : 0;
                     pw[b] |= (up ? 1u : 0u) << c;
                 }
-            const float r = y[c] - n16 * (hi ? prm.centroids_hi[idx] : prm.centroids[idx]);
+            const float r = y[c] - n16 * (hi ? s_cen_hi[idx] : s_cen[idx]);
             y[c] = r;
             rs = fmaf(r, r, rs);
         }

@@ -465,6 +465,10 @@ int tq_attn_output(tq_ctx* c, const tq_ctx* vc, const float* q, int B, int Hq, i
 static size_t values_ws_bytes(int d, int B, int Hq, int Hkv, int64_t cap) {
     int chunk, nchunk;
     attn_chunking(nullptr, B, Hq, Hkv, cap, &chunk, &nchunk);
+    // the tensor-core value kernel's chunks (values_tc_chunk) may be shorter: room for either
+    const int tchunk = values_tc_chunk(B, Hq, Hkv, cap);
+    const int64_t tn = (cap + tchunk - 1) / tchunk;
+    if (tn > nchunk) nchunk = (int)tn;
     return round_up((size_t)B * Hq * nchunk * (d + 2) * sizeof(float), 256);
 }
 

@@ -67,9 +67,21 @@ cudaError_t launch_attn_output(const tq_ctx* kc, const tq_ctx* vc, const float* 
 // Softmax + value sum from precomputed logits, then the combine (vc NULL: bf16 values of dim d).
 // part_out non-NULL: instead of the combine, one unnormalised partial state per (batch, head),
 // [B*Hq][d + 2] = (max, sum of weights, weighted sum in the rotated basis), for a shard merge.
+// allow_tc: the tensor-core kernel may be chosen (its chunking needs the workspace of
+// values_ws_bytes in tq_api.cu; callers with a fixed smaller scratch pass false).
 cudaError_t launch_attn_values(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
                                const int32_t* len, const void* values, const uint16_t* vnorm, int* err,
-                               float* partials, float* out, cudaStream_t s, float* part_out = nullptr);
+                               float* partials, float* out, cudaStream_t s, float* part_out = nullptr,
+                               bool allow_tc = true);
+
+// Tensor-core value sum (tcgen05, k_values_tc.cu): MSE value contexts with 96 < d <= 128, 1..3 bits,
+// symmetric tables, not split.  Writes the chunk partials of launch_attn_values' layout for chunks
+// of values_tc_chunk() keys.
+bool values_tc_supported(const tq_ctx* vc, int d);
+int values_tc_chunk(int B, int Hq, int Hkv, int64_t cap);
+cudaError_t launch_values_tc(const tq_ctx* vc, int d, const float* logits, int B, int Hq, int Hkv, int64_t cap,
+                             const int32_t* len, const void* values, const uint16_t* vnorm, int* err, float* partials,
+                             int chunk, int nchunk, cudaStream_t s);
 
 // out[bh] from R shards' partial states parts [R][BH][d + 2] (log-sum-exp merge, then Pi_v^T).
 cudaError_t launch_merge_partials(const tq_ctx* vc, int d, const float* parts, int R, int64_t BH, float* out,

@@ -172,13 +172,17 @@ int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_wo
 /* Kernel family on this context.  TQ_PATH_AUTO (the default) picks the fastest measured
  * family: tcgen05 tensor cores for bulk tq_quantize of bf16 rows at d = 128 (n >= 4096,
  * ld_x a multiple of 8, 16-byte aligned x), mma.sync tensor cores for tq_search_topk at d in
- * (96,128], (192,256] or d = 200-224, and the table kernels for tq_attn_logits.
- * TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere; TQ_PATH_TENSOR also
- * moves tq_attn_logits to its tcgen05 kernel (kind::f8f6f4, key bits as e4m3 in tensor
- * memory, fp32 accumulation; 96 < d <= 128, m <= 128, 1-3 MSE bits, a cache capacity that
- * is a multiple of 8 and 16-byte aligned code arrays, else the table kernels).  Its waits
- * are bounded: one that runs out sets TQ_DEVERR_TIMEOUT.  Both families compute the same
- * estimator within the documented tolerance.                                            */
+ * (96,128], (192,256] or d = 200-224, the tcgen05 logits kernel (below) for tq_attn_logits on
+ * keys of 2 MSE bits + QJL when batch x KV heads x head quads x cap >= 2^18, and the table
+ * kernels for the other logits.  TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere;
+ * TQ_PATH_TENSOR takes the tcgen05 kernels wherever they apply: tq_attn_logits (kind::f8f6f4,
+ * key bits as e4m3 in tensor memory, fp32 accumulation; 96 < d <= 128, m <= 128, 1-3 MSE
+ * bits, a cache capacity that is a multiple of 8 and 16-byte aligned code arrays, else the
+ * table kernels) and the value sum of tq_attn_values / tq_attn_values_partial (coded values
+ * of 1-3 MSE bits at 96 < d <= 128, even capacity, 4-byte aligned norms; the softmax weights
+ * as e4m3 pieces, the value bits transposed per 32-key block).  Their waits are bounded: one
+ * that runs out sets TQ_DEVERR_TIMEOUT.  All families compute the same estimator within the
+ * documented tolerance.                                                                  */
 enum tq_kernel_path { TQ_PATH_AUTO = 0, TQ_PATH_CUDA_CORE = 1, TQ_PATH_TENSOR = 2 };
 int tq_set_kernel_path(tq_ctx* ctx, int path);
 

@@ -295,6 +295,35 @@ def test_attention_values_code_widths(vbits, d):
     assert_close(got.cpu().numpy(), ref, f"values at {vbits} bits, d = {d}")
 
 
+@pytest.mark.parametrize("vbits,d,B,Hkv,G,N,lens", [
+    (3, 128, 2, 2, 4, 1500, [1500, 333]),       # several chunks, a ragged tail
+    (3, 128, 3, 1, 6, 700, [700, 1, 0]),       # a padded head quad, a 1-key and an empty sequence
+    (2, 128, 1, 2, 4, 5000, [4999]),
+    (1, 112, 1, 2, 4, 2100, [2100]),
+    (3, 100, 2, 1, 4, 900, [900, 31]),
+])
+def test_attention_values_tensor_cores(vbits, d, B, Hkv, G, N, lens):
+    """The tcgen05 value sum (TQ_PATH_TENSOR on the value context): bit masks transposed per
+    block of 32 keys, Walsh terms as e4m3 A in tensor memory, the softmax weights as e4m3 pieces,
+    two-pass softmax per chunk; against the oracle."""
+    tq = _tq()
+    c = _kv_case(B, Hkv, G, N, d, 3, "mse", seed=37, lens=lens, vbits=vbits)
+    kp, vp = c["kp"], c["vp"]
+    vp.ctx.set_kernel_path(tq.TQ_PATH_TENSOR)
+    ref_l = oracle.attention_logits(c["q"].numpy(), c["kz"], c["lens"], kp.Pi, kp.S, kp.cb, 1.0 / sqrt(d))
+    logits = torch.from_numpy(np.nan_to_num(ref_l, nan=0.0).astype(np.float32)).cuda()
+    length = torch.tensor(lens, dtype=torch.int32).cuda()
+    got = tq.attn_values(logits, length, c["vcodes"], vctx=vp.ctx)
+    assert vp.ctx.sync_status() == 0
+    ref = oracle.attention_values(logits.cpu().numpy(), c["lens"], Hkv, values=c["vz"], Pi_v=vp.Pi, cb_v=vp.cb)
+    assert_close(got.cpu().numpy(), ref, f"tensor-core values at {vbits} bits, d = {d}")
+    # the partial states of the same path merge to the same output
+    part = tq.attn_values_partial(logits, length, c["vcodes"], vctx=vp.ctx)
+    merged = tq.attn_merge_partials(part[None], vctx=vp.ctx)
+    torch.cuda.synchronize()
+    assert_close(merged.cpu().numpy(), ref, "tensor-core values through the partial states")
+
+
 def test_decode_append_and_advance():
     """Decode-step append: every appended row lands at position len[b] + s of its (batch, head)
     and passes the quantize parity rules there (codes by the threshold band, signs on the GPU's
