@@ -7,107 +7,16 @@
 // shared candidate buffer, which is merged into the sorted top-k list whenever another
 // tile could overflow it.  Scores never go to HBM.  Pass 2: one CTA per query sorts the
 // per-chunk lists and keeps the first k.
-#include <climits>
-
 #include "lut.cuh"
 #include "mma_e4m3.cuh"
-#include "tq_kernels.h"
+#include "search_topk.cuh"
 
 namespace tq {
 namespace {
 
 constexpr int kThreads = 256;      // one tile = kThreads vectors
-constexpr int kCand = 512;         // candidate buffer per query (>= kThreads + TQ_MAX_TOPK)
-constexpr int kMergeMax = 4096;    // per-query candidates entering pass 2
 constexpr size_t kSmemLimit = 227 * 1024;
-
-__device__ __forceinline__ bool better(float s1, int i1, float s2, int i2) {
-    return s1 > s2 || (s1 == s2 && i1 < i2);
-}
-
-// Sorts n (a power of two) pairs best-first; all threads of the block take part.
-__device__ void bitonic_sort(float* s, int* id, int n) {
-    for (int size = 2; size <= n; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < n / 2; t += blockDim.x) {
-                const int lo = 2 * stride * (t / stride) + (t % stride), hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const bool hi_better = better(s[hi], id[hi], s[lo], id[lo]);
-                if (up ? hi_better : !hi_better) {
-                    const float ts = s[lo]; s[lo] = s[hi]; s[hi] = ts;
-                    const int ti = id[lo]; id[lo] = id[hi]; id[hi] = ti;
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// Number of entries of the best-first array a[0..n) that are better than (s, i).
-__device__ __forceinline__ int count_better(const float* as, const int* ai, int n, float s, int i) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (better(as[mid], ai[mid], s, i)) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-}
-
-template <int NQ>
-struct SearchStateT {
-    float bs[NQ][TQ_MAX_TOPK];
-    int bi[NQ][TQ_MAX_TOPK];
-    float cs[NQ][kCand];
-    int ci[NQ][kCand];
-    int nb[NQ], cnt[NQ];
-    float ts[NQ];
-    int ti[NQ];
-};
 using SearchState = SearchStateT<4>;
-
-// Merges query h's candidates into its best list (both in shared memory).
-template <int NQ>
-__device__ void merge_candidates(SearchStateT<NQ>& st, int h, int k) {
-    const int n = st.cnt[h];
-    for (int t = threadIdx.x; t < kCand; t += blockDim.x)
-        if (t >= n) { st.cs[h][t] = -INFINITY; st.ci[h][t] = INT_MAX; }
-    __syncthreads();
-    bitonic_sort(st.cs[h], st.ci[h], kCand);
-    const int nc = min(n, k), nbb = st.nb[h];
-    float* os = st.cs[h] + k;   // scratch: entries k..2k of the sorted buffer are never read
-    int* oi = st.ci[h] + k;
-    for (int t = threadIdx.x; t < nbb + nc; t += blockDim.x) {
-        float s; int i, r;
-        if (t < nbb) { s = st.bs[h][t]; i = st.bi[h][t]; r = t + count_better(st.cs[h], st.ci[h], nc, s, i); }
-        else { const int u = t - nbb; s = st.cs[h][u]; i = st.ci[h][u]; r = u + count_better(st.bs[h], st.bi[h], nbb, s, i); }
-        if (r < k) { os[r] = s; oi[r] = i; }
-    }
-    __syncthreads();
-    const int nn = min(k, nbb + nc);
-    for (int t = threadIdx.x; t < nn; t += blockDim.x) { st.bs[h][t] = os[t]; st.bi[h][t] = oi[t]; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        st.nb[h] = nn;
-        st.cnt[h] = 0;
-        if (nn == k) { st.ts[h] = st.bs[h][k - 1]; st.ti[h] = st.bi[h][k - 1]; }
-    }
-    __syncthreads();
-}
-
-struct SearchArgs {
-    Params prm;
-    const float* qrot;
-    const float* qproj;
-    int64_t nq;
-    const uint32_t* planes;
-    const uint32_t* signs;
-    const uint16_t* norm;
-    const uint16_t* rnorm;
-    int64_t n;
-    int k, chunk, nchunk;
-    float* cand_s;   // [nq][nchunk][k]
-    int* cand_i;
-};
 
 template <int W, int P>
 __global__ void __launch_bounds__(kThreads) search_chunk_kernel(const SearchArgs a) {
@@ -152,10 +61,10 @@ __global__ void __launch_bounds__(kThreads) search_chunk_kernel(const SearchArgs
         }
         __syncthreads();
         for (int h = 0; h < nh; ++h)
-            if (st.cnt[h] > kCand - kThreads) merge_candidates(st, h, a.k);
+            if (st.cnt[h] > kCand - kThreads) merge_candidates<4, kThreads, 0>(st, h, a.k);
     }
     for (int h = 0; h < nh; ++h)
-        if (st.cnt[h] > 0) merge_candidates(st, h, a.k);
+        if (st.cnt[h] > 0) merge_candidates<4, kThreads, 0>(st, h, a.k);
     for (int h = 0; h < nh; ++h) {
         const size_t base = ((size_t)(q0 + h) * a.nchunk + blockIdx.x) * a.k;
         for (int t = threadIdx.x; t < a.k; t += blockDim.x) {
@@ -179,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) search_merge_kernel(const float* __r
         id[t] = ok ? cand_i[q * per_query + t] : INT_MAX;
     }
     __syncthreads();
-    bitonic_sort(s, id, npow);
+    bitonic_sort<kThreads, 0>(s, id, npow);
     for (int t = threadIdx.x; t < k; t += blockDim.x) {
         top_s[q * k + t] = s[t];
         top_i[q * k + t] = id[t];
@@ -212,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) shard_topk_merge_kernel(const float*
         id[t] = ix;
     }
     __syncthreads();
-    bitonic_sort(s, id, npow);
+    bitonic_sort<kThreads, 0>(s, id, npow);
     for (int t = threadIdx.x; t < k; t += blockDim.x) {
         top_s[q * k + t] = s[t];
         top_i[q * k + t] = id[t];
@@ -409,10 +318,10 @@ __global__ void __launch_bounds__(kThreads) search_mma_kernel(const SearchArgs a
         }
         __syncthreads();
         for (int ql = 0; ql < nqt; ++ql)
-            if (S.st.cnt[ql] > kCand - kSTile) merge_candidates(S.st, ql, a.k);
+            if (S.st.cnt[ql] > kCand - kSTile) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k);
     }
     for (int ql = 0; ql < nqt; ++ql)
-        if (S.st.cnt[ql] > 0) merge_candidates(S.st, ql, a.k);
+        if (S.st.cnt[ql] > 0) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k);
     for (int ql = 0; ql < nqt; ++ql) {
         const size_t base = ((size_t)(q0 + ql) * a.nchunk + blockIdx.x) * a.k;
         for (int t = threadIdx.x; t < a.k; t += blockDim.x) {
@@ -535,12 +444,15 @@ cudaError_t launch_search(const tq_ctx* c, const float* qrot, const float* qproj
     a.cand_s = cand_s;
     a.cand_i = cand_i;
     search_chunking(n, k, &a.chunk, &a.nchunk);
+    a.err = c->derr;
+    static int sms = 0;
+    if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) sms = 148;
     cudaError_t e;
-    if (search_mma_ok(c)) {
+    if (search_tc_ok(c)) {
+        e = launch_search_tc(a, sms, s);
+    } else if (search_mma_ok(c)) {
         // Few chunks when there are many query tiles: the per-CTA set-up and top-k merging
         // then amortise over long scans; at least ~4 CTAs per SM overall.
-        static int sms = 0;
-        if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) sms = 148;
         const int64_t qtiles = (nq + kSQ - 1) / kSQ;
         int64_t want = (4 * (int64_t)sms + qtiles - 1) / qtiles;
         if (want > a.nchunk) want = a.nchunk;

@@ -394,7 +394,10 @@ def _topk_ok(got_s, got_i, ref_s, ref_i, all_scores):
 
 
 @pytest.mark.parametrize("d,bits,n,nq,k", [(200, 2, 5000, 13, 10), (200, 4, 3000, 8, 100), (128, 3, 4096, 16, 1),
-                                         (200, 4, 1000, 5, 128), (64, 2, 300, 3, 50)])
+                                         (200, 4, 1000, 5, 128), (64, 2, 300, 3, 50),
+                                         # several 16-query groups and row chunks, ragged last tile and group
+                                         (200, 2, 20011, 40, 100), (128, 3, 9001, 33, 7), (256, 4, 6000, 17, 64),
+                                         (200, 3, 130, 20, 128)])
 def test_search_topk(d, bits, n, nq, k, kernel_path):
     tq = _tq()
     pr = Pair(d, bits, seed=5)
