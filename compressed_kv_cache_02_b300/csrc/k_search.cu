@@ -61,10 +61,10 @@ __global__ void __launch_bounds__(kThreads) search_chunk_kernel(const SearchArgs
         }
         __syncthreads();
         for (int h = 0; h < nh; ++h)
-            if (st.cnt[h] > kCand - kThreads) merge_candidates<4, kThreads, 0>(st, h, a.k);
+            if (st.cnt[h] > kCand - kThreads) merge_candidates<4, kThreads, 0>(st, h, a.k, threadIdx.x);
     }
     for (int h = 0; h < nh; ++h)
-        if (st.cnt[h] > 0) merge_candidates<4, kThreads, 0>(st, h, a.k);
+        if (st.cnt[h] > 0) merge_candidates<4, kThreads, 0>(st, h, a.k, threadIdx.x);
     for (int h = 0; h < nh; ++h) {
         const size_t base = ((size_t)(q0 + h) * a.nchunk + blockIdx.x) * a.k;
         for (int t = threadIdx.x; t < a.k; t += blockDim.x) {
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) search_merge_kernel(const float* __r
         id[t] = ok ? cand_i[q * per_query + t] : INT_MAX;
     }
     __syncthreads();
-    bitonic_sort<kThreads, 0>(s, id, npow);
+    bitonic_sort<kThreads, 0>(s, id, npow, threadIdx.x);
     for (int t = threadIdx.x; t < k; t += blockDim.x) {
         top_s[q * k + t] = s[t];
         top_i[q * k + t] = id[t];
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) shard_topk_merge_kernel(const float*
         id[t] = ix;
     }
     __syncthreads();
-    bitonic_sort<kThreads, 0>(s, id, npow);
+    bitonic_sort<kThreads, 0>(s, id, npow, threadIdx.x);
     for (int t = threadIdx.x; t < k; t += blockDim.x) {
         top_s[q * k + t] = s[t];
         top_i[q * k + t] = id[t];
@@ -318,10 +318,10 @@ __global__ void __launch_bounds__(kThreads) search_mma_kernel(const SearchArgs a
         }
         __syncthreads();
         for (int ql = 0; ql < nqt; ++ql)
-            if (S.st.cnt[ql] > kCand - kSTile) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k);
+            if (S.st.cnt[ql] > kCand - kSTile) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k, threadIdx.x);
     }
     for (int ql = 0; ql < nqt; ++ql)
-        if (S.st.cnt[ql] > 0) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k);
+        if (S.st.cnt[ql] > 0) merge_candidates<kSQ, kThreads, 0>(S.st, ql, a.k, threadIdx.x);
     for (int ql = 0; ql < nqt; ++ql) {
         const size_t base = ((size_t)(q0 + ql) * a.nchunk + blockIdx.x) * a.k;
         for (int t = threadIdx.x; t < a.k; t += blockDim.x) {

@@ -16,18 +16,19 @@
 //   b0 + b1/16 + b2/256 + b3/4096 (~16 bits; e0_h puts the query's largest value in [128, 256));
 // D (TMEM, fp32): 64 MSE columns (the T terms accumulate) and 64 QJL columns per buffer.
 //
-// A CTA owns 16 queries and a chunk of rows: 8 worker warps (thread = row of the tile = TMEM lane;
-// warps w and w + 4 share their 32 lanes, one scoring queries 0-7 and expanding the even bit
-// vectors, the other queries 8-15 and the odd vectors) and two MMA warps whose lane 0 issues the
-// MMAs of the even and of the odd tiles (one thread issues about one MMA per 75-90 cycles, measured,
-// so two keep up with the tensor pipe at N = 64).  Each MMA warp has two one-vector A slots (64
-// columns each) and a D buffer (128 columns): the 512 TMEM columns, so one CTA runs per SM.  While
-// the tensor cores work on tiles t and t + 1, the workers expand the next vectors into slots as
-// they free up and score tile t - 1.  A row that beats a query's current k-th best (score
+// A CTA owns 16 queries and a chunk of rows, with three roles that meet only at mbarriers:
+//  * 4 expander warps (warp 8 + q: TMEM lanes 32 q ..) turn each row's codes into its bit vectors
+//    and store them into the A slots as the slots free up;
+//  * two MMA warps whose lane 0 issues the MMAs of the even and of the odd tiles (one thread issues
+//    about one MMA per 75-90 cycles, measured, so two keep up with the tensor pipe at N = 64);
+//  * 8 scorer warps (warps w and w + 4 share TMEM lanes 32 (w % 4) ..; one takes queries 0-7, the
+//    other 8-15) copy a tile's D into registers, free the buffer, and score and select.
+// Each MMA warp has two one-vector A slots (64 columns each) and a D buffer (128 columns): the 512
+// TMEM columns, so one CTA runs per SM.  A row that beats a query's current k-th best (score
 // descending, equal scores by lower row) goes to the query's candidate buffer: the thresholds are
 // read once per row and one warp vote skips the (rare, once the lists are full) appends; a buffer
-// that could overflow with the next tile is
-// merged into the query's sorted best list (search_topk.cuh).  The CTA's k best per
+// that could overflow with the next tile is merged into the query's sorted best list
+// (search_topk.cuh) by the scorers of its half, which meet once per tile.  The CTA's k best per
 // query go to HBM and search_merge_kernel keeps the first k over the chunks.  Every wait is
 // bounded in time; one that runs out sets TQ_DEVERR_TIMEOUT, after which the CTA waits (bounded)
 // for the MMAs it issued and frees its tensor memory.
@@ -41,9 +42,10 @@ namespace {
 constexpr int kQ = 16;                      // queries per CTA
 constexpr int kN = 4 * kQ;                  // B rows (D columns) per family: query x piece
 constexpr int kRows = 128;                  // database rows per tile
-constexpr int kWorkers = 256;               // 8 warps
-constexpr int kThreadsSt = kWorkers + 64;   // + two MMA warps (even and odd tiles)
-constexpr int kQG = kQ / 2;                 // queries scored by each half of the workers
+constexpr int kScorers = 256;               // warps 0-7: D -> scores -> top-k
+constexpr int kExpanders = 128;             // warps 8-11: codes -> A slots
+constexpr int kThreadsSt = kScorers + kExpanders + 64;   // + two MMA warps (even and odd tiles)
+constexpr int kQG = kQ / 2;                 // queries scored by each half of the scorers
 constexpr int kSlots = 4;                   // A slots, one bit vector each: 0-1 even tiles, 2-3 odd tiles
 constexpr int kSlotCols = 64;               // up to 8 words x 8 columns
 constexpr int kDCols = 2 * kN;              // a D buffer: MSE then QJL columns
@@ -87,16 +89,22 @@ __device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
     return d;
 }
 
-// AND of p over the worker threads (named barrier 1), which also orders their shared-memory
-// accesses around it.
-__device__ __forceinline__ bool workers_and(bool p) {
+// AND of p over the 128 scorer threads of a query half (named barrier bar), which also orders
+// their shared-memory accesses around it.
+__device__ __forceinline__ bool half_and(bool p, int bar) {
     uint32_t r;
     asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}\n"
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}\n"
         : "=r"(r)
-        : "r"((uint32_t)p), "n"(kWorkers)
+        : "r"((uint32_t)p), "r"(bar)
         : "memory");
     return r != 0;
+}
+// Query h's merge by the scorers of its half g (rank r in the half; named barrier 1 + g).
+template <int NQ>
+__device__ __forceinline__ void half_merge(SearchStateT<NQ>& st, int h, int k, int g, int r) {
+    if (g == 0) merge_candidates<NQ, 128, 1>(st, h, k, r);
+    else merge_candidates<NQ, 128, 2>(st, h, k, r);
 }
 
 template <int P, int W>
@@ -133,12 +141,12 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
     }
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
-            tc::mbar_init(&a_full[s], 4);   // the 4 warps of the group that writes the vector
+            tc::mbar_init(&a_full[s], kExpanders / 32);
             tc::mbar_init(&a_free[s], 1);
         }
         for (int u = 0; u < 2; ++u) {
             tc::mbar_init(&d_full[u], 1);
-            tc::mbar_init(&d_free[u], kWorkers / 32);
+            tc::mbar_init(&d_free[u], kScorers / 32);
         }
         tc::mbar_init(&drain[0], 1);
         tc::mbar_init(&drain[1], 1);
@@ -183,7 +191,8 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
         }
     }
     __syncthreads();
-    // B: vector v (terms, then the signs), query h, coordinate j -> the 4 pieces in rows 4h .. 4h+3
+    // B: vector v (terms, then the signs), query h, coordinate j -> piece pc in row 32 (h / 8) + 8 pc +
+    // h % 8 (each half's D columns piece-major, so the epilogue meets query pairs in adjacent registers)
     for (int e = tid; e < (T + 1) * kQ * K; e += kThreadsSt) {
         const int v = e / (kQ * K), r = e - v * (kQ * K), h = r / K, j = r - h * K;
         const bool isq = v == T;
@@ -195,7 +204,7 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
 #pragma unroll
         for (int pc = 0; pc < 4; ++pc) {
             const uint32_t b = to_e4m3(x);
-            fam[tc::kmajor8(4 * h + pc, kk, ktot)] = (unsigned char)b;
+            fam[tc::kmajor8(32 * (h >> 3) + 8 * pc + (h & 7), kk, ktot)] = (unsigned char)b;
             x = (x - from_e4m3(b)) * 16.f;
         }
     }
@@ -212,35 +221,19 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
     tc::fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp < kWorkers / 32) {
-        // ---------------------------------------------------------------- workers
-        // group g = warp / 4 scores queries 8 g .. 8 g + 7 and expands the bit vectors v = g, g + 2, ..;
-        // warps w and w + 4 share TMEM lanes 32 (w % 4) .. (the rows of this thread's lane)
+    if (warp < kScorers / 32) {
+        // ---------------------------------------------------------------- scorers
+        // group g = warp / 4 scores queries 8 g .. 8 g + 7 of the rows of TMEM lanes 32 (warp % 4) ..
         const int g = warp >> 2, rl = 32 * (warp & 3) + lane;
         const uint32_t lane_tmem = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const bool need_planes = g < T, need_signs = qjl && (T & 1) == g;
-        uint32_t npl[P * W], nsg[W];   // the next tile's codes of this thread's row (the words this group uses)
-        float nn = 0.f, nr = 0.f;
+        // the next tile's norms of this thread's row, raw (converted when used, so the loads stay in
+        // flight for a tile); rows past the chunk read row c0 and are never reported
+        uint16_t nn = 0, nr = 0;
         auto load = [&](int t) {
             const int64_t row = c0 + (int64_t)t * kRows + rl;
-            const bool ok = row < cend;
-            const size_t rr = (size_t)(ok ? row : c0);   // rows past the chunk read row c0, then drop it
-#pragma unroll
-            for (int i = 0; i < P * W; ++i) npl[i] = 0u;
-#pragma unroll
-            for (int i = 0; i < W; ++i) nsg[i] = 0u;
-            if (need_planes && ok) {
-                const uint32_t* pl = a.planes + rr * (P * W);
-#pragma unroll
-                for (int i = 0; i < P * W; ++i) npl[i] = __ldg(pl + i);
-            }
-            if (need_signs && ok) {
-                const uint32_t* sg = a.signs + rr * W;
-#pragma unroll
-                for (int i = 0; i < W; ++i) nsg[i] = __ldg(sg + i);
-            }
-            nn = ok ? half_bits_to_float(__ldg(a.norm + rr)) : 0.f;
-            nr = (ok && qjl) ? half_bits_to_float(__ldg(a.rnorm + rr)) : 0.f;
+            const size_t rr = (size_t)(row < cend ? row : c0);
+            nn = __ldg(a.norm + rr);
+            if (qjl) nr = __ldg(a.rnorm + rr);
         };
         // scores of this thread's row of tile tp against the group's 8 queries, from D buffer tp % 2
         // (query pairs in packed fp32x2 arithmetic)
@@ -251,24 +244,27 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
             ok = __all_sync(0xffffffffu, ok);
             tc::fence_after();
             if (ok) {
-                const uint32_t d = lane_tmem + (uint32_t)(buf * kDCols + 32 * g);
+                const uint32_t d = lane_tmem + (uint32_t)(buf * kDCols + 32 * g);   // [piece][query] of this half
                 float dm[32], dq[32];
                 tc::tmem_ld32(d, dm);
                 if (qjl) tc::tmem_ld32(d + kN, dq);
                 tc::wait_ld();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&d_free[buf]);   // D is in registers: the buffer is free
                 const u64 n2 = pk2(n, n), r2 = pk2(rho, rho), s16 = pk2(1.f / 16.f, 1.f / 16.f);
 #pragma unroll
                 for (int pp = 0; pp < kQG / 2; ++pp) {
                     const float4 cm = s_cst2[4 * g + pp][0], cq = s_cst2[4 * g + pp][1];
-                    const int a0 = 8 * pp, a1 = a0 + 4;   // the two queries' piece columns
-                    u64 m = fma2(pk2(dm[a0 + 3], dm[a1 + 3]), s16, pk2(dm[a0 + 2], dm[a1 + 2]));
-                    m = fma2(m, s16, pk2(dm[a0 + 1], dm[a1 + 1]));
-                    m = fma2(m, s16, pk2(dm[a0], dm[a1]));
+                    const int i = 2 * pp;   // the pair's columns: 8 pc + i, 8 pc + i + 1
+                    u64 m = fma2(pk2(dm[24 + i], dm[25 + i]), s16, pk2(dm[16 + i], dm[17 + i]));
+                    m = fma2(m, s16, pk2(dm[8 + i], dm[9 + i]));
+                    m = fma2(m, s16, pk2(dm[i], dm[i + 1]));
                     u64 e = mul2(n2, fma2(pk2(cm.x, cm.y), m, pk2(cm.z, cm.w)));
                     if (qjl) {
-                        u64 u = fma2(pk2(dq[a0 + 3], dq[a1 + 3]), s16, pk2(dq[a0 + 2], dq[a1 + 2]));
-                        u = fma2(u, s16, pk2(dq[a0 + 1], dq[a1 + 1]));
-                        u = fma2(u, s16, pk2(dq[a0], dq[a1]));
+                        u64 u = fma2(pk2(dq[24 + i], dq[25 + i]), s16, pk2(dq[16 + i], dq[17 + i]));
+                        u = fma2(u, s16, pk2(dq[8 + i], dq[9 + i]));
+                        u = fma2(u, s16, pk2(dq[i], dq[i + 1]));
                         e = fma2(r2, fma2(pk2(cq.x, cq.y), u, pk2(cq.z, cq.w)), e);
                     }
                     const float2 ev = upk2(e);
@@ -276,9 +272,6 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
                     est[2 * pp + 1] = ev.y;
                 }
             }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) tc::mbar_arrive(&d_free[buf]);
             return ok;
         };
         // Appends the scored row (index idx, -1: none) where it beats one of the group's queries' k-th
@@ -319,88 +312,107 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
             }
         };
 
+        // the query half's 128 threads meet once per tile (named barrier 1 + g): merge decisions are
+        // uniform, and appends and merges of its queries do not overlap
+        const int hr = tid - 128 * g, hbar = 1 + g, hlo = kQG * g, hhi = min(nqt, kQG * g + kQG);
+        const uint32_t hmask = 0xFFu << (kQG * g);
         bool ok = true;
-        float pn = 0.f, pr = 0.f;   // the previous tile's row of this thread: norm, residual norm, index
-        int64_t pidx = -1;
         load(0);
         for (int t = 0; t < ntile; ++t) {
-            uint32_t pl[P * W], sg[W];
-#pragma unroll
-            for (int i = 0; i < P * W; ++i) pl[i] = npl[i];
-#pragma unroll
-            for (int i = 0; i < W; ++i) sg[i] = nsg[i];
-            const float n = nn, rho = nr;
+            const float n = half_bits_to_float(nn), rho = qjl ? half_bits_to_float(nr) : 0.f;
             const int64_t row = c0 + (int64_t)t * kRows + rl;
             if (t + 1 < ntile) load(t + 1);
-            // this group's bit vectors of tile t into the A slots of the tile's MMA warp (t % 2)
-            for (int v = g; v < nv; v += 2) {
-                const int sw = (t >> 1) * nv + v, slot = 2 * (t & 1) + (sw & 1), use = sw >> 1;
-                if (ok && use >= 1) ok = tc::mbar_wait(&a_free[slot], (uint32_t)((use - 1) & 1));
-                ok = __all_sync(0xffffffffu, ok);
-                tc::fence_after();
-                if (ok) {
-                    uint32_t w[W];
-#pragma unroll
-                    for (int wd = 0; wd < W; ++wd) {
-                        uint32_t x = 0u;
-                        if (v == T) {
-                            x = sg[wd];
-                        } else {
-#pragma unroll
-                            for (int p = 0; p < P; ++p)
-                                if ((odd_mask(v) >> p) & 1) x ^= pl[p * W + wd];
-                        }
-                        w[wd] = x;
-                    }
-                    tc::store_bits<W>(lane_tmem + (uint32_t)(kSlot0 + slot * kSlotCols), w);
-                    tc::wait_st();
-                }
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0 && ok) tc::mbar_arrive(&a_full[slot]);
-            }
-            // tile t - 1: scores, candidates, merges
-            if (t >= 1) {
-                ok = score(t - 1, pn, pr, ok);
-                if (ok) append(pidx);
-            }
-            if (!workers_and(ok)) {
+            ok = score(t, n, rho, ok);
+            if (ok) append(row < cend ? row : -1);
+            if (!half_and(ok, hbar)) {
                 ok = false;
                 break;
             }
-            const uint32_t mm = *(volatile uint32_t*)&s_merge;
+            const uint32_t mm = *(volatile uint32_t*)&s_merge & hmask;
             if (mm) {
-                for (int h = 0; h < nqt; ++h)
-                    if ((mm >> h) & 1u) merge_candidates<kQ, kWorkers, 1>(st, h, a.k);
-                if (tid == 0) *(volatile uint32_t*)&s_merge = 0u;
-                group_sync<kWorkers, 1>();
+                for (int h = hlo; h < hhi; ++h)
+                    if ((mm >> h) & 1u) half_merge(st, h, a.k, g, hr);
+                if (hr == 0) atomicAnd(&s_merge, ~hmask);
+                half_and(true, hbar);
             }
-            pn = n;
-            pr = rho;
-            pidx = row < cend ? row : -1;
         }
         if (ok) {
-            ok = score(ntile - 1, pn, pr, ok);
-            if (ok) append(pidx);
-            ok = workers_and(ok);
-        }
-        if (ok) {
-            for (int h = 0; h < nqt; ++h)
-                if (st.cnt[h] > 0) merge_candidates<kQ, kWorkers, 1>(st, h, a.k);
-        } else if (tid == 0) {
+            for (int h = hlo; h < hhi; ++h)
+                if (st.cnt[h] > 0) half_merge(st, h, a.k, g, hr);
+        } else if (hr == 0) {
             *(volatile int*)&s_abort = 1;
         }
-        for (int h = 0; h < nqt; ++h) {
+        for (int h = hlo; h < hhi; ++h) {
             const size_t base = ((size_t)(q0 + h) * a.nchunk + blockIdx.x) * a.k;
-            for (int t = tid; t < a.k; t += kWorkers) {
+            for (int t = hr; t < a.k; t += 128) {
                 const bool have = ok && t < st.nb[h];
                 a.cand_s[base + t] = have ? st.bs[h][t] : -INFINITY;
                 a.cand_i[base + t] = have ? st.bi[h][t] : INT_MAX;
             }
         }
+    } else if (warp < (kScorers + kExpanders) / 32) {
+        // ---------------------------------------------------------------- expanders
+        // warp 8 + q writes TMEM lanes 32 q .. 32 q + 31: every bit vector of those rows
+        const int q = warp & 3, rl = 32 * q + lane;
+        const uint32_t lane_tmem = tmem + ((uint32_t)(32 * q) << 16);
+        uint32_t npl[P * W], nsg[W];   // the next tile's codes of this thread's row
+        // rows past the chunk repeat row c0: their scores are never reported
+        auto load = [&](int t) {
+            const int64_t row = c0 + (int64_t)t * kRows + rl;
+            const size_t rr = (size_t)(row < cend ? row : c0);
+            const uint32_t* pl = a.planes + rr * (P * W);
+#pragma unroll
+            for (int i = 0; i < P * W; ++i) npl[i] = __ldg(pl + i);
+            if (qjl) {
+                const uint32_t* sg = a.signs + rr * W;
+#pragma unroll
+                for (int i = 0; i < W; ++i) nsg[i] = __ldg(sg + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) nsg[i] = 0u;
+            }
+        };
+        bool ok = true;
+        load(0);
+        for (int t = 0; t < ntile && ok; ++t) {
+            if (__any_sync(0xffffffffu, *(volatile int*)&s_abort != 0)) break;
+            uint32_t pl[P * W], sg[W];
+#pragma unroll
+            for (int i = 0; i < P * W; ++i) pl[i] = npl[i];
+#pragma unroll
+            for (int i = 0; i < W; ++i) sg[i] = nsg[i];
+            if (t + 1 < ntile) load(t + 1);
+            // tile t's bit vectors into the A slots of its MMA warp (t % 2), alternately
+            for (int v = 0; v < nv; ++v) {
+                const int sw = (t >> 1) * nv + v, slot = 2 * (t & 1) + (sw & 1), use = sw >> 1;
+                if (use >= 1) ok = tc::mbar_wait(&a_free[slot], (uint32_t)((use - 1) & 1));
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc::fence_after();
+                uint32_t w[W];
+#pragma unroll
+                for (int wd = 0; wd < W; ++wd) {
+                    uint32_t x = 0u;
+                    if (v == T) {
+                        x = sg[wd];
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            if ((odd_mask(v) >> p) & 1) x ^= pl[p * W + wd];
+                    }
+                    w[wd] = x;
+                }
+                tc::store_bits<W>(lane_tmem + (uint32_t)(kSlot0 + slot * kSlotCols), w);
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&a_full[slot]);
+            }
+        }
+        if (!ok && lane == 0) *(volatile int*)&s_abort = 1;
     } else {
         // ---------------------------------------------------------------- MMA issue (lane 0 of the last two warps)
-        const int mw = warp - kWorkers / 32;   // issues tiles mw, mw + 2, ... into D buffer mw and A slots 2 mw, 2 mw + 1
+        const int mw = warp - (kScorers + kExpanders) / 32;   // issues tiles mw, mw + 2, ... into D buffer mw and A slots 2 mw, 2 mw + 1
         if (lane == 0) {
             const uint32_t bimg = tc::smem_u32(img);
             const uint64_t bm0 = tc::kmajor_desc(bimg, (uint32_t)(T * K * 8));

@@ -2,7 +2,9 @@
 // with the largest estimate per query): the order (score descending, equal scores by lower row),
 // a bitonic sort over shared memory, and per-query candidate buffers merged into a sorted best
 // list.  The helpers take the number of participating threads (threads 0 .. NT-1) and the barrier
-// they meet at (0: the whole CTA, __syncthreads; otherwise named barrier BAR of NT threads).
+// they meet at (0: the whole CTA, __syncthreads; -1: one warp, __syncwarp; otherwise named barrier
+// BAR of NT threads); r is
+// the calling thread's rank 0 .. NT-1 among them.
 #pragma once
 
 #include <climits>
@@ -40,7 +42,8 @@ namespace {
 
 template <int NT, int BAR>
 __device__ __forceinline__ void group_sync() {
-    if (BAR == 0) __syncthreads();
+    if (BAR < 0) __syncwarp();
+    else if (BAR == 0) __syncthreads();
     else asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
 }
 
@@ -48,12 +51,12 @@ __device__ __forceinline__ bool better(float s1, int i1, float s2, int i2) {
     return s1 > s2 || (s1 == s2 && i1 < i2);
 }
 
-// Sorts n (a power of two) pairs best-first; threads 0 .. NT-1 take part.
+// Sorts n (a power of two) pairs best-first.
 template <int NT, int BAR>
-__device__ void bitonic_sort(float* s, int* id, int n) {
+__device__ void bitonic_sort(float* s, int* id, int n, int r) {
     for (int size = 2; size <= n; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < n / 2; t += NT) {
+            for (int t = r; t < n / 2; t += NT) {
                 const int lo = 2 * stride * (t / stride) + (t % stride), hi = lo + stride;
                 const bool up = (lo & size) == 0;
                 const bool hi_better = better(s[hi], id[hi], s[lo], id[lo]);
@@ -88,18 +91,18 @@ struct SearchStateT {
     int ti[NQ];
 };
 
-// Merges query h's candidates into its best list (both in shared memory); threads 0 .. NT-1.
+// Merges query h's candidates into its best list (both in shared memory).
 template <int NQ, int NT, int BAR>
-__device__ void merge_candidates(SearchStateT<NQ>& st, int h, int k) {
+__device__ void merge_candidates(SearchStateT<NQ>& st, int h, int k, int r) {
     const int n = st.cnt[h];
-    for (int t = threadIdx.x; t < kCand; t += NT)
+    for (int t = r; t < kCand; t += NT)
         if (t >= n) { st.cs[h][t] = -INFINITY; st.ci[h][t] = INT_MAX; }
     group_sync<NT, BAR>();
-    bitonic_sort<NT, BAR>(st.cs[h], st.ci[h], kCand);
+    bitonic_sort<NT, BAR>(st.cs[h], st.ci[h], kCand, r);
     const int nc = min(n, k), nbb = st.nb[h];
     float* os = st.cs[h] + k;   // scratch: entries k..2k of the sorted buffer are never read
     int* oi = st.ci[h] + k;
-    for (int t = threadIdx.x; t < nbb + nc; t += NT) {
+    for (int t = r; t < nbb + nc; t += NT) {
         float s; int i, r;
         if (t < nbb) { s = st.bs[h][t]; i = st.bi[h][t]; r = t + count_better(st.cs[h], st.ci[h], nc, s, i); }
         else { const int u = t - nbb; s = st.cs[h][u]; i = st.ci[h][u]; r = u + count_better(st.bs[h], st.bi[h], nbb, s, i); }
@@ -107,9 +110,9 @@ __device__ void merge_candidates(SearchStateT<NQ>& st, int h, int k) {
     }
     group_sync<NT, BAR>();
     const int nn = min(k, nbb + nc);
-    for (int t = threadIdx.x; t < nn; t += NT) { st.bs[h][t] = os[t]; st.bi[h][t] = oi[t]; }
+    for (int t = r; t < nn; t += NT) { st.bs[h][t] = os[t]; st.bi[h][t] = oi[t]; }
     group_sync<NT, BAR>();
-    if (threadIdx.x == 0) {
+    if (r == 0) {
         st.nb[h] = nn;
         st.cnt[h] = 0;
         if (nn == k) { st.ts[h] = st.bs[h][k - 1]; st.ti[h] = st.bi[h][k - 1]; }
