@@ -58,13 +58,13 @@ def set_batch(b: int) -> None:
 # DRAM traffic of the decode kernels from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum; batch 2 of the same workload, one launch each, scaled to a launch here by
 # the keys it scores).  A figure is reported only while the sources it was taken on are unchanged.
-NCU_SOURCES = ["k_attn.cu", "attn_q8.cuh", "lut.cuh", "values.cuh", "tq_device.cuh", "tq_internal.h"]
-NCU_SOURCES_SHA = "0073d5492f32b543"
+NCU_SOURCES = ['k_attn.cu', 'attn_q8.cuh', 'lut.cuh', 'values.cuh', 'tq_device.cuh', 'tq_internal.h', 'k_logits_tc.cu', 'tcgen05.cuh', 'mma_e4m3.cuh']
+NCU_SOURCES_SHA = "4d3473faf2d1c39a"
 NCU_BYTES_PER_KEY = {
-    # values_coded128_kernel<3, false>: 138.520 MB read + 0.125 MB written, 2 x 8 x 131071 keys
-    "attn_values": (138.520064e6 + 0.124928e6) / (2 * 8 * 131071),
-    # logits_q8_kernel<2>: 109.214 MB read + 14.308 MB written (part of the logits still in L2)
-    "attn_logits": (109.214464e6 + 14.308352e6) / (2 * 8 * 131071),
+    # values_coded128_kernel<3, false>: 138.491 MB read + 0.115 MB written, 2 x 8 x 131071 keys
+    "attn_values": (138.491136e6 + 0.115456e6) / (2 * 8 * 131071),
+    # logits_tc_kernel<2>: 109.185 MB read + 13.807 MB written (part of the logits still in L2)
+    "attn_logits": (109.184768e6 + 13.806848e6) / (2 * 8 * 131071),
 }
 
 
