@@ -1,5 +1,6 @@
-// e4m3 tensor-core helpers shared by the logits and search kernels: exact query splitting
-// into e4m3 pieces, bit-plane to e4m3 fragment extraction, and mma.sync m16n8k32.
+// e4m3 helpers shared by the tensor-core kernels: exact splitting of a value into e4m3 pieces,
+// the exact value of an e4m3 byte, and the per-column exponent that scales a family of values
+// into the e4m3 range.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -30,24 +31,6 @@ __device__ __forceinline__ uint32_t piece(float v, int e0, int pc) {
     }
     return b;
 }
-// bits q, q+8, q+16, q+24 of x as e4m3 bytes 0 / 2^-6
-__device__ __forceinline__ uint32_t ext(uint32_t x, int q) {
-    return (q <= 3 ? (x << (3 - q)) : (x >> (q - 3))) & 0x08080808u;
-}
-
-__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint2 b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
-}
-
-// bits 4t..4t+3 of x (t = 0..3) as e4m3 bytes 0 / 2^-6, in order (byte i <- bit 4t + i)
-__device__ __forceinline__ uint32_t ext_nibble(uint32_t x, int t) {
-    return (((x >> (4 * t)) & 15u) * (0x00204081u << 3)) & 0x08080808u;
-}
-
 // Column exponent e0 for a family whose largest scaled magnitude is mx: mx 2^e0 in [128, 256).
 __device__ __forceinline__ int column_exponent(float mx) {
     int E = 0;

@@ -171,8 +171,8 @@ int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_wo
 
 /* Kernel family on this context.  TQ_PATH_AUTO (the default) picks the fastest measured
  * family: tcgen05 tensor cores for bulk tq_quantize of bf16 rows at d = 128 (n >= 4096,
- * ld_x a multiple of 8, 16-byte aligned x), mma.sync tensor cores for tq_search_topk at d in
- * (96,128], (192,256] or d = 200-224, the tcgen05 logits kernel (below) for tq_attn_logits on
+ * ld_x a multiple of 8, 16-byte aligned x), tcgen05 for tq_search_topk at d in (96,128] or
+ * (192,256] with 1-3 MSE bits, the tcgen05 logits kernel (below) for tq_attn_logits on
  * keys of 2 MSE bits + QJL when batch x KV heads x head quads x cap >= 2^18, and the table
  * kernels for the other logits.  TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere;
  * TQ_PATH_TENSOR takes the tcgen05 kernels wherever they apply: tq_attn_logits (kind::f8f6f4,
