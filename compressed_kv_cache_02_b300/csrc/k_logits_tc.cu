@@ -32,14 +32,14 @@
 // per 32 cycles per SM measured), not by its arithmetic.  Every wait is bounded in time; one that
 // runs out sets TQ_DEVERR_TIMEOUT.
 #include "mma_e4m3.cuh"
+#include "tcgen05.cuh"
 #include "tq_kernels.h"
 
 namespace tq {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kSuspendNs = 20000;                 // suspend-time hint of one try_wait
-constexpr uint64_t kWaitNs = 1000000000ull;       // a wait gives up after one second
+constexpr uint32_t kIdesc = tc::idesc_e4m3(16);   // M 128, N 16 (4 heads x 4 pieces), K 32
 
 template <int P>
 struct TcCfg {
@@ -67,70 +67,6 @@ struct TcArgs {
     unsigned char* img;
     int* err;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Waits for the phase with the given parity to complete.  Each try_wait may suspend the thread
-// for up to kSuspendNs (it resumes as soon as the phase completes); false once kWaitNs of
-// wall-clock time (the GPU's global timer) have passed.
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
-
-// K-major no-swizzle operand: core matrices of 8 rows x 16 bytes, LBO = 128 B along K,
-// SBO = sbo bytes between 8-row groups; descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
-           ((uint64_t)1 << 46);
-}
-// byte offset of element (row r, k) in a [rows x ktot] 8-bit K-major operand
-__host__ __device__ __forceinline__ uint32_t kmajor8(int r, int k, int ktot) {
-    return (uint32_t)(((r >> 3) * (ktot >> 4) + (k >> 4)) * 128 + (r & 7) * 16 + (k & 15));
-}
-
-// kind::f8f6f4: D f32, A and B e4m3, N = 16, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)));
-}
-__device__ __forceinline__ void bar_init_n(uint64_t* bar, int n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(n));
-}
-
-// The 8 A registers of one 32-bit bit-vector word (see the file comment).
-__device__ __forceinline__ void expand_word(uint32_t x, uint32_t (&r)[8]) {
-    const uint32_t y = x >> 2, z = x >> 4, u = x << 2;
-    r[0] = x & 0x04040404u;
-    r[1] = x & 0x08080808u;
-    r[2] = y & 0x04040404u;
-    r[3] = y & 0x08080808u;
-    r[4] = z & 0x04040404u;
-    r[5] = z & 0x08080808u;
-    r[6] = u & 0x04040404u;
-    r[7] = u & 0x08080808u;
-}
 
 struct GroupPos {
     int nh;
@@ -210,7 +146,7 @@ __global__ void __launch_bounds__(128) tc_image_kernel(const TcArgs a) {
         const float f = (c & 1) ? 64.f : 128.f;
         const float x = isq ? su_[h][j] : prm.kappa[v] * sq_[h][j];
         const uint32_t byte = piece(x * f, e0[isq ? 1 : 0][h], pc);
-        img[(isq ? kM : 0) + kmajor8(n, kk, ktot)] = (unsigned char)byte;
+        img[(isq ? kM : 0) + tc::kmajor8(n, kk, ktot)] = (unsigned char)byte;
     }
     if (tid < 16) {
         float* cst = reinterpret_cast<float*>(img + C::kConstOff);
@@ -249,55 +185,23 @@ __device__ __forceinline__ void load_vectors(const unsigned char* st, int row, b
     x[T] = qjl ? *reinterpret_cast<const uint4*>(st + C::kSignOff + row * 16) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-
 // ------------------------------------------------------------------ scoring, one CTA per chunk
 
 constexpr int kT2Threads = 128;
 constexpr int kT2ChunkMax = 2048;
-
-#ifndef TQ_LOGITS_TC_BUFFERS
-#define TQ_LOGITS_TC_BUFFERS 1
-#endif
 
 template <int P>
 struct Tc2Cfg {
     using C = TcCfg<P>;
     static constexpr int kACols = 32 * C::NV;                       // A: one 32-column slot per vector
     static constexpr int kBufCols = kACols + 32;                    // A and D (16 MSE + 16 QJL columns)
-    // two A + D buffers where they fit 256 columns (the MMAs of one tile then overlap the next
-    // tile's expansion and the finish of the one before), else one
-    static constexpr int NB = (TQ_LOGITS_TC_BUFFERS >= 2 && 2 * kBufCols <= 256) ? 2 : 1;
-    static constexpr int kTmemCols = (NB * kBufCols <= 128) ? 128 : 256;
+    static constexpr int kTmemCols = kBufCols <= 128 ? 128 : 256;
     static constexpr int kStageOff = C::kImgBytes;                  // B image, then two code stages
     static constexpr int kSmemUsed = kStageOff + 2 * C::kStageBytes;
     // dynamic shared memory requested: caps the CTAs per SM at 512 / kTmemCols
     static constexpr int kSmem = kTmemCols == 128 ? 52 * 1024 : 100 * 1024;
     static_assert(kSmemUsed <= kSmem, "shared memory layout");
 };
-
-__device__ __forceinline__ void cp_async16_tc(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
-}
 
 // Codes of the keys [k0, k0 + nk) of the cache rows starting at `row` into a stage (TcCfg
 // lays them out), 16-byte cp.async pieces, one commit group.  The norm fields are copied in whole
@@ -311,10 +215,10 @@ __device__ __forceinline__ void stage_codes(const TcArgs& a, size_t row, int nk,
     const uint4* nm = reinterpret_cast<const uint4*>(a.k.norm + row);
     const uint4* rn = reinterpret_cast<const uint4*>(a.k.rnorm + row);
     for (int e = threadIdx.x; e < npl + nsg + nn + nr; e += kT2Threads) {
-        if (e < npl) cp_async16_tc(st + 16 * e, pl + e);
-        else if (e < npl + nsg) cp_async16_tc(st + C::kSignOff + 16 * (e - npl), sg + (e - npl));
-        else if (e < npl + nsg + nn) cp_async16_tc(st + C::kNormOff + 16 * (e - npl - nsg), nm + (e - npl - nsg));
-        else cp_async16_tc(st + C::kRnormOff + 16 * (e - npl - nsg - nn), rn + (e - npl - nsg - nn));
+        if (e < npl) tc::cp_async16(st + 16 * e, pl + e);
+        else if (e < npl + nsg) tc::cp_async16(st + C::kSignOff + 16 * (e - npl), sg + (e - npl));
+        else if (e < npl + nsg + nn) tc::cp_async16(st + C::kNormOff + 16 * (e - npl - nsg), nm + (e - npl - nsg));
+        else tc::cp_async16(st + C::kRnormOff + 16 * (e - npl - nsg - nn), rn + (e - npl - nsg - nn));
     }
     asm volatile("cp.async.commit_group;");
 }
@@ -324,11 +228,10 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
     using C = TcCfg<P>;
     using K2 = Tc2Cfg<P>;
     constexpr int T = C::T;
-    constexpr int NB = K2::NB;
     extern __shared__ __align__(128) unsigned char sm[];
     unsigned char* img = sm;
     unsigned char* stages = sm + K2::kStageOff;
-    __shared__ __align__(8) uint64_t s_mma[NB];   // buffer u: the MMAs of its latest tile are done
+    __shared__ __align__(8) uint64_t s_mma, s_drain;   // the latest tile's MMAs are done; all MMAs are done
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int bh = blockIdx.y, b = bh / a.Hkv;
@@ -343,66 +246,58 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
     const size_t row0 = (size_t)bh * a.k.cap + (size_t)i0;
 
     for (int e = tid; e < C::kImgBytes / 16; e += kT2Threads)
-        cp_async16_tc(img + 16 * e, a.img + (size_t)g * C::kImgBytes + 16 * e);
+        tc::cp_async16(img + 16 * e, a.img + (size_t)g * C::kImgBytes + 16 * e);
     stage_codes<P>(a, row0, min(kTile, nkeys), stages, qjl);
     if (tid == 0) {
-        for (int u = 0; u < NB; ++u) bar_init_n(&s_mma[u], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tc::mbar_init(&s_mma, 1);
+        tc::mbar_init(&s_drain, 1);
+        tc::mbar_init_fence();
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "n"(K2::kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;");
+    if (warp == 0) tc::tmem_alloc<K2::kTmemCols>(&s_tmem);
+    tc::fence_before();
     __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;");
+    tc::fence_after();
     const uint32_t tmem = s_tmem;
     const uint32_t lane_tmem = tmem + ((uint32_t)(32 * warp) << 16);
-    const uint32_t bimg = smem_u32(img);
-    const uint64_t bm0 = smem_desc(bimg, T * 128 * 8), bq0 = smem_desc(bimg + C::kBmBytes, 128 * 8);
+    const uint32_t bimg = tc::smem_u32(img);
+    const uint64_t bm0 = tc::kmajor_desc(bimg, T * 128 * 8), bq0 = tc::kmajor_desc(bimg + C::kBmBytes, 128 * 8);
     const float k2 = 2.f * a.prm.qjl_scale;
     float cst[16];
-    // this thread's key of the tiles in flight: norm, residual norm, index (-1: none); `newer` is
-    // the latest tile's, `older` the one before (two buffers)
-    struct KeyState {
-        float n, rho;
-        int key;
-    };
-    KeyState older{0.f, 0.f, -1}, newer{0.f, 0.f, -1};
+    // this thread's key of the tile in flight: norm, residual norm, index (-1: none)
+    float pn = 0.f, pr = 0.f;
+    int pkey = -1;
     bool ok = true;
 
-    // logits of this thread's key of a tile whose MMAs (on buffer u) are done
-    auto finish = [&](int u, const KeyState& ks) {
-        const uint32_t d = lane_tmem + (uint32_t)(u * K2::kBufCols + K2::kACols);
+    // logits of this thread's key of the tile whose MMAs are done
+    auto finish = [&]() {
+        const uint32_t d = lane_tmem + (uint32_t)K2::kACols;
         float dm[16], dq[16];
-        tmem_ld16(d, dm);
-        if (qjl) tmem_ld16(d + 16, dq);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (ks.key < 0) return;
+        tc::tmem_ld16(d, dm);
+        if (qjl) tc::tmem_ld16(d + 16, dq);
+        tc::wait_ld();
+        if (pkey < 0) return;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const float m = cst[h] * fmaf(dm[4 * h + 3], 1.f / 4096.f,
                                           fmaf(dm[4 * h + 2], 1.f / 256.f, fmaf(dm[4 * h + 1], 1.f / 16.f, dm[4 * h])));
-            float est = ks.n * (cst[8 + h] + m);
+            float est = pn * (cst[8 + h] + m);
             if (qjl) {
                 const float qv = cst[4 + h] * fmaf(dq[4 * h + 3], 1.f / 4096.f,
                                                    fmaf(dq[4 * h + 2], 1.f / 256.f, fmaf(dq[4 * h + 1], 1.f / 16.f, dq[4 * h])));
-                est = fmaf(ks.rho, fmaf(k2, qv, cst[12 + h]), est);
+                est = fmaf(pr, fmaf(k2, qv, cst[12 + h]), est);
             }
-            if (h < gp.nh) a.logits[(gp.qrow0 + h) * (size_t)a.k.cap + (size_t)(i0 + ks.key)] = a.scale * est;
+            if (h < gp.nh) a.logits[(gp.qrow0 + h) * (size_t)a.k.cap + (size_t)(i0 + pkey)] = a.scale * est;
         }
     };
-    // waits (every thread, CTA-uniform outcome) for the MMAs of the tile that used buffer u last
-    auto wait_buffer = [&](int u, int tile) -> bool {
-        const bool w = bar_wait(&s_mma[u], (uint32_t)((tile / NB) & 1));
+    // waits (every thread, CTA-uniform outcome) for the MMAs of tile t
+    auto wait_tile = [&](int t) -> bool {
+        const bool w = tc::mbar_wait(&s_mma, (uint32_t)(t & 1));
         if (!__syncthreads_and(w)) return false;
-        asm volatile("tcgen05.fence::after_thread_sync;");
+        tc::fence_after();
         return true;
     };
 
-    for (int t = 0; t < ntile && ok; ++t) {
-        const int u = t % NB;
+    for (int t = 0; t < ntile; ++t) {
         unsigned char* st = stages + (t & 1) * C::kStageBytes;
         if (t + 1 < ntile)
             stage_codes<P>(a, row0 + (size_t)(t + 1) * kTile, min(kTile, nkeys - (t + 1) * kTile),
@@ -410,7 +305,7 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
         else
             asm volatile("cp.async.commit_group;");
         asm volatile("cp.async.wait_group 1;");
-        asm volatile("fence.proxy.async.shared::cta;");   // the image is read by the tensor cores
+        tc::fence_proxy_async();   // the image is read by the tensor cores
         __syncthreads();
         if (t == 0) {
 #pragma unroll
@@ -423,68 +318,60 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
         load_vectors<P>(st, tid, qjl, x);
         const float n = valid ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kNormOff)[tid]) : 0.f;
         const float rho = (valid && qjl) ? half_bits_to_float(reinterpret_cast<const uint16_t*>(st + C::kRnormOff)[tid]) : 0.f;
-        // buffer u was last used by tile t - NB: wait for its MMAs, finish it
-        if (t >= NB) {
-            if (!wait_buffer(u, t - NB)) {
+        // A and D are reused: wait for tile t - 1's MMAs, finish it
+        if (t >= 1) {
+            if (!wait_tile(t - 1)) {
                 ok = false;
                 break;
             }
-            finish(u, NB == 2 ? older : newer);
+            finish();
         }
-        const uint32_t abuf = (uint32_t)(u * K2::kBufCols);
 #pragma unroll
         for (int v = 0; v < C::NV; ++v) {
             if (v == T && !qjl) break;
-            uint32_t r[32];
             const uint32_t w4[4] = {x[v].x, x[v].y, x[v].z, x[v].w};
-#pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-                uint32_t e8[8];
-                expand_word(w4[wd], e8);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) r[8 * wd + c] = e8[c];
-            }
-            tmem_st32(lane_tmem + abuf + 32 * v, r);
+            tc::store_bits<4>(lane_tmem + 32 * v, w4);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;");
+        tc::wait_st();
+        tc::fence_before();
         __syncthreads();
         if (tid == 0) {
-            asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint32_t dm_t = tmem + abuf + K2::kACols, dq_t = dm_t + 16;
+            tc::fence_after();
+            const uint32_t dm_t = tmem + K2::kACols, dq_t = dm_t + 16;
 #pragma unroll
             for (int v = 0; v < T; ++v)
 #pragma unroll
                 for (int wd = 0; wd < 4; ++wd)
-                    mma_ts(dm_t, tmem + abuf + 32 * v + 8 * wd, bm0 + (uint64_t)((v * 4 + wd) * 16),
-                           (v == 0 && wd == 0) ? 0u : 1u);
+                    tc::mma_e4m3_ts<kIdesc>(dm_t, tmem + 32 * v + 8 * wd, bm0 + (uint64_t)((v * 4 + wd) * 16),
+                                            (v == 0 && wd == 0) ? 0u : 1u);
             if (qjl) {
 #pragma unroll
                 for (int wd = 0; wd < 4; ++wd)
-                    mma_ts(dq_t, tmem + abuf + 32 * T + 8 * wd, bq0 + (uint64_t)(wd * 16), wd == 0 ? 0u : 1u);
+                    tc::mma_e4m3_ts<kIdesc>(dq_t, tmem + 32 * T + 8 * wd, bq0 + (uint64_t)(wd * 16), wd == 0 ? 0u : 1u);
             }
-            mma_commit(&s_mma[u]);
+            tc::commit(&s_mma);
         }
-        older = newer;
-        newer = KeyState{n, rho, valid ? key : -1};
+        pn = n;
+        pr = rho;
+        pkey = valid ? key : -1;
     }
     asm volatile("cp.async.wait_all;");
-    // the tiles still in flight, oldest first
-    if (ok && NB == 2 && ntile >= 2) {
-        ok = wait_buffer((ntile - 2) % NB, ntile - 2);
-        if (ok) finish((ntile - 2) % NB, older);
-    }
     if (ok) {
-        ok = wait_buffer((ntile - 1) % NB, ntile - 1);
-        if (ok) finish((ntile - 1) % NB, newer);
+        ok = wait_tile(ntile - 1);
+        if (ok) finish();
     }
-    if (!ok) {
-        if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
-        return;   // an MMA may still be in flight: the TMEM allocation is left to the context teardown
+    bool drained = true;
+    if (!ok) {   // a wait ran out: flag it, and let every MMA this CTA issued finish (bounded)
+        if (tid == 0) {
+            set_error(a.err, TQ_DEVERR_TIMEOUT);
+            tc::commit(&s_drain);
+        }
+        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&s_drain, 0u));
     }
-    asm volatile("tcgen05.fence::before_thread_sync;");
+    tc::fence_before();
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(K2::kTmemCols));
+    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
+    if (warp == 0 && drained) tc::tmem_dealloc<K2::kTmemCols>(tmem);
 }
 
 template <int P>

@@ -25,6 +25,7 @@
 #include <cstring>
 #include <vector>
 
+#include "tcgen05.cuh"
 #include "tq_device.cuh"
 #include "tq_kernels.h"
 
@@ -40,14 +41,10 @@ constexpr uint32_t kSmemX = 2 * kMatBytes;             // two x tiles (the curre
 constexpr uint32_t kSmemR = kMatBytes;                 // r' hi, then r' lo
 constexpr uint32_t kSmemTotal = kSmemB + kSmemX + kSmemR + 4 * kTile * sizeof(float);   // + norm partials [4][128]
 constexpr uint32_t kTmemCols = 256;                    // D1 (Y) in columns 0..127, D2 (Z) in 128..255
-constexpr uint64_t kWaitNs = 1000000000ull;   // a wait gives up after one second
-constexpr int kSuspendNs = 20000;             // suspend-time hint of one try_wait
 
 __host__ __device__ constexpr uint32_t kmajor_off(int r, int k) {
     return (uint32_t)(((r >> 3) * 16 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(2048 >> 4) << 32) |
@@ -77,49 +74,11 @@ __device__ __forceinline__ void issue_pieces(uint32_t tmem, uint32_t a_saddr, ui
                      (accumulate || p > 0 || s > 0) ? 1u : 0u);
 }
 
-__device__ __forceinline__ void commit(uint64_t* mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar)));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for the given phase parity; false once kWaitNs of wall-clock time (the GPU's global
-// nanosecond timer) have passed.  Each try_wait may suspend the thread for up to kSuspendNs and
-// resumes as soon as the phase completes.
-__device__ __forceinline__ bool wait_phase(uint64_t* mbar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(done)
-            : "r"(smem_u32(mbar)), "r"(parity), "n"(kSuspendNs)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-
 // The 32 coordinates [32 part, 32 part + 32) of this thread's row from the accumulator at tmem_row.
 __device__ __forceinline__ void load_row_part(uint32_t tmem_row, int part, float (&y)[32]) {
     float v0[16], v1[16];
-    ld16(tmem_row + 32 * part, v0);
-    ld16(tmem_row + 32 * part + 16, v1);
+    tc::tmem_ld16(tmem_row + 32 * part, v0);
+    tc::tmem_ld16(tmem_row + 32 * part + 16, v1);
     asm volatile("tcgen05.wait::ld.sync.aligned;");
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -154,9 +113,6 @@ struct TcArgs {
     int* err;
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
-}
 
 // The x rows of tile `tile` into buffer sX (cp.async, zeros beyond n), one commit group.
 __device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char* sX) {
@@ -165,7 +121,7 @@ __device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char
     for (int e = threadIdx.x; e < kTile * 16; e += kTcThreads) {
         const int r = e >> 4, kc = e & 15;
         unsigned char* dst = sX + kmajor_off(r, 8 * kc);
-        if (r < nvalid) cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+        if (r < nvalid) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("cp.async.commit_group;");
@@ -178,7 +134,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
     unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]
     unsigned char* sR = sm + kSmemB + kSmemX;
     float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128] x-norm, then r-norm parts
-    __shared__ __align__(8) uint64_t mbar;
+    __shared__ __align__(8) uint64_t mbar, s_drain;   // MMAs of the current phase done; all MMAs done (error path)
     __shared__ uint32_t s_tmem;
     // the tables in shared memory: the binary search indexes them per lane, which the kernel-
     // parameter (constant) space would serialise
@@ -195,18 +151,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         s_cen_hi[tid] = prm.centroids_hi[tid];
     }
 
-    for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) cp_async16(sB + 16 * e, a.bops + e);
+    for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
     asm volatile("cp.async.commit_group;");
     stage_x(a, blockIdx.x, sX);
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar)));
-        asm volatile("fence.mbarrier_init.release.cluster;");
+        tc::mbar_init(&mbar, 1);
+        tc::mbar_init(&s_drain, 1);
+        tc::mbar_init_fence();
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "n"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
+    if (warp == 0) tc::tmem_alloc<kTmemCols>(&s_tmem);
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
@@ -228,8 +181,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         asm volatile("tcgen05.fence::after_thread_sync;");
         // phase 1: Y = X Pi^T
         if (tid == 0) {
-            issue_pieces(tmem, smem_u32(sXc), smem_u32(sB), false);
-            commit(&mbar);
+            issue_pieces(tmem, tc::smem_u32(sXc), tc::smem_u32(sB), false);
+            tc::commit(&mbar);
         }
         // the next tile's rows into the other buffer (its last readers, the previous tile's phase 1
         // and norms, are done) while this tile computes
@@ -249,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
             }
         }
         s_part[part * kTile + row] = xs;
-        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;   // also: x-norm partials visible
+        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;   // also: x-norm partials visible
         phase ^= 1u;
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
@@ -308,10 +261,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
         // phase 2a: Z = r'_hi (S Pi^T)^T
         if (tid == 0) {
-            issue_pieces(tmem + 128, smem_u32(sR), smem_u32(sB) + kPieces * kMatBytes, false);
-            commit(&mbar);
+            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
+            tc::commit(&mbar);
         }
-        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
+        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
         phase ^= 1u;
         if (!ok) break;
 #pragma unroll
@@ -323,10 +276,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         asm volatile("tcgen05.fence::after_thread_sync;");
         // phase 2b: Z += r'_lo (S Pi^T)^T
         if (tid == 0) {
-            issue_pieces(tmem + 128, smem_u32(sR), smem_u32(sB) + kPieces * kMatBytes, true);
-            commit(&mbar);
+            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, true);
+            tc::commit(&mbar);
         }
-        ok = __syncthreads_and(wait_phase(&mbar, phase)) != 0;
+        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
         phase ^= 1u;
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
@@ -348,12 +301,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
     }
     asm volatile("cp.async.wait_all;");   // a prefetch still in flight lands before the CTA leaves
-    if (!ok) {
-        if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
-        return;   // an MMA may still be in flight: leave the TMEM allocation to the context teardown
+    bool drained = true;
+    if (!ok) {   // a wait ran out: flag it, and let every MMA this CTA issued finish (bounded)
+        if (tid == 0) {
+            set_error(a.err, TQ_DEVERR_TIMEOUT);
+            tc::commit(&s_drain);
+        }
+        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&s_drain, 0u));
     }
+    tc::fence_before();
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
+    if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
 }
 
 }  // namespace

@@ -29,17 +29,17 @@
 // chunk's partial state (max, sum of exp, weighted sum in the value context's rotated basis) for
 // attn_combine_kernel.
 #include "mma_e4m3.cuh"
+#include "tcgen05.cuh"
 #include "tq_kernels.h"
 
 namespace tq {
 namespace {
 
+constexpr uint32_t kVIdesc = tc::idesc_e4m3(16);   // M 128 (coordinates), N 16 (4 heads x 4 pieces), K 32 keys
 constexpr int kVThreads = 128;                   // worker threads (4 warps); one more warp issues the MMAs
 constexpr int kVChunkMax = 2048;                  // logits staged: 4 x 2048 floats = 32 KB
 constexpr int kVSlots = 2;
 constexpr int kVTmemCols = 128;                   // D: T x 16 columns, A slots: 2 x T x 8 (T <= 4)
-constexpr uint64_t kVWaitNs = 1000000000ull;      // a wait gives up after one second
-constexpr int kVSuspendNs = 20000;
 // dynamic shared memory per CTA: sized so that at most 4 CTAs share an SM (4 x 128 TMEM columns)
 constexpr size_t kVSmem = 52 * 1024;
 
@@ -56,66 +56,6 @@ struct VtcArgs {
     float kappa[4];
     float* partials;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity), "n"(kVSuspendNs)
-            : "memory");
-        if (done) return true;
-        if (global_ns() - t0 > kVWaitNs) return false;
-    }
-}
-__device__ __forceinline__ void bar_init(uint64_t* bar, int n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(n));
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)));
-}
-// kind::f8f6f4: D f32, A and B e4m3, N = 16, M = 128
-constexpr uint32_t kVIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(kVIdesc), "r"(accumulate));
-}
-// K-major no-swizzle B operand of 16 rows (columns n) x 32 bytes (k): core matrices of 8 rows x
-// 16 bytes; LBO = 128 B between the two core matrices along K, SBO = 256 B between 8-row groups.
-__device__ __forceinline__ uint64_t b_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) |
-           ((uint64_t)1 << 46);
-}
-__device__ __forceinline__ uint32_t b_off(int n, int k) {
-    return (uint32_t)(((n >> 3) * 2 + (k >> 4)) * 128 + (n & 7) * 16 + (k & 15));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
-}
 
 // 32 x 32 bit transposes across the warp, N matrices at once (their rounds interleaved so the
 // shuffles overlap): on entry lane i holds row i of each (bit j = element (i, j)); on exit lane j
@@ -144,19 +84,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
     return __half2float(__half(h));
 }
 
-// The 8 e4m3 registers of one 32-bit mask (see the file comment).
-__device__ __forceinline__ void expand_word(uint32_t x, uint32_t (&r)[8]) {
-    const uint32_t y = x >> 2, z = x >> 4, u = x << 2;
-    r[0] = x & 0x04040404u;
-    r[1] = x & 0x08080808u;
-    r[2] = y & 0x04040404u;
-    r[3] = y & 0x08080808u;
-    r[4] = z & 0x04040404u;
-    r[5] = z & 0x08080808u;
-    r[6] = u & 0x04040404u;
-    r[7] = u & 0x08080808u;
-}
-
 struct VShared {
     uint64_t ready[kVSlots];      // the 4 worker warps have written A and B of a block
     uint64_t slot_free[kVSlots];  // the block's MMAs are done (tcgen05.commit)
@@ -166,16 +93,13 @@ struct VShared {
     float red[4][8];
 };
 
-__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // A bounded wait that also gives up at once once the CTA has aborted; on a time-out it records the
 // abort (the CTA then runs to its end without further waiting and sets TQ_DEVERR_TIMEOUT).
 __device__ __forceinline__ void wait_or_abort(VShared& S, uint64_t* bar, uint32_t parity) {
     if (*(volatile int*)&S.abort) return;
-    if (!bar_wait(bar, parity)) *(volatile int*)&S.abort = 1;
+    if (!tc::mbar_wait(bar, parity)) *(volatile int*)&S.abort = 1;
 }
 
 template <int P>
@@ -205,17 +129,15 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
 
     if (tid == 0) {
         for (int s = 0; s < kVSlots; ++s) {
-            bar_init(&S.ready[s], 4);
-            bar_init(&S.slot_free[s], 1);
+            tc::mbar_init(&S.ready[s], 4);
+            tc::mbar_init(&S.slot_free[s], 1);
         }
-        bar_init(&S.done, 1);
+        tc::mbar_init(&S.done, 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem)),
-                     "n"(kVTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc::tmem_alloc<kVTmemCols>(&S.tmem);
     }
     // pass 1 (worker warps): the chunk's logits (-inf beyond the keys and heads) and value norms
     // into shared memory, the maxima
@@ -231,10 +153,10 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
         for (int h = 0; h < 4; ++h)
             if (h < nh)
                 for (int i = tid; i < nkeys; i += kVThreads)
-                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(s_l + h * kVChunkMax + i)),
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(tc::smem_u32(s_l + h * kVChunkMax + i)),
                                  "l"(lg + (size_t)h * a.cap + i0 + i));
         for (int i = tid; i < (nkeys + 1) / 2; i += kVThreads)
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(s_nh + 2 * i)),
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(tc::smem_u32(s_nh + 2 * i)),
                          "l"(a.vnorm + rowbase + i0 + 2 * i));
         asm volatile("cp.async.commit_group;");
         asm volatile("cp.async.wait_all;");
@@ -273,13 +195,13 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
                 wait_or_abort(S, &S.ready[slot], (uint32_t)((j / kVSlots) & 1));
                 if (*(volatile int*)&S.abort) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
-                const uint64_t bd = b_desc(smem_u32(s_b + slot * 512));
+                const uint64_t bd = tc::kmajor_desc(tc::smem_u32(s_b + slot * 512), 256);   // 16 rows x 32 k
 #pragma unroll
                 for (int t = 0; t < T; ++t)
-                    mma_ts(tmem + 16 * t, tmem + 16 * T + slot * 8 * T + 8 * t, bd, j > 0 ? 1u : 0u);
-                mma_commit(&S.slot_free[slot]);
+                    tc::mma_e4m3_ts<kVIdesc>(tmem + 16 * t, tmem + 16 * T + slot * 8 * T + 8 * t, bd, j > 0 ? 1u : 0u);
+                tc::commit(&S.slot_free[slot]);
             }
-            mma_commit(&S.done);   // completes once every MMA issued before it has
+            tc::commit(&S.done);   // completes once every MMA issued before it has
         }
         __syncwarp();
     } else {
@@ -301,7 +223,7 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
             const int k0 = 32 * j, n = min(32, nkeys - k0);
             const uint4* src = reinterpret_cast<const uint4*>(a.vplanes + (rowbase + i0 + k0) * ROW);
             uint4* dst = reinterpret_cast<uint4*>(s_v + (j % kStages) * 32 * ROW);
-            for (int q = tid; q < n * P; q += kVThreads) cp_async16(dst + q, src + q);
+            for (int q = tid; q < n * P; q += kVThreads) tc::cp_async16(dst + q, src + q);
             asm volatile("cp.async.commit_group;");
         };
         stage_rows(0);
@@ -327,7 +249,7 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
 #pragma unroll
                 for (int pc = 0; pc < 4; ++pc) {
                     const uint32_t byte = to_e4m3(x);
-                    bt[b_off(4 * hq + pc, kperm)] = (unsigned char)byte;
+                    bt[tc::kmajor8(4 * hq + pc, kperm, 32)] = (unsigned char)byte;
                     x = (x - e4m3_value(byte)) * 16.f;
                 }
             }
@@ -349,14 +271,14 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
                     for (int p = 0; p < P; ++p)
                         if ((odd_mask(t) >> p) & 1) x ^= msk[p];
                     uint32_t r[8];
-                    expand_word(x, r);
-                    tmem_st8(at + 8 * t, r);
+                    tc::expand_word(x, r);
+                    tc::tmem_st8(at + 8 * t, r);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
-            if (lane == 0) bar_arrive(&S.ready[slot]);
+            if (lane == 0) tc::mbar_arrive(&S.ready[slot]);
         }
         asm volatile("cp.async.wait_all;");
         wait_or_abort(S, &S.done, 0);
@@ -376,7 +298,7 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
         float dv[4][16];
         const uint32_t d_tmem = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-        for (int t = 0; t < T; ++t) tmem_ld16(d_tmem + 16 * t, dv[t]);
+        for (int t = 0; t < T; ++t) tc::tmem_ld16(d_tmem + 16 * t, dv[t]);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         workers_sync();
         if (!*(volatile int*)&S.abort) {
@@ -402,13 +324,16 @@ __global__ void __launch_bounds__(kVThreads + 32) values_tc_kernel(const VtcArgs
             }
         }
     }
-    asm volatile("tcgen05.fence::before_thread_sync;");
+    tc::fence_before();
     __syncthreads();
-    if (*(volatile int*)&S.abort) {
+    bool drained = true;
+    if (*(volatile int*)&S.abort) {   // a wait ran out: flag it, and let the issued MMAs finish (bounded)
         if (tid == 0) set_error(a.err, TQ_DEVERR_TIMEOUT);
-        return;   // an MMA may still be in flight: the TMEM allocation is left to the context teardown
+        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&S.done, 0u));
     }
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kVTmemCols));
+    tc::fence_after();
+    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
+    if (warp == 0 && drained) tc::tmem_dealloc<kVTmemCols>(tmem);
 }
 
 }  // namespace

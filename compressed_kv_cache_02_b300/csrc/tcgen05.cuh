@@ -114,7 +114,7 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 
 // Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 D, both K-major, M = 128.
-constexpr uint32_t idesc_e4m3(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24); }
+__host__ __device__ constexpr uint32_t idesc_e4m3(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24); }
 
 // D[128 x N] (+)= A[128 x 32] B[32 x N]: A from tensor memory, B from shared memory.
 template <uint32_t IDESC>
