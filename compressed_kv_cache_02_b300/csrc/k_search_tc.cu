@@ -17,8 +17,9 @@
 // D (TMEM, fp32): 64 MSE columns (the T terms accumulate) and 64 QJL columns per buffer.
 //
 // A CTA owns 16 queries and a chunk of rows, with three roles that meet only at mbarriers:
-//  * 4 expander warps (warp 8 + q: TMEM lanes 32 q ..) turn each row's codes into its bit vectors
-//    and store them into the A slots as the slots free up;
+//  * expander warps (one group of 4 at 1 MSE bit, one per MMA warp from 2 bits: warp 8 + 4 e + q,
+//    TMEM lanes 32 q ..) turn each row's codes into its bit vectors and store them into the A
+//    slots as the slots free up;
 //  * two MMA warps whose lane 0 issues the MMAs of the even and of the odd tiles (one thread issues
 //    about one MMA per 75-90 cycles, measured, so two keep up with the tensor pipe at N = 64);
 //  * 8 scorer warps (warps w and w + 4 share TMEM lanes 32 (w % 4) ..; one takes queries 0-7, the
@@ -43,8 +44,15 @@ constexpr int kQ = 16;                      // queries per CTA
 constexpr int kN = 4 * kQ;                  // B rows (D columns) per family: query x piece
 constexpr int kRows = 128;                  // database rows per tile
 constexpr int kScorers = 256;               // warps 0-7: D -> scores -> top-k
-constexpr int kExpanders = 128;             // warps 8-11: codes -> A slots
-constexpr int kThreadsSt = kScorers + kExpanders + 64;   // + two MMA warps (even and odd tiles)
+// Expander groups of 4 warps (warps 8, 9, ..): one at 1 MSE bit (2 bit vectors per row), one per
+// MMA warp from 2 bits up, where a tile's 3-5 vectors cycle through its MMA warp's two A slots and
+// one group waiting on those would leave the other MMA warp idle (4 bits: 91 -> 68 ms measured).
+template <int P>
+struct StRoles {
+    static constexpr int kGroups = P == 1 ? 1 : 2;
+    static constexpr int kExpanders = 128 * kGroups;
+    static constexpr int kThreads = kScorers + kExpanders + 64;   // + two MMA warps (even and odd tiles)
+};
 constexpr int kQG = kQ / 2;                 // queries scored by each half of the scorers
 constexpr int kSlots = 4;                   // A slots, one bit vector each: 0-1 even tiles, 2-3 odd tiles
 constexpr int kSlotCols = 64;               // up to 8 words x 8 columns
@@ -108,9 +116,11 @@ __device__ __forceinline__ void half_merge(SearchStateT<NQ>& st, int h, int k, i
 }
 
 template <int P, int W>
-__global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchArgs a) {
+__global__ void __launch_bounds__(StRoles<P>::kThreads, 1) search_tc_kernel(const SearchArgs a) {
     using C = StCfg<P, W>;
     constexpr int T = C::T, K = C::K;
+    constexpr int kThreadsSt_ = StRoles<P>::kThreads, kExpanders = StRoles<P>::kExpanders;
+    constexpr int kGroups = StRoles<P>::kGroups;
     extern __shared__ __align__(128) unsigned char sm[];
     unsigned char* img = sm;
     SearchStateT<kQ>& st = *reinterpret_cast<SearchStateT<kQ>*>(sm + C::kStateOff);
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
     // ---- prologue: the queries (scratch in the candidate buffers), barriers, tensor memory
     float* qv = &st.cs[0][0];
     float* uv = qv + kQ * K;
-    for (int e = tid; e < kQ * K; e += kThreadsSt) {
+    for (int e = tid; e < kQ * K; e += kThreadsSt_) {
         const int h = e / K, j = e - h * K;
         const bool ok = h < nqt;
         qv[e] = (ok && j < prm.d) ? a.qrot[(size_t)(q0 + h) * prm.d + j] : 0.f;
@@ -141,7 +151,7 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
     }
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
-            tc::mbar_init(&a_full[s], kExpanders / 32);
+            tc::mbar_init(&a_full[s], 4);   // the 4 warps of the expander group of the slot's tiles
             tc::mbar_init(&a_free[s], 1);
         }
         for (int u = 0; u < 2; ++u) {
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
         float kmax = 0.f;
 #pragma unroll
         for (int t = 0; t < T; ++t) kmax = fmaxf(kmax, fabsf(prm.kappa[t]));
-        for (int h = warp; h < kQ; h += kThreadsSt / 32) {
+        for (int h = warp; h < kQ; h += kThreadsSt_ / 32) {
             float mq = 0.f, sq = 0.f, mu = 0.f, su = 0.f;
             for (int j = lane; j < K; j += 32) {
                 const float x = qv[h * K + j], u = uv[h * K + j];
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
     __syncthreads();
     // B: vector v (terms, then the signs), query h, coordinate j -> piece pc in row 32 (h / 8) + 8 pc +
     // h % 8 (each half's D columns piece-major, so the epilogue meets query pairs in adjacent registers)
-    for (int e = tid; e < (T + 1) * kQ * K; e += kThreadsSt) {
+    for (int e = tid; e < (T + 1) * kQ * K; e += kThreadsSt_) {
         const int v = e / (kQ * K), r = e - v * (kQ * K), h = r / K, j = r - h * K;
         const bool isq = v == T;
         const int k = 32 * (j >> 5) + tc::expanded_k(j & 31);
@@ -352,8 +362,9 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
         }
     } else if (warp < (kScorers + kExpanders) / 32) {
         // ---------------------------------------------------------------- expanders
-        // warp 8 + q writes TMEM lanes 32 q .. 32 q + 31: every bit vector of those rows
-        const int q = warp & 3, rl = 32 * q + lane;
+        // group e = (warp - 8) / 4 takes tiles e, e + kGroups, .. (with two groups: the tiles of MMA warp
+        // e); warp 8 + 4 e + q writes TMEM lanes 32 q .. 32 q + 31: every bit vector of those rows
+        const int e = (warp - kScorers / 32) >> 2, q = warp & 3, rl = 32 * q + lane;
         const uint32_t lane_tmem = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t npl[P * W], nsg[W];   // the next tile's codes of this thread's row
         // rows past the chunk repeat row c0: their scores are never reported
@@ -373,15 +384,15 @@ __global__ void __launch_bounds__(kThreadsSt, 1) search_tc_kernel(const SearchAr
             }
         };
         bool ok = true;
-        load(0);
-        for (int t = 0; t < ntile && ok; ++t) {
+        if (e < ntile) load(e);
+        for (int t = e; t < ntile && ok; t += kGroups) {
             if (__any_sync(0xffffffffu, *(volatile int*)&s_abort != 0)) break;
             uint32_t pl[P * W], sg[W];
 #pragma unroll
             for (int i = 0; i < P * W; ++i) pl[i] = npl[i];
 #pragma unroll
             for (int i = 0; i < W; ++i) sg[i] = nsg[i];
-            if (t + 1 < ntile) load(t + 1);
+            if (t + kGroups < ntile) load(t + kGroups);
             // tile t's bit vectors into the A slots of its MMA warp (t % 2), alternately
             for (int v = 0; v < nv; ++v) {
                 const int sw = (t >> 1) * nv + v, slot = 2 * (t & 1) + (sw & 1), use = sw >> 1;
@@ -469,7 +480,7 @@ cudaError_t run_tc(const SearchArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(search_tc_kernel<P, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)a.nchunk, (unsigned)((a.nq + kQ - 1) / kQ));
-    search_tc_kernel<P, W><<<grid, kThreadsSt, C::kSmem, s>>>(a);
+    search_tc_kernel<P, W><<<grid, StRoles<P>::kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
 
