@@ -127,7 +127,9 @@ __device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char
     asm volatile("cp.async.commit_group;");
 }
 
-template <bool SPLIT>
+// P: MSE bits of an ordinary context, known at compile time (0 for split contexts, whose width per
+// coordinate word is P or P + 1 at run time).
+template <int P, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];   // no-swizzle operands need 16-byte alignment
     unsigned char* sB = sm;
@@ -212,35 +214,86 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         const float n16 = half_bits_to_float(float_to_half_bits(nrm));
         const int64_t grow = r0 + row;
         const bool valid = row < nvalid;
-        // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (P steps, the step
-        // for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
+        // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (one step per bit, the
+        // step for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
         const float nv = nrm > 0.f ? nrm : 1.f;
         // split contexts: this thread's 32 coordinates (one word) are below d_hi or not as a whole
         const bool hi = SPLIT && 32 * part < prm.d_hi;   // ordinary contexts: false at compile time
-        const int nb = prm.P + (hi ? 1 : 0);
         uint32_t pw[kFastBits] = {};
         float rs = 0.f;
+        if constexpr (SPLIT) {
+            const int nb = prm.P + (hi ? 1 : 0);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float yc = nrm > 0.f ? y[c] : 0.f;
-            int idx = 0;
+            for (int c = 0; c < 32; ++c) {
+                const float yc = nrm > 0.f ? y[c] : 0.f;
+                int idx = 0;
 #pragma unroll
-            for (int b = kFastBits - 1; b >= 0; --b)
-                if (b < nb) {
+                for (int b = kFastBits - 1; b >= 0; --b)
+                    if (b < nb) {
+                        const int k = idx + (1 << b) - 1;
+                        const bool up = yc > (hi ? s_thr_hi[k] : s_thr[k]) * nv;
+                        idx += up ? (1 << b) : 0;
+                        pw[b] |= (up ? 1u : 0u) << c;
+                    }
+                const float r = y[c] - n16 * (hi ? s_cen_hi[idx] : s_cen[idx]);
+                y[c] = r;
+                rs = fmaf(r, r, rs);
+            }
+        } else if constexpr (P <= 2) {
+            // the 1 or 3 thresholds (times the norm: the same rounded products as t_k * n) and the
+            // centroids in registers
+            constexpr int NT = (1 << P) - 1;
+            float ts[NT], cv[NT + 1];
+#pragma unroll
+            for (int k = 0; k < NT; ++k) ts[k] = s_thr[k] * nv;
+#pragma unroll
+            for (int k = 0; k <= NT; ++k) cv[k] = s_cen[k];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float yc = nrm > 0.f ? y[c] : 0.f;
+                float cen;
+                if constexpr (P == 1) {
+                    const bool up = yc > ts[0];
+                    pw[0] |= (up ? 1u : 0u) << c;
+                    cen = up ? cv[1] : cv[0];
+                } else {
+                    const bool u1 = yc > ts[1];
+                    const bool u0 = yc > (u1 ? ts[2] : ts[0]);
+                    pw[1] |= (u1 ? 1u : 0u) << c;
+                    pw[0] |= (u0 ? 1u : 0u) << c;
+                    cen = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
+                }
+                const float r = y[c] - n16 * cen;
+                y[c] = r;
+                rs = fmaf(r, r, rs);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float yc = nrm > 0.f ? y[c] : 0.f;
+                int idx = 0;
+#pragma unroll
+                for (int b = P - 1; b >= 0; --b) {
                     const int k = idx + (1 << b) - 1;
-                    const bool up = yc > (hi ? s_thr_hi[k] : s_thr[k]) * nv;
+                    const bool up = yc > s_thr[k] * nv;
                     idx += up ? (1 << b) : 0;
                     pw[b] |= (up ? 1u : 0u) << c;
                 }
-            const float r = y[c] - n16 * (hi ? s_cen_hi[idx] : s_cen[idx]);
-            y[c] = r;
-            rs = fmaf(r, r, rs);
+                const float r = y[c] - n16 * s_cen[idx];
+                y[c] = r;
+                rs = fmaf(r, r, rs);
+            }
         }
         if (valid) {
-            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
-            if (hi) {
-                const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
-                a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
+            if constexpr (SPLIT) {
+                for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+                if (hi) {
+                    const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
+                    a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
+                }
+            } else {
+#pragma unroll
+                for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
             }
         }
         if (!prm.qjl) {   // MSE mode: no residual sketch
@@ -363,16 +416,23 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     a.norm = norm;
     a.rnorm = rnorm;
     a.err = c->derr;
-    const bool split = c->prm.d_hi > 0;
-    cudaError_t e = split ? cudaFuncSetAttribute(quantize_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal)
-                          : cudaFuncSetAttribute(quantize_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
-    if (e != cudaSuccess) return e;
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
     const int64_t ntiles = (n + kTile - 1) / kTile;
     const int grid = (int)(ntiles < sms ? ntiles : sms);
-    if (split) quantize_tc_kernel<true><<<grid, kTcThreads, kSmemTotal, s>>>(a);
-    else quantize_tc_kernel<false><<<grid, kTcThreads, kSmemTotal, s>>>(a);
+    auto run = [&](auto kernel) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+        if (e != cudaSuccess) return e;
+        kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
+        return cudaSuccess;
+    };
+    cudaError_t e = cudaErrorInvalidValue;
+    if (c->prm.d_hi > 0) e = run(quantize_tc_kernel<0, true>);
+    else if (c->prm.P == 1) e = run(quantize_tc_kernel<1, false>);
+    else if (c->prm.P == 2) e = run(quantize_tc_kernel<2, false>);
+    else if (c->prm.P == 3) e = run(quantize_tc_kernel<3, false>);
+    else if (c->prm.P == 4) e = run(quantize_tc_kernel<4, false>);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
