@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
                 y[c] = r;
                 rs = fmaf(r, r, rs);
             }
-        } else if constexpr (P <= 2) {
-            // the 1 or 3 thresholds (times the norm: the same rounded products as t_k * n) and the
+        } else if constexpr (P <= 3) {
+            // the 1, 3 or 7 thresholds (times the norm: the same rounded products as t_k * n) and the
             // centroids in registers
             constexpr int NT = (1 << P) - 1;
             float ts[NT], cv[NT + 1];
@@ -256,12 +256,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
                     const bool up = yc > ts[0];
                     pw[0] |= (up ? 1u : 0u) << c;
                     cen = up ? cv[1] : cv[0];
-                } else {
+                } else if constexpr (P == 2) {
                     const bool u1 = yc > ts[1];
                     const bool u0 = yc > (u1 ? ts[2] : ts[0]);
                     pw[1] |= (u1 ? 1u : 0u) << c;
                     pw[0] |= (u0 ? 1u : 0u) << c;
                     cen = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
+                } else {
+                    const bool u2 = yc > ts[3];
+                    const bool u1 = yc > (u2 ? ts[5] : ts[1]);
+                    const float t0 = u2 ? (u1 ? ts[6] : ts[4]) : (u1 ? ts[2] : ts[0]);
+                    const bool u0 = yc > t0;
+                    pw[2] |= (u2 ? 1u : 0u) << c;
+                    pw[1] |= (u1 ? 1u : 0u) << c;
+                    pw[0] |= (u0 ? 1u : 0u) << c;
+                    const float clo = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
+                    const float chi = u1 ? (u0 ? cv[7] : cv[6]) : (u0 ? cv[5] : cv[4]);
+                    cen = u2 ? chi : clo;
                 }
                 const float r = y[c] - n16 * cen;
                 y[c] = r;
@@ -307,29 +318,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
             continue;
         }
         store_row_part(sR, row, part, y);   // r' hi (rounded to bf16 by the store)
-        asm volatile("tcgen05.fence::before_thread_sync;");
-        asm volatile("fence.proxy.async.shared::cta;");
-        __syncthreads();   // everyone has read its x-norm partials and written r' hi
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
-        // phase 2a: Z = r'_hi (S Pi^T)^T
-        if (tid == 0) {
-            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
-            tc::commit(&mbar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
-        phase ^= 1u;
-        if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
-        store_row_part(sR, row, part, y);   // r' lo = r' - bf16(r')
-        asm volatile("fence.proxy.async.shared::cta;");
+        // r' lo = r' - bf16(r') into this tile's x buffer: phase 1 and the x-norm partials are done
+        // with it, and the next tile's rows go to the other buffer
+        store_row_part(sXc, row, part, y);
         asm volatile("tcgen05.fence::before_thread_sync;");
-        __syncthreads();
+        asm volatile("fence.proxy.async.shared::cta;");
+        __syncthreads();   // everyone has read its x-norm partials and written r' hi and lo
         asm volatile("tcgen05.fence::after_thread_sync;");
-        // phase 2b: Z += r'_lo (S Pi^T)^T
+        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
+        // phase 2: Z = r'_hi (S Pi^T)^T + r'_lo (S Pi^T)^T
         if (tid == 0) {
-            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, true);
+            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
+            issue_pieces(tmem + 128, tc::smem_u32(sXc), tc::smem_u32(sB) + kPieces * kMatBytes, true);
             tc::commit(&mbar);
         }
         ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
