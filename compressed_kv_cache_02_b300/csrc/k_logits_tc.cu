@@ -88,11 +88,11 @@ __global__ void __launch_bounds__(128) tc_image_kernel(const TcArgs a) {
     __shared__ float red[4][4][4];   // [warp][head][mq, sq, mu, su]
     __shared__ int e0[2][4];
     __shared__ float sums[2][4];
+    __shared__ __align__(16) unsigned char img[C::kImgBytes];   // built here, then copied out whole
     const Params& prm = a.prm;
     const bool qjl = prm.qjl != 0;
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const GroupPos gp = group_pos(a, g);
-    unsigned char* img = a.img + (size_t)g * C::kImgBytes;
     for (int e = tid; e < 4 * 128; e += 128) {
         const int h = e >> 7, j = e & 127;
         sq_[h][j] = (h < gp.nh && j < prm.d) ? a.qrot[(gp.qrow0 + h) * prm.d + j] : 0.f;
@@ -134,19 +134,25 @@ __global__ void __launch_bounds__(128) tc_image_kernel(const TcArgs a) {
         sums[1][h] = su;
     }
     __syncthreads();
-    // B bytes: (family, column n, k); k -> (term or sign vector v, word wd, register c, byte i)
-    constexpr int kM = 16 * T * 128, kQ = 16 * 128;
-    for (int e = tid; e < kM + kQ; e += 128) {
-        const bool isq = e >= kM;
-        const int ee = isq ? e - kM : e, ktot = isq ? 128 : T * 128;
-        const int n = ee / ktot, kk = ee % ktot;
+    // B bytes: (family, head h, k) -> its 4 pieces (one chain) in columns 4 h .. 4 h + 3;
+    // k -> (term or sign vector v, word wd, register c, byte i)
+    constexpr int kM = 16 * T * 128, kMk = T * 128;
+    for (int e = tid; e < 4 * (kMk + 128); e += 128) {
+        const bool isq = e >= 4 * kMk;
+        const int ee = isq ? e - 4 * kMk : e, ktot = isq ? 128 : kMk;
+        const int h = ee / ktot, kk = ee % ktot;
         const int v = kk >> 7, k = kk & 127, wd = k >> 5, c = (k >> 2) & 7, i = k & 3;
         const int j = 32 * wd + 8 * i + ((c + 2) & 7);
-        const int h = n >> 2, pc = n & 3;
         const float f = (c & 1) ? 64.f : 128.f;
-        const float x = isq ? su_[h][j] : prm.kappa[v] * sq_[h][j];
-        const uint32_t byte = piece(x * f, e0[isq ? 1 : 0][h], pc);
-        img[(isq ? kM : 0) + tc::kmajor8(n, kk, ktot)] = (unsigned char)byte;
+        const float val = isq ? su_[h][j] : prm.kappa[v] * sq_[h][j];
+        float x = ldexpf(val * f, e0[isq ? 1 : 0][h]);   // pieces b0 + b1/16 + b2/256 + b3/4096
+        unsigned char* fam = img + (isq ? kM : 0);
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+            const uint32_t b = to_e4m3(x);
+            fam[tc::kmajor8(4 * h + pc, kk, ktot)] = (unsigned char)b;
+            x = (x - from_e4m3(b)) * 16.f;
+        }
     }
     if (tid < 16) {
         float* cst = reinterpret_cast<float*>(img + C::kConstOff);
@@ -158,6 +164,9 @@ __global__ void __launch_bounds__(128) tc_image_kernel(const TcArgs a) {
         else val = -prm.qjl_scale * sums[1][h];
         cst[tid] = val;
     }
+    __syncthreads();
+    uint4* out = reinterpret_cast<uint4*>(a.img + (size_t)g * C::kImgBytes);
+    for (int e = tid; e < C::kImgBytes / 16; e += 128) out[e] = reinterpret_cast<const uint4*>(img)[e];
 }
 
 // ------------------------------------------------------------------ scoring

@@ -1,6 +1,6 @@
-// e4m3 helpers shared by the tensor-core kernels: exact splitting of a value into e4m3 pieces,
-// the exact value of an e4m3 byte, and the per-column exponent that scales a family of values
-// into the e4m3 range.
+// e4m3 helpers shared by the tensor-core kernels: rounding to e4m3, the exact value of an e4m3
+// byte (a value is split into pieces b0 + b1/16 + b2/256 + b3/4096 by rounding the scaled
+// remainder again), and the per-column exponent that scales a family of values into range.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -20,16 +20,6 @@ __device__ __forceinline__ float from_e4m3(uint32_t b) {
     const uint32_t e = (b >> 3) & 15u, m = b & 7u;
     float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
     return (b & 0x80u) ? -v : v;
-}
-// piece pc of v * 2^e0 (pieces b0 + b1/16 + b2/256 + b3/4096)
-__device__ __forceinline__ uint32_t piece(float v, int e0, int pc) {
-    float x = ldexpf(v, e0);
-    uint32_t b = to_e4m3(x);
-    for (int p = 0; p < pc; ++p) {
-        x = (x - from_e4m3(b)) * 16.f;
-        b = to_e4m3(x);
-    }
-    return b;
 }
 // Column exponent e0 for a family whose largest scaled magnitude is mx: mx 2^e0 in [128, 256).
 __device__ __forceinline__ int column_exponent(float mx) {
