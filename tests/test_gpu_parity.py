@@ -413,6 +413,24 @@ def test_search_topk(d, bits, n, nq, k, kernel_path):
     _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
 
 
+@pytest.mark.parametrize("bits,d,n,nq,k", [(2, 200, 3001, 21, 10), (3, 128, 2000, 17, 64), (1, 256, 1500, 5, 7)])
+def test_search_topk_mse(bits, d, n, nq, k, kernel_path):
+    """Search over MSE-mode codes of 1-3 bits (no QJL signs): the tcgen05 kernel with only its
+    Walsh-term vectors (tensor path) and the byte-table kernel (CUDA-core path)."""
+    tq = _tq()
+    pr = Pair(d, bits, mode=tq.TQ_MODE_MSE, seed=6)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
+    X = inputs.cone(n, d, seed=15, mu_seed=77)
+    Q = inputs.cone(nq, d, seed=16, mu_seed=77)
+    z = pr.oquant(X.numpy())
+    db = pr.to_device(z, (n,))
+    s, i = pr.ctx.search_topk(Q.cuda(), db, k)
+    assert pr.ctx.sync_status() == 0
+    ref_s, ref_i = oracle.search_topk(Q.numpy(), z, pr.Pi, pr.cb, None, k)
+    scores = oracle.estimate_all(Q.numpy(), z, pr.Pi, pr.cb, None)
+    _topk_ok(s.cpu().numpy(), i.cpu().numpy().astype(np.int64), ref_s, ref_i, scores)
+
+
 @pytest.mark.parametrize("bits,d", [(8, 200), (6, 64)])
 def test_search_topk_wide_mse(bits, d):
     """Search over MSE-mode codes of 6 and 8 bits (generic scorer, table from device memory)."""
