@@ -87,6 +87,20 @@ def peaks():
     return 6400.0, "fallback"
 
 
+def _bf16_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if j.get("bf16_tflops"):
+            return float(j["bf16_tflops"]), "measured"
+    return 1800.0, "fallback"
+
+
+BF16_PEAK = _bf16_peak()
+
+
 class Clocks:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
     FIELDS = "clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
@@ -459,8 +473,15 @@ def measure_prefill(dev):
         den = Qs.pow(2).sum(1)[:, None] * xs[:ks].pow(2).sum(1)[None, :]
         d_prod = float(((est - exact) ** 2 / den).mean())
         bytes_per_vec = 2 * D + (ctx.P * ctx.W + ctx.Ws) * 4 + 4
+        # the rotation and the JL projection: 2 d (d + m) algorithmic flops per vector (the bf16
+        # pieces the kernel splits its operands into are not counted)
+        tflops = 2 * D * (D + ctx.m) * n / t / 1e12
         res[f"{bits - 1}+1bit"] = {"quantize_ms": t * 1e3, "vectors_per_s": n / t,
-                                  "GB_s": n * bytes_per_vec / t / 1e9, "D_mse": d_mse, "D_prod": d_prod}
+                                  "GB_s": n * bytes_per_vec / t / 1e9, "GB_s_frac_of_measured_hbm": None,
+                                  "tensor_TFLOPs_algorithmic": tflops,
+                                  "tensor_frac_of_measured_bf16": (tflops / BF16_PEAK[0]) if BF16_PEAK[0] else None,
+                                  "D_mse": d_mse, "D_prod": d_prod}
+        res[f"{bits - 1}+1bit"]["GB_s_frac_of_measured_hbm"] = res[f"{bits - 1}+1bit"]["GB_s"] / peaks()[0]
         del out
     return {"workload": "32 layers x 8 KV heads x 16384 tokens x d=128 bf16", **res}
 
