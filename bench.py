@@ -822,6 +822,11 @@ def measure_polar(dev):
         ctx = tq.PolarContext(D, bits, qjl=True, seed=0)
         pc = ctx.alloc_codes(n, device=dev)
         ctx.quantize(X, out=pc)
+        ctx.set_kernel_path(tq.TQ_PATH_CUDA_CORE)   # the CUDA-core encoder, for comparison
+        ctx.quantize(X, out=pc)
+        t_qc, _ = _event_time(lambda: ctx.quantize(X, out=pc))
+        ctx.set_kernel_path(tq.TQ_PATH_AUTO)        # tcgen05 for these bf16 rows at d = 128
+        ctx.quantize(X, out=pc)
         t_q, _ = _event_time(lambda: ctx.quantize(X, out=pc))
         out = torch.empty(Gf, n, device=dev)
         ctx.scores(q[:Gf], pc, 1.0, out=out)
@@ -844,7 +849,8 @@ def measure_polar(dev):
         key_bytes = (ctx.code_words + ctx.sign_words) * 4 + 4
         score_bytes = n * (key_bytes + Gf * 4)
         res[label] = {"angle_bits": bits, "code_bytes_per_key": key_bytes, "quantize_ms": t_q * 1e3,
-                      "vectors_per_s": n / t_q, "scores_ms": t_s * 1e3, "scores_per_s": n * Gf / t_s,
+                      "quantize_ms_cuda_core": t_qc * 1e3, "vectors_per_s": n / t_q,
+                      "quantize_GB_s": n * (D * 2 + key_bytes) / t_q / 1e9, "scores_ms": t_s * 1e3, "scores_per_s": n * Gf / t_s,
                       "scores_GB_s": score_bytes / t_s / 1e9, "scores_frac_of_measured_hbm": score_bytes / t_s / 1e9 / hbm,
                       "D_mse": d_mse, "D_prod": d_prod}
         del pc, out, ctx

@@ -20,6 +20,7 @@
 #include "lut.cuh"
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_kernels.h"
 
 constexpr int kPolarMaxLevels = 8;   // d <= 256
 constexpr int kPolarMaxCodes = 16;   // bits <= 4
@@ -41,6 +42,9 @@ struct tq_polar {
     float* dPi = nullptr;    // [d][d] row-major
     float* dST = nullptr;    // [d][m] ST[j*m+i] = S[i][j]
     int* derr = nullptr;
+    uint16_t* dbops = nullptr;   // d = 128: tcgen05 operands (Pi, S Pi^T as bf16 pieces)
+    float* dcs = nullptr;        // d = 128: [7][32] centroid cosines then sines per level
+    int kernel_path = TQ_PATH_AUTO;
 };
 
 namespace tq {
@@ -467,6 +471,8 @@ void free_polar(tq_polar* c) {
     cudaFree(c->dPi);
     cudaFree(c->dST);
     cudaFree(c->derr);
+    cudaFree(c->dbops);
+    cudaFree(c->dcs);
     delete c;
 }
 
@@ -476,16 +482,42 @@ int polar_levels(int d) {
     return (1 << L) == d ? L : -1;
 }
 
-int upload_floats(float** dst, const std::vector<float>& src) {
-    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(float));
+template <typename T>
+int upload_floats(T** dst, const std::vector<T>& src) {
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
     if (e != cudaSuccess) {
         *dst = nullptr;
         cudaGetLastError();
         return tq::fail(TQ_ERR_OOM, std::string("cudaMalloc of polar tables failed: ") + cudaGetErrorString(e));
     }
-    e = cudaMemcpy(*dst, src.data(), src.size() * sizeof(float), cudaMemcpyHostToDevice);
+    e = cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return polar_cuda_fail(e, "cudaMemcpy of polar tables");
     return TQ_OK;
+}
+
+// The tensor-core encoder's operands and centroid table (d = 128 only).
+int upload_tc_tables(tq_polar* c) {
+    std::vector<float> St;
+    if (c->qjl) {   // (S Pi^T)[i][j] = sum_k S[i][k] Pi[j][k], in float64 from the float32 matrices
+        St.resize((size_t)128 * 128);
+        for (int i = 0; i < 128; ++i)
+            for (int j = 0; j < 128; ++j) {
+                double acc = 0.0;
+                for (int k = 0; k < 128; ++k) acc += (double)c->S[(size_t)i * 128 + k] * (double)c->Pi[(size_t)j * 128 + k];
+                St[(size_t)i * 128 + j] = static_cast<float>(acc);
+            }
+    }
+    std::vector<uint16_t> ops;
+    tq::build_tc_operands(c->Pi.data(), c->qjl ? St.data() : nullptr, ops);
+    int rc = upload_floats(&c->dbops, ops);
+    if (rc != TQ_OK) return rc;
+    std::vector<float> cs((size_t)7 * 32, 0.f);
+    for (int l = 0; l < 7; ++l)
+        for (int j = 0; j < (1 << c->bits); ++j) {
+            cs[(size_t)32 * l + j] = c->prm.ccos[l][j];
+            cs[(size_t)32 * l + 16 + j] = c->prm.csin[l][j];
+        }
+    return upload_floats(&c->dcs, cs);
 }
 
 }  // namespace
@@ -564,6 +596,7 @@ int tq_polar_init(tq_polar** out, uint64_t seed, int d, int bits, int qjl, const
             for (int j = 0; j < d; ++j) ST[(size_t)j * d + i] = c->S[(size_t)i * d + j];
         rc = upload_floats(&c->dST, ST);
     }
+    if (rc == TQ_OK && d == 128) rc = upload_tc_tables(c);
     if (rc == TQ_OK) {
         ce = cudaMalloc(reinterpret_cast<void**>(&c->derr), sizeof(int));
         if (ce == cudaSuccess) ce = cudaMemset(c->derr, 0, sizeof(int));
@@ -595,6 +628,28 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
     if (n == 0) return TQ_OK;
     if (!x || !codes || !r16 || (ctx->qjl && (!signs || !rnorm16)))
         return tq::fail(TQ_ERR_ARG, "tq_polar_quantize: NULL buffer");
+    const bool tc_fits = ctx->dbops && dtype == TQ_BF16 && (ld_x % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
+    if (tc_fits && (ctx->kernel_path == TQ_PATH_TENSOR || (ctx->kernel_path == TQ_PATH_AUTO && n >= 4096))) {
+        tq::PolarTcLaunch L{};
+        L.device = ctx->device;
+        L.x = x;
+        L.n = n;
+        L.ld_x = ld_x;
+        L.bops = ctx->dbops;
+        L.cs = ctx->dcs;
+        L.bits = ctx->bits;
+        L.qjl = ctx->qjl;
+        L.cw = ctx->prm.cw;
+        for (int l = 0; l < 7; ++l)
+            for (int t = 0; t < 15; ++t) L.thr[l][t] = ctx->prm.thr[l][t];
+        L.codes = codes;
+        L.r16 = r16;
+        L.signs = signs;
+        L.rnorm = rnorm16;
+        L.err = ctx->derr;
+        cudaError_t e = tq::launch_polar_tc(L, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? TQ_OK : polar_cuda_fail(e, "polar_tc_kernel launch");
+    }
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device);
     tq::PolarQuantArgs a{ctx->prm, x, dtype, n, ld_x, ctx->dPiT, ctx->dPi, ctx->dST, codes, r16, signs, rnorm16, ctx->derr};
@@ -603,6 +658,14 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
     tq::polar_quantize_kernel<<<grid, tq::kPolarQThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TQ_OK : polar_cuda_fail(e, "polar_quantize_kernel launch");
+}
+
+int tq_polar_set_kernel_path(tq_polar* ctx, int path) {
+    if (!ctx) return tq::fail(TQ_ERR_ARG, "tq_polar_set_kernel_path: context is NULL");
+    if (path != TQ_PATH_AUTO && path != TQ_PATH_CUDA_CORE && path != TQ_PATH_TENSOR)
+        return tq::fail(TQ_ERR_ARG, "tq_polar_set_kernel_path: path must be TQ_PATH_AUTO, TQ_PATH_CUDA_CORE or TQ_PATH_TENSOR");
+    ctx->kernel_path = path;
+    return TQ_OK;
 }
 
 int tq_polar_scores(tq_polar* ctx, const float* q, int64_t nq, const uint32_t* codes, const uint16_t* r16,

@@ -370,6 +370,270 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
     if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
 }
 
+// ---------------------------------------------------------------- polar-angle encoder
+// The recursive polar encoder (k_polar.cu; csdn tutorial, section 将笛卡尔积坐标转为极坐标, and
+// freelamp article, section 技术突破：极坐标量化) with its two d x d products on the tensor cores, for
+// bf16 rows at d = 128 (7 levels, 127 angles): phase 1 Y = X Pi^T as above; the epilogue runs the
+// polar transform — each thread's 32 consecutive coordinates are the subtree of one level-5 node,
+// so levels 1-5 are thread-local and one thread per row combines the 4 level-5 radii into levels 6
+// and 7 — codes each angle against its level's thresholds, packs the code stream, rebuilds y_hat
+// top-down from the stored fp16 radius and the centroids' cos / sin, and with QJL projects
+// r' = y - y_hat as in phase 2 above (r = Pi^T r', so S r = (S Pi^T) r').
+constexpr int kPolarTcLevels = 7;
+constexpr int kCodeStride = 132;   // bytes per row of the code stream in shared memory (33 words: no bank conflicts)
+
+struct PolarTcArgs {
+    const uint16_t* x;
+    int64_t n, ld_x;
+    const uint4* bops;
+    const float* cs;          // [level][32]: cos then sin of the level's 2^B centroids
+    uint32_t* codes;
+    uint16_t* r16;
+    uint32_t* signs;
+    uint16_t* rnorm;
+    int* err;
+    int cw;                   // code words per row
+    float thr[kPolarTcLevels][15];   // per level, ascending (read at uniform indices)
+};
+
+template <int B>
+__device__ __forceinline__ int polar_code(float psi, const float* thr) {
+    int c = 0;
+#pragma unroll
+    for (int t = 0; t < (1 << B) - 1; ++t) c += psi > thr[t] ? 1 : 0;
+    return c;
+}
+
+template <int B, bool QJL>
+__global__ void __launch_bounds__(kTcThreads, 1) polar_tc_kernel(const PolarTcArgs a) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    unsigned char* sB = sm;
+    unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]; the spent one holds codes, then r' lo
+    unsigned char* sR = sm + kSmemB + kSmemX;
+    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128]
+    __shared__ __align__(8) uint64_t mbar, s_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ float s_cs[kPolarTcLevels * 32];   // indexed by code per lane: shared, not parameter space
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, part = warp >> 2, row = 32 * q + lane;
+    const int ntiles = (int)((a.n + kTile - 1) / kTile);
+    if (blockIdx.x >= ntiles) return;
+    if (QJL && tid < kPolarTcLevels * 32) s_cs[tid] = a.cs[tid];
+
+    for (int e = tid; e < (int)((QJL ? kSmemB : kSmemB / 2) / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
+    asm volatile("cp.async.commit_group;");
+    {   // the first tile's rows
+        const int64_t r0 = (int64_t)blockIdx.x * kTile;
+        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+        for (int e = tid; e < kTile * 16; e += kTcThreads) {
+            const int r = e >> 4, kc = e & 15;
+            unsigned char* dst = sX + kmajor_off(r, 8 * kc);
+            if (r < nvalid) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("cp.async.commit_group;");
+    }
+    if (tid == 0) {
+        tc::mbar_init(&mbar, 1);
+        tc::mbar_init(&s_drain, 1);
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc<kTmemCols>(&s_tmem);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t d1_row = tmem + ((uint32_t)(32 * q) << 16);
+    const uint32_t d2_row = d1_row + 128;
+    uint32_t phase = 0;
+    bool ok = true;
+    int buf = 0;
+
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, buf ^= 1) {
+        const int64_t r0 = (int64_t)tile * kTile;
+        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+        unsigned char* sXc = sX + buf * kMatBytes;
+        asm volatile("cp.async.wait_group 0;");
+        asm volatile("fence.proxy.async.shared::cta;");
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (tid == 0) {   // phase 1: Y = X Pi^T
+            issue_pieces(tmem, tc::smem_u32(sXc), tc::smem_u32(sB), false);
+            tc::commit(&mbar);
+        }
+        const int next = tile + gridDim.x;
+        if (next < ntiles) {
+            const int64_t n0 = (int64_t)next * kTile;
+            const int nv2 = (int)min((int64_t)kTile, a.n - n0);
+            unsigned char* sXn = sX + (buf ^ 1) * kMatBytes;
+            for (int e = tid; e < kTile * 16; e += kTcThreads) {
+                const int r = e >> 4, kc = e & 15;
+                unsigned char* dst = sXn + kmajor_off(r, 8 * kc);
+                if (r < nv2) tc::cp_async16(dst, a.x + (size_t)(n0 + r) * a.ld_x + 8 * kc);
+                else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        asm volatile("cp.async.commit_group;");
+        float xs = 0.f;   // ||x||^2 partial while the MMAs run
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+            const uint4 w = *reinterpret_cast<const uint4*>(sXc + kmajor_off(row, 32 * part + 8 * kc));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
+                xs = fmaf(lo, lo, xs);
+                xs = fmaf(hi, hi, xs);
+            }
+        }
+        s_part[part * kTile + row] = xs;
+        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
+        phase ^= 1u;
+        if (!ok) break;
+        tc::fence_after();
+        float y[32];
+        load_row_part(d1_row, part, y);
+        const float nrm = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
+        const int64_t grow = r0 + row;
+        const bool valid = row < nvalid;
+        unsigned char* code = sXc + row * kCodeStride;   // this row's 127 angle codes in stream order (sXc is spent)
+        // levels 1-5 of this thread's subtree (level-l node i of the subtree is global node
+        // (32 >> l) part + i, at stream position 128 - (256 >> l) + that)
+        float rad[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float lo = y[2 * i], hi = y[2 * i + 1];
+            float psi = atan2f(hi, lo);
+            if (psi < 0.f) psi += 6.28318530717958647692f;
+            rad[i] = sqrtf(fmaf(lo, lo, hi * hi));
+            code[16 * part + i] = (unsigned char)polar_code<B>(psi, a.thr[0]);
+        }
+#pragma unroll
+        for (int l = 2; l <= 5; ++l) {
+            const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
+#pragma unroll
+            for (int i = 0; i < nodes; ++i) {
+                const float lo = rad[2 * i], hi = rad[2 * i + 1];
+                rad[i] = sqrtf(fmaf(lo, lo, hi * hi));
+                code[pos + i] = (unsigned char)polar_code<B>(atan2f(hi, lo), a.thr[l - 1]);
+            }
+        }
+        __syncthreads();   // every thread has read its x-norm partials
+        s_part[part * kTile + row] = rad[0];   // the level-5 radius of this quarter
+        __syncthreads();
+        if (part == 0) {   // levels 6 and 7 of the row
+            const float r5[4] = {s_part[row], s_part[kTile + row], s_part[2 * kTile + row], s_part[3 * kTile + row]};
+            float r6[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                r6[i] = sqrtf(fmaf(r5[2 * i], r5[2 * i], r5[2 * i + 1] * r5[2 * i + 1]));
+                code[124 + i] = (unsigned char)polar_code<B>(atan2f(r5[2 * i + 1], r5[2 * i]), a.thr[5]);
+            }
+            code[126] = (unsigned char)polar_code<B>(atan2f(r6[1], r6[0]), a.thr[6]);
+        }
+        __syncthreads();   // the code stream of every row is complete
+        // pack: word w holds stream bits 32 w .. 32 w + 31, stream bit t being bit t - B an of code
+        // an = t / B; the codes from a0 = 32 w / B on are laid side by side in a 64-bit window
+        // (code a0 + k at bit B k), whose bits sh .. sh + 31 (sh = 32 w - B a0) are the word
+        for (int w = part; w < a.cw; w += 4) {
+            const int a0 = 32 * w / B, sh = 32 * w - B * a0;
+            constexpr int K = (31 + B - 1) / B + 1;
+            uint64_t win = 0u;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+                if (a0 + k < 127) win |= (uint64_t)code[a0 + k] << (B * k);
+            if (valid) a.codes[(size_t)grow * a.cw + w] = (uint32_t)(win >> sh);
+        }
+        const uint16_t nh = float_to_half_bits(nrm);
+        if (valid && part == 0) {
+            a.r16[grow] = nh;
+            if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+        }
+        if constexpr (!QJL) {
+            tc::fence_before();
+            __syncthreads();   // TMEM reads and code reads done before the next tile
+            continue;
+        }
+        // y_hat top-down from the stored radius: the path root -> level 6 -> this quarter's level-5
+        // node, then the subtree
+        const float* cs = s_cs;
+        float rho = half_bits_to_float(nh);
+        {
+            const int c7 = code[126], c6 = code[124 + (part >> 1)];
+            rho *= (part >> 1) ? cs[6 * 32 + 16 + c7] : cs[6 * 32 + c7];
+            rho *= (part & 1) ? cs[5 * 32 + 16 + c6] : cs[5 * 32 + c6];
+        }
+        rad[0] = rho;
+#pragma unroll
+        for (int l = 5; l >= 2; --l) {   // node i of level l -> children 2 i, 2 i + 1 of level l - 1
+            const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
+#pragma unroll
+            for (int i = nodes - 1; i >= 0; --i) {
+                const int c = code[pos + i];
+                const float r = rad[i];
+                rad[2 * i] = r * cs[(l - 1) * 32 + c];
+                rad[2 * i + 1] = r * cs[(l - 1) * 32 + 16 + c];
+            }
+        }
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = code[16 * part + i];
+            const float lo = rad[i] * cs[c], hi = rad[i] * cs[16 + c];
+            y[2 * i] -= lo;
+            y[2 * i + 1] -= hi;
+            rs = fmaf(y[2 * i], y[2 * i], rs);
+            rs = fmaf(y[2 * i + 1], y[2 * i + 1], rs);
+        }
+        store_row_part(sR, row, part, y);   // r' hi
+#pragma unroll
+        for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
+        __syncthreads();   // every row's codes have been read: the spent x buffer takes r' lo
+        store_row_part(sXc, row, part, y);
+        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
+        tc::fence_before();
+        asm volatile("fence.proxy.async.shared::cta;");
+        __syncthreads();
+        tc::fence_after();
+        if (tid == 0) {   // phase 2: Z = r'_hi (S Pi^T)^T + r'_lo (S Pi^T)^T
+            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
+            issue_pieces(tmem + 128, tc::smem_u32(sXc), tc::smem_u32(sB) + kPieces * kMatBytes, true);
+            tc::commit(&mbar);
+        }
+        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
+        phase ^= 1u;
+        if (!ok) break;
+        tc::fence_after();
+        float z[32];
+        load_row_part(d2_row, part, z);
+        uint32_t sw = 0u;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
+        if (valid) a.signs[(size_t)grow * 4 + part] = sw;
+        if (valid && part == 0) {
+            const float rn = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
+            const uint16_t rh = float_to_half_bits(rn);
+            a.rnorm[grow] = rh;
+            if (__hisinf(__ushort_as_half(rh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+        }
+        tc::fence_before();
+        __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
+    }
+    asm volatile("cp.async.wait_all;");
+    bool drained = true;
+    if (!ok) {   // a wait ran out: flag it, and let every MMA this CTA issued finish (bounded)
+        if (tid == 0) {
+            set_error(a.err, TQ_DEVERR_TIMEOUT);
+            tc::commit(&s_drain);
+        }
+        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&s_drain, 0u));
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
+}
+
 }  // namespace
 
 bool quantize_tc_supported(const tq_ctx* c, int dtype, const void* x, int64_t n, int64_t ld_x) {
@@ -436,6 +700,48 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     else if (c->prm.P == 4) e = run(quantize_tc_kernel<4, false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+}  // namespace tq
+
+namespace tq {
+
+cudaError_t launch_polar_tc(const PolarTcLaunch& L, cudaStream_t s) {
+    PolarTcArgs a{};
+    a.x = static_cast<const uint16_t*>(L.x);
+    a.n = L.n;
+    a.ld_x = L.ld_x;
+    a.bops = reinterpret_cast<const uint4*>(L.bops);
+    a.cs = L.cs;
+    a.codes = L.codes;
+    a.r16 = L.r16;
+    a.signs = L.signs;
+    a.rnorm = L.rnorm;
+    a.err = L.err;
+    a.cw = L.cw;
+    for (int l = 0; l < kPolarTcLevels; ++l)
+        for (int t = 0; t < 15; ++t) a.thr[l][t] = L.thr[l][t];
+    int sms = 148;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L.device);
+    const int64_t ntiles = (L.n + kTile - 1) / kTile;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    auto run = [&](auto kernel) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+        if (e != cudaSuccess) return e;
+        kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
+        return cudaGetLastError();
+    };
+    switch (L.bits * 2 + (L.qjl ? 1 : 0)) {
+        case 2: return run(polar_tc_kernel<1, false>);
+        case 3: return run(polar_tc_kernel<1, true>);
+        case 4: return run(polar_tc_kernel<2, false>);
+        case 5: return run(polar_tc_kernel<2, true>);
+        case 6: return run(polar_tc_kernel<3, false>);
+        case 7: return run(polar_tc_kernel<3, true>);
+        case 8: return run(polar_tc_kernel<4, false>);
+        case 9: return run(polar_tc_kernel<4, true>);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tq

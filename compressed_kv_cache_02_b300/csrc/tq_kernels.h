@@ -26,6 +26,26 @@ void build_tc_operands(const float* Pi, const float* St, std::vector<uint16_t>& 
 cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_t ld_x, uint32_t* planes,
                                uint32_t* signs, uint16_t* norm, uint16_t* rnorm, cudaStream_t s);
 
+// tcgen05 polar-angle encoder (bf16 rows, d = 128, 7 levels of angles), k_quantize_tc.cu.
+// bops: build_tc_operands(Pi, S Pi^T or NULL) on the device; cs: [7][32] floats, level l - 1 at
+// 32 (l - 1): the cosines of its 2^bits centroids, then at + 16 their sines; thr: per level the
+// 2^bits - 1 ascending thresholds.  Needs x 16-byte aligned and ld_x a multiple of 8.
+struct PolarTcLaunch {
+    int device;
+    const void* x;
+    int64_t n, ld_x;
+    const void* bops;
+    const float* cs;
+    int bits, qjl, cw;
+    float thr[7][15];
+    uint32_t* codes;
+    uint16_t* r16;
+    uint32_t* signs;
+    uint16_t* rnorm;
+    int* err;
+};
+cudaError_t launch_polar_tc(const PolarTcLaunch& L, cudaStream_t s);
+
 cudaError_t launch_advance_len(int32_t* len, int B, int64_t cap, int step, int* err, cudaStream_t s);
 
 struct KeyCache {

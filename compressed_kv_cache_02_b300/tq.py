@@ -65,6 +65,7 @@ _SIGS = {
     "tq_polar_init": [ctypes.POINTER(_p), _u64, _i, _i, _i, _p, _p],
     "tq_polar_layout": [_p, _p, _p],
     "tq_polar_quantize": [_p, _p, _i, _i64, _i64, _p, _p, _p, _p, _p],
+    "tq_polar_set_kernel_path": [_p, _i],
     "tq_polar_scores": [_p, _p, _i64, _p, _p, _p, _p, _i64, _f, _p, _p],
     "tq_polar_sync_status": [_p, _p, _p],
     "tq_paged_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
@@ -408,6 +409,9 @@ class PolarContext:
             self.close()
         except Exception:
             pass
+
+    def set_kernel_path(self, path: int) -> None:
+        _check(lib.tq_polar_set_kernel_path(self.h, path), "tq_polar_set_kernel_path")
 
     def alloc_codes(self, n: int, device="cuda") -> PolarCodes:
         codes = torch.zeros(n, self.code_words, dtype=torch.int32, device=device)

@@ -374,6 +374,15 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
                       uint32_t* codes, uint16_t* r16, uint32_t* signs, uint16_t* rnorm16,
                       void* stream);
 
+/* Kernel family of tq_polar_quantize (enum tq_kernel_path).  TQ_PATH_AUTO (the default)
+ * encodes bf16 rows at d = 128 with n >= 4096 (ld_x a multiple of 8, x 16-byte aligned) on
+ * the tcgen05 tensor cores (y = Pi x and the QJL projection (S Pi^T) r' as bf16 MMAs with the
+ * matrices split into two bf16 pieces, fp32 accumulation; r' = y - y_hat in the rotated basis)
+ * and everything else on CUDA cores; TQ_PATH_TENSOR takes the tensor-core encoder for every n
+ * where the dtype, d and alignment allow it; TQ_PATH_CUDA_CORE never.  Both families give the
+ * same codes up to angles within float rounding of a threshold.  TQ_ERR_ARG for another path.  */
+int tq_polar_set_kernel_path(tq_polar* ctx, int path);
+
 /* out[i][k] = scale * est(q_i, x_k) for nq fp32 queries q [nq][d] against n coded rows
  * (device buffers, out [nq][n] fp32 row-major).  Asynchronous on `stream`.                 */
 int tq_polar_scores(tq_polar* ctx, const float* q, int64_t nq, const uint32_t* codes,

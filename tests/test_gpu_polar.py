@@ -106,6 +106,42 @@ def test_polar_quantize_zero_rows_and_strides():
     assert int(pc.r16[3]) == 0 and int(pc.codes[3].abs().sum()) == 0
 
 
+@pytest.mark.parametrize("bits,qjl", [(1, True), (2, True), (3, True), (4, True), (2, False), (4, False)])
+@pytest.mark.parametrize("path", ["tensor", "auto"])
+def test_polar_quantize_tcgen05(bits, qjl, path):
+    """The tensor-core encoder (bf16 rows at d = 128): forced on 1037 rows (8 full tiles of 128
+    and a ragged tail of 13) with a zero row and a row stride of 192, or taken by AUTO on 4100
+    rows (past the 4096-row cut, a tail of 4); same parity rules as the CUDA-core encoder."""
+    tq = _tq()
+    pr = PolarPair(128, bits, qjl, seed=14 + bits)
+    n = 1037 if path == "tensor" else 4100
+    if path == "tensor":
+        pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR)
+    fac = inputs.anisotropic_factors(1, 192, seed=15)
+    X = inputs.anisotropic(1, 1, n, 192, fac, seed=15)[0, 0].to(torch.bfloat16).cuda()
+    X[5] = 0.0
+    view = X[:, :128] if path == "tensor" else X[:, :128].contiguous()
+    pc = pr.ctx.quantize(view)
+    assert pr.ctx.sync_status() == 0
+    same = pr.check_codes(view.float().cpu().numpy(), pc)
+    assert same.mean() > 0.97
+    assert int(pc.r16[5]) == 0 and int(pc.codes[5].abs().sum()) == 0
+    if qjl:
+        assert int(pc.rnorm[5]) == 0 and int(pc.signs[5].abs().sum()) == 0
+
+
+def test_polar_kernel_path_argument():
+    tq = _tq()
+    pr = PolarPair(64, 2, True, seed=3)
+    with pytest.raises(tq.TQError):
+        pr.ctx.set_kernel_path(7)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR)   # d = 64: the CUDA-core encoder still runs
+    X = torch.randn(50, 64, device="cuda", dtype=torch.bfloat16)
+    pc = pr.ctx.quantize(X)
+    assert pr.ctx.sync_status() == 0
+    pr.check_codes(X.float().cpu().numpy(), pc)
+
+
 @pytest.mark.parametrize("d,bits,qjl,nq", [(128, 3, True, 4), (128, 2, True, 6), (64, 4, False, 3),
                                            (256, 3, True, 5), (32, 1, True, 8)])
 def test_polar_scores(d, bits, qjl, nq):
