@@ -597,9 +597,11 @@ constexpr int kV2Threads = 256;
 // max grows) and meets the other warps only once, at the end of the chunk (log-sum-exp merge of
 // the 8 warp partials).  Lane l owns the coordinates 32 (l / 8) + l % 8 + 8 c, c = 0..3: bits
 // l % 8 + 8 c of word l / 8 of each plane, so one rotate and one and-or per plane leave byte c of
-// z = 4 * index of coordinate c, and a byte-permute plus one shared load fetch its centroid.
-// The packed FFMA2 runs over coordinate pairs (0, 1), (2, 3) against each head's weight, which
-// shared memory holds duplicated as (w_h, w_h).
+// z = 4 * index of coordinate c, and a byte-permute plus one 4-byte shared load fetch its
+// centroid.  The packed FFMA2 runs over the head pairs (0, 1) and (2, 3) against the centroid
+// doubled in registers, so a key's four weights are one 16-byte broadcast load.  What bounds this
+// loop is the shared-memory data return (lanes x bytes per load): per key 12 B of plane words,
+// 16 B of centroids and 16 B of weights per lane.
 template <int P, bool SPLIT>
 __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const ValuesArgs a) {
     constexpr int NW = kV2Threads / 32;
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     constexpr int BUFW = 32 * (SPLIT ? ROW + 4 : ROW);   // words per 32-key buffer
     constexpr int SVW = NW * 2 * BUFW > 4 * NW * 32 * 4 ? NW * 2 * BUFW : 4 * NW * 32 * 4;   // + room for the merge
     __shared__ __align__(16) uint32_t sV[SVW];
-    __shared__ ulonglong2 sW[NW][32][2];
+    __shared__ ulonglong2 sW[NW][32];           // per key: (w0, w1), (w2, w3)
     __shared__ float4 s_wm[NW], s_wl[NW];
     __shared__ float s_cv[kMaxLevels], s_cv_hi[kMaxLevels];
     const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh - b * a.Hkv;
@@ -628,7 +630,6 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     const float* lg = a.logits + ((size_t)b * a.Hq + hbase) * a.cap;
     const uint32_t* vrows = static_cast<const uint32_t*>(a.v.values);
     uint32_t* buf0 = sV + warp * 2 * BUFW;
-    const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s_cv);
 
     auto issue_block = [&](int j, int buf) {   // the value rows of block j into buffer buf
         const int64_t k0 = i0 + (int64_t)j * 32;
@@ -656,9 +657,9 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
         }
     };
 
-    u64 alo[4], ahi[4];   // head h: owned coordinates (0, 1) in alo[h], (2, 3) in ahi[h]
+    u64 acc[4][2];   // owned coordinate c: heads (0, 1) in acc[c][0], (2, 3) in acc[c][1]
 #pragma unroll
-    for (int h = 0; h < 4; ++h) alo[h] = ahi[h] = 0ull;
+    for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0ull;
     float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4 ls = make_float4(0.f, 0.f, 0.f, 0.f);   // this lane's share of the softmax sums
     float4 l4, nl4;
@@ -667,13 +668,14 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     if (warp < nblk) issue_block(warp, 0);
     cp_async_commit();
     const int wsel = lane >> 3;
-    int rot[P];   // right-rotation moving bit lane % 8 + 8 c of plane pp to bit 8 c + pp + 3
+    int rot[P];   // right-rotation moving bit lane % 8 + 8 c of plane pp to bit 8 c + pp + 2
 #pragma unroll
     for (int pp = 0; pp < P; ++pp) rot[pp] = ((lane & 7) - pp - 2) & 31;
     // split contexts: a lane's coordinates share word wsel, so the (P+1)-bit table is per lane
     const bool hi = SPLIT && 32 * wsel < a.vprm.d_hi;
     const int rot_top = ((lane & 7) - P - 2) & 31;
-    const unsigned char* cvl = hi ? reinterpret_cast<const unsigned char*>(s_cv_hi) : cvb;
+    const unsigned char* cvl = reinterpret_cast<const unsigned char*>(hi ? s_cv_hi : s_cv);
+    const ulonglong2* sWw = sW[warp];
     int buf = 0;
     for (int j = warp; j < nblk; j += NW, buf ^= 1) {
         const int jn = j + NW;
@@ -687,25 +689,22 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
             const float4 alpha = make_float4(rescale(m4.x, mn.x), rescale(m4.y, mn.y), rescale(m4.z, mn.z), rescale(m4.w, mn.w));
             m4 = mn;
             ls = make_float4(ls.x * alpha.x, ls.y * alpha.y, ls.z * alpha.z, ls.w * alpha.w);
-            const float av[4] = {alpha.x, alpha.y, alpha.z, alpha.w};
+            const u64 a01 = pk2(alpha.x, alpha.y), a23 = pk2(alpha.z, alpha.w);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const u64 al = pk2(av[h], av[h]);
-                alo[h] = mul2(alo[h], al);
-                ahi[h] = mul2(ahi[h], al);
+            for (int c = 0; c < 4; ++c) {
+                acc[c][0] = mul2(acc[c][0], a01);
+                acc[c][1] = mul2(acc[c][1], a23);
             }
         }
         const float4 p = make_float4(safe_exp(l4.x, m4.x), safe_exp(l4.y, m4.y), safe_exp(l4.z, m4.z), safe_exp(l4.w, m4.w));
         ls = f4_add(ls, p);
         {
             const float4 w = f4_scale(vn, p);
-            sW[warp][lane][0] = make_ulonglong2(pk2(w.x, w.x), pk2(w.y, w.y));
-            sW[warp][lane][1] = make_ulonglong2(pk2(w.z, w.z), pk2(w.w, w.w));
+            sW[warp][lane] = make_ulonglong2(pk2(w.x, w.y), pk2(w.z, w.w));
         }
         cp_async_wait1();   // this block's value rows have landed
         __syncwarp();
         const uint32_t* tile = buf0 + buf * BUFW;
-        const ulonglong2* sW2 = &sW[warp][0][0];
         // All 32 rows, also in a partial block: a key past the end has weight exactly 0 (vn = 0,
         // p = 0) and its stale row still selects finite centroids, so it adds nothing.
 #pragma unroll 8
@@ -722,19 +721,14 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
                 const uint32_t wd = row[P * 4 + wsel];
                 z |= __funnelshift_r(wd, wd, rot_top) & (0x04040404u << P);
             }
-            const u64 v01 = pk2(*reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4440)),
-                                *reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4441)));
-            const u64 v23 = pk2(*reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4442)),
-                                *reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4443)));
-            const ulonglong2 wa = sW2[2 * t], wb = sW2[2 * t + 1];
-            alo[0] = fma2(v01, wa.x, alo[0]);
-            ahi[0] = fma2(v23, wa.x, ahi[0]);
-            alo[1] = fma2(v01, wa.y, alo[1]);
-            ahi[1] = fma2(v23, wa.y, ahi[1]);
-            alo[2] = fma2(v01, wb.x, alo[2]);
-            ahi[2] = fma2(v23, wb.x, ahi[2]);
-            alo[3] = fma2(v01, wb.y, alo[3]);
-            ahi[3] = fma2(v23, wb.y, ahi[3]);
+            const ulonglong2 w = sWw[t];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float cv = *reinterpret_cast<const float*>(cvl + __byte_perm(z, 0u, 0x4440 + c));
+                const u64 cc = pk2(cv, cv);
+                acc[c][0] = fma2(cc, w.x, acc[c][0]);
+                acc[c][1] = fma2(cc, w.y, acc[c][1]);
+            }
         }
         __syncwarp();   // sW and this buffer are reused
         l4 = nl4;
@@ -752,13 +746,10 @@ __global__ void __launch_bounds__(kV2Threads, 4) values_coded128_kernel(const Va
     for (int w = 1; w < NW; ++w) M = f4_max(M, s_wm[w]);
     const float4 sc = make_float4(rescale(m4.x, M.x), rescale(m4.y, M.y), rescale(m4.z, M.z), rescale(m4.w, M.w));
     float4* red = reinterpret_cast<float4*>(sV);   // [NW][4][32]
-    {
-        const float2 a0 = upk2(alo[0]), a1 = upk2(alo[1]), a2 = upk2(alo[2]), a3 = upk2(alo[3]);
-        const float2 b0 = upk2(ahi[0]), b1 = upk2(ahi[1]), b2 = upk2(ahi[2]), b3 = upk2(ahi[3]);
-        red[(warp * 4 + 0) * 32 + lane] = make_float4(a0.x * sc.x, a1.x * sc.y, a2.x * sc.z, a3.x * sc.w);
-        red[(warp * 4 + 1) * 32 + lane] = make_float4(a0.y * sc.x, a1.y * sc.y, a2.y * sc.z, a3.y * sc.w);
-        red[(warp * 4 + 2) * 32 + lane] = make_float4(b0.x * sc.x, b1.x * sc.y, b2.x * sc.z, b3.x * sc.w);
-        red[(warp * 4 + 3) * 32 + lane] = make_float4(b0.y * sc.x, b1.y * sc.y, b2.y * sc.z, b3.y * sc.w);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 h01 = upk2(acc[c][0]), h23 = upk2(acc[c][1]);
+        red[(warp * 4 + c) * 32 + lane] = make_float4(h01.x * sc.x, h01.y * sc.y, h23.x * sc.z, h23.y * sc.w);
     }
     __syncthreads();
     const size_t stride = (size_t)a.d + 2;
