@@ -640,8 +640,11 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
         L.bits = ctx->bits;
         L.qjl = ctx->qjl;
         L.cw = ctx->prm.cw;
-        for (int l = 0; l < 7; ++l)
-            for (int t = 0; t < 15; ++t) L.thr[l][t] = ctx->prm.thr[l][t];
+        for (int l = 2; l <= 7; ++l)
+            for (int t = 0; t + 1 < (1 << ctx->bits); ++t) {
+                const double tn = std::tan(ctx->thresholds[l - 1][t]);
+                L.tau[l - 2][t] = (float)(tn * tn);
+            }
         L.codes = codes;
         L.r16 = r16;
         L.signs = signs;

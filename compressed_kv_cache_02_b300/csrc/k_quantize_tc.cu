@@ -379,8 +379,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
 // and 7 — codes each angle against its level's thresholds, packs the code stream, rebuilds y_hat
 // top-down from the stored fp16 radius and the centroids' cos / sin, and with QJL projects
 // r' = y - y_hat as in phase 2 above (r = Pi^T r', so S r = (S Pi^T) r').
+// The angle codes need neither the angles nor the radii themselves: a level-1 code is the index of
+// the uniform sector holding (y_2i, y_2i+1), found by halving the turn (sector_code); a level-l
+// angle atan2(r_hi, r_lo) in [0, pi/2] passes threshold t exactly when R_hi > tan^2(t) R_lo, with R
+// the squared radii, which add up the tree without square roots (level_code).  Both decide as the
+// angle comparisons do, up to float rounding at a threshold.
 constexpr int kPolarTcLevels = 7;
 constexpr int kCodeStride = 132;   // bytes per row of the code stream in shared memory (33 words: no bank conflicts)
+constexpr float kTanPi8 = 0.41421356237309504880f;   // tan(pi / 8)
 
 struct PolarTcArgs {
     const uint16_t* x;
@@ -393,14 +399,40 @@ struct PolarTcArgs {
     uint16_t* rnorm;
     int* err;
     int cw;                   // code words per row
-    float thr[kPolarTcLevels][15];   // per level, ascending (read at uniform indices)
+    float tau[kPolarTcLevels - 1][15];   // levels 2..7: tan^2 of the ascending thresholds (uniform indices)
 };
 
+// Level-1 code: #{k >= 1 : psi > 2 pi k / 2^B} for psi = atan2(hi, lo) taken in [0, 2 pi).  Halving
+// the turn: psi > pi is hi < 0, after which the point turns by pi; the remaining angle exceeds
+// pi / 2 when x < 0, after which the point turns by pi / 2; it then exceeds pi / 4 when y > x,
+// after which it turns by pi / 4 (scaled by sqrt 2); last, it exceeds pi / 8 when
+// y > tan(pi / 8) x.  Signed zeros fall as atan2 puts them (hi = -0 counts as the upper
+// half-plane, as atan2(-0, lo) in {-0, pi} does after the wrap).
 template <int B>
-__device__ __forceinline__ int polar_code(float psi, const float* thr) {
+__device__ __forceinline__ int sector_code(float lo, float hi) {
+    const bool s1 = hi < 0.f;
+    if constexpr (B == 1) return s1 ? 1 : 0;
+    const float x1 = s1 ? -lo : lo, y1 = s1 ? -hi : hi;
+    const bool s2 = x1 < 0.f;
+    int c = (s1 ? 2 : 0) + (s2 ? 1 : 0);
+    if constexpr (B == 2) return c;
+    const float x2 = s2 ? y1 : x1, y2 = s2 ? -x1 : y1;
+    const bool s3 = y2 > x2;
+    c = 2 * c + (s3 ? 1 : 0);
+    if constexpr (B == 3) return c;
+    const float x3 = s3 ? x2 + y2 : x2, y3 = s3 ? y2 - x2 : y2;
+    return 2 * c + (y3 > kTanPi8 * x3 ? 1 : 0);
+}
+
+// Level-l code (l >= 2): #{k : atan2(r_hi, r_lo) > t_k}, t_k in (0, pi/2), from the squared radii:
+// the angle passes t_k iff R_hi / R_lo > tan^2 t_k (the ratio is +inf for R_lo = 0 < R_hi and NaN
+// for 0 / 0, whose angle atan2(0, 0) = 0 passes nothing).
+template <int B>
+__device__ __forceinline__ int level_code(float Rlo, float Rhi, const float* tau) {
+    const float qv = __fdividef(Rhi, Rlo);
     int c = 0;
 #pragma unroll
-    for (int t = 0; t < (1 << B) - 1; ++t) c += psi > thr[t] ? 1 : 0;
+    for (int t = 0; t < (1 << B) - 1; ++t) c += qv > tau[t] ? 1 : 0;
     return c;
 }
 
@@ -499,15 +531,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) polar_tc_kernel(const PolarTcAr
         const bool valid = row < nvalid;
         unsigned char* code = sXc + row * kCodeStride;   // this row's 127 angle codes in stream order (sXc is spent)
         // levels 1-5 of this thread's subtree (level-l node i of the subtree is global node
-        // (32 >> l) part + i, at stream position 128 - (256 >> l) + that)
+        // (32 >> l) part + i, at stream position 128 - (256 >> l) + that), with squared radii
         float rad[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float lo = y[2 * i], hi = y[2 * i + 1];
-            float psi = atan2f(hi, lo);
-            if (psi < 0.f) psi += 6.28318530717958647692f;
-            rad[i] = sqrtf(fmaf(lo, lo, hi * hi));
-            code[16 * part + i] = (unsigned char)polar_code<B>(psi, a.thr[0]);
+            rad[i] = fmaf(lo, lo, hi * hi);
+            code[16 * part + i] = (unsigned char)sector_code<B>(lo, hi);
         }
 #pragma unroll
         for (int l = 2; l <= 5; ++l) {
@@ -515,22 +545,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) polar_tc_kernel(const PolarTcAr
 #pragma unroll
             for (int i = 0; i < nodes; ++i) {
                 const float lo = rad[2 * i], hi = rad[2 * i + 1];
-                rad[i] = sqrtf(fmaf(lo, lo, hi * hi));
-                code[pos + i] = (unsigned char)polar_code<B>(atan2f(hi, lo), a.thr[l - 1]);
+                rad[i] = lo + hi;
+                code[pos + i] = (unsigned char)level_code<B>(lo, hi, a.tau[l - 2]);
             }
         }
         __syncthreads();   // every thread has read its x-norm partials
-        s_part[part * kTile + row] = rad[0];   // the level-5 radius of this quarter
+        s_part[part * kTile + row] = rad[0];   // the squared level-5 radius of this quarter
         __syncthreads();
         if (part == 0) {   // levels 6 and 7 of the row
             const float r5[4] = {s_part[row], s_part[kTile + row], s_part[2 * kTile + row], s_part[3 * kTile + row]};
-            float r6[2];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                r6[i] = sqrtf(fmaf(r5[2 * i], r5[2 * i], r5[2 * i + 1] * r5[2 * i + 1]));
-                code[124 + i] = (unsigned char)polar_code<B>(atan2f(r5[2 * i + 1], r5[2 * i]), a.thr[5]);
-            }
-            code[126] = (unsigned char)polar_code<B>(atan2f(r6[1], r6[0]), a.thr[6]);
+            for (int i = 0; i < 2; ++i) code[124 + i] = (unsigned char)level_code<B>(r5[2 * i], r5[2 * i + 1], a.tau[4]);
+            code[126] = (unsigned char)level_code<B>(r5[0] + r5[1], r5[2] + r5[3], a.tau[5]);
         }
         __syncthreads();   // the code stream of every row is complete
         // pack: word w holds stream bits 32 w .. 32 w + 31, stream bit t being bit t - B an of code
@@ -719,8 +745,8 @@ cudaError_t launch_polar_tc(const PolarTcLaunch& L, cudaStream_t s) {
     a.rnorm = L.rnorm;
     a.err = L.err;
     a.cw = L.cw;
-    for (int l = 0; l < kPolarTcLevels; ++l)
-        for (int t = 0; t < 15; ++t) a.thr[l][t] = L.thr[l][t];
+    for (int l = 0; l + 1 < kPolarTcLevels; ++l)
+        for (int t = 0; t < 15; ++t) a.tau[l][t] = L.tau[l][t];
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L.device);
     const int64_t ntiles = (L.n + kTile - 1) / kTile;

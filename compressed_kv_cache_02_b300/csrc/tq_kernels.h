@@ -28,8 +28,9 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
 
 // tcgen05 polar-angle encoder (bf16 rows, d = 128, 7 levels of angles), k_quantize_tc.cu.
 // bops: build_tc_operands(Pi, S Pi^T or NULL) on the device; cs: [7][32] floats, level l - 1 at
-// 32 (l - 1): the cosines of its 2^bits centroids, then at + 16 their sines; thr: per level the
-// 2^bits - 1 ascending thresholds.  Needs x 16-byte aligned and ld_x a multiple of 8.
+// 32 (l - 1): the cosines of its 2^bits centroids, then at + 16 their sines; tau: levels 2..7 (at
+// l - 2), tan^2 of the level's 2^bits - 1 ascending thresholds (level 1 is the uniform sectors).
+// Needs x 16-byte aligned and ld_x a multiple of 8.
 struct PolarTcLaunch {
     int device;
     const void* x;
@@ -37,7 +38,7 @@ struct PolarTcLaunch {
     const void* bops;
     const float* cs;
     int bits, qjl, cw;
-    float thr[7][15];
+    float tau[6][15];
     uint32_t* codes;
     uint16_t* r16;
     uint32_t* signs;
