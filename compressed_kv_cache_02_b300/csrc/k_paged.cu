@@ -84,7 +84,7 @@ struct PagedShared {
     float qs[4 * 128];
     float us[4 * 128];
     float x[128], y[128], r[128];
-    ulonglong2 sW[kPWarps][32][2];
+    ulonglong2 sW[kPWarps][32];   // per key: (w0, w1), (w2, w3)
     uint4 vbuf[kPWarps][2][32 * 4];   // per warp, double-buffered value rows (up to 4 planes)
     float4 s_wm[kPWarps], s_wl[kPWarps];
     float red[kPWarps];
@@ -248,9 +248,9 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
 #pragma unroll
     for (int pp = 0; pp < PV; ++pp) rot[pp] = ((lane & 7) - pp - 2) & 31;
     const unsigned char* cvb = reinterpret_cast<const unsigned char*>(s.cv);
-    u64 alo[4], ahi[4];   // head h: owned coordinates (0, 1) in alo[h], (2, 3) in ahi[h]
+    u64 acc[4][2];   // owned coordinate c: heads (0, 1) in acc[c][0], (2, 3) in acc[c][1]
 #pragma unroll
-    for (int h = 0; h < 4; ++h) alo[h] = ahi[h] = 0ull;
+    for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = 0ull;
     float4 m4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4 ls = make_float4(0.f, 0.f, 0.f, 0.f);
     const int nblk = (k_hi - k_lo + 31) / 32;
@@ -305,19 +305,17 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
             const float4 al = make_float4(rescale(m4.x, mn.x), rescale(m4.y, mn.y), rescale(m4.z, mn.z), rescale(m4.w, mn.w));
             m4 = mn;
             ls = make_float4(ls.x * al.x, ls.y * al.y, ls.z * al.z, ls.w * al.w);
-            const float av[4] = {al.x, al.y, al.z, al.w};
+            const u64 a01 = pk2(al.x, al.y), a23 = pk2(al.z, al.w);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const u64 ap = pk2(av[h], av[h]);
-                alo[h] = mul2(alo[h], ap);
-                ahi[h] = mul2(ahi[h], ap);
+            for (int c = 0; c < 4; ++c) {
+                acc[c][0] = mul2(acc[c][0], a01);
+                acc[c][1] = mul2(acc[c][1], a23);
             }
         }
         const float4 pr = make_float4(safe_exp(l4.x, m4.x), safe_exp(l4.y, m4.y), safe_exp(l4.z, m4.z), safe_exp(l4.w, m4.w));
         ls = f4_add(ls, pr);
         const float4 w = f4_scale(vn, pr);
-        s.sW[warp][lane][0] = make_ulonglong2(pk2(w.x, w.x), pk2(w.y, w.y));
-        s.sW[warp][lane][1] = make_ulonglong2(pk2(w.z, w.z), pk2(w.w, w.w));
+        s.sW[warp][lane] = make_ulonglong2(pk2(w.x, w.y), pk2(w.z, w.w));
         size_t row0 = 0;
         const bool have = slot_of(a, b, k_lo + j * 32, kvh, row0);
         const int nk = min(32, k_hi - (k_lo + j * 32));
@@ -333,19 +331,15 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
                     const uint32_t wd = vr[pp * 4 + wsel];
                     z |= __funnelshift_r(wd, wd, rot[pp]) & (0x04040404u << pp);
                 }
-                const u64 v01 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4440)),
-                                    *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4441)));
-                const u64 v23 = pk2(*reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4442)),
-                                    *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4443)));
-                const ulonglong2 wa = s.sW[warp][t][0], wb = s.sW[warp][t][1];
-                alo[0] = fma2(v01, wa.x, alo[0]);
-                ahi[0] = fma2(v23, wa.x, ahi[0]);
-                alo[1] = fma2(v01, wa.y, alo[1]);
-                ahi[1] = fma2(v23, wa.y, ahi[1]);
-                alo[2] = fma2(v01, wb.x, alo[2]);
-                ahi[2] = fma2(v23, wb.x, ahi[2]);
-                alo[3] = fma2(v01, wb.y, alo[3]);
-                ahi[3] = fma2(v23, wb.y, ahi[3]);
+                // the centroid of owned coordinate c doubled, against the head pairs' weights
+                const ulonglong2 wv = s.sW[warp][t];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float cv = *reinterpret_cast<const float*>(cvb + __byte_perm(z, 0u, 0x4440 + c));
+                    const u64 cc = pk2(cv, cv);
+                    acc[c][0] = fma2(cc, wv.x, acc[c][0]);
+                    acc[c][1] = fma2(cc, wv.y, acc[c][1]);
+                }
             }
         }
         __syncwarp();   // sW and this buffer are reused
@@ -363,13 +357,10 @@ __device__ void attend_chunk(const PagedArgs& a, PagedShared& s, int b, int kvh,
     for (int w = 1; w < kPWarps; ++w) M = f4_max(M, s.s_wm[w]);
     const float4 sc = make_float4(rescale(m4.x, M.x), rescale(m4.y, M.y), rescale(m4.z, M.z), rescale(m4.w, M.w));
     float4* red = s.Tq;   // [warps][4 coordinates][32 lanes]
-    {
-        const float2 a0 = upk2(alo[0]), a1 = upk2(alo[1]), a2 = upk2(alo[2]), a3 = upk2(alo[3]);
-        const float2 b0 = upk2(ahi[0]), b1 = upk2(ahi[1]), b2 = upk2(ahi[2]), b3 = upk2(ahi[3]);
-        red[(warp * 4 + 0) * 32 + lane] = make_float4(a0.x * sc.x, a1.x * sc.y, a2.x * sc.z, a3.x * sc.w);
-        red[(warp * 4 + 1) * 32 + lane] = make_float4(a0.y * sc.x, a1.y * sc.y, a2.y * sc.z, a3.y * sc.w);
-        red[(warp * 4 + 2) * 32 + lane] = make_float4(b0.x * sc.x, b1.x * sc.y, b2.x * sc.z, b3.x * sc.w);
-        red[(warp * 4 + 3) * 32 + lane] = make_float4(b0.y * sc.x, b1.y * sc.y, b2.y * sc.z, b3.y * sc.w);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float2 h01 = upk2(acc[c][0]), h23 = upk2(acc[c][1]);
+        red[(warp * 4 + c) * 32 + lane] = make_float4(h01.x * sc.x, h01.y * sc.y, h23.x * sc.z, h23.y * sc.w);
     }
     __syncthreads();
     if (threadIdx.x < 128) {
