@@ -370,6 +370,281 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
     if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
 }
 
+// ---------------------------------------------------------------- two tiles in flight
+// The same arithmetic as quantize_tc_kernel (ordinary contexts), with the CTA split into two
+// groups of 8 warps that each take every other tile, so one group's CUDA-core epilogue runs while
+// the other group's MMAs do.  Per group: one x buffer (the next tile's rows are copied into it as
+// soon as the current tile's Y = X Pi^T is done), a 128-column accumulator D (Y, then Z) and a
+// 128-column A operand in tensor memory holding r' as bf16 hi (columns 0..63) and lo (64..127),
+// so the projection Z = r' (S Pi^T)^T reads A from tensor memory (kind::f16, A in TMEM) and no
+// shared-memory r' buffer is needed; the two groups use all 512 columns.  Warp w of group g owns
+// TMEM lanes 32 (w % 4).. (rows) and coordinates 64 (w / 4 % 2).. in two passes of 32.
+constexpr int kTc2Groups = 2;
+constexpr int kTc2GThreads = kTcThreads / kTc2Groups;   // 256
+constexpr uint32_t kSmemTc2 = kSmemB + kTc2Groups * kMatBytes + kTc2Groups * 4 * kTile * sizeof(float);
+
+__device__ __forceinline__ bool group_and(bool v, int id) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "n"(kTc2GThreads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(db), "r"(kIdesc), "r"(accumulate));
+}
+
+// D = (A_hi + A_lo) (B_0 + B_1)^T, A in tensor memory (8 columns per K-step of 16), B in shared memory.
+__device__ __forceinline__ void issue_pieces_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr) {
+    const uint64_t db = smem_desc(b_saddr);
+#pragma unroll 1
+    for (int ap = 0; ap < 2; ++ap)
+#pragma unroll 1
+        for (int p = 0; p < kPieces; ++p)
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_bf16_ts(d_tmem, a_tmem + 64 * ap + 8 * s, db + (uint64_t)((p * kMatBytes + s * 256) >> 4),
+                            (ap > 0 || p > 0 || s > 0) ? 1u : 0u);
+}
+
+// The x rows of `tile` into sXg (cp.async by the group's threads, zeros beyond n), one commit group.
+__device__ __forceinline__ void stage_x_group(const TcArgs& a, int tile, unsigned char* sXg, int gtid) {
+    const int64_t r0 = (int64_t)tile * kTile;
+    const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+    for (int e = gtid; e < kTile * 16; e += kTc2GThreads) {
+        const int r = e >> 4, kc = e & 15;
+        unsigned char* dst = sXg + kmajor_off(r, 8 * kc);
+        if (r < nvalid) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;");
+}
+
+template <int P>
+__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArgs a) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    __shared__ __align__(8) uint64_t mbar[kTc2Groups], s_drain[kTc2Groups];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_drained;
+    __shared__ float s_thr[kMaxLevels], s_cen[kMaxLevels];
+    const Params& prm = a.prm;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = warp >> 3, gw = warp & 7, q = gw & 3, hh = gw >> 2, gtid = tid & (kTc2GThreads - 1);
+    const int row = 32 * q + lane, bar_id = 1 + g;
+    const bool leader = gtid == 0;
+    unsigned char* sB = sm;
+    unsigned char* sX = sm + kSmemB + g * kMatBytes;
+    float* s_xn = reinterpret_cast<float*>(sm + kSmemB + kTc2Groups * kMatBytes) + g * 4 * kTile;   // [2][128]
+    float* s_rs = s_xn + 2 * kTile;                                                                  // [2][128]
+    const int ntiles = (int)((a.n + kTile - 1) / kTile);
+    if (tid < kMaxLevels) {
+        s_thr[tid] = prm.thresholds[tid];
+        s_cen[tid] = prm.centroids[tid];
+    }
+    for (int e = tid; e < (int)((prm.qjl ? kSmemB : kSmemB / 2) / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
+    asm volatile("cp.async.commit_group;");
+    int tile = kTc2Groups * blockIdx.x + g;
+    if (tile < ntiles) stage_x_group(a, tile, sX, gtid);
+    else asm volatile("cp.async.commit_group;");   // an empty group keeps the wait counts alike
+    if (tid == 0) {
+        for (int i = 0; i < kTc2Groups; ++i) {
+            tc::mbar_init(&mbar[i], 1);
+            tc::mbar_init(&s_drain[i], 1);
+        }
+        s_drained = 1;
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc<512>(&s_tmem);
+    asm volatile("cp.async.wait_group 1;");   // this thread's share of the B operands has landed
+    asm volatile("fence.proxy.async.shared::cta;");
+    tc::fence_before();
+    __syncthreads();   // both groups' shares: the B operands are whole before either group's MMAs
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t d_col = tmem + 256 * g, a_col = d_col + 128;
+    const uint32_t d_row = d_col + lane_off, a_row = a_col + lane_off;
+    uint32_t phase = 0;
+    bool ok = true;
+
+    for (; tile < ntiles && ok; tile += kTc2Groups * gridDim.x) {
+        const int64_t r0 = (int64_t)tile * kTile;
+        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
+        asm volatile("cp.async.wait_group 0;");   // this tile's rows (and, at first, the B operands)
+        asm volatile("fence.proxy.async.shared::cta;");
+        tc::fence_before();
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");
+        tc::fence_after();
+        if (leader) {   // phase 1: Y = X Pi^T
+            issue_pieces(d_col, tc::smem_u32(sX), tc::smem_u32(sB), false);
+            tc::commit(&mbar[g]);
+        }
+        {   // ||x||^2 partial over this thread's 64 coordinates while the MMAs run
+            float xs = 0.f;
+#pragma unroll
+            for (int kc = 0; kc < 8; ++kc) {
+                const uint4 w = *reinterpret_cast<const uint4*>(sX + kmajor_off(row, 64 * hh + 8 * kc));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
+                    xs = fmaf(lo, lo, xs);
+                    xs = fmaf(hi, hi, xs);
+                }
+            }
+            s_xn[hh * kTile + row] = xs;
+        }
+        ok = group_and(tc::mbar_wait(&mbar[g], phase), bar_id);   // also: the x reads are done
+        phase ^= 1u;
+        if (!ok) break;
+        tc::fence_after();
+        const int next = tile + kTc2Groups * gridDim.x;
+        if (next < ntiles) stage_x_group(a, next, sX, gtid);   // lands while this tile finishes
+        const float nrm = sqrtf(s_xn[row] + s_xn[kTile + row]);
+        const float n16 = half_bits_to_float(float_to_half_bits(nrm));
+        const float nv = nrm > 0.f ? nrm : 1.f;
+        const int64_t grow = r0 + row;
+        const bool valid = row < nvalid;
+        float rs = 0.f;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int part = 2 * hh + pass;
+            float y[32];
+            load_row_part(d_row, part, y);
+            uint32_t pw[kFastBits] = {};
+            if constexpr (P <= 3) {
+                constexpr int NT = (1 << P) - 1;
+                float ts[NT], cv[NT + 1];
+#pragma unroll
+                for (int k = 0; k < NT; ++k) ts[k] = s_thr[k] * nv;
+#pragma unroll
+                for (int k = 0; k <= NT; ++k) cv[k] = s_cen[k];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    float cen;
+                    if constexpr (P == 1) {
+                        const bool up = yc > ts[0];
+                        pw[0] |= (up ? 1u : 0u) << c;
+                        cen = up ? cv[1] : cv[0];
+                    } else if constexpr (P == 2) {
+                        const bool u1 = yc > ts[1];
+                        const bool u0 = yc > (u1 ? ts[2] : ts[0]);
+                        pw[1] |= (u1 ? 1u : 0u) << c;
+                        pw[0] |= (u0 ? 1u : 0u) << c;
+                        cen = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
+                    } else {
+                        const bool u2 = yc > ts[3];
+                        const bool u1 = yc > (u2 ? ts[5] : ts[1]);
+                        const float t0 = u2 ? (u1 ? ts[6] : ts[4]) : (u1 ? ts[2] : ts[0]);
+                        const bool u0 = yc > t0;
+                        pw[2] |= (u2 ? 1u : 0u) << c;
+                        pw[1] |= (u1 ? 1u : 0u) << c;
+                        pw[0] |= (u0 ? 1u : 0u) << c;
+                        const float clo = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
+                        const float chi = u1 ? (u0 ? cv[7] : cv[6]) : (u0 ? cv[5] : cv[4]);
+                        cen = u2 ? chi : clo;
+                    }
+                    const float r = y[c] - n16 * cen;
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    int idx = 0;
+#pragma unroll
+                    for (int b = P - 1; b >= 0; --b) {
+                        const int k = idx + (1 << b) - 1;
+                        const bool up = yc > s_thr[k] * nv;
+                        idx += up ? (1 << b) : 0;
+                        pw[b] |= (up ? 1u : 0u) << c;
+                    }
+                    const float r = y[c] - n16 * s_cen[idx];
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+            }
+            if (valid) {
+#pragma unroll
+                for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+            }
+            if (prm.qjl) {   // r' as bf16 hi and lo into the A operand
+                uint32_t h[16], l[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __nv_bfloat162 hp = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+                    h[i] = *reinterpret_cast<const uint32_t*>(&hp);
+                    const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xffff0000u);
+                    const __nv_bfloat162 lp = __floats2bfloat162_rn(y[2 * i] - h0, y[2 * i + 1] - h1);
+                    l[i] = *reinterpret_cast<const uint32_t*>(&lp);
+                }
+                tc::tmem_st16(a_row + 16 * part, h);
+                tc::tmem_st16(a_row + 64 + 16 * part, l);
+            }
+        }
+        if (!prm.qjl) {   // MSE mode: no residual sketch
+            if (valid && hh == 0) {
+                const uint16_t nh = float_to_half_bits(nrm);
+                a.norm[grow] = nh;
+                if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+            }
+            tc::fence_before();
+            continue;   // the next iteration's group barrier orders these TMEM reads before its MMAs
+        }
+        s_rs[hh * kTile + row] = rs;
+        tc::wait_st();
+        tc::fence_before();
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");   // Y read, A written
+        if (leader) {   // phase 2: Z = r' (S Pi^T)^T, A from tensor memory
+            tc::fence_after();
+            issue_pieces_ta(d_col, a_col, tc::smem_u32(sB) + kPieces * kMatBytes);
+            tc::commit(&mbar[g]);
+        }
+        ok = group_and(tc::mbar_wait(&mbar[g], phase), bar_id);
+        phase ^= 1u;
+        if (!ok) break;
+        tc::fence_after();
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int part = 2 * hh + pass;
+            float z[32];
+            load_row_part(d_row, part, z);
+            uint32_t sw = 0u;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
+            if (valid) a.signs[(size_t)grow * 4 + part] = sw;
+        }
+        if (valid && hh == 0) {
+            const uint16_t nh = float_to_half_bits(nrm);
+            const uint16_t rh = float_to_half_bits(sqrtf(s_rs[row] + s_rs[kTile + row]));
+            a.norm[grow] = nh;
+            a.rnorm[grow] = rh;
+            if (__hisinf(__ushort_as_half(nh)) || __hisinf(__ushort_as_half(rh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
+        }
+        tc::fence_before();
+    }
+    asm volatile("cp.async.wait_all;");
+    if (!ok) {   // a wait ran out: flag it, and let every MMA this group issued finish (bounded)
+        if (leader) {
+            set_error(a.err, TQ_DEVERR_TIMEOUT);
+            tc::commit(&s_drain[g]);
+        }
+        if (!group_and(!leader || tc::mbar_wait(&s_drain[g], 0u), bar_id) && leader) s_drained = 0;
+    }
+    tc::fence_before();
+    __syncthreads();
+    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
+    if (warp == 0 && s_drained) tc::tmem_dealloc<512>(tmem);
+}
+
 // ---------------------------------------------------------------- polar-angle encoder
 // The recursive polar encoder (k_polar.cu; csdn tutorial, section 将笛卡尔积坐标转为极坐标, and
 // freelamp article, section 技术突破：极坐标量化) with its two d x d products on the tensor cores, for
@@ -718,12 +993,21 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
         kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
         return cudaSuccess;
     };
+    // ordinary contexts: two tiles in flight per CTA (quantize_tc2_kernel)
+    const int64_t pairs = (ntiles + kTc2Groups - 1) / kTc2Groups;
+    const int grid2 = (int)(pairs < sms ? pairs : sms);
+    auto run2 = [&](auto kernel) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc2);
+        if (e2 != cudaSuccess) return e2;
+        kernel<<<grid2, kTcThreads, kSmemTc2, s>>>(a);
+        return cudaSuccess;
+    };
     cudaError_t e = cudaErrorInvalidValue;
     if (c->prm.d_hi > 0) e = run(quantize_tc_kernel<0, true>);
-    else if (c->prm.P == 1) e = run(quantize_tc_kernel<1, false>);
-    else if (c->prm.P == 2) e = run(quantize_tc_kernel<2, false>);
-    else if (c->prm.P == 3) e = run(quantize_tc_kernel<3, false>);
-    else if (c->prm.P == 4) e = run(quantize_tc_kernel<4, false>);
+    else if (c->prm.P == 1) e = run2(quantize_tc2_kernel<1>);
+    else if (c->prm.P == 2) e = run2(quantize_tc2_kernel<2>);
+    else if (c->prm.P == 3) e = run2(quantize_tc2_kernel<3>);
+    else if (c->prm.P == 4) e = run2(quantize_tc2_kernel<4>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
