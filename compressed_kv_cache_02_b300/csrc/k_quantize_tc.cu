@@ -426,7 +426,12 @@ __device__ __forceinline__ void stage_x_group(const TcArgs& a, int tile, unsigne
     asm volatile("cp.async.commit_group;");
 }
 
-template <int P>
+// SYM: the table is odd-symmetric (c_k = -c_{2^P-1-k}, so t_k = -t_{2^P-2-k} and the middle
+// threshold is 0).  For P = 2, 3 the code is then decided as a sign (y > 0) and magnitude bits of
+// |y| against the upper half of the table; on the negative side the lower code bits are the
+// magnitude bits inverted (the bins mirror), applied to whole plane words.  The decisions agree
+// with the ordered comparisons except where |y| equals a threshold exactly.
+template <int P, bool SYM>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ __align__(8) uint64_t mbar[kTc2Groups], s_drain[kTc2Groups];
@@ -518,7 +523,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
             float y[32];
             load_row_part(d_row, part, y);
             uint32_t pw[kFastBits] = {};
-            if constexpr (P <= 3) {
+            if constexpr (SYM && (P == 2 || P == 3)) {
+                constexpr int H = 1 << (P - 1);   // first index of the upper half
+                float ts[H - 1], cm[H];
+#pragma unroll
+                for (int k = 0; k + 1 < H; ++k) ts[k] = s_thr[H + k] * nv;
+#pragma unroll
+                for (int k = 0; k < H; ++k) cm[k] = s_cen[H + k];
+                uint32_t mw[2] = {0u, 0u};   // magnitude bits (lower code bits on the positive side)
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    const float av = fabsf(yc);
+                    const bool up = yc > 0.f;
+                    pw[P - 1] |= (up ? 1u : 0u) << c;
+                    float mag;
+                    if constexpr (P == 2) {
+                        const bool m0 = av > ts[0];
+                        mw[0] |= (m0 ? 1u : 0u) << c;
+                        mag = m0 ? cm[1] : cm[0];
+                    } else {
+                        const bool m1 = av > ts[1];
+                        const bool m0 = av > (m1 ? ts[2] : ts[0]);
+                        mw[1] |= (m1 ? 1u : 0u) << c;
+                        mw[0] |= (m0 ? 1u : 0u) << c;
+                        mag = m1 ? (m0 ? cm[3] : cm[2]) : (m0 ? cm[1] : cm[0]);
+                    }
+                    const float r = y[c] - n16 * (up ? mag : -mag);
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+#pragma unroll
+                for (int p = 0; p + 1 < P; ++p) pw[p] = mw[p] ^ ~pw[P - 1];
+            } else if constexpr (P <= 3) {
                 constexpr int NT = (1 << P) - 1;
                 float ts[NT], cv[NT + 1];
 #pragma unroll
@@ -1003,11 +1040,12 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
         return cudaSuccess;
     };
     cudaError_t e = cudaErrorInvalidValue;
+    const bool sym = c->prm.odd_walsh != 0;
     if (c->prm.d_hi > 0) e = run(quantize_tc_kernel<0, true>);
-    else if (c->prm.P == 1) e = run2(quantize_tc2_kernel<1>);
-    else if (c->prm.P == 2) e = run2(quantize_tc2_kernel<2>);
-    else if (c->prm.P == 3) e = run2(quantize_tc2_kernel<3>);
-    else if (c->prm.P == 4) e = run2(quantize_tc2_kernel<4>);
+    else if (c->prm.P == 1) e = run2(quantize_tc2_kernel<1, false>);
+    else if (c->prm.P == 2) e = sym ? run2(quantize_tc2_kernel<2, true>) : run2(quantize_tc2_kernel<2, false>);
+    else if (c->prm.P == 3) e = sym ? run2(quantize_tc2_kernel<3, true>) : run2(quantize_tc2_kernel<3, false>);
+    else if (c->prm.P == 4) e = run2(quantize_tc2_kernel<4, false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
