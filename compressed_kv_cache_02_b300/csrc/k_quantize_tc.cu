@@ -531,25 +531,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
 #pragma unroll
                 for (int k = 0; k < H; ++k) cm[k] = s_cen[H + k];
                 uint32_t mw[2] = {0u, 0u};   // magnitude bits (lower code bits on the positive side)
+                // Each decision a > b is the sign bit of b - a (exact in sign; +0 on a tie), shifted
+                // into its plane word from the top, coordinate 31 first.
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 31; c >= 0; --c) {
                     const float yc = nrm > 0.f ? y[c] : 0.f;
                     const float av = fabsf(yc);
-                    const bool up = yc > 0.f;
-                    pw[P - 1] |= (up ? 1u : 0u) << c;
+                    const float dz = 0.f - yc;   // negative iff yc > 0 (+0 for yc = +-0)
+                    pw[P - 1] = __funnelshift_l(__float_as_uint(dz), pw[P - 1], 1);
                     float mag;
                     if constexpr (P == 2) {
-                        const bool m0 = av > ts[0];
-                        mw[0] |= (m0 ? 1u : 0u) << c;
-                        mag = m0 ? cm[1] : cm[0];
+                        const float d0 = ts[0] - av;
+                        mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                        mag = d0 < 0.f ? cm[1] : cm[0];
                     } else {
-                        const bool m1 = av > ts[1];
-                        const bool m0 = av > (m1 ? ts[2] : ts[0]);
-                        mw[1] |= (m1 ? 1u : 0u) << c;
-                        mw[0] |= (m0 ? 1u : 0u) << c;
+                        const float d1 = ts[1] - av;
+                        const bool m1 = d1 < 0.f;
+                        const float d0 = (m1 ? ts[2] : ts[0]) - av;
+                        mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
+                        mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                        const bool m0 = d0 < 0.f;
                         mag = m1 ? (m0 ? cm[3] : cm[2]) : (m0 ? cm[1] : cm[0]);
                     }
-                    const float r = y[c] - n16 * (up ? mag : -mag);
+                    // y - n16 c with c = +mag for yc > 0, -mag otherwise: -c carries the sign of dz
+                    const float r = fmaf(n16, copysignf(mag, dz), y[c]);
                     y[c] = r;
                     rs = fmaf(r, r, rs);
                 }
