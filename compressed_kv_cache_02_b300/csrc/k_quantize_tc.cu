@@ -659,9 +659,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
             const int part = 2 * hh + pass;
             float z[32];
             load_row_part(d_row, part, z);
-            uint32_t sw = 0u;
+            uint32_t sw = 0u;   // bit c = [z_c > 0]: the sign bit of 0 - z_c (+0 for z_c = +-0)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
+            for (int c = 31; c >= 0; --c) sw = __funnelshift_l(__float_as_uint(0.f - z[c]), sw, 1);
             if (valid) a.signs[(size_t)grow * 4 + part] = sw;
         }
         if (valid && hh == 0) {
