@@ -427,7 +427,7 @@ __device__ __forceinline__ void stage_x_group(const TcArgs& a, int tile, unsigne
 }
 
 // SYM: the table is odd-symmetric (c_k = -c_{2^P-1-k}, so t_k = -t_{2^P-2-k} and the middle
-// threshold is 0).  For P = 2, 3 the code is then decided as a sign (y > 0) and magnitude bits of
+// threshold is 0).  The code is then decided as a sign (y > 0) and magnitude bits of
 // |y| against the upper half of the table; on the negative side the lower code bits are the
 // magnitude bits inverted (the bins mirror), applied to whole plane words.  The decisions agree
 // with the ordered comparisons except where |y| equals a threshold exactly.
@@ -523,7 +523,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
             float y[32];
             load_row_part(d_row, part, y);
             uint32_t pw[kFastBits] = {};
-            if constexpr (SYM && (P == 2 || P == 3)) {
+            if constexpr (SYM && P == 1) {   // the threshold is 0: the code is the sign
+                const float cm = s_cen[1];
+#pragma unroll
+                for (int c = 31; c >= 0; --c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    const float dz = 0.f - yc;   // negative iff yc > 0 (+0 for yc = +-0)
+                    pw[0] = __funnelshift_l(__float_as_uint(dz), pw[0], 1);
+                    const float r = fmaf(n16, copysignf(cm, dz), y[c]);
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+            } else if constexpr (SYM && P == 4) {   // sign, then 3 magnitude bits by binary search
+                float ts[7];
+#pragma unroll
+                for (int k = 0; k < 7; ++k) ts[k] = s_thr[8 + k] * nv;
+                uint32_t mw[3] = {0u, 0u, 0u};
+#pragma unroll
+                for (int c = 31; c >= 0; --c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    const float av = fabsf(yc);
+                    const float dz = 0.f - yc;
+                    pw[3] = __funnelshift_l(__float_as_uint(dz), pw[3], 1);
+                    const float d2 = ts[3] - av;
+                    const bool m2 = d2 < 0.f;
+                    const float d1 = (m2 ? ts[5] : ts[1]) - av;
+                    const bool m1 = d1 < 0.f;
+                    const float d0 = (m2 ? (m1 ? ts[6] : ts[4]) : (m1 ? ts[2] : ts[0])) - av;
+                    const bool m0 = d0 < 0.f;
+                    mw[2] = __funnelshift_l(__float_as_uint(d2), mw[2], 1);
+                    mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
+                    mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                    const float mag = s_cen[8 + (m2 ? 4 : 0) + (m1 ? 2 : 0) + (m0 ? 1 : 0)];
+                    const float r = fmaf(n16, copysignf(mag, dz), y[c]);
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+#pragma unroll
+                for (int p = 0; p < 3; ++p) pw[p] = mw[p] ^ ~pw[3];
+            } else if constexpr (SYM && (P == 2 || P == 3)) {
                 constexpr int H = 1 << (P - 1);   // first index of the upper half
                 float ts[H - 1], cm[H];
 #pragma unroll
@@ -1047,10 +1085,10 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     cudaError_t e = cudaErrorInvalidValue;
     const bool sym = c->prm.odd_walsh != 0;
     if (c->prm.d_hi > 0) e = run(quantize_tc_kernel<0, true>);
-    else if (c->prm.P == 1) e = run2(quantize_tc2_kernel<1, false>);
+    else if (c->prm.P == 1) e = sym ? run2(quantize_tc2_kernel<1, true>) : run2(quantize_tc2_kernel<1, false>);
     else if (c->prm.P == 2) e = sym ? run2(quantize_tc2_kernel<2, true>) : run2(quantize_tc2_kernel<2, false>);
     else if (c->prm.P == 3) e = sym ? run2(quantize_tc2_kernel<3, true>) : run2(quantize_tc2_kernel<3, false>);
-    else if (c->prm.P == 4) e = run2(quantize_tc2_kernel<4, false>);
+    else if (c->prm.P == 4) e = sym ? run2(quantize_tc2_kernel<4, true>) : run2(quantize_tc2_kernel<4, false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

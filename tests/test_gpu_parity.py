@@ -52,7 +52,7 @@ def test_quantize_bf16_anisotropic(bits):
     assert same.mean() > 0.99
 
 
-@pytest.mark.parametrize("mode,bits", [(0, 3), (0, 4), (0, 5), (1, 3), (1, 4)])
+@pytest.mark.parametrize("mode,bits", [(0, 2), (0, 3), (0, 4), (0, 5), (1, 1), (1, 2), (1, 3), (1, 4)])
 @pytest.mark.parametrize("n,ld", [(4096, 128), (5003, 128), (4500, 136)])
 def test_quantize_bulk_bf16(mode, bits, n, ld, kernel_path):
     """Bulk bf16 rows at d=128: tcgen05 tensor-core path (n >= 4096) and CUDA-core path."""
