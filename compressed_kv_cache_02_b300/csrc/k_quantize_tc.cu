@@ -13,13 +13,14 @@
 //                                accumulator), B = S Pi^T as 2 bf16 pieces (z moves by ~2e-6 of
 //                                ||x||, inside the 1e-5 band of the sign rule); sign_j = [z_j > 0].
 // Pi and S Pi^T stay resident in shared memory (4 x 32 KB), so one CTA per SM walks the tiles of
-// 128 rows.  The next tile's x rows are copied (cp.async) into the second of two x buffers while
-// the current tile runs, so the copy overlaps the MMAs and the epilogues.  Operands use the
-// K-major no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix; LBO = 128 B between
-// core matrices along K, SBO = 2048 B between 8-row groups).  Warps w, w+4, w+8, w+12 share TMEM
-// lanes 32(w%4)..+31 (rows) and split each row's 128 coordinates in quarters of 32, one bit-plane
-// word each.  One thread issues the MMAs; tcgen05.commit signals an mbarrier whose waits are
-// bounded in time (TQ_DEVERR_TIMEOUT).
+// 128 rows.  Ordinary contexts (quantize_tc2_kernel) and the polar encoder (polar_tc2_kernel) run
+// two 8-warp groups per CTA, each on its own tile with its own x buffer and TMEM accumulator, r'
+// held in tensor memory as the phase-2 A operand, so one group's epilogue overlaps the other's
+// MMAs.  Split contexts (quantize_tc_split_kernel) walk one tile at a time with all 16 warps, r'
+// staged in shared memory.  Operands in shared memory use the K-major no-swizzle
+// core-matrix layout (8 rows x 16 bytes per core matrix; LBO = 128 B between core matrices along
+// K, SBO = 2048 B between 8-row groups).  One thread per group issues the MMAs; tcgen05.commit
+// signals an mbarrier whose waits are bounded in time (TQ_DEVERR_TIMEOUT).
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -127,10 +128,9 @@ __device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char
     asm volatile("cp.async.commit_group;");
 }
 
-// P: MSE bits of an ordinary context, known at compile time (0 for split contexts, whose width per
-// coordinate word is P or P + 1 at run time).
-template <int P, bool SPLIT>
-__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs a) {
+// Split (fractional bit width) contexts, whose width per coordinate word is P or P + 1 at run time:
+// one tile at a time per CTA, 4 threads per row; ordinary contexts take quantize_tc2_kernel below.
+__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_split_kernel(const TcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];   // no-swizzle operands need 16-byte alignment
     unsigned char* sB = sm;
     unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]
@@ -217,11 +217,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
         // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (one step per bit, the
         // step for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
         const float nv = nrm > 0.f ? nrm : 1.f;
-        // split contexts: this thread's 32 coordinates (one word) are below d_hi or not as a whole
-        const bool hi = SPLIT && 32 * part < prm.d_hi;   // ordinary contexts: false at compile time
+        // this thread's 32 coordinates (one word) are below d_hi or not as a whole
+        const bool hi = 32 * part < prm.d_hi;
         uint32_t pw[kFastBits] = {};
         float rs = 0.f;
-        if constexpr (SPLIT) {
+        {
             const int nb = prm.P + (hi ? 1 : 0);
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -239,72 +239,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
                 y[c] = r;
                 rs = fmaf(r, r, rs);
             }
-        } else if constexpr (P <= 3) {
-            // the 1, 3 or 7 thresholds (times the norm: the same rounded products as t_k * n) and the
-            // centroids in registers
-            constexpr int NT = (1 << P) - 1;
-            float ts[NT], cv[NT + 1];
-#pragma unroll
-            for (int k = 0; k < NT; ++k) ts[k] = s_thr[k] * nv;
-#pragma unroll
-            for (int k = 0; k <= NT; ++k) cv[k] = s_cen[k];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float yc = nrm > 0.f ? y[c] : 0.f;
-                float cen;
-                if constexpr (P == 1) {
-                    const bool up = yc > ts[0];
-                    pw[0] |= (up ? 1u : 0u) << c;
-                    cen = up ? cv[1] : cv[0];
-                } else if constexpr (P == 2) {
-                    const bool u1 = yc > ts[1];
-                    const bool u0 = yc > (u1 ? ts[2] : ts[0]);
-                    pw[1] |= (u1 ? 1u : 0u) << c;
-                    pw[0] |= (u0 ? 1u : 0u) << c;
-                    cen = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
-                } else {
-                    const bool u2 = yc > ts[3];
-                    const bool u1 = yc > (u2 ? ts[5] : ts[1]);
-                    const float t0 = u2 ? (u1 ? ts[6] : ts[4]) : (u1 ? ts[2] : ts[0]);
-                    const bool u0 = yc > t0;
-                    pw[2] |= (u2 ? 1u : 0u) << c;
-                    pw[1] |= (u1 ? 1u : 0u) << c;
-                    pw[0] |= (u0 ? 1u : 0u) << c;
-                    const float clo = u1 ? (u0 ? cv[3] : cv[2]) : (u0 ? cv[1] : cv[0]);
-                    const float chi = u1 ? (u0 ? cv[7] : cv[6]) : (u0 ? cv[5] : cv[4]);
-                    cen = u2 ? chi : clo;
-                }
-                const float r = y[c] - n16 * cen;
-                y[c] = r;
-                rs = fmaf(r, r, rs);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float yc = nrm > 0.f ? y[c] : 0.f;
-                int idx = 0;
-#pragma unroll
-                for (int b = P - 1; b >= 0; --b) {
-                    const int k = idx + (1 << b) - 1;
-                    const bool up = yc > s_thr[k] * nv;
-                    idx += up ? (1 << b) : 0;
-                    pw[b] |= (up ? 1u : 0u) << c;
-                }
-                const float r = y[c] - n16 * s_cen[idx];
-                y[c] = r;
-                rs = fmaf(r, r, rs);
-            }
         }
         if (valid) {
-            if constexpr (SPLIT) {
-                for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
-                if (hi) {
-                    const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
-                    a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
-                }
-            } else {
-#pragma unroll
-                for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+            if (hi) {
+                const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
+                a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
             }
         }
         if (!prm.qjl) {   // MSE mode: no residual sketch
@@ -371,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_kernel(const TcArgs
 }
 
 // ---------------------------------------------------------------- two tiles in flight
-// The same arithmetic as quantize_tc_kernel (ordinary contexts), with the CTA split into two
+// The same arithmetic as quantize_tc_split_kernel for ordinary contexts, with the CTA split into two
 // groups of 8 warps that each take every other tile, so one group's CUDA-core epilogue runs while
 // the other group's MMAs do.  Per group: one x buffer (the next tile's rows are copied into it as
 // soon as the current tile's Y = X Pi^T is done), a 128-column accumulator D (Y, then Z) and a
@@ -729,9 +669,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
 // The recursive polar encoder (k_polar.cu; csdn tutorial, section 将笛卡尔积坐标转为极坐标, and
 // freelamp article, section 技术突破：极坐标量化) with its two d x d products on the tensor cores, for
 // bf16 rows at d = 128 (7 levels, 127 angles): phase 1 Y = X Pi^T as above; the epilogue runs the
-// polar transform — each thread's 32 consecutive coordinates are the subtree of one level-5 node,
-// so levels 1-5 are thread-local and one thread per row combines the 4 level-5 radii into levels 6
-// and 7 — codes each angle against its level's thresholds, packs the code stream, rebuilds y_hat
+// polar transform — each 32 consecutive coordinates are the subtree of one level-5 node, so levels
+// 1-5 are thread-local and one thread per row combines the 4 level-5 radii into levels 6 and 7 —
+// codes each angle against its level's thresholds, packs the code stream, rebuilds y_hat
 // top-down from the stored fp16 radius and the centroids' cos / sin, and with QJL projects
 // r' = y - y_hat as in phase 2 above (r = Pi^T r', so S r = (S Pi^T) r').
 // The angle codes need neither the angles nor the radii themselves: a level-1 code is the index of
@@ -791,133 +731,144 @@ __device__ __forceinline__ int level_code(float Rlo, float Rhi, const float* tau
     return c;
 }
 
+// The polar encoder runs two tiles in flight per CTA, as quantize_tc2_kernel: two 8-warp groups,
+// each with its own x buffer, accumulator D and A operand (r' hi and lo) in tensor memory.  A
+// thread owns 64 coordinates of its row (two level-5 subtrees, taken in two passes); the thread
+// holding the row's first half adds levels 6 and 7.  The codes use the group's spent x buffer as
+// scratch, so the next tile's rows are copied in once they are packed and, with QJL, y_hat has
+// been rebuilt: during the projection and the signs.  Per group six 128-float slots: x-norm
+// partials (0, 1), the squared level-5 radii of parts 0..3 (2..5), then the r'-norm partials (2, 3).
+constexpr uint32_t kSmemPolar2 = kSmemB + kTc2Groups * kMatBytes + kTc2Groups * 6 * kTile * sizeof(float);
+
 template <int B, bool QJL>
-__global__ void __launch_bounds__(kTcThreads, 1) polar_tc_kernel(const PolarTcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1) polar_tc2_kernel(const PolarTcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
-    unsigned char* sB = sm;
-    unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]; the spent one holds codes, then r' lo
-    unsigned char* sR = sm + kSmemB + kSmemX;
-    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128]
-    __shared__ __align__(8) uint64_t mbar, s_drain;
+    __shared__ __align__(8) uint64_t mbar[kTc2Groups], s_drain[kTc2Groups];
     __shared__ uint32_t s_tmem;
+    __shared__ int s_drained;
     __shared__ float s_cs[kPolarTcLevels * 32];   // indexed by code per lane: shared, not parameter space
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, part = warp >> 2, row = 32 * q + lane;
+    const int g = warp >> 3, gw = warp & 7, q = gw & 3, hh = gw >> 2, gtid = tid & (kTc2GThreads - 1);
+    const int row = 32 * q + lane, bar_id = 1 + g;
+    const bool leader = gtid == 0;
+    unsigned char* sB = sm;
+    unsigned char* sX = sm + kSmemB + g * kMatBytes;
+    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kTc2Groups * kMatBytes) + g * 6 * kTile;
     const int ntiles = (int)((a.n + kTile - 1) / kTile);
-    if (blockIdx.x >= ntiles) return;
     if (QJL && tid < kPolarTcLevels * 32) s_cs[tid] = a.cs[tid];
-
     for (int e = tid; e < (int)((QJL ? kSmemB : kSmemB / 2) / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
     asm volatile("cp.async.commit_group;");
-    {   // the first tile's rows
-        const int64_t r0 = (int64_t)blockIdx.x * kTile;
-        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
-        for (int e = tid; e < kTile * 16; e += kTcThreads) {
+    auto stage = [&](int t) {   // the x rows of tile t into this group's buffer, one commit group
+        const int64_t r0 = (int64_t)t * kTile;
+        const int nv = (int)min((int64_t)kTile, a.n - r0);
+        for (int e = gtid; e < kTile * 16; e += kTc2GThreads) {
             const int r = e >> 4, kc = e & 15;
             unsigned char* dst = sX + kmajor_off(r, 8 * kc);
-            if (r < nvalid) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
+            if (r < nv) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
             else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
         asm volatile("cp.async.commit_group;");
-    }
+    };
+    int tile = kTc2Groups * blockIdx.x + g;
+    if (tile < ntiles) stage(tile);
+    else asm volatile("cp.async.commit_group;");   // an empty group keeps the wait counts alike
     if (tid == 0) {
-        tc::mbar_init(&mbar, 1);
-        tc::mbar_init(&s_drain, 1);
+        for (int i = 0; i < kTc2Groups; ++i) {
+            tc::mbar_init(&mbar[i], 1);
+            tc::mbar_init(&s_drain[i], 1);
+        }
+        s_drained = 1;
         tc::mbar_init_fence();
     }
-    if (warp == 0) tc::tmem_alloc<kTmemCols>(&s_tmem);
+    if (warp == 0) tc::tmem_alloc<512>(&s_tmem);
+    asm volatile("cp.async.wait_group 1;");   // this thread's share of the B operands has landed
+    asm volatile("fence.proxy.async.shared::cta;");
     tc::fence_before();
-    __syncthreads();
+    __syncthreads();   // both groups' shares: the B operands (and the cos/sin table) are whole
     tc::fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t d1_row = tmem + ((uint32_t)(32 * q) << 16);
-    const uint32_t d2_row = d1_row + 128;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t d_col = tmem + 256 * g, a_col = d_col + 128;
+    const uint32_t d_row = d_col + lane_off, a_row = a_col + lane_off;
+    const float* cs = s_cs;
     uint32_t phase = 0;
     bool ok = true;
-    int buf = 0;
 
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, buf ^= 1) {
+    for (; tile < ntiles && ok; tile += kTc2Groups * gridDim.x) {
         const int64_t r0 = (int64_t)tile * kTile;
         const int nvalid = (int)min((int64_t)kTile, a.n - r0);
-        unsigned char* sXc = sX + buf * kMatBytes;
+        const int next = tile + kTc2Groups * gridDim.x;
         asm volatile("cp.async.wait_group 0;");
         asm volatile("fence.proxy.async.shared::cta;");
         tc::fence_before();
-        __syncthreads();
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");
         tc::fence_after();
-        if (tid == 0) {   // phase 1: Y = X Pi^T
-            issue_pieces(tmem, tc::smem_u32(sXc), tc::smem_u32(sB), false);
-            tc::commit(&mbar);
+        if (leader) {   // phase 1: Y = X Pi^T
+            issue_pieces(d_col, tc::smem_u32(sX), tc::smem_u32(sB), false);
+            tc::commit(&mbar[g]);
         }
-        const int next = tile + gridDim.x;
-        if (next < ntiles) {
-            const int64_t n0 = (int64_t)next * kTile;
-            const int nv2 = (int)min((int64_t)kTile, a.n - n0);
-            unsigned char* sXn = sX + (buf ^ 1) * kMatBytes;
-            for (int e = tid; e < kTile * 16; e += kTcThreads) {
-                const int r = e >> 4, kc = e & 15;
-                unsigned char* dst = sXn + kmajor_off(r, 8 * kc);
-                if (r < nv2) tc::cp_async16(dst, a.x + (size_t)(n0 + r) * a.ld_x + 8 * kc);
-                else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        asm volatile("cp.async.commit_group;");
-        float xs = 0.f;   // ||x||^2 partial while the MMAs run
+        {   // ||x||^2 partial over this thread's 64 coordinates while the MMAs run
+            float xs = 0.f;
 #pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {
-            const uint4 w = *reinterpret_cast<const uint4*>(sXc + kmajor_off(row, 32 * part + 8 * kc));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int kc = 0; kc < 8; ++kc) {
+                const uint4 w = *reinterpret_cast<const uint4*>(sX + kmajor_off(row, 64 * hh + 8 * kc));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
-                xs = fmaf(lo, lo, xs);
-                xs = fmaf(hi, hi, xs);
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
+                    xs = fmaf(lo, lo, xs);
+                    xs = fmaf(hi, hi, xs);
+                }
             }
+            s_part[hh * kTile + row] = xs;
         }
-        s_part[part * kTile + row] = xs;
-        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
+        ok = group_and(tc::mbar_wait(&mbar[g], phase), bar_id);   // also: the x reads are done
         phase ^= 1u;
         if (!ok) break;
         tc::fence_after();
-        float y[32];
-        load_row_part(d1_row, part, y);
-        const float nrm = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
+        const float nrm = sqrtf(s_part[row] + s_part[kTile + row]);
         const int64_t grow = r0 + row;
         const bool valid = row < nvalid;
-        unsigned char* code = sXc + row * kCodeStride;   // this row's 127 angle codes in stream order (sXc is spent)
-        // levels 1-5 of this thread's subtree (level-l node i of the subtree is global node
-        // (32 >> l) part + i, at stream position 128 - (256 >> l) + that), with squared radii
-        float rad[16];
+        unsigned char* code = sX + row * kCodeStride;   // this row's 127 angle codes (the x buffer is spent)
+        // levels 1-5 of this thread's two level-5 subtrees (part p = 2 hh + pass; level-l node i of
+        // subtree p is global node (32 >> l) p + i, at stream position 128 - (256 >> l) + that)
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int part = 2 * hh + pass;
+            float y[32];
+            load_row_part(d_row, part, y);
+            float rad[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float lo = y[2 * i], hi = y[2 * i + 1];
-            rad[i] = fmaf(lo, lo, hi * hi);
-            code[16 * part + i] = (unsigned char)sector_code<B>(lo, hi);
-        }
-#pragma unroll
-        for (int l = 2; l <= 5; ++l) {
-            const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
-#pragma unroll
-            for (int i = 0; i < nodes; ++i) {
-                const float lo = rad[2 * i], hi = rad[2 * i + 1];
-                rad[i] = lo + hi;
-                code[pos + i] = (unsigned char)level_code<B>(lo, hi, a.tau[l - 2]);
+            for (int i = 0; i < 16; ++i) {
+                const float lo = y[2 * i], hi = y[2 * i + 1];
+                rad[i] = fmaf(lo, lo, hi * hi);
+                code[16 * part + i] = (unsigned char)sector_code<B>(lo, hi);
             }
+#pragma unroll
+            for (int l = 2; l <= 5; ++l) {
+                const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
+#pragma unroll
+                for (int i = 0; i < nodes; ++i) {
+                    const float lo = rad[2 * i], hi = rad[2 * i + 1];
+                    rad[i] = lo + hi;
+                    code[pos + i] = (unsigned char)level_code<B>(lo, hi, a.tau[l - 2]);
+                }
+            }
+            s_part[(2 + part) * kTile + row] = rad[0];
         }
-        __syncthreads();   // every thread has read its x-norm partials
-        s_part[part * kTile + row] = rad[0];   // the squared level-5 radius of this quarter
-        __syncthreads();
-        if (part == 0) {   // levels 6 and 7 of the row
-            const float r5[4] = {s_part[row], s_part[kTile + row], s_part[2 * kTile + row], s_part[3 * kTile + row]};
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");   // level-5 radii visible
+        if (hh == 0) {   // levels 6 and 7 of the row
+            const float r5[4] = {s_part[2 * kTile + row], s_part[3 * kTile + row], s_part[4 * kTile + row],
+                                 s_part[5 * kTile + row]};
 #pragma unroll
             for (int i = 0; i < 2; ++i) code[124 + i] = (unsigned char)level_code<B>(r5[2 * i], r5[2 * i + 1], a.tau[4]);
             code[126] = (unsigned char)level_code<B>(r5[0] + r5[1], r5[2] + r5[3], a.tau[5]);
         }
-        __syncthreads();   // the code stream of every row is complete
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");   // every code written
         // pack: word w holds stream bits 32 w .. 32 w + 31, stream bit t being bit t - B an of code
         // an = t / B; the codes from a0 = 32 w / B on are laid side by side in a 64-bit window
         // (code a0 + k at bit B k), whose bits sh .. sh + 31 (sh = 32 w - B a0) are the word
-        for (int w = part; w < a.cw; w += 4) {
+        for (int w = hh; w < a.cw; w += 2) {
             const int a0 = 32 * w / B, sh = 32 * w - B * a0;
             constexpr int K = (31 + B - 1) / B + 1;
             uint64_t win = 0u;
@@ -927,92 +878,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) polar_tc_kernel(const PolarTcAr
             if (valid) a.codes[(size_t)grow * a.cw + w] = (uint32_t)(win >> sh);
         }
         const uint16_t nh = float_to_half_bits(nrm);
-        if (valid && part == 0) {
+        if (valid && hh == 0) {
             a.r16[grow] = nh;
             if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
         }
         if constexpr (!QJL) {
+            asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");   // codes read
+            if (next < ntiles) stage(next);
             tc::fence_before();
-            __syncthreads();   // TMEM reads and code reads done before the next tile
             continue;
         }
-        // y_hat top-down from the stored radius: the path root -> level 6 -> this quarter's level-5
-        // node, then the subtree
-        const float* cs = s_cs;
-        float rho = half_bits_to_float(nh);
-        {
-            const int c7 = code[126], c6 = code[124 + (part >> 1)];
-            rho *= (part >> 1) ? cs[6 * 32 + 16 + c7] : cs[6 * 32 + c7];
-            rho *= (part & 1) ? cs[5 * 32 + 16 + c6] : cs[5 * 32 + c6];
-        }
-        rad[0] = rho;
-#pragma unroll
-        for (int l = 5; l >= 2; --l) {   // node i of level l -> children 2 i, 2 i + 1 of level l - 1
-            const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
-#pragma unroll
-            for (int i = nodes - 1; i >= 0; --i) {
-                const int c = code[pos + i];
-                const float r = rad[i];
-                rad[2 * i] = r * cs[(l - 1) * 32 + c];
-                rad[2 * i + 1] = r * cs[(l - 1) * 32 + 16 + c];
-            }
-        }
+        // y_hat top-down from the stored radius: root -> level 6 -> the part's level-5 node -> its
+        // subtree; r' = y - y_hat into the A operand as bf16 hi and lo
         float rs = 0.f;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int part = 2 * hh + pass;
+            float y[32];
+            load_row_part(d_row, part, y);
+            float rho = half_bits_to_float(nh);
+            {
+                const int c7 = code[126], c6 = code[124 + (part >> 1)];
+                rho *= (part >> 1) ? cs[6 * 32 + 16 + c7] : cs[6 * 32 + c7];
+                rho *= (part & 1) ? cs[5 * 32 + 16 + c6] : cs[5 * 32 + c6];
+            }
+            float rad[16];
+            rad[0] = rho;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c = code[16 * part + i];
-            const float lo = rad[i] * cs[c], hi = rad[i] * cs[16 + c];
-            y[2 * i] -= lo;
-            y[2 * i + 1] -= hi;
-            rs = fmaf(y[2 * i], y[2 * i], rs);
-            rs = fmaf(y[2 * i + 1], y[2 * i + 1], rs);
+            for (int l = 5; l >= 2; --l) {   // node i of level l -> children 2 i, 2 i + 1 of level l - 1
+                const int nodes = 32 >> l, pos = 128 - (256 >> l) + nodes * part;
+#pragma unroll
+                for (int i = nodes - 1; i >= 0; --i) {
+                    const int c = code[pos + i];
+                    const float r = rad[i];
+                    rad[2 * i] = r * cs[(l - 1) * 32 + c];
+                    rad[2 * i + 1] = r * cs[(l - 1) * 32 + 16 + c];
+                }
+            }
+            uint32_t h[16], lo16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = code[16 * part + i];
+                const float r0v = y[2 * i] - rad[i] * cs[c], r1v = y[2 * i + 1] - rad[i] * cs[16 + c];
+                rs = fmaf(r0v, r0v, rs);
+                rs = fmaf(r1v, r1v, rs);
+                const __nv_bfloat162 hp = __floats2bfloat162_rn(r0v, r1v);
+                h[i] = *reinterpret_cast<const uint32_t*>(&hp);
+                const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xffff0000u);
+                const __nv_bfloat162 lp = __floats2bfloat162_rn(r0v - h0, r1v - h1);
+                lo16[i] = *reinterpret_cast<const uint32_t*>(&lp);
+            }
+            tc::tmem_st16(a_row + 16 * part, h);
+            tc::tmem_st16(a_row + 64 + 16 * part, lo16);
         }
-        store_row_part(sR, row, part, y);   // r' hi
-#pragma unroll
-        for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
-        __syncthreads();   // every row's codes have been read: the spent x buffer takes r' lo
-        store_row_part(sXc, row, part, y);
-        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
+        s_part[(2 + hh) * kTile + row] = rs;   // the level-5 slots were last read before the code barrier
+        tc::wait_st();
         tc::fence_before();
-        asm volatile("fence.proxy.async.shared::cta;");
-        __syncthreads();
-        tc::fence_after();
-        if (tid == 0) {   // phase 2: Z = r'_hi (S Pi^T)^T + r'_lo (S Pi^T)^T
-            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
-            issue_pieces(tmem + 128, tc::smem_u32(sXc), tc::smem_u32(sB) + kPieces * kMatBytes, true);
-            tc::commit(&mbar);
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kTc2GThreads) : "memory");   // codes read, A written
+        if (next < ntiles) stage(next);   // the code scratch is free: the next tile's rows land meanwhile
+        if (leader) {   // phase 2: Z = r' (S Pi^T)^T, A from tensor memory
+            tc::fence_after();
+            issue_pieces_ta(d_col, a_col, tc::smem_u32(sB) + kPieces * kMatBytes);
+            tc::commit(&mbar[g]);
         }
-        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
+        ok = group_and(tc::mbar_wait(&mbar[g], phase), bar_id);
         phase ^= 1u;
         if (!ok) break;
         tc::fence_after();
-        float z[32];
-        load_row_part(d2_row, part, z);
-        uint32_t sw = 0u;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int part = 2 * hh + pass;
+            float z[32];
+            load_row_part(d_row, part, z);
+            uint32_t sw = 0u;   // bit c = [z_c > 0]: the sign bit of 0 - z_c (+0 for z_c = +-0)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
-        if (valid) a.signs[(size_t)grow * 4 + part] = sw;
-        if (valid && part == 0) {
-            const float rn = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
-            const uint16_t rh = float_to_half_bits(rn);
+            for (int c = 31; c >= 0; --c) sw = __funnelshift_l(__float_as_uint(0.f - z[c]), sw, 1);
+            if (valid) a.signs[(size_t)grow * 4 + part] = sw;
+        }
+        if (valid && hh == 0) {
+            const uint16_t rh = float_to_half_bits(sqrtf(s_part[2 * kTile + row] + s_part[3 * kTile + row]));
             a.rnorm[grow] = rh;
             if (__hisinf(__ushort_as_half(rh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
         }
         tc::fence_before();
-        __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
     }
     asm volatile("cp.async.wait_all;");
-    bool drained = true;
-    if (!ok) {   // a wait ran out: flag it, and let every MMA this CTA issued finish (bounded)
-        if (tid == 0) {
+    if (!ok) {   // a wait ran out: flag it, and let every MMA this group issued finish (bounded)
+        if (leader) {
             set_error(a.err, TQ_DEVERR_TIMEOUT);
-            tc::commit(&s_drain);
+            tc::commit(&s_drain[g]);
         }
-        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&s_drain, 0u));
+        if (!group_and(!leader || tc::mbar_wait(&s_drain[g], 0u), bar_id) && leader) s_drained = 0;
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
+    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
+    if (warp == 0 && s_drained) tc::tmem_dealloc<512>(tmem);
 }
 
 }  // namespace
@@ -1084,7 +1045,7 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     };
     cudaError_t e = cudaErrorInvalidValue;
     const bool sym = c->prm.odd_walsh != 0;
-    if (c->prm.d_hi > 0) e = run(quantize_tc_kernel<0, true>);
+    if (c->prm.d_hi > 0) e = run(quantize_tc_split_kernel);
     else if (c->prm.P == 1) e = sym ? run2(quantize_tc2_kernel<1, true>) : run2(quantize_tc2_kernel<1, false>);
     else if (c->prm.P == 2) e = sym ? run2(quantize_tc2_kernel<2, true>) : run2(quantize_tc2_kernel<2, false>);
     else if (c->prm.P == 3) e = sym ? run2(quantize_tc2_kernel<3, true>) : run2(quantize_tc2_kernel<3, false>);
@@ -1115,22 +1076,23 @@ cudaError_t launch_polar_tc(const PolarTcLaunch& L, cudaStream_t s) {
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L.device);
     const int64_t ntiles = (L.n + kTile - 1) / kTile;
-    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    const int64_t pairs = (ntiles + kTc2Groups - 1) / kTc2Groups;   // two tiles in flight per CTA
+    const int grid = (int)(pairs < sms ? pairs : sms);
     auto run = [&](auto kernel) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemPolar2);
         if (e != cudaSuccess) return e;
-        kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
+        kernel<<<grid, kTcThreads, kSmemPolar2, s>>>(a);
         return cudaGetLastError();
     };
     switch (L.bits * 2 + (L.qjl ? 1 : 0)) {
-        case 2: return run(polar_tc_kernel<1, false>);
-        case 3: return run(polar_tc_kernel<1, true>);
-        case 4: return run(polar_tc_kernel<2, false>);
-        case 5: return run(polar_tc_kernel<2, true>);
-        case 6: return run(polar_tc_kernel<3, false>);
-        case 7: return run(polar_tc_kernel<3, true>);
-        case 8: return run(polar_tc_kernel<4, false>);
-        case 9: return run(polar_tc_kernel<4, true>);
+        case 2: return run(polar_tc2_kernel<1, false>);
+        case 3: return run(polar_tc2_kernel<1, true>);
+        case 4: return run(polar_tc2_kernel<2, false>);
+        case 5: return run(polar_tc2_kernel<2, true>);
+        case 6: return run(polar_tc2_kernel<3, false>);
+        case 7: return run(polar_tc2_kernel<3, true>);
+        case 8: return run(polar_tc2_kernel<4, false>);
+        case 9: return run(polar_tc2_kernel<4, true>);
     }
     return cudaErrorInvalidValue;
 }
