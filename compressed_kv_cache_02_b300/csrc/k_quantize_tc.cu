@@ -13,11 +13,10 @@
 //                                accumulator), B = S Pi^T as 2 bf16 pieces (z moves by ~2e-6 of
 //                                ||x||, inside the 1e-5 band of the sign rule); sign_j = [z_j > 0].
 // Pi and S Pi^T stay resident in shared memory (4 x 32 KB), so one CTA per SM walks the tiles of
-// 128 rows.  Ordinary contexts (quantize_tc2_kernel) and the polar encoder (polar_tc2_kernel) run
-// two 8-warp groups per CTA, each on its own tile with its own x buffer and TMEM accumulator, r'
-// held in tensor memory as the phase-2 A operand, so one group's epilogue overlaps the other's
-// MMAs.  Split contexts (quantize_tc_split_kernel) walk one tile at a time with all 16 warps, r'
-// staged in shared memory.  Operands in shared memory use the K-major no-swizzle
+// 128 rows.  The scalar quantizer (quantize_tc2_kernel, ordinary and split contexts) and the
+// polar encoder (polar_tc2_kernel) run two 8-warp groups per CTA, each on its own tile with its
+// own x buffer and TMEM accumulator, r' held in tensor memory as the phase-2 A operand, so one
+// group's epilogue overlaps the other's MMAs.  Operands in shared memory use the K-major no-swizzle
 // core-matrix layout (8 rows x 16 bytes per core matrix; LBO = 128 B between core matrices along
 // K, SBO = 2048 B between 8-row groups).  One thread per group issues the MMAs; tcgen05.commit
 // signals an mbarrier whose waits are bounded in time (TQ_DEVERR_TIMEOUT).
@@ -33,15 +32,11 @@
 namespace tq {
 namespace {
 
-constexpr int kTcThreads = 512;   // 4 threads per row, 32 coordinates each
+constexpr int kTcThreads = 512;   // two groups of 8 warps; 2 threads per row of a group's tile, 64 coordinates each
 constexpr int kTile = 128;
 constexpr uint32_t kMatBytes = 128 * 128 * 2;   // one 128 x 128 bf16 operand
 constexpr int kPieces = 2;                      // bf16 pieces of Pi and of S Pi^T
 constexpr uint32_t kSmemB = 2 * kPieces * kMatBytes;   // Pi pieces then S Pi^T pieces (128 KB)
-constexpr uint32_t kSmemX = 2 * kMatBytes;             // two x tiles (the current one, the next)
-constexpr uint32_t kSmemR = kMatBytes;                 // r' hi, then r' lo
-constexpr uint32_t kSmemTotal = kSmemB + kSmemX + kSmemR + 4 * kTile * sizeof(float);   // + norm partials [4][128]
-constexpr uint32_t kTmemCols = 256;                    // D1 (Y) in columns 0..127, D2 (Z) in 128..255
 
 __host__ __device__ constexpr uint32_t kmajor_off(int r, int k) {
     return (uint32_t)(((r >> 3) * 16 + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
@@ -88,20 +83,6 @@ __device__ __forceinline__ void load_row_part(uint32_t tmem_row, int part, float
     }
 }
 
-// Writes 32 bf16 values (coordinates [32 part, 32 part + 32) of row r) into a K-major operand.
-__device__ __forceinline__ void store_row_part(unsigned char* sA, int r, int part, const float (&v)[32]) {
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * kc + 2 * i], v[8 * kc + 2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&pr);
-        }
-        *reinterpret_cast<uint4*>(sA + kmajor_off(r, 32 * part + 8 * kc)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
 struct TcArgs {
     Params prm;
     const uint16_t* x;       // bf16 rows
@@ -115,205 +96,10 @@ struct TcArgs {
 };
 
 
-// The x rows of tile `tile` into buffer sX (cp.async, zeros beyond n), one commit group.
-__device__ __forceinline__ void stage_x(const TcArgs& a, int tile, unsigned char* sX) {
-    const int64_t r0 = (int64_t)tile * kTile;
-    const int nvalid = (int)min((int64_t)kTile, a.n - r0);
-    for (int e = threadIdx.x; e < kTile * 16; e += kTcThreads) {
-        const int r = e >> 4, kc = e & 15;
-        unsigned char* dst = sX + kmajor_off(r, 8 * kc);
-        if (r < nvalid) tc::cp_async16(dst, a.x + (size_t)(r0 + r) * a.ld_x + 8 * kc);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("cp.async.commit_group;");
-}
-
-// Split (fractional bit width) contexts, whose width per coordinate word is P or P + 1 at run time:
-// one tile at a time per CTA, 4 threads per row; ordinary contexts take quantize_tc2_kernel below.
-__global__ void __launch_bounds__(kTcThreads, 1) quantize_tc_split_kernel(const TcArgs a) {
-    extern __shared__ __align__(128) unsigned char sm[];   // no-swizzle operands need 16-byte alignment
-    unsigned char* sB = sm;
-    unsigned char* sX = sm + kSmemB;                    // [2][kMatBytes]
-    unsigned char* sR = sm + kSmemB + kSmemX;
-    float* s_part = reinterpret_cast<float*>(sm + kSmemB + kSmemX + kSmemR);   // [4][128] x-norm, then r-norm parts
-    __shared__ __align__(8) uint64_t mbar, s_drain;   // MMAs of the current phase done; all MMAs done (error path)
-    __shared__ uint32_t s_tmem;
-    // the tables in shared memory: the binary search indexes them per lane, which the kernel-
-    // parameter (constant) space would serialise
-    __shared__ float s_thr[kMaxLevels], s_cen[kMaxLevels], s_thr_hi[kMaxLevels], s_cen_hi[kMaxLevels];
-    const Params& prm = a.prm;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, part = warp >> 2, row = 32 * q + lane;
-    const int ntiles = (int)((a.n + kTile - 1) / kTile);
-    if (blockIdx.x >= ntiles) return;
-    if (tid < kMaxLevels) {
-        s_thr[tid] = prm.thresholds[tid];
-        s_cen[tid] = prm.centroids[tid];
-        s_thr_hi[tid] = prm.thresholds_hi[tid];
-        s_cen_hi[tid] = prm.centroids_hi[tid];
-    }
-
-    for (int e = tid; e < (int)(kSmemB / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
-    asm volatile("cp.async.commit_group;");
-    stage_x(a, blockIdx.x, sX);
-    if (tid == 0) {
-        tc::mbar_init(&mbar, 1);
-        tc::mbar_init(&s_drain, 1);
-        tc::mbar_init_fence();
-    }
-    if (warp == 0) tc::tmem_alloc<kTmemCols>(&s_tmem);
-    asm volatile("tcgen05.fence::before_thread_sync;");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;");
-    const uint32_t tmem = s_tmem;
-    const uint32_t d1_row = tmem + ((uint32_t)(32 * q) << 16);
-    const uint32_t d2_row = d1_row + 128;
-    uint32_t phase = 0;
-    bool ok = true;
-    int buf = 0;
-
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, buf ^= 1) {
-        const int64_t r0 = (int64_t)tile * kTile;
-        const int nvalid = (int)min((int64_t)kTile, a.n - r0);
-        unsigned char* sXc = sX + buf * kMatBytes;
-        asm volatile("cp.async.wait_group 0;");          // this tile's rows (and, at first, Pi) have landed
-        asm volatile("fence.proxy.async.shared::cta;");
-        asm volatile("tcgen05.fence::before_thread_sync;");
-        __syncthreads();
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        // phase 1: Y = X Pi^T
-        if (tid == 0) {
-            issue_pieces(tmem, tc::smem_u32(sXc), tc::smem_u32(sB), false);
-            tc::commit(&mbar);
-        }
-        // the next tile's rows into the other buffer (its last readers, the previous tile's phase 1
-        // and norms, are done) while this tile computes
-        const int next = tile + gridDim.x;
-        if (next < ntiles) stage_x(a, next, sX + (buf ^ 1) * kMatBytes);
-        // ||x|| partial from the staged tile while the MMAs run
-        float xs = 0.f;
-#pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {
-            const uint4 w = *reinterpret_cast<const uint4*>(sXc + kmajor_off(row, 32 * part + 8 * kc));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = bf16_bits_to_float(ws[i] & 0xffffu), hi = bf16_bits_to_float(ws[i] >> 16);
-                xs = fmaf(lo, lo, xs);
-                xs = fmaf(hi, hi, xs);
-            }
-        }
-        s_part[part * kTile + row] = xs;
-        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;   // also: x-norm partials visible
-        phase ^= 1u;
-        if (!ok) break;
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        float y[32];
-        load_row_part(d1_row, part, y);
-        const float nrm = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
-        const float n16 = half_bits_to_float(float_to_half_bits(nrm));
-        const int64_t grow = r0 + row;
-        const bool valid = row < nvalid;
-        // idx = #{k : t_k < y / n} by binary search over the sorted thresholds (one step per bit, the
-        // step for bit b deciding bit b of idx), compared as t_k n < y; all u = 0 when n = 0.
-        const float nv = nrm > 0.f ? nrm : 1.f;
-        // this thread's 32 coordinates (one word) are below d_hi or not as a whole
-        const bool hi = 32 * part < prm.d_hi;
-        uint32_t pw[kFastBits] = {};
-        float rs = 0.f;
-        {
-            const int nb = prm.P + (hi ? 1 : 0);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float yc = nrm > 0.f ? y[c] : 0.f;
-                int idx = 0;
-#pragma unroll
-                for (int b = kFastBits - 1; b >= 0; --b)
-                    if (b < nb) {
-                        const int k = idx + (1 << b) - 1;
-                        const bool up = yc > (hi ? s_thr_hi[k] : s_thr[k]) * nv;
-                        idx += up ? (1 << b) : 0;
-                        pw[b] |= (up ? 1u : 0u) << c;
-                    }
-                const float r = y[c] - n16 * (hi ? s_cen_hi[idx] : s_cen[idx]);
-                y[c] = r;
-                rs = fmaf(r, r, rs);
-            }
-        }
-        if (valid) {
-            for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
-            if (hi) {
-                const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
-                a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
-            }
-        }
-        if (!prm.qjl) {   // MSE mode: no residual sketch
-            if (valid && part == 0) {
-                const uint16_t nh = float_to_half_bits(nrm);
-                a.norm[grow] = nh;
-                if (__hisinf(__ushort_as_half(nh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;");
-            __syncthreads();   // TMEM reads and x-norm reads done before the next tile
-            continue;
-        }
-        store_row_part(sR, row, part, y);   // r' hi (rounded to bf16 by the store)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) y[c] -= __bfloat162float(__float2bfloat16_rn(y[c]));
-        // r' lo = r' - bf16(r') into this tile's x buffer: phase 1 and the x-norm partials are done
-        // with it, and the next tile's rows go to the other buffer
-        store_row_part(sXc, row, part, y);
-        asm volatile("tcgen05.fence::before_thread_sync;");
-        asm volatile("fence.proxy.async.shared::cta;");
-        __syncthreads();   // everyone has read its x-norm partials and written r' hi and lo
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        s_part[part * kTile + row] = rs;   // the partials now hold ||r'||^2 parts
-        // phase 2: Z = r'_hi (S Pi^T)^T + r'_lo (S Pi^T)^T
-        if (tid == 0) {
-            issue_pieces(tmem + 128, tc::smem_u32(sR), tc::smem_u32(sB) + kPieces * kMatBytes, false);
-            issue_pieces(tmem + 128, tc::smem_u32(sXc), tc::smem_u32(sB) + kPieces * kMatBytes, true);
-            tc::commit(&mbar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(&mbar, phase)) != 0;
-        phase ^= 1u;
-        if (!ok) break;
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        float z[32];
-        load_row_part(d2_row, part, z);
-        uint32_t sw = 0u;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sw |= (z[c] > 0.f ? 1u : 0u) << c;
-        if (valid) a.signs[(size_t)grow * 4 + part] = sw;
-        if (valid && part == 0) {
-            const uint16_t nh = float_to_half_bits(nrm);
-            const float rn = sqrtf((s_part[row] + s_part[kTile + row]) + (s_part[2 * kTile + row] + s_part[3 * kTile + row]));
-            const uint16_t rh = float_to_half_bits(rn);
-            a.norm[grow] = nh;
-            a.rnorm[grow] = rh;
-            if (__hisinf(__ushort_as_half(nh)) || __hisinf(__ushort_as_half(rh))) set_error(a.err, TQ_DEVERR_NORM_OVERFLOW);
-        }
-        asm volatile("tcgen05.fence::before_thread_sync;");
-        __syncthreads();   // r-norm partials read and TMEM reads done before the next tile
-    }
-    asm volatile("cp.async.wait_all;");   // a prefetch still in flight lands before the CTA leaves
-    bool drained = true;
-    if (!ok) {   // a wait ran out: flag it, and let every MMA this CTA issued finish (bounded)
-        if (tid == 0) {
-            set_error(a.err, TQ_DEVERR_TIMEOUT);
-            tc::commit(&s_drain);
-        }
-        drained = __syncthreads_and(tid != 0 || tc::mbar_wait(&s_drain, 0u));
-    }
-    tc::fence_before();
-    __syncthreads();
-    // an MMA that outlived the bounded drain still writes this memory: it is then left allocated
-    if (warp == 0 && drained) tc::tmem_dealloc<kTmemCols>(tmem);
-}
-
 // ---------------------------------------------------------------- two tiles in flight
-// The same arithmetic as quantize_tc_split_kernel for ordinary contexts, with the CTA split into two
-// groups of 8 warps that each take every other tile, so one group's CUDA-core epilogue runs while
-// the other group's MMAs do.  Per group: one x buffer (the next tile's rows are copied into it as
+// The CTA is split into two groups of 8 warps that each take every other tile, so one group's
+// CUDA-core epilogue runs while the other group's MMAs do.  Per group: one x buffer (the next
+// tile's rows are copied into it as
 // soon as the current tile's Y = X Pi^T is done), a 128-column accumulator D (Y, then Z) and a
 // 128-column A operand in tensor memory holding r' as bf16 hi (columns 0..63) and lo (64..127),
 // so the projection Z = r' (S Pi^T)^T reads A from tensor memory (kind::f16, A in TMEM) and no
@@ -371,13 +157,15 @@ __device__ __forceinline__ void stage_x_group(const TcArgs& a, int tile, unsigne
 // |y| against the upper half of the table; on the negative side the lower code bits are the
 // magnitude bits inverted (the bins mirror), applied to whole plane words.  The decisions agree
 // with the ordered comparisons except where |y| equals a threshold exactly.
-template <int P, bool SYM>
+// SPLIT (P = 0 at compile time): a split context, each coordinate word coded with prm.P or, below
+// d_hi, prm.P + 1 bits from its own table, by a binary search over the shared-memory tables.
+template <int P, bool SYM, bool SPLIT = false>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
     __shared__ __align__(8) uint64_t mbar[kTc2Groups], s_drain[kTc2Groups];
     __shared__ uint32_t s_tmem;
     __shared__ int s_drained;
-    __shared__ float s_thr[kMaxLevels], s_cen[kMaxLevels];
+    __shared__ float s_thr[kMaxLevels], s_cen[kMaxLevels], s_thr_hi[kMaxLevels], s_cen_hi[kMaxLevels];
     const Params& prm = a.prm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = warp >> 3, gw = warp & 7, q = gw & 3, hh = gw >> 2, gtid = tid & (kTc2GThreads - 1);
@@ -391,6 +179,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
     if (tid < kMaxLevels) {
         s_thr[tid] = prm.thresholds[tid];
         s_cen[tid] = prm.centroids[tid];
+        if (SPLIT) {
+            s_thr_hi[tid] = prm.thresholds_hi[tid];
+            s_cen_hi[tid] = prm.centroids_hi[tid];
+        }
     }
     for (int e = tid; e < (int)((prm.qjl ? kSmemB : kSmemB / 2) / 16); e += kTcThreads) tc::cp_async16(sB + 16 * e, a.bops + e);
     asm volatile("cp.async.commit_group;");
@@ -463,7 +255,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
             float y[32];
             load_row_part(d_row, part, y);
             uint32_t pw[kFastBits] = {};
-            if constexpr (SYM && P == 1) {   // the threshold is 0: the code is the sign
+            const bool hi = SPLIT && 32 * part < prm.d_hi;   // this word's coordinates take P + 1 bits
+            if constexpr (SPLIT) {
+                const int nb = prm.P + (hi ? 1 : 0);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float yc = nrm > 0.f ? y[c] : 0.f;
+                    int idx = 0;
+#pragma unroll
+                    for (int b = kFastBits - 1; b >= 0; --b)
+                        if (b < nb) {
+                            const int k = idx + (1 << b) - 1;
+                            const bool up = yc > (hi ? s_thr_hi[k] : s_thr[k]) * nv;
+                            idx += up ? (1 << b) : 0;
+                            pw[b] |= (up ? 1u : 0u) << c;
+                        }
+                    const float r = y[c] - n16 * (hi ? s_cen_hi[idx] : s_cen[idx]);
+                    y[c] = r;
+                    rs = fmaf(r, r, rs);
+                }
+            } else if constexpr (SYM && P == 1) {   // the threshold is 0: the code is the sign
                 const float cm = s_cen[1];
 #pragma unroll
                 for (int c = 31; c >= 0; --c) {
@@ -593,8 +404,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
                 }
             }
             if (valid) {
+                if constexpr (SPLIT) {   // P planes, then the top plane of the words below d_hi
+                    for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+                    if (hi) {
+                        const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
+                        a.planes[(size_t)grow * prm.row_words + prm.P * 4 + part] = top;
+                    }
+                } else {
 #pragma unroll
-                for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+                    for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+                }
             }
             if (prm.qjl) {   // r' as bf16 hi and lo into the A operand
                 uint32_t h[16], l[16];
@@ -1027,14 +846,7 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
     const int64_t ntiles = (n + kTile - 1) / kTile;
-    const int grid = (int)(ntiles < sms ? ntiles : sms);
-    auto run = [&](auto kernel) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
-        if (e != cudaSuccess) return e;
-        kernel<<<grid, kTcThreads, kSmemTotal, s>>>(a);
-        return cudaSuccess;
-    };
-    // ordinary contexts: two tiles in flight per CTA (quantize_tc2_kernel)
+    // two tiles in flight per CTA (quantize_tc2_kernel)
     const int64_t pairs = (ntiles + kTc2Groups - 1) / kTc2Groups;
     const int grid2 = (int)(pairs < sms ? pairs : sms);
     auto run2 = [&](auto kernel) -> cudaError_t {
@@ -1045,7 +857,7 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     };
     cudaError_t e = cudaErrorInvalidValue;
     const bool sym = c->prm.odd_walsh != 0;
-    if (c->prm.d_hi > 0) e = run(quantize_tc_split_kernel);
+    if (c->prm.d_hi > 0) e = run2(quantize_tc2_kernel<0, false, true>);
     else if (c->prm.P == 1) e = sym ? run2(quantize_tc2_kernel<1, true>) : run2(quantize_tc2_kernel<1, false>);
     else if (c->prm.P == 2) e = sym ? run2(quantize_tc2_kernel<2, true>) : run2(quantize_tc2_kernel<2, false>);
     else if (c->prm.P == 3) e = sym ? run2(quantize_tc2_kernel<3, true>) : run2(quantize_tc2_kernel<3, false>);

@@ -53,7 +53,7 @@ def test_quantize_bf16_anisotropic(bits):
 
 
 @pytest.mark.parametrize("mode,bits", [(0, 2), (0, 3), (0, 4), (0, 5), (1, 1), (1, 2), (1, 3), (1, 4)])
-@pytest.mark.parametrize("n,ld", [(4096, 128), (5003, 128), (4500, 136)])
+@pytest.mark.parametrize("n,ld", [(4096, 128), (5003, 128), (4500, 136), (4200, 128)])
 def test_quantize_bulk_bf16(mode, bits, n, ld, kernel_path):
     """Bulk bf16 rows at d=128: tcgen05 tensor-core path (n >= 4096) and CUDA-core path."""
     tq = _tq()
@@ -61,10 +61,36 @@ def test_quantize_bulk_bf16(mode, bits, n, ld, kernel_path):
     pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR if kernel_path == "tensor" else tq.TQ_PATH_CUDA_CORE)
     fac = inputs.anisotropic_factors(1, ld, seed=12)
     X = inputs.anisotropic(1, 1, n, ld, fac, seed=13)[0, 0]          # rows of ld values; the first 128 are used
+    X[7] = 0.0                                                        # zero rows: one inside, the last
+    X[n - 1] = 0.0
     Xd = X.cuda()[:, :128]
     codes = pr.ctx.quantize(Xd)
     assert pr.ctx.sync_status() == 0
     same = check_codes(pr, X[:, :128].float().numpy(), codes)
+    assert same.mean() > 0.99
+    idx, n16, signs, r16 = pr.from_device(codes)
+    for r in (7, n - 1):
+        assert n16[r] == 0
+        if mode == 0:
+            assert r16[r] == 0 and not signs[r].any()
+
+
+def test_quantize_bulk_norm_overflow_flag():
+    """The tensor-core quantizer flags a norm that rounds to fp16 infinity, and the rest stays coded."""
+    tq = _tq()
+    pr = Pair(128, 3, seed=12)
+    pr.ctx.set_kernel_path(tq.TQ_PATH_TENSOR)
+    X = inputs.gaussian(4200, 128, seed=14).to(torch.bfloat16)
+    X[4100] = 1.0e4                                                   # ||x|| = 1.1e5 > fp16 max
+    codes = pr.ctx.quantize(X.cuda())
+    assert pr.ctx.sync_status() == tq.TQ_DEVERR_NORM_OVERFLOW
+    keep = np.ones(4200, dtype=bool)
+    keep[4100] = False
+    idx, n16, signs, r16 = pr.from_device(codes)
+    assert np.isinf(n16[4100])
+    rows = torch.from_numpy(np.nonzero(keep)[0]).cuda()
+    sub = tq.Codes(codes.planes[rows], codes.norm[rows], codes.signs[rows], codes.rnorm[rows])
+    same = check_codes(pr, X.float().numpy()[keep], sub)
     assert same.mean() > 0.99
 
 
