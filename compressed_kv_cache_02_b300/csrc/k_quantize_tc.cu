@@ -152,13 +152,82 @@ __device__ __forceinline__ void stage_x_group(const TcArgs& a, int tile, unsigne
     asm volatile("cp.async.commit_group;");
 }
 
-// SYM: the table is odd-symmetric (c_k = -c_{2^P-1-k}, so t_k = -t_{2^P-2-k} and the middle
-// threshold is 0).  The code is then decided as a sign (y > 0) and magnitude bits of
-// |y| against the upper half of the table; on the negative side the lower code bits are the
-// magnitude bits inverted (the bins mirror), applied to whole plane words.  The decisions agree
-// with the ordered comparisons except where |y| equals a threshold exactly.
-// SPLIT (P = 0 at compile time): a split context, each coordinate word coded with prm.P or, below
-// d_hi, prm.P + 1 bits from its own table, by a binary search over the shared-memory tables.
+// Codes of a thread's 32 coordinates y with an odd-symmetric NB-bit table (thr: the 2^NB - 1
+// thresholds, cen: the 2^NB centroids, shared memory): a sign (y > 0, the middle threshold being 0)
+// and magnitude bits of |y| against the upper half of the table, the lower planes mirrored on the
+// negative side word-wise.  Each decision a > b is the sign bit of b - a (exact in sign; +0 on a
+// tie), shifted into its plane word from the top, coordinate 31 first.  pw[0..NB-1] receive the
+// planes, y the residual y - n16 c[idx], rs its squared norm.  The decisions agree with ordered
+// comparisons except where |y| equals a threshold exactly.
+template <int NB>
+__device__ __forceinline__ void sym_codes(float (&y)[32], float nrm, float n16, float nv, const float* thr,
+                                          const float* cen, uint32_t* pw, float& rs) {
+    constexpr int H = 1 << (NB - 1);   // first index of the upper half
+    uint32_t sg = 0u, mw[3] = {0u, 0u, 0u};
+    if constexpr (NB == 1) {
+        const float cm = cen[1];
+#pragma unroll
+        for (int c = 31; c >= 0; --c) {
+            const float yc = nrm > 0.f ? y[c] : 0.f;
+            const float dz = 0.f - yc;   // negative iff yc > 0 (+0 for yc = +-0)
+            sg = __funnelshift_l(__float_as_uint(dz), sg, 1);
+            const float r = fmaf(n16, copysignf(cm, dz), y[c]);   // y - n16 c, c = +-cm with the sign of yc
+            y[c] = r;
+            rs = fmaf(r, r, rs);
+        }
+    } else {
+        float ts[H - 1];
+#pragma unroll
+        for (int k = 0; k + 1 < H; ++k) ts[k] = thr[H + k] * nv;
+        float cm[NB == 4 ? 1 : H];
+        if constexpr (NB < 4) {
+#pragma unroll
+            for (int k = 0; k < H; ++k) cm[k] = cen[H + k];
+        }
+#pragma unroll
+        for (int c = 31; c >= 0; --c) {
+            const float yc = nrm > 0.f ? y[c] : 0.f;
+            const float av = fabsf(yc);
+            const float dz = 0.f - yc;
+            sg = __funnelshift_l(__float_as_uint(dz), sg, 1);
+            float mag;
+            if constexpr (NB == 2) {
+                const float d0 = ts[0] - av;
+                mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                mag = d0 < 0.f ? cm[1] : cm[0];
+            } else if constexpr (NB == 3) {
+                const float d1 = ts[1] - av;
+                const bool m1 = d1 < 0.f;
+                const float d0 = (m1 ? ts[2] : ts[0]) - av;
+                mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
+                mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                const bool m0 = d0 < 0.f;
+                mag = m1 ? (m0 ? cm[3] : cm[2]) : (m0 ? cm[1] : cm[0]);
+            } else {   // 3 magnitude bits by binary search, the magnitude from the table
+                const float d2 = ts[3] - av;
+                const bool m2 = d2 < 0.f;
+                const float d1 = (m2 ? ts[5] : ts[1]) - av;
+                const bool m1 = d1 < 0.f;
+                const float d0 = (m2 ? (m1 ? ts[6] : ts[4]) : (m1 ? ts[2] : ts[0])) - av;
+                const bool m0 = d0 < 0.f;
+                mw[2] = __funnelshift_l(__float_as_uint(d2), mw[2], 1);
+                mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
+                mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
+                mag = cen[H + (m2 ? 4 : 0) + (m1 ? 2 : 0) + (m0 ? 1 : 0)];
+            }
+            const float r = fmaf(n16, copysignf(mag, dz), y[c]);
+            y[c] = r;
+            rs = fmaf(r, r, rs);
+        }
+    }
+    pw[NB - 1] = sg;
+#pragma unroll
+    for (int p = 0; p + 1 < NB; ++p) pw[p] = mw[p] ^ ~sg;
+}
+
+// SYM: the table (for SPLIT, both tables) is odd-symmetric, c_k = -c_{2^P-1-k}: codes by sym_codes.
+// SPLIT: a split context, each coordinate word coded with P or, below d_hi, P + 1 bits from its own
+// table (P = 0 when not SYM: the width is then read at run time and the tables searched in order).
 template <int P, bool SYM, bool SPLIT = false>
 __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArgs a) {
     extern __shared__ __align__(128) unsigned char sm[];
@@ -256,7 +325,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
             load_row_part(d_row, part, y);
             uint32_t pw[kFastBits] = {};
             const bool hi = SPLIT && 32 * part < prm.d_hi;   // this word's coordinates take P + 1 bits
-            if constexpr (SPLIT) {
+            if constexpr (SPLIT && SYM) {   // the word's table is the P- or (P+1)-bit one, both symmetric
+                if (hi) sym_codes<P + 1>(y, nrm, n16, nv, s_thr_hi, s_cen_hi, pw, rs);
+                else sym_codes<P>(y, nrm, n16, nv, s_thr, s_cen, pw, rs);
+            } else if constexpr (SPLIT) {
                 const int nb = prm.P + (hi ? 1 : 0);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -274,81 +346,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
                     y[c] = r;
                     rs = fmaf(r, r, rs);
                 }
-            } else if constexpr (SYM && P == 1) {   // the threshold is 0: the code is the sign
-                const float cm = s_cen[1];
-#pragma unroll
-                for (int c = 31; c >= 0; --c) {
-                    const float yc = nrm > 0.f ? y[c] : 0.f;
-                    const float dz = 0.f - yc;   // negative iff yc > 0 (+0 for yc = +-0)
-                    pw[0] = __funnelshift_l(__float_as_uint(dz), pw[0], 1);
-                    const float r = fmaf(n16, copysignf(cm, dz), y[c]);
-                    y[c] = r;
-                    rs = fmaf(r, r, rs);
-                }
-            } else if constexpr (SYM && P == 4) {   // sign, then 3 magnitude bits by binary search
-                float ts[7];
-#pragma unroll
-                for (int k = 0; k < 7; ++k) ts[k] = s_thr[8 + k] * nv;
-                uint32_t mw[3] = {0u, 0u, 0u};
-#pragma unroll
-                for (int c = 31; c >= 0; --c) {
-                    const float yc = nrm > 0.f ? y[c] : 0.f;
-                    const float av = fabsf(yc);
-                    const float dz = 0.f - yc;
-                    pw[3] = __funnelshift_l(__float_as_uint(dz), pw[3], 1);
-                    const float d2 = ts[3] - av;
-                    const bool m2 = d2 < 0.f;
-                    const float d1 = (m2 ? ts[5] : ts[1]) - av;
-                    const bool m1 = d1 < 0.f;
-                    const float d0 = (m2 ? (m1 ? ts[6] : ts[4]) : (m1 ? ts[2] : ts[0])) - av;
-                    const bool m0 = d0 < 0.f;
-                    mw[2] = __funnelshift_l(__float_as_uint(d2), mw[2], 1);
-                    mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
-                    mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
-                    const float mag = s_cen[8 + (m2 ? 4 : 0) + (m1 ? 2 : 0) + (m0 ? 1 : 0)];
-                    const float r = fmaf(n16, copysignf(mag, dz), y[c]);
-                    y[c] = r;
-                    rs = fmaf(r, r, rs);
-                }
-#pragma unroll
-                for (int p = 0; p < 3; ++p) pw[p] = mw[p] ^ ~pw[3];
-            } else if constexpr (SYM && (P == 2 || P == 3)) {
-                constexpr int H = 1 << (P - 1);   // first index of the upper half
-                float ts[H - 1], cm[H];
-#pragma unroll
-                for (int k = 0; k + 1 < H; ++k) ts[k] = s_thr[H + k] * nv;
-#pragma unroll
-                for (int k = 0; k < H; ++k) cm[k] = s_cen[H + k];
-                uint32_t mw[2] = {0u, 0u};   // magnitude bits (lower code bits on the positive side)
-                // Each decision a > b is the sign bit of b - a (exact in sign; +0 on a tie), shifted
-                // into its plane word from the top, coordinate 31 first.
-#pragma unroll
-                for (int c = 31; c >= 0; --c) {
-                    const float yc = nrm > 0.f ? y[c] : 0.f;
-                    const float av = fabsf(yc);
-                    const float dz = 0.f - yc;   // negative iff yc > 0 (+0 for yc = +-0)
-                    pw[P - 1] = __funnelshift_l(__float_as_uint(dz), pw[P - 1], 1);
-                    float mag;
-                    if constexpr (P == 2) {
-                        const float d0 = ts[0] - av;
-                        mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
-                        mag = d0 < 0.f ? cm[1] : cm[0];
-                    } else {
-                        const float d1 = ts[1] - av;
-                        const bool m1 = d1 < 0.f;
-                        const float d0 = (m1 ? ts[2] : ts[0]) - av;
-                        mw[1] = __funnelshift_l(__float_as_uint(d1), mw[1], 1);
-                        mw[0] = __funnelshift_l(__float_as_uint(d0), mw[0], 1);
-                        const bool m0 = d0 < 0.f;
-                        mag = m1 ? (m0 ? cm[3] : cm[2]) : (m0 ? cm[1] : cm[0]);
-                    }
-                    // y - n16 c with c = +mag for yc > 0, -mag otherwise: -c carries the sign of dz
-                    const float r = fmaf(n16, copysignf(mag, dz), y[c]);
-                    y[c] = r;
-                    rs = fmaf(r, r, rs);
-                }
-#pragma unroll
-                for (int p = 0; p + 1 < P; ++p) pw[p] = mw[p] ^ ~pw[P - 1];
+            } else if constexpr (SYM) {
+                sym_codes<P>(y, nrm, n16, nv, s_thr, s_cen, pw, rs);
             } else if constexpr (P <= 3) {
                 constexpr int NT = (1 << P) - 1;
                 float ts[NT], cv[NT + 1];
@@ -404,7 +403,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) quantize_tc2_kernel(const TcArg
                 }
             }
             if (valid) {
-                if constexpr (SPLIT) {   // P planes, then the top plane of the words below d_hi
+                if constexpr (SPLIT && SYM) {   // P planes, then the top plane of the words below d_hi
+#pragma unroll
+                    for (int p = 0; p < P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
+                    if (hi) a.planes[(size_t)grow * prm.row_words + P * 4 + part] = pw[P];
+                } else if constexpr (SPLIT) {
                     for (int p = 0; p < prm.P; ++p) a.planes[(size_t)grow * prm.row_words + p * 4 + part] = pw[p];
                     if (hi) {
                         const uint32_t top = prm.P == 1 ? pw[1] : (prm.P == 2 ? pw[2] : pw[3]);
@@ -857,7 +860,12 @@ cudaError_t launch_quantize_tc(const tq_ctx* c, const void* x, int64_t n, int64_
     };
     cudaError_t e = cudaErrorInvalidValue;
     const bool sym = c->prm.odd_walsh != 0;
-    if (c->prm.d_hi > 0) e = run2(quantize_tc2_kernel<0, false, true>);
+    if (c->prm.d_hi > 0) {
+        if (c->prm.split_walsh && c->prm.P == 1) e = run2(quantize_tc2_kernel<1, true, true>);
+        else if (c->prm.split_walsh && c->prm.P == 2) e = run2(quantize_tc2_kernel<2, true, true>);
+        else if (c->prm.split_walsh && c->prm.P == 3) e = run2(quantize_tc2_kernel<3, true, true>);
+        else e = run2(quantize_tc2_kernel<0, false, true>);
+    }
     else if (c->prm.P == 1) e = sym ? run2(quantize_tc2_kernel<1, true>) : run2(quantize_tc2_kernel<1, false>);
     else if (c->prm.P == 2) e = sym ? run2(quantize_tc2_kernel<2, true>) : run2(quantize_tc2_kernel<2, false>);
     else if (c->prm.P == 3) e = sym ? run2(quantize_tc2_kernel<3, true>) : run2(quantize_tc2_kernel<3, false>);
