@@ -223,12 +223,12 @@ __device__ __forceinline__ void stage_codes(const TcArgs& a, size_t row, int nk,
     const uint4* sg = reinterpret_cast<const uint4*>(a.k.signs + row * 4);
     const uint4* nm = reinterpret_cast<const uint4*>(a.k.norm + row);
     const uint4* rn = reinterpret_cast<const uint4*>(a.k.rnorm + row);
-    for (int e = threadIdx.x; e < npl + nsg + nn + nr; e += kT2Threads) {
-        if (e < npl) tc::cp_async16(st + 16 * e, pl + e);
-        else if (e < npl + nsg) tc::cp_async16(st + C::kSignOff + 16 * (e - npl), sg + (e - npl));
-        else if (e < npl + nsg + nn) tc::cp_async16(st + C::kNormOff + 16 * (e - npl - nsg), nm + (e - npl - nsg));
-        else tc::cp_async16(st + C::kRnormOff + 16 * (e - npl - nsg - nn), rn + (e - npl - nsg - nn));
-    }
+    static_assert(kT2Threads >= kTile && kT2Threads >= 48, "one thread per sign row; norms by warps 0 and 1");
+    const int t = threadIdx.x;
+    for (int e = t; e < npl; e += kT2Threads) tc::cp_async16(st + 16 * e, pl + e);
+    if (t < nsg) tc::cp_async16(st + C::kSignOff + 16 * t, sg + t);   // nsg <= kTile = kT2Threads
+    if (t < nn) tc::cp_async16(st + C::kNormOff + 16 * t, nm + t);
+    else if (t - 32 >= 0 && t - 32 < nr) tc::cp_async16(st + C::kRnormOff + 16 * (t - 32), rn + (t - 32));
     asm volatile("cp.async.commit_group;");
 }
 
@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
     const uint32_t bimg = tc::smem_u32(img);
     const uint64_t bm0 = tc::kmajor_desc(bimg, T * 128 * 8), bq0 = tc::kmajor_desc(bimg + C::kBmBytes, 128 * 8);
     const float k2 = 2.f * a.prm.qjl_scale;
+    float* lrow = a.logits + gp.qrow0 * (size_t)a.k.cap + (size_t)i0;   // logits of this chunk's first key, head 0
     float cst[16];
     // this thread's key of the tile in flight: norm, residual norm, index (-1: none)
     float pn = 0.f, pr = 0.f;
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kT2Threads) logits_tc_kernel(const TcArgs a, i
                                                    fmaf(dq[4 * h + 2], 1.f / 256.f, fmaf(dq[4 * h + 1], 1.f / 16.f, dq[4 * h])));
                 est = fmaf(pr, fmaf(k2, qv, cst[12 + h]), est);
             }
-            if (h < gp.nh) a.logits[(gp.qrow0 + h) * (size_t)a.k.cap + (size_t)(i0 + pkey)] = a.scale * est;
+            if (h < gp.nh) lrow[(size_t)h * a.k.cap + pkey] = a.scale * est;
         }
     };
     // waits (every thread, CTA-uniform outcome) for the MMAs of tile t
