@@ -55,27 +55,29 @@ def set_batch(b: int) -> None:
         B = b
 
 
-# DRAM traffic of the decode kernels from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum; batch 2 of the same workload, one launch each, scaled to a launch here by
-# the keys it scores).  A figure is reported only while the sources it was taken on are unchanged.
-NCU_SOURCES = ['k_attn.cu', 'attn_q8.cuh', 'lut.cuh', 'values.cuh', 'tq_device.cuh', 'tq_internal.h', 'k_logits_tc.cu', 'tcgen05.cuh', 'mma_e4m3.cuh']
-NCU_SOURCES_SHA = "f36e71ad4d311133"
-NCU_BYTES_PER_KEY = {
+# DRAM traffic of the decode kernels from one-kernel ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum; batch 2 of the same workload, one launch, scaled to a launch here by the
+# keys it scores).  A figure is reported only while the sources it was taken on are unchanged.
+NCU_CAPTURES = {
     # values_coded128_kernel<3, false>: 138.446 MB read + 2.834 MB written, 2 x 8 x 131071 keys
-    "attn_values": (138.445568e6 + 2.83392e6) / (2 * 8 * 131071),
-    # logits_tc_kernel<2>: 109.184 MB read + 13.840 MB written (part of the logits still in L2)
-    "attn_logits": (109.184e6 + 13.840384e6) / (2 * 8 * 131071),
+    "attn_values": (['k_attn.cu', 'attn_q8.cuh', 'lut.cuh', 'values.cuh', 'tq_device.cuh', 'tq_internal.h'], "b83f70a6c3e9b48a", (138.445568e6 + 2.83392e6) / (2 * 8 * 131071)),
+    # logits_tc_kernel<2>: 109.181 MB read + 13.929 MB written (part of the logits still in L2)
+    "attn_logits": (['k_logits_tc.cu', 'tcgen05.cuh', 'mma_e4m3.cuh', 'k_attn.cu', 'lut.cuh', 'attn_q8.cuh', 'tq_device.cuh', 'tq_internal.h'], "0f385a557dd290bb",
+                    (109.18144e6 + 13.929472e6) / (2 * 8 * 131071)),
 }
 
 
 def ncu_traffic(kernel: str, keys: float):
+    if kernel not in NCU_CAPTURES:
+        return None
+    sources, sha, per_key = NCU_CAPTURES[kernel]
     h = hashlib.sha256()
-    for f in NCU_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "compressed_kv_cache_02_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if h.hexdigest()[:16] != NCU_SOURCES_SHA or kernel not in NCU_BYTES_PER_KEY:
+    if per_key is None or h.hexdigest()[:16] != sha:
         return None
-    return NCU_BYTES_PER_KEY[kernel] * keys
+    return per_key * keys
 
 
 def peaks():
