@@ -9,9 +9,10 @@
 //                                moves by ~3e-7, far inside the 1e-5 band of the code parity
 //                                rule), both accumulated into one TMEM accumulator (128 columns).
 //   epilogue n = ||x||, n16, u = y / n, idx, bit planes, r' = y - n16 c[idx], ||r'||.
-//   phase 2  Z = r' (S Pi^T)^T   A = r' split into bf16 hi and lo (two passes into one
-//                                accumulator), B = S Pi^T as 2 bf16 pieces (z moves by ~2e-6 of
-//                                ||x||, inside the 1e-5 band of the sign rule); sign_j = [z_j > 0].
+//   phase 2  Z = r' (S Pi^T)^T   A = r' split into bf16 hi and lo, B = S Pi^T as 2 bf16 pieces,
+//                                all products but lo x the second piece into one accumulator (z
+//                                moves by a few 1e-6 of ||x||, inside the 1e-5 band of the sign
+//                                rule); sign_j = [z_j > 0].
 // Pi and S Pi^T stay resident in shared memory (4 x 32 KB), so one CTA per SM walks the tiles of
 // 128 rows.  The scalar quantizer (quantize_tc2_kernel, ordinary and split contexts) and the
 // polar encoder (polar_tc2_kernel) run two 8-warp groups per CTA, each on its own tile with its
@@ -126,13 +127,15 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(db), "r"(kIdesc), "r"(accumulate));
 }
 
-// D = (A_hi + A_lo) (B_0 + B_1)^T, A in tensor memory (8 columns per K-step of 16), B in shared memory.
+// D = A_hi (B_0 + B_1)^T + A_lo B_0^T, A in tensor memory (8 columns per K-step of 16), B in shared
+// memory.  The product left out, A_lo B_1^T, has entries below 2^-9 |r'| times 2^-9 |S Pi^T| each:
+// about 2^-18 ||r'|| in z (4e-6 of ||r'||), inside the 1e-5 ||x|| band of the sign rule.
 __device__ __forceinline__ void issue_pieces_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr) {
     const uint64_t db = smem_desc(b_saddr);
 #pragma unroll 1
     for (int ap = 0; ap < 2; ++ap)
 #pragma unroll 1
-        for (int p = 0; p < kPieces; ++p)
+        for (int p = 0; p < kPieces - ap; ++p)
 #pragma unroll
             for (int s = 0; s < 8; ++s)
                 mma_bf16_ts(d_tmem, a_tmem + 64 * ap + 8 * s, db + (uint64_t)((p * kMatBytes + s * 256) >> 4),
