@@ -546,14 +546,33 @@ __device__ __forceinline__ int sector_code(float lo, float hi) {
 
 // Level-l code (l >= 2): #{k : atan2(r_hi, r_lo) > t_k}, t_k in (0, pi/2), from the squared radii:
 // the angle passes t_k iff R_hi / R_lo > tan^2 t_k (the ratio is +inf for R_lo = 0 < R_hi and NaN
-// for 0 / 0, whose angle atan2(0, 0) = 0 passes nothing).
+// for 0 / 0, whose angle atan2(0, 0) = 0 passes nothing).  The tan^2 t_k ascend, so the count is a
+// B-step binary search (the step for bit b deciding bit b of the code); tau indices are compile-
+// time constants, the thresholds picked by selects.
 template <int B>
 __device__ __forceinline__ int level_code(float Rlo, float Rhi, const float* tau) {
     const float qv = __fdividef(Rhi, Rlo);
-    int c = 0;
-#pragma unroll
-    for (int t = 0; t < (1 << B) - 1; ++t) c += qv > tau[t] ? 1 : 0;
-    return c;
+    if constexpr (B == 1) {
+        return qv > tau[0] ? 1 : 0;
+    } else if constexpr (B == 2) {
+        const bool u1 = qv > tau[1];
+        const bool u0 = qv > (u1 ? tau[2] : tau[0]);
+        return (u1 ? 2 : 0) + (u0 ? 1 : 0);
+    } else if constexpr (B == 3) {
+        const bool u2 = qv > tau[3];
+        const bool u1 = qv > (u2 ? tau[5] : tau[1]);
+        const bool u0 = qv > (u2 ? (u1 ? tau[6] : tau[4]) : (u1 ? tau[2] : tau[0]));
+        return (u2 ? 4 : 0) + (u1 ? 2 : 0) + (u0 ? 1 : 0);
+    } else {
+        const bool u3 = qv > tau[7];
+        const bool u2 = qv > (u3 ? tau[11] : tau[3]);
+        const float t1 = u3 ? (u2 ? tau[13] : tau[9]) : (u2 ? tau[5] : tau[1]);
+        const bool u1 = qv > t1;
+        const float t0 = u3 ? (u2 ? (u1 ? tau[14] : tau[12]) : (u1 ? tau[10] : tau[8]))
+                            : (u2 ? (u1 ? tau[6] : tau[4]) : (u1 ? tau[2] : tau[0]));
+        const bool u0 = qv > t0;
+        return (u3 ? 8 : 0) + (u2 ? 4 : 0) + (u1 ? 2 : 0) + (u0 ? 1 : 0);
+    }
 }
 
 // The polar encoder runs two tiles in flight per CTA, as quantize_tc2_kernel: two 8-warp groups,
