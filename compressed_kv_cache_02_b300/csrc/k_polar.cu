@@ -651,7 +651,7 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
         L.rnorm = rnorm16;
         L.err = ctx->derr;
         cudaError_t e = tq::launch_polar_tc(L, static_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? TQ_OK : polar_cuda_fail(e, "polar_tc_kernel launch");
+        return e == cudaSuccess ? TQ_OK : polar_cuda_fail(e, "polar_tc2_kernel launch");
     }
     int sms = 148;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device);
