@@ -171,7 +171,9 @@ int tq_layout(const tq_ctx* ctx, int* planes, int* words_per_plane, int* sign_wo
 
 /* Kernel family on this context.  TQ_PATH_AUTO (the default) picks the fastest measured
  * family: tcgen05 tensor cores for bulk tq_quantize of bf16 rows at d = 128 (n >= 4096,
- * ld_x a multiple of 8, 16-byte aligned x), tcgen05 for tq_search_topk at d in (96,128] or
+ * ld_x a multiple of 8, 16-byte aligned x; Pi, S Pi^T and r' as two bf16 pieces each, fp32
+ * accumulation: codes and signs agree with exact arithmetic except within ~1e-5 of |x| of a
+ * decision boundary), tcgen05 for tq_search_topk at d in (96,128] or
  * (192,256] with 1-3 MSE bits, the tcgen05 logits kernel (below) for tq_attn_logits on
  * keys of 2 MSE bits + QJL when batch x KV heads x head quads x cap >= 2^18, and the table
  * kernels for the other logits.  TQ_PATH_CUDA_CORE forces CUDA-core kernels everywhere;
@@ -377,7 +379,8 @@ int tq_polar_quantize(tq_polar* ctx, const void* x, int dtype, int64_t n, int64_
 /* Kernel family of tq_polar_quantize (enum tq_kernel_path).  TQ_PATH_AUTO (the default)
  * encodes bf16 rows at d = 128 with n >= 4096 (ld_x a multiple of 8, x 16-byte aligned) on
  * the tcgen05 tensor cores (y = Pi x and the QJL projection (S Pi^T) r' as bf16 MMAs with the
- * matrices split into two bf16 pieces, fp32 accumulation; r' = y - y_hat in the rotated basis)
+ * matrices and r' split into two bf16 pieces each, fp32 accumulation, the product of the two
+ * small pieces left out; r' = y - y_hat in the rotated basis)
  * and everything else on CUDA cores; TQ_PATH_TENSOR takes the tensor-core encoder for every n
  * where the dtype, d and alignment allow it; TQ_PATH_CUDA_CORE never.  Both families give the
  * same codes up to angles within float rounding of a threshold.  TQ_ERR_ARG for another path.  */
